@@ -1,0 +1,68 @@
+"""Planted mistakes in a copy of the oracle must each fail at least one pin.
+
+Each mutant is a one-line textual change to a temporary copy of
+oracle/moe_oracle.c, compiled with gcc on the CPU. The oracle under oracle/
+is never modified. A mutant that every pin accepts would mean the pins cannot
+see that kind of mistake.
+"""
+import os
+import subprocess
+import tempfile
+
+import pytest
+
+import oracle
+import oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.c")
+
+MUTANTS = {
+    "nibble_order_reversed": ("(word >> (4 * (j % 8)))", "(word >> (4 * (7 - j % 8)))"),
+    "scale_bias_swapped": ("return fmaf(s, q, b);", "return fmaf(b, q, s);"),
+    "bias_dropped": ("return fmaf(s, q, b);", "return s * q;"),
+    "group_index_ignored": ("float s = bf16_widen(srow[j / ORACLE_GROUP]);", "float s = bf16_widen(srow[0]);"),
+    "router_bias_dropped": ("if (bias) acc += bias[e];", ""),
+    "no_renormalise": ("topk_w[(size_t)t * k + j] = p[topk_idx[(size_t)t * k + j]] / psum;",
+                       "topk_w[(size_t)t * k + j] = p[topk_idx[(size_t)t * k + j]];"),
+    "tie_to_higher_index": ("if (best < 0 || l[e] > l[best])", "if (best < 0 || l[e] >= l[best])"),
+    "silu_sign": ("float silu = g / (1.0f + expf(-g));", "float silu = g / (1.0f + expf(g));"),
+    "gate_up_swapped": ("float silu = g / (1.0f + expf(-g));\n        h[f] = silu * u;",
+                        "float silu = u / (1.0f + expf(-u));\n        h[f] = silu * g;"),
+    "x_index_reversed": ("g = fmaf(dequant_at(gqr, gsr, gbr, d), x[d], g);",
+                         "g = fmaf(dequant_at(gqr, gsr, gbr, d), x[D - 1 - d], g);"),
+    "combine_rank0_weight": ("acc = fmaf(topk_w[(size_t)t * k + j], y[",
+                             "acc = fmaf(topk_w[(size_t)t * k], y["),
+    "group_rank_reversed": ("slot_k[pos] = j;", "slot_k[pos] = k - 1 - j;"),
+    "offsets_inclusive": ("offsets[e + 1] = offsets[e] + counts[e];",
+                          "offsets[e + 1] = offsets[e] + counts[e] + (e == 0);"),
+    "final_round_truncates": ("u += 0x7FFFu + ((u >> 16) & 1u);", ""),
+}
+
+
+def _build_mutant(name, old, new, tmp):
+    text = open(SRC).read()
+    assert text.count(old) == 1, f"mutation site for {name} not unique"
+    path_c = os.path.join(tmp, f"{name}.c")
+    path_so = os.path.join(tmp, f"lib{name}.so")
+    with open(path_c, "w") as f:
+        f.write(text.replace(old, new))
+    subprocess.run(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-o", path_so,
+                    path_c, "-lm"], check=True)
+    return path_so
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name):
+    old, new = MUTANTS[name]
+    with tempfile.TemporaryDirectory() as tmp:
+        so = _build_mutant(name, old, new, tmp)
+        failed = []
+        with oracle.using(so):
+            for check in pins.ALL_CHECKS:
+                try:
+                    check()
+                except AssertionError:
+                    failed.append(check.__name__)
+                except Exception as exc:  # a mutant may also break an invariant loudly
+                    failed.append(f"{check.__name__}:{type(exc).__name__}")
+        assert failed, f"no pin catches mutant {name}"
