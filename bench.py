@@ -1,0 +1,407 @@
+#!/usr/bin/env python
+"""Benchmark of one quantized MoE layer's decode step on GB300.
+
+Workload (default): a 128-expert, top-8 MoE layer with D=2048, Dff=768 and
+affine 4-bit group-64 experts (the Qwen3-30B-A3B layer shape), decoding one
+token per step. x is bf16 N(0,1), the router is bf16 N(0,0.02) with top-k
+logit margins >= 1e-2, and expert weights are N(0,0.02) before quantisation.
+All data is synthetic and seeded.
+
+A step is one moe_decode_forward call: the router, grouping, gate/up, down
+and combine for one cohort. Steps cycle through R resident layer replicas and
+P pre-drawn cohorts, so an expert plane read in one step was last read at
+least R-1 steps (hundreds of MB of other traffic) earlier and is not
+L2-resident.
+
+Output: one JSON line (rank 0). `value` is tokens/s of the whole job over the
+timed K steps, which run as a captured CUDA graph; `e2e` is the same metric
+through the host-buffer entry point, with the H2D and D2H copies inside the
+timed region; `roofline` relates the unique expert bytes per step to the
+measured HBM peak.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer decode tokens/s; unique-expert-byte HBM GB/s vs GB300 peak"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--shape", default="qwen3", choices=["qwen3", "e256", "tiny"])
+    ap.add_argument("--n-tokens", type=int, default=1)
+    ap.add_argument("--kind", default="independent", choices=["independent", "shared", "disjoint"])
+    ap.add_argument("--replicas", type=int, default=16)
+    ap.add_argument("--cohorts", type=int, default=64)
+    ap.add_argument("--flags", type=int, default=0, help="MOE_FLAG_* for the plan")
+    ap.add_argument("--mma-min-tokens", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU work of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+SEEDS = {"qwen3": 1, "e256": 3, "tiny": 0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------------------
+# clocks sampler
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smmax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smmax = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smmax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# distributed helpers (one process per GPU; independent replicas)
+# ----------------------------------------------------------------------------
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg, device=None):
+    if pg is not None:
+        if device is not None:
+            pg.barrier(device_ids=[device])
+        else:
+            pg.barrier()
+
+
+def max_over_ranks(pg, value: float, device=None) -> float:
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device if device is not None else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# oracle (CPU) timing: the reference arm and the cpu_baseline key
+# ----------------------------------------------------------------------------
+def oracle_sample(shape_name, n, kind, cohorts, seconds):
+    """Time the CPU oracle on cohorts of the workload for about `seconds`."""
+    import numpy as np
+
+    import moe_synth as ms
+    import oracle
+    shape = ms.SHAPES[shape_name]
+    seed = SEEDS[shape_name]
+    router_w, bias = ms.draw_router(shape, seed, 0)
+    xs = [ms.draw_tokens(shape, router_w, bias, seed, 0, n, kind, cohort=c) for c in range(cohorts)]
+    experts = sorted({e for x in xs for e in ms.routed_experts(x, router_w, bias, shape.top_k)})
+    lay = ms.make_layer(shape, seed, 0, experts)
+    threads = oracle.set_threads(os.cpu_count() or 1)
+    oracle.moe_forward(xs[0], router_w, bias, lay.planes, shape.top_k)  # warm
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.moe_forward(xs[steps % cohorts], router_w, bias, lay.planes, shape.top_k)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": n * steps / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{steps} steps of n_tokens={n} ({kind} cohorts), {el:.1f} s, "
+                      f"OpenMP over (token, expert) slots"}, steps, el
+
+
+def run_reference(args, world, rank, pg):
+    """The oracle, as it stands, on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    shape_name, n = args.shape, args.n_tokens
+    seconds = max(1.0, min(30.0, args.cpu_seconds))
+    cb, steps, el = oracle_sample(shape_name, n, args.kind, min(args.cohorts, 16), seconds)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": steps, "warmup": 1, "ms_per_step": 1000.0 * el / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": workload_config(args),
+        "cpu_baseline": cb,
+        "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(args):
+    import moe_synth as ms
+    shape = ms.SHAPES[args.shape]
+    names = {"qwen3": "qwen3-30b-a3b-shaped MoE layer", "e256": "256-expert top-6 MoE layer",
+             "tiny": "tiny MoE layer"}
+    return {"workload": f"{names[args.shape]} decode, n_tokens={args.n_tokens}",
+            "E": shape.E, "top_k": shape.top_k, "D": shape.D, "Dff": shape.F,
+            "quant": "affine 4-bit, group 64, bf16 scale+bias", "n_tokens": args.n_tokens,
+            "cohorts": args.kind, "global_batch": args.n_tokens * args.gpus,
+            "l2": f"{args.replicas} resident layer replicas cycled, {args.cohorts} cohorts",
+            "parallelism": f"replicas x{args.gpus}"}
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+def run_ours(args, world, rank, local, pg):
+    import numpy as np
+    import torch
+
+    import moe_synth as ms
+    import quantized_moe_decode_softmax_gb300 as q
+
+    shape = ms.SHAPES[args.shape]
+    seed = SEEDS[args.shape]
+    n = args.n_tokens
+    workers = max(1, min(16, os.cpu_count() or 1))
+
+    # host-side generation (spawn pool: safe before or after CUDA init)
+    lay = ms.make_layer(shape, seed, 0, workers=workers)
+    cohorts = [ms.draw_tokens(shape, lay.router_w, lay.router_bias, seed, 0, n, args.kind, cohort=c)
+               for c in range(args.cohorts)]
+    U_of = [len(ms.routed_experts(x, lay.router_w, lay.router_bias, shape.top_k)) for x in cohorts]
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    base = q.DeviceLayer.from_host(ms.router_storage(shape, lay.router_w), lay.router_bias,
+                                   lay.planes, shape.top_k, device=dev)
+    reps = [base]
+    for _ in range(args.replicas - 1):
+        planes = {f: t.clone() for f, t in base.planes.items()}
+        rb = None if base.router_bias is None else base.router_bias.clone()
+        reps.append(q.DeviceLayer(base.router_w.clone(), rb, planes, base.E, base.top_k, base.D,
+                                  base.Dff))
+    del lay
+    act = torch.bfloat16 if shape.act_dtype == "bf16" else torch.float32
+
+    def to_dev(x):
+        st = ms.x_storage(shape, x)
+        t = torch.from_numpy(st.view(np.int16) if st.dtype == np.uint16 else st)
+        return t.to(dev).view(act) if st.dtype == np.uint16 else t.to(dev)
+
+    xs = [to_dev(x) for x in cohorts]
+    outs = [torch.empty((n, shape.D), dtype=act, device=dev) for _ in range(2)]
+    layer = q.MoeDecodeLayer(shape.E, shape.top_k, shape.D, shape.F, max_tokens=max(n, 1),
+                             act_dtype=shape.act_dtype, flags=args.flags,
+                             mma_min_tokens=args.mma_min_tokens)
+    stream = torch.cuda.Stream(device=dev)
+    K, W = args.steps, args.warmup
+
+    def step(i, s):
+        layer.forward(xs[i % len(xs)], reps[i % len(reps)], outs[i % 2], stream=s)
+
+    c0 = q.moe_plan_launch_count(layer.plan)
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            step(i, stream)
+    stream.synchronize()
+    layer.check()
+    launches_per_step = (q.moe_plan_launch_count(layer.plan) - c0) / max(W, 1)
+
+    # capture exactly K steps; a second graph brackets each step with events
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(K):
+            step(W + i, stream)
+    ev_graph = None
+    try:
+        ev = [(torch.cuda.Event(enable_timing=True, external=True),
+               torch.cuda.Event(enable_timing=True, external=True)) for _ in range(K)]
+        ev_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ev_graph, stream=stream):
+            for i in range(K):
+                ev[i][0].record(stream)
+                step(W + i, stream)
+                ev[i][1].record(stream)
+    except TypeError:
+        ev_graph = None
+
+    # sustained replays for the clock record, then the timed replay
+    sampler = None if args.no_clocks else ClockSampler(local)
+    with torch.cuda.stream(stream):
+        graph.replay()
+        stream.synchronize()
+        if sampler:
+            sampler.start()
+        t_end = time.perf_counter() + 1.5
+        while time.perf_counter() < t_end:
+            graph.replay()
+            stream.synchronize()
+        barrier(pg, local)
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        stop = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        graph.replay()
+        stop.record(stream)
+        stop.synchronize()
+        torch.cuda.synchronize()
+        barrier(pg, local)
+        clocks = sampler.stop() if sampler else None
+    elapsed_ms = start.elapsed_time(stop)
+    layer.check()
+    elapsed_ms = max_over_ranks(pg, elapsed_ms, dev)
+    ms_per_step = elapsed_ms / K
+
+    # per-step device time (each step's events), same inputs
+    kernel_ms = None
+    if ev_graph is not None:
+        with torch.cuda.stream(stream):
+            ev_graph.replay()
+            stream.synchronize()
+        kernel_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+
+    # e2e: host buffers through the public API, copies inside the timed region
+    E2E = max(1, min(args.e2e_steps, K))
+    x_host = [xs[i % len(xs)].cpu().pin_memory() for i in range(min(E2E, len(xs)))]
+    out_host = torch.empty((n, shape.D), dtype=act).pin_memory()
+    with torch.cuda.stream(stream):
+        layer.forward_host(x_host[0], reps[0], out_host, stream=stream)
+        barrier(pg, local)
+        t0 = time.perf_counter()
+        for i in range(E2E):
+            layer.forward_host(x_host[i % len(x_host)], reps[i % len(reps)], out_host, stream=stream)
+        t1 = time.perf_counter()
+    e2e_s = max_over_ranks(pg, t1 - t0, dev)
+    esize = 2 if shape.act_dtype == "bf16" else 4
+
+    # algorithmic bytes of the timed steps
+    steps_U = [U_of[(W + i) % len(U_of)] for i in range(K)]
+    avg_U = sum(steps_U) / K
+    act_bytes = n * shape.D * esize * 2
+    bytes_per_step = avg_U * shape.plane_bytes + act_bytes
+    router_bytes = shape.E * shape.D * esize
+    peak, peak_kind = load_peaks()
+    t_kernel = (kernel_ms if kernel_ms is not None else ms_per_step) / 1000.0
+    achieved = bytes_per_step / t_kernel / 1e9
+    value = world * n * K / (elapsed_ms / 1000.0)
+
+    if rank == 0:
+        cb = None
+        if not args.no_cpu_baseline:
+            cb, _, _ = oracle_sample(args.shape, n, args.kind, min(args.cohorts, 16),
+                                     max(1.0, min(30.0, args.cpu_seconds)))
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": K, "warmup": W, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; random-init weights of the layer shape)",
+            "config": workload_config(args),
+            "hbm_gbs_unique_expert_bytes": bytes_per_step / (ms_per_step / 1000.0) / 1e9,
+            "unique_experts_per_step": avg_U,
+            "bytes_per_step": bytes_per_step,
+            "router_bytes_per_step": router_bytes,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                         if peak_kind == "measured" else "fallback",
+                         "kernel_us": t_kernel * 1e6,
+                         "timing": "per-step CUDA events inside the captured graph"
+                         if kernel_ms is not None else "graph replay time / steps"},
+            "e2e": {"value": world * n * E2E / e2e_s, "unit": "tokens/s",
+                    "h2d_bytes_per_step": n * shape.D * esize,
+                    "d2h_bytes_per_step": n * shape.D * esize, "steps": E2E},
+            "gpu_launches": int(round(K * launches_per_step)),
+            "clocks": clocks,
+            "cpu_baseline": cb,
+        }
+        print(json.dumps(line), flush=True)
+    layer.close()
+
+
+def main():
+    args = parse_args()
+    world, rank, local, pg = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank, pg)
+    else:
+        run_ours(args, world, rank, local, pg)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+/*
+ * moe_decode.h -- C ABI of the quantized MoE decode library (GB300, sm_103a).
+ *
+ * One call runs one MoE layer's decode step for a cohort of 1..64 tokens:
+ *   1. router GEMV, softmax over all experts, top-k, renormalise the k weights
+ *   2. group the n*k (token, rank) slots by expert, de-duplicated, so every
+ *      selected expert's planes are streamed from HBM once per step
+ *   3. per selected expert: h = silu(Wg x) * (Wu x) on affine 4-bit weights
+ *   4. y = Wd h, and out[t] = sum_j w[t,j] * y[t,j] in rank order j,
+ *      f32 partials with a single final rounding
+ *
+ * Sources (mlxcel GitHub issues):
+ *   #1616 "perf(moe): batched decode scales 1.55x against 3.25x on dense"
+ *     Current Behavior - the decode MoE block (SwitchGLU + moe_weighted_sum),
+ *       the B=1-only fused kernel and the 4-bit group-64 expert format;
+ *     Leading hypothesis - per-slot expert traffic, no de-duplication;
+ *     Proposed Solution - a token dimension for the fused kernel and
+ *       de-duplicated expert planes;
+ *     Implementation Notes - n_tokens as a runtime extent, f32 partials with
+ *       a single final rounding, decline unsupported shapes instead of
+ *       failing, validate shapes before dispatch.
+ *   #1859 "perf(moe): attribute the MoE decode gap at the M = 1 expert
+ *     gather", Problem / Background - one expert row per (token, k) slot.
+ *
+ * Conventions
+ *   - Every pointer passed to moe_decode_forward is a DEVICE pointer owned by
+ *     the caller, except where a comment says host. The library never frees
+ *     or retains caller memory beyond the call.
+ *   - The plan owns its workspace (device memory sized at plan creation for
+ *     max_tokens). moe_decode_forward allocates nothing.
+ *   - Calls are asynchronous on the given CUDA stream (NULL = legacy default
+ *     stream) unless documented otherwise. Calls on one plan must not overlap
+ *     on the device (they share the workspace): issue them on one stream, or
+ *     order the streams.
+ *   - Errors are returned as moe_status, never thrown or trapped. Argument
+ *     checks happen on the host before any launch; on a non-OK return from
+ *     a check, nothing was launched.
+ *
+ * Data formats (MLX-style affine 4-bit quantisation, group 64)
+ *   plane q : uint32 [E, rows, cols/8]; nibble j (bits 4j..4j+3) of word i
+ *             is the code (0..15) of input column 8*i + j
+ *   scale s : bf16 [E, rows, cols/64]; bias b : bf16 [E, rows, cols/64]
+ *   weight  : w = s * q + b, groups of 64 consecutive input columns
+ *   gate, up: rows = Dff, cols = D;  down: rows = D, cols = Dff
+ *   All planes row-major, expert-major, densely packed; 16-byte aligned.
+ */
+#ifndef MOE_DECODE_H
+#define MOE_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* null pointer, bad n_tokens / top_k / dims */
+    MOE_ERR_UNSUPPORTED = 2,  /* a shape or format this library declines */
+    MOE_ERR_CUDA = 3,         /* a CUDA call or launch failed */
+    MOE_ERR_OOM = 4,          /* workspace allocation failed */
+    MOE_ERR_TIMEOUT = 5       /* a device-side wait gave up (bounded spin) */
+} moe_status;
+
+/* element types of x, router weights and out */
+enum { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1 };
+
+/* plan flags */
+enum {
+    /* CUDA-core f32 path for every expert: weights dequantised exactly to f32,
+     * f32 accumulation throughout. Slower; used to check numerics. */
+    MOE_FLAG_F32_DEBUG = 1u << 0,
+    /* print the chosen path of each forward call to stderr */
+    MOE_FLAG_TRACE = 1u << 1
+};
+
+typedef struct {
+    int E;              /* experts, 1..1024 */
+    int top_k;          /* experts per token, 1..min(E, 16) */
+    int D;              /* hidden size; multiple of 64 */
+    int Dff;            /* expert intermediate size; multiple of 64, <= 8192 */
+    int bits;           /* must be 4 */
+    int group_size;     /* must be 64 */
+    int max_tokens;     /* largest cohort a forward call may pass, 1..64 */
+    int x_dtype;        /* MOE_DTYPE_* of x */
+    int router_dtype;   /* MOE_DTYPE_* of the router weights */
+    int out_dtype;      /* MOE_DTYPE_* of out */
+    unsigned flags;     /* MOE_FLAG_* */
+    int mma_min_tokens; /* per-expert token count from which an expert takes
+                           the tensor-core tile path; 0 = library default */
+} moe_config;
+
+typedef struct {
+    const uint32_t *gate_q; /* [E, Dff, D/8]  */
+    const uint16_t *gate_s; /* [E, Dff, D/64] bf16 */
+    const uint16_t *gate_b; /* [E, Dff, D/64] bf16 */
+    const uint32_t *up_q;   /* [E, Dff, D/8]  */
+    const uint16_t *up_s;   /* [E, Dff, D/64] bf16 */
+    const uint16_t *up_b;   /* [E, Dff, D/64] bf16 */
+    const uint32_t *down_q; /* [E, D, Dff/8]  */
+    const uint16_t *down_s; /* [E, D, Dff/64] bf16 */
+    const uint16_t *down_b; /* [E, D, Dff/64] bf16 */
+} moe_expert_planes;
+
+typedef struct moe_plan moe_plan;
+
+/* Library ABI version (MOE_ABI_VERSION of the build). */
+int moe_abi_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char *moe_status_str(moe_status s);
+
+/* Device bytes a plan for cfg would allocate. Host-only; no CUDA call.
+ * Returns INVALID_ARG / UNSUPPORTED exactly as moe_plan_create would. */
+moe_status moe_plan_workspace_bytes(const moe_config *cfg, size_t *bytes);
+
+/* Validate cfg and allocate the plan's workspace on the current device.
+ * The plan is bound to that device. Decline (UNSUPPORTED): bits != 4,
+ * group_size != 64, D or Dff not a multiple of 64, Dff > 8192, E > 1024,
+ * top_k > 16. INVALID_ARG: null pointers, non-positive sizes,
+ * top_k > E, max_tokens outside 1..64, unknown dtypes. OOM / CUDA: the
+ * allocation failed (nothing leaks). On success *out owns the workspace
+ * until moe_plan_free. */
+moe_status moe_plan_create(const moe_config *cfg, moe_plan **out);
+
+/* One decode step.
+ *   x           [n_tokens, D] of cfg.x_dtype (device)
+ *   router_w    [E, D] of cfg.router_dtype (device)
+ *   router_bias [E] f32 added to the logits, or NULL (device)
+ *   planes      expert planes (struct in host memory, pointers to device)
+ *   n_tokens    cohort size, 1..cfg.max_tokens (runtime extent: no
+ *               re-specialisation per n)
+ *   top_k       must equal cfg.top_k (checked, INVALID_ARG otherwise)
+ *   out         [n_tokens, D] of cfg.out_dtype (device); must not alias x
+ *   stream      cudaStream_t, or NULL for the legacy default stream
+ * Asynchronous. Returns INVALID_ARG before any launch on a bad argument,
+ * CUDA if a launch fails. A device-side timeout of the step's internal
+ * waits is reported by the NEXT call on the plan, or by moe_plan_check. */
+moe_status moe_decode_forward(moe_plan *plan, const void *x, const void *router_w,
+                              const float *router_bias, const moe_expert_planes *planes,
+                              int n_tokens, int top_k, void *out, void *stream);
+
+/* The same step with x and out in HOST memory: copies x to the plan's device
+ * staging buffer, runs moe_decode_forward, copies out back and synchronises
+ * the stream before returning. Pinned host memory gives asynchronous copies;
+ * pageable memory works but is slower. */
+moe_status moe_decode_forward_host(moe_plan *plan, const void *x_host, const void *router_w,
+                                   const float *router_bias, const moe_expert_planes *planes,
+                                   int n_tokens, int top_k, void *out_host, void *stream);
+
+/* Synchronise the plan's last stream and report a device-side timeout or
+ * internal error recorded by earlier calls (then clear it). */
+moe_status moe_plan_check(moe_plan *plan);
+
+/* Copy the routing and grouping of the plan's last forward call to HOST
+ * arrays (any pointer may be NULL to skip it). Synchronises the last stream.
+ *   topk_idx [n,k] int32, topk_w [n,k] f32   (rank order: descending logit,
+ *                                             ties to the lower expert id)
+ *   counts [E], offsets [E+1]                (exclusive scan of counts)
+ *   slot_token [n*k], slot_k [n*k]           (slots grouped by expert
+ *                                             ascending, token ascending)
+ *   unique [E] (first *U entries valid), U   (experts with count > 0) */
+moe_status moe_get_routing(moe_plan *plan, int32_t *topk_idx, float *topk_w,
+                           int32_t *counts, int32_t *offsets, int32_t *slot_token,
+                           int32_t *slot_k, int32_t *unique, int32_t *U);
+
+/* Number of CUDA kernels this plan has enqueued since creation (host
+ * counter; forward calls captured into a CUDA graph count once, at capture). */
+moe_status moe_plan_launch_count(const moe_plan *plan, uint64_t *count);
+
+/* Free the plan's workspace (synchronises its last stream). NULL is a no-op. */
+moe_status moe_plan_free(moe_plan *plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_DECODE_H */

@@ -199,11 +199,22 @@ def draw_router(shape: LayerShape, seed: int, layer: int):
     return w, bias
 
 
+def expert_planes(shape: LayerShape, seed: int, layer: int, e: int):
+    """The nine quantised arrays of expert e (gate q/s/b, up q/s/b, down q/s/b)."""
+    gate, up, down = draw_expert_weights(shape, seed, layer, e)
+    return (*quantize_affine4(gate), *quantize_affine4(up), *quantize_affine4(down))
+
+
+def _expert_planes_job(args):
+    return args[3], expert_planes(*args)
+
+
 def make_layer(shape: LayerShape, seed: int, layer: int = 0,
-               experts: Optional[Sequence[int]] = None) -> Layer:
+               experts: Optional[Sequence[int]] = None, workers: int = 1) -> Layer:
     """Draw a layer. If `experts` is given, only those experts' planes are drawn
     and the others are left zero (their bytes are never read by a decode step
-    that does not route to them)."""
+    that does not route to them). workers > 1 draws experts in a process pool
+    started with the 'spawn' method (safe after CUDA has been initialised)."""
     router_w, router_bias = draw_router(shape, seed, layer)
     E, D, F = shape.E, shape.D, shape.F
     planes = ExpertPlanes(
@@ -218,13 +229,23 @@ def make_layer(shape: LayerShape, seed: int, layer: int = 0,
         down_b=np.zeros((E, D, F // GROUP), np.uint16),
     )
     mat = np.zeros(E, bool)
-    todo = range(E) if experts is None else sorted(set(int(e) for e in experts))
-    for e in todo:
-        gate, up, down = draw_expert_weights(shape, seed, layer, e)
-        planes.gate_q[e], planes.gate_s[e], planes.gate_b[e] = quantize_affine4(gate)
-        planes.up_q[e], planes.up_s[e], planes.up_b[e] = quantize_affine4(up)
-        planes.down_q[e], planes.down_s[e], planes.down_b[e] = quantize_affine4(down)
-        mat[e] = True
+    todo = list(range(E)) if experts is None else sorted(set(int(e) for e in experts))
+    jobs = [(shape, seed, layer, e) for e in todo]
+    if workers > 1 and len(jobs) > 1:
+        import concurrent.futures as cf
+        import multiprocessing as mp
+        with cf.ProcessPoolExecutor(max_workers=workers, mp_context=mp.get_context("spawn")) as ex:
+            results = ex.map(_expert_planes_job, jobs, chunksize=max(1, len(jobs) // (4 * workers)))
+            for e, arrs in results:
+                for f, a in zip(ExpertPlanes.FIELDS, arrs):
+                    getattr(planes, f)[e] = a
+                mat[e] = True
+    else:
+        for job in jobs:
+            e, arrs = _expert_planes_job(job)
+            for f, a in zip(ExpertPlanes.FIELDS, arrs):
+                getattr(planes, f)[e] = a
+            mat[e] = True
     return Layer(shape, seed, layer, router_w, router_bias, planes, mat)
 
 
@@ -315,13 +336,13 @@ def routed_experts(x, router_w, bias, k) -> List[int]:
 
 
 def make_case(shape_name: str, seed: int, n: int, kind: str = "independent",
-              layer: int = 0, cohort: int = 0, lazy: bool = False):
+              layer: int = 0, cohort: int = 0, lazy: bool = False, workers: int = 1):
     """A layer and a cohort. lazy=True draws only the experts the cohort routes to."""
     shape = SHAPES[shape_name]
     router_w, bias = draw_router(shape, seed, layer)
     x = draw_tokens(shape, router_w, bias, seed, layer, n, kind, cohort)
     experts = routed_experts(x, router_w, bias, shape.top_k) if lazy else None
-    lay = make_layer(shape, seed, layer, experts)
+    lay = make_layer(shape, seed, layer, experts, workers=workers)
     return lay, x
 
 

@@ -1,0 +1,299 @@
+// moe_api.cu -- the C ABI: plan creation and validation, workspace, dispatch.
+//
+// The shape checks and the decline rule follow mlxcel issue #1616
+// "perf(moe): batched decode scales 1.55x against 3.25x on dense",
+// Implementation Notes: unsupported configurations decline (here
+// MOE_ERR_UNSUPPORTED) instead of failing, shapes are validated before any
+// dispatch because a bad shape must never reach a kernel, n_tokens is a
+// runtime extent and never a specialisation key.
+#include <cuda_runtime.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "moe_internal.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+size_t elem_size(int dtype) { return dtype == MOE_DTYPE_F32 ? 4 : 2; }
+
+moe_status validate_config(const moe_config *c) {
+    if (!c) return MOE_ERR_INVALID_ARG;
+    if (c->bits != 4 || c->group_size != kGroup) return MOE_ERR_UNSUPPORTED;
+    if (c->E < 1 || c->top_k < 1 || c->D < 1 || c->Dff < 1 || c->max_tokens < 1)
+        return MOE_ERR_INVALID_ARG;
+    if (c->top_k > c->E) return MOE_ERR_INVALID_ARG;
+    if (c->max_tokens > kMaxTokens) return MOE_ERR_INVALID_ARG;
+    for (int dt : {c->x_dtype, c->router_dtype, c->out_dtype})
+        if (dt != MOE_DTYPE_F32 && dt != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
+    if (c->mma_min_tokens < 0) return MOE_ERR_INVALID_ARG;
+    if (c->E > kMaxE || c->top_k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
+    if (c->D % kGroup || c->Dff % kGroup) return MOE_ERR_UNSUPPORTED;
+    if (c->Dff > kMaxDff || c->D > kMaxD) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+// carve the workspace; with base == nullptr only computes the size
+size_t carve(const moe_config &c, char *base, Workspace *ws) {
+    const size_t n = c.max_tokens, E = c.E, k = c.top_k, D = c.D, F = c.Dff;
+    const size_t S = n * k;
+    size_t off = 0;
+    auto take = [&](size_t bytes) -> char * {
+        char *p = base ? base + off : nullptr;
+        off += align_up(bytes);
+        return p;
+    };
+    Workspace w{};
+    w.logits = (float *)take(n * E * 4);
+    w.topk_idx = (int *)take(S * 4);
+    w.topk_w = (float *)take(S * 4);
+    w.counts = (int *)take(E * 4);
+    w.offsets = (int *)take((E + 1) * 4);
+    w.slot_token = (int *)take(S * 4);
+    w.slot_k = (int *)take(S * 4);
+    w.slot_of = (int *)take(S * 4);
+    w.unique = (int *)take(E * 4);
+    w.U = (int *)take(4);
+    w.h = (float *)take(S * F * 4);
+    w.y = (float *)take(S * D * 4);
+    w.status = (unsigned *)take(4 * 4);
+    w.sync = (unsigned *)take(64 * 4);
+    w.phase_ns = (unsigned long long *)take(256 * 8);
+    w.x_stage = take(n * D * elem_size(c.x_dtype));
+    w.out_stage = take(n * D * elem_size(c.out_dtype));
+    if (ws) *ws = w;
+    return off;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+moe_status check_planes(const moe_expert_planes *p) {
+    if (!p) return MOE_ERR_INVALID_ARG;
+    const void *ptrs[9] = {p->gate_q, p->gate_s, p->gate_b, p->up_q, p->up_s,
+                           p->up_b, p->down_q, p->down_s, p->down_b};
+    for (const void *q : ptrs)
+        if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+struct DeviceGuard {
+    int prev = -1;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        if (prev != dev) cudaSetDevice(dev);
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+bool trace_enabled(const moe_plan *p) {
+    if (p->cfg.flags & MOE_FLAG_TRACE) return true;
+    const char *env = getenv("MOE_TRACE");
+    return env && env[0] && env[0] != '0';
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char *moe_status_str(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+        case MOE_ERR_OOM: return "MOE_ERR_OOM";
+        case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    }
+    return "MOE_ERR_UNKNOWN";
+}
+
+moe_status moe_plan_workspace_bytes(const moe_config *cfg, size_t *bytes) {
+    moe_status st = validate_config(cfg);
+    if (st != MOE_OK) return st;
+    if (!bytes) return MOE_ERR_INVALID_ARG;
+    *bytes = carve(*cfg, nullptr, nullptr);
+    return MOE_OK;
+}
+
+moe_status moe_plan_create(const moe_config *cfg, moe_plan **out) {
+    if (!out) return MOE_ERR_INVALID_ARG;
+    *out = nullptr;
+    moe_status st = validate_config(cfg);
+    if (st != MOE_OK) return st;
+    moe_plan *p = (moe_plan *)calloc(1, sizeof(moe_plan));
+    if (!p) return MOE_ERR_OOM;
+    p->cfg = *cfg;
+    p->mma_min_tokens = cfg->mma_min_tokens > 0 ? cfg->mma_min_tokens : 16;
+    if (const char *env = getenv("MOE_MMA_MIN_TOKENS")) {
+        int v = atoi(env);
+        if (v > 0) p->mma_min_tokens = v;
+    }
+    if (cudaGetDevice(&p->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess) {
+        cudaGetLastError();
+        free(p);
+        return MOE_ERR_CUDA;
+    }
+    p->ws_bytes = carve(*cfg, nullptr, nullptr);
+    cudaError_t err = cudaMalloc(&p->ws_base, p->ws_bytes);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        free(p);
+        return err == cudaErrorMemoryAllocation ? MOE_ERR_OOM : MOE_ERR_CUDA;
+    }
+    carve(*cfg, (char *)p->ws_base, &p->ws);
+    if (cudaMemset(p->ws_base, 0, p->ws_bytes) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(p->ws_base);
+        free(p);
+        return MOE_ERR_CUDA;
+    }
+    p->last_stream = nullptr;
+    *out = p;
+    return MOE_OK;
+}
+
+moe_status moe_decode_forward(moe_plan *plan, const void *x, const void *router_w,
+                              const float *router_bias, const moe_expert_planes *planes,
+                              int n_tokens, int top_k, void *out, void *stream) {
+    if (!plan || !x || !router_w || !out) return MOE_ERR_INVALID_ARG;
+    if (n_tokens < 1 || n_tokens > plan->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+    if (top_k != plan->cfg.top_k) return MOE_ERR_INVALID_ARG;
+    if (x == out) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(router_w) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+    if (router_bias && ((uintptr_t)router_bias & 3u)) return MOE_ERR_INVALID_ARG;
+    moe_status st = check_planes(planes);
+    if (st != MOE_OK) return st;
+
+    DeviceGuard guard(plan->device);
+    cudaStream_t s = (cudaStream_t)stream;
+    StepArgs a{};
+    a.s = Shape{plan->cfg.E, plan->cfg.top_k, plan->cfg.D, plan->cfg.Dff, n_tokens,
+                plan->cfg.x_dtype, plan->cfg.router_dtype, plan->cfg.out_dtype};
+    a.x = x;
+    a.router_w = router_w;
+    a.router_bias = router_bias;
+    a.planes = *planes;
+    a.out = out;
+
+    if (trace_enabled(plan))
+        fprintf(stderr, "[moe] forward n=%d E=%d k=%d D=%d Dff=%d path=%s\n", n_tokens,
+                a.s.E, a.s.k, a.s.D, a.s.F, "f32-check");
+    int launched = 0;
+    cudaError_t err = launch_router_logits(a, plan->ws, s, launched);
+    if (err == cudaSuccess) err = launch_topk_group(a, plan->ws, s, launched);
+    if (err == cudaSuccess) err = launch_experts_f32(a, plan->ws, s, launched);
+    plan->launches += launched;
+    plan->last_stream = s;
+    plan->last_n = n_tokens;
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+moe_status moe_decode_forward_host(moe_plan *plan, const void *x_host, const void *router_w,
+                                   const float *router_bias, const moe_expert_planes *planes,
+                                   int n_tokens, int top_k, void *out_host, void *stream) {
+    if (!plan || !x_host || !out_host) return MOE_ERR_INVALID_ARG;
+    if (n_tokens < 1 || n_tokens > plan->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+    DeviceGuard guard(plan->device);
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t xb = (size_t)n_tokens * plan->cfg.D * elem_size(plan->cfg.x_dtype);
+    const size_t ob = (size_t)n_tokens * plan->cfg.D * elem_size(plan->cfg.out_dtype);
+    if (cudaMemcpyAsync(plan->ws.x_stage, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    moe_status st = moe_decode_forward(plan, plan->ws.x_stage, router_w, router_bias, planes,
+                                       n_tokens, top_k, plan->ws.out_stage, stream);
+    if (st != MOE_OK) return st;
+    if (cudaMemcpyAsync(out_host, plan->ws.out_stage, ob, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
+moe_status moe_plan_check(moe_plan *plan) {
+    if (!plan) return MOE_ERR_INVALID_ARG;
+    DeviceGuard guard(plan->device);
+    if (cudaStreamSynchronize(plan->last_stream) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    unsigned status = 0;
+    if (cudaMemcpy(&status, plan->ws.status, sizeof status, cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    if (status) {
+        unsigned zero = 0;
+        cudaMemcpy(plan->ws.status, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        return (status & kDevErrTimeout) ? MOE_ERR_TIMEOUT : MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
+moe_status moe_get_routing(moe_plan *plan, int32_t *topk_idx, float *topk_w, int32_t *counts,
+                           int32_t *offsets, int32_t *slot_token, int32_t *slot_k,
+                           int32_t *unique, int32_t *U) {
+    if (!plan) return MOE_ERR_INVALID_ARG;
+    if (plan->last_n < 1) return MOE_ERR_INVALID_ARG;  // no forward call yet
+    DeviceGuard guard(plan->device);
+    if (cudaStreamSynchronize(plan->last_stream) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    const Workspace &w = plan->ws;
+    const size_t S = (size_t)plan->last_n * plan->cfg.top_k, E = plan->cfg.E;
+    struct Copy { void *dst; const void *src; size_t bytes; } copies[] = {
+        {topk_idx, w.topk_idx, S * 4}, {topk_w, w.topk_w, S * 4},
+        {counts, w.counts, E * 4},     {offsets, w.offsets, (E + 1) * 4},
+        {slot_token, w.slot_token, S * 4}, {slot_k, w.slot_k, S * 4},
+        {unique, w.unique, E * 4},     {U, w.U, 4},
+    };
+    for (const Copy &c : copies)
+        if (c.dst && cudaMemcpy(c.dst, c.src, c.bytes, cudaMemcpyDeviceToHost) != cudaSuccess) {
+            cudaGetLastError();
+            return MOE_ERR_CUDA;
+        }
+    return MOE_OK;
+}
+
+moe_status moe_plan_launch_count(const moe_plan *plan, uint64_t *count) {
+    if (!plan || !count) return MOE_ERR_INVALID_ARG;
+    *count = plan->launches;
+    return MOE_OK;
+}
+
+moe_status moe_plan_free(moe_plan *plan) {
+    if (!plan) return MOE_OK;
+    moe_status st = MOE_OK;
+    {
+        DeviceGuard guard(plan->device);
+        if (cudaStreamSynchronize(plan->last_stream) != cudaSuccess) {
+            cudaGetLastError();
+            st = MOE_ERR_CUDA;
+        }
+        if (cudaFree(plan->ws_base) != cudaSuccess) {
+            cudaGetLastError();
+            st = MOE_ERR_CUDA;
+        }
+    }
+    free(plan);
+    return st;
+}
+
+}  // extern "C"

@@ -1,0 +1,124 @@
+// route_kernels.cu -- stand-alone routing kernels (used by the f32 check path):
+// the router GEMV, and a single-CTA kernel for softmax / top-k / grouping.
+//
+// Router: logits[t, e] = sum_d x[t, d] * Wr[e, d] (+ bias[e]), f32 accumulate.
+// Source: mlxcel issue #1616 "perf(moe): batched decode scales 1.55x against
+// 3.25x on dense", Proposed Solution (the per-step split into router, expert
+// GEMV and combine) -- the page names the router as a stage; its formula (a
+// dense linear gate followed by softmax and a renormalised top-k) is the
+// plainest reading and is stated in the public header.
+#include <cuda_bf16.h>
+
+#include "moe_internal.h"
+#include "routing.cuh"
+
+namespace moe {
+namespace {
+
+template <int DT>
+__device__ __forceinline__ void load8(const void *p, size_t i, float (&v)[8]);
+
+template <>
+__device__ __forceinline__ void load8<MOE_DTYPE_F32>(const void *p, size_t i, float (&v)[8]) {
+    const float4 *q = reinterpret_cast<const float4 *>(static_cast<const float *>(p) + i);
+    float4 a = __ldg(q), b = __ldg(q + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+template <>
+__device__ __forceinline__ void load8<MOE_DTYPE_BF16>(const void *p, size_t i, float (&v)[8]) {
+    uint4 a = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p) + i));
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        v[2 * j] = __uint_as_float(w[j] << 16);
+        v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+}
+
+// one warp per (expert, token); grid (ceil(E / warps), n)
+template <int XT, int WT>
+__global__ void router_logits_kernel(const void *__restrict__ x, const void *__restrict__ w,
+                                     const float *__restrict__ bias, float *__restrict__ logits,
+                                     int E, int D) {
+    const int lane = threadIdx.x & 31;
+    const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int t = blockIdx.y;
+    if (e >= E) return;
+    float acc = 0.f;
+    for (int i = lane * 8; i < D; i += 256) {
+        float xv[8], wv[8];
+        load8<XT>(x, (size_t)t * D + i, xv);
+        load8<WT>(w, (size_t)e * D + i, wv);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc = fmaf(xv[j], wv[j], acc);
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) logits[(size_t)t * E + e] = acc + (bias ? bias[e] : 0.f);
+}
+
+// one CTA: softmax, top-k, renormalise, then group; writes the workspace
+__global__ void __launch_bounds__(1024) topk_group_kernel(Workspace ws, int n, int E, int k) {
+    __shared__ int s_idx[kMaxSlots];
+    __shared__ float s_w[kMaxSlots];
+    __shared__ unsigned long long s_mask[kMaxE];
+    __shared__ int s_counts[kMaxE];
+    __shared__ int s_off[kMaxE + 1];
+    __shared__ int s_st[kMaxSlots], s_sk[kMaxSlots], s_of[kMaxSlots];
+    __shared__ int s_unique[kMaxE];
+    __shared__ int s_U;
+    block_topk(ws.logits, n, E, k, s_idx, s_w);
+    __syncthreads();
+    block_group(s_idx, n, E, k, s_mask, s_counts, s_off, s_st, s_sk, s_of, s_unique, &s_U);
+    const int S = n * k;
+    for (int s = threadIdx.x; s < S; s += blockDim.x) {
+        ws.topk_idx[s] = s_idx[s];
+        ws.topk_w[s] = s_w[s];
+        ws.slot_token[s] = s_st[s];
+        ws.slot_k[s] = s_sk[s];
+        ws.slot_of[s] = s_of[s];
+    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        ws.counts[e] = s_counts[e];
+        ws.offsets[e] = s_off[e];
+        ws.unique[e] = e < s_U ? s_unique[e] : -1;
+    }
+    if (threadIdx.x == 0) {
+        ws.offsets[E] = s_off[E];
+        *ws.U = s_U;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_router_logits(const StepArgs &a, const Workspace &ws, cudaStream_t st,
+                                 int &launched) {
+    const int warps = 8;
+    dim3 grid((a.s.E + warps - 1) / warps, a.s.n);
+    dim3 block(32 * warps);
+    const bool xf = a.s.x_dtype == MOE_DTYPE_F32, wf = a.s.w_dtype == MOE_DTYPE_F32;
+    if (xf && wf)
+        router_logits_kernel<MOE_DTYPE_F32, MOE_DTYPE_F32><<<grid, block, 0, st>>>(
+            a.x, a.router_w, a.router_bias, ws.logits, a.s.E, a.s.D);
+    else if (xf)
+        router_logits_kernel<MOE_DTYPE_F32, MOE_DTYPE_BF16><<<grid, block, 0, st>>>(
+            a.x, a.router_w, a.router_bias, ws.logits, a.s.E, a.s.D);
+    else if (wf)
+        router_logits_kernel<MOE_DTYPE_BF16, MOE_DTYPE_F32><<<grid, block, 0, st>>>(
+            a.x, a.router_w, a.router_bias, ws.logits, a.s.E, a.s.D);
+    else
+        router_logits_kernel<MOE_DTYPE_BF16, MOE_DTYPE_BF16><<<grid, block, 0, st>>>(
+            a.x, a.router_w, a.router_bias, ws.logits, a.s.E, a.s.D);
+    launched += 1;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_topk_group(const StepArgs &a, const Workspace &ws, cudaStream_t st,
+                              int &launched) {
+    topk_group_kernel<<<1, 1024, 0, st>>>(ws, a.s.n, a.s.E, a.s.k);
+    launched += 1;
+    return cudaGetLastError();
+}
+
+}  // namespace moe

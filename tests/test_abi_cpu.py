@@ -1,0 +1,98 @@
+"""The C-ABI library builds, loads and exports what include/moe_decode.h
+declares; host-side argument checks (no CUDA work, no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import quantized_moe_decode_softmax_gb300 as q
+from quantized_moe_decode_softmax_gb300 import _abi
+from quantized_moe_decode_softmax_gb300 import build as qbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_decode.h")
+
+
+@pytest.fixture(scope="module")
+def libpath():
+    return qbuild.build()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(moe_\w+)\s*\(", text, re.M))
+
+
+def test_header_declares_the_bound_functions():
+    assert header_functions() == set(q.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(libpath):
+    L = ctypes.CDLL(libpath)
+    for name in header_functions():
+        assert hasattr(L, name), name
+
+
+def test_abi_version_and_status_strings(libpath):
+    assert q.moe_abi_version() == 1
+    assert q.moe_status_str(q.MOE_OK) == "MOE_OK"
+    assert q.moe_status_str(q.MOE_ERR_UNSUPPORTED) == "MOE_ERR_UNSUPPORTED"
+    assert q.moe_status_str(99) == "MOE_ERR_UNKNOWN"
+
+
+GOOD = dict(E=128, top_k=8, D=2048, Dff=768, max_tokens=64)
+
+
+@pytest.mark.parametrize("change,status", [
+    (dict(), q.MOE_OK),
+    (dict(bits=8), q.MOE_ERR_UNSUPPORTED),
+    (dict(group_size=32), q.MOE_ERR_UNSUPPORTED),
+    (dict(D=2047), q.MOE_ERR_UNSUPPORTED),
+    (dict(Dff=770), q.MOE_ERR_UNSUPPORTED),
+    (dict(Dff=8256), q.MOE_ERR_UNSUPPORTED),
+    (dict(E=2048), q.MOE_ERR_UNSUPPORTED),
+    (dict(E=64, top_k=17), q.MOE_ERR_UNSUPPORTED),
+    (dict(top_k=0), q.MOE_ERR_INVALID_ARG),
+    (dict(E=4, top_k=5), q.MOE_ERR_INVALID_ARG),
+    (dict(max_tokens=0), q.MOE_ERR_INVALID_ARG),
+    (dict(max_tokens=65), q.MOE_ERR_INVALID_ARG),
+    (dict(x_dtype=7), q.MOE_ERR_INVALID_ARG),
+    (dict(mma_min_tokens=-1), q.MOE_ERR_INVALID_ARG),
+])
+def test_config_validation(libpath, change, status):
+    args = dict(GOOD)
+    bits = change.pop("bits", 4) if "bits" in change else 4
+    gs = change.pop("group_size", 64) if "group_size" in change else 64
+    xd = change.pop("x_dtype", q.MOE_DTYPE_BF16) if "x_dtype" in change else q.MOE_DTYPE_BF16
+    mm = change.pop("mma_min_tokens", 0) if "mma_min_tokens" in change else 0
+    args.update(change)
+    cfg = q.make_config(args["E"], args["top_k"], args["D"], args["Dff"], args["max_tokens"],
+                        x_dtype=xd, router_dtype=q.MOE_DTYPE_BF16, out_dtype=q.MOE_DTYPE_BF16,
+                        mma_min_tokens=mm, bits=bits, group_size=gs)
+    n = ctypes.c_size_t(0)
+    st = q.lib().moe_plan_workspace_bytes(ctypes.byref(cfg), ctypes.byref(n))
+    assert st == status
+    if status == q.MOE_OK:
+        assert n.value > 64 * 8 * (768 + 2048) * 4  # at least h and y scratch
+
+
+def test_null_arguments_rejected_before_any_cuda_call(libpath):
+    L = q.lib()
+    planes = q.moe_expert_planes()
+    assert L.moe_decode_forward(None, None, None, None, ctypes.byref(planes), 1, 8, None, None) \
+        == q.MOE_ERR_INVALID_ARG
+    assert L.moe_plan_create(None, None) == q.MOE_ERR_INVALID_ARG
+    assert L.moe_plan_check(None) == q.MOE_ERR_INVALID_ARG
+    assert L.moe_get_routing(None, *([None] * 8)) == q.MOE_ERR_INVALID_ARG
+    assert L.moe_plan_free(None) == q.MOE_OK
+    cfg = q.make_config(**GOOD)
+    assert L.moe_plan_workspace_bytes(ctypes.byref(cfg), None) == q.MOE_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    monkeypatch.setattr(_abi, "LIB_PATH", os.path.join(ROOT, "does-not-exist.so"))
+    monkeypatch.setattr(_abi, "_lib", None)
+    with pytest.raises(RuntimeError, match="no fallback"):
+        _abi.lib()

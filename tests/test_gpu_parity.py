@@ -1,0 +1,156 @@
+"""GPU path (through the C ABI) against the CPU oracle, element by element.
+
+Routing and grouping must match bit for bit (inputs are drawn with top-k
+logit margins of at least 1e-2). Outputs must be within 2e-2 * RMS(out) on
+the default path and within 1e-4 * RMS(out) on the f32 check path.
+"""
+import numpy as np
+import pytest
+
+import moe_synth as ms
+from gpu_cases import (TOL_BF16, TOL_F32, assert_out_close, assert_routing_equal, case,
+                       device_layer, make_plan, run_gpu, run_oracle, x_tensor)
+
+pytestmark = pytest.mark.gpu
+
+F32_DEBUG = 1
+
+
+def _check(shape_name, seed, n, kind="independent", full=False, flags=0, out_dtype=None,
+           tol=None):
+    lay, x = case(shape_name, seed, n, kind, full=full)
+    shape = lay.shape
+    ref = run_oracle(lay, x)
+    plan = make_plan(shape, flags=flags, out_dtype=out_dtype)
+    out, routing = run_gpu(plan, device_layer(lay), shape, x)
+    assert_routing_equal(routing, ref)
+    if tol is None:
+        tol = TOL_F32 if flags & F32_DEBUG else TOL_BF16
+    return assert_out_close(out, ref["out"], tol)
+
+
+# ---- tiny layer (E=8, top-2, D=256, Dff=128, f32 activations) -------------------
+@pytest.mark.parametrize("flags", [0, F32_DEBUG])
+def test_tiny(flags):
+    _check("tiny", 0, 1, full=True, flags=flags)
+
+
+@pytest.mark.parametrize("n", [2, 3, 5, 8])
+def test_tiny_cohorts(n):
+    _check("tiny", 0, n, full=True, flags=F32_DEBUG)
+    _check("tiny", 0, n, full=True)
+
+
+# ---- 128-expert top-8 layer (D=2048, Dff=768) -------------------------------------
+def test_qwen3_n1_full_layer():
+    _check("qwen3", 1, 1, full=True)
+
+
+def test_qwen3_n1_f32_check_path():
+    _check("qwen3", 1, 1, full=True, flags=F32_DEBUG, out_dtype="f32")
+
+
+@pytest.mark.parametrize("n", [2, 4, 8])
+@pytest.mark.parametrize("kind", ["independent", "shared", "disjoint"])
+def test_qwen3_ladder(n, kind):
+    _check("qwen3", 2, n, kind)
+
+
+@pytest.mark.parametrize("n", [16, 64])
+def test_qwen3_large_cohorts(n):
+    _check("qwen3", 2, n)
+
+
+def test_qwen3_shared_64_tokens_single_expert_set():
+    # every token routes to the same 8 experts: per-expert count 64
+    _check("qwen3", 2, 64, "shared")
+
+
+# ---- 256-expert top-6 layer (D=4096, Dff=2048, Zipf router bias) ------------------
+@pytest.mark.parametrize("n", [1, 4, 16])
+def test_e256(n):
+    _check("e256", 3, n)
+
+
+def test_e256_f32_check_path():
+    _check("e256", 3, 4, flags=F32_DEBUG, out_dtype="f32")
+
+
+# ---- properties --------------------------------------------------------------------
+def test_deterministic_and_identical_tokens():
+    import torch
+    lay, x = case("qwen3", 2, 4)
+    x = np.repeat(x[1:2], 4, axis=0)  # four identical tokens
+    shape = lay.shape
+    lay = ms.make_layer(shape, 2, 0, ms.routed_experts(x, lay.router_w, None, shape.top_k))
+    dl = device_layer(lay)
+    plan = make_plan(shape)
+    xt = x_tensor(shape, x)
+    outs = []
+    for _ in range(10):
+        outs.append(plan.forward(xt, dl).clone())
+    torch.cuda.synchronize()
+    ref = outs[0].view(torch.int16)
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), ref), "run-to-run bits differ"
+    for t in range(1, 4):
+        assert torch.equal(outs[0][t].view(torch.int16), outs[0][0].view(torch.int16))
+
+
+def test_cohort_size_changes_between_calls():
+    """One plan, n varying call to call (no re-specialisation per n)."""
+    lay, x = case("qwen3", 2, 8)
+    shape = lay.shape
+    dl = device_layer(lay)
+    plan = make_plan(shape)
+    for n in (3, 1, 8, 5):
+        ref = run_oracle(lay, x[:n])
+        out, routing = run_gpu(plan, dl, shape, x[:n])
+        assert_routing_equal(routing, ref)
+        assert_out_close(out, ref["out"], TOL_BF16)
+
+
+def test_host_entry_point_matches_device_entry_point():
+    import torch
+    lay, x = case("qwen3", 2, 4)
+    shape = lay.shape
+    dl = device_layer(lay)
+    plan = make_plan(shape)
+    xt = x_tensor(shape, x)
+    dev = plan.forward(xt, dl)
+    torch.cuda.synchronize()
+    x_host = xt.cpu().pin_memory()
+    out_host = torch.empty((4, shape.D), dtype=torch.bfloat16).pin_memory()
+    plan.forward_host(x_host, dl, out_host)
+    assert torch.equal(out_host.view(torch.int16), dev.cpu().view(torch.int16))
+
+
+def test_zero_input():
+    import torch
+    lay, _ = case("qwen3", 2, 2)
+    shape = lay.shape
+    x = np.zeros((2, shape.D), np.float32)
+    lay = ms.make_layer(shape, 2, 0, range(shape.top_k))
+    ref = run_oracle(lay, x)
+    plan = make_plan(shape)
+    out, routing = run_gpu(plan, device_layer(lay), shape, x)
+    assert np.array_equal(routing["topk_idx"], np.tile(np.arange(shape.top_k), (2, 1)))
+    assert np.all(out == 0.0) and np.all(ref["out"] == 0.0)
+
+
+def test_runtime_argument_errors_launch_nothing():
+    import torch
+    import quantized_moe_decode_softmax_gb300 as q
+    lay, x = case("tiny", 0, 1, full=True)
+    shape = lay.shape
+    dl = device_layer(lay)
+    plan = make_plan(shape, max_tokens=4)
+    xt = x_tensor(shape, np.zeros((8, shape.D), np.float32))
+    out = torch.empty((8, shape.D), device="cuda")
+    for n, k in ((0, 2), (5, 2), (1, 3)):
+        with pytest.raises(q.MoeError) as ei:
+            q.moe_decode_forward(plan.plan, xt, dl.router_w, None, dl.c_planes, n, k, out)
+        assert ei.value.status == q.MOE_ERR_INVALID_ARG
+    with pytest.raises(q.MoeError):
+        q.moe_decode_forward(plan.plan, xt, dl.router_w, None, dl.c_planes, 1, 2, xt)  # out aliases x
+    plan.check()
