@@ -55,6 +55,10 @@ def parse_args():
                     help="CPU work of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--phases", action="store_true",
+                    help="also time the fused kernel's phases (router / gate-up / down)")
+    ap.add_argument("--sustain-seconds", type=float, default=1.5,
+                    help="graph replays before the timed one, while clocks are sampled")
     return ap.parse_args()
 
 
@@ -306,7 +310,7 @@ def run_ours(args, world, rank, local, pg):
         stream.synchronize()
         if sampler:
             sampler.start()
-        t_end = time.perf_counter() + 1.5
+        t_end = time.perf_counter() + args.sustain_seconds
         while time.perf_counter() < t_end:
             graph.replay()
             stream.synchronize()
@@ -359,6 +363,10 @@ def run_ours(args, world, rank, local, pg):
     achieved = bytes_per_step / t_kernel / 1e9
     value = world * n * K / (elapsed_ms / 1000.0)
 
+    phases = None
+    if args.phases:
+        phases = phase_split(q, shape, args, xs, reps, dev, n)
+
     if rank == 0:
         cb = None
         if not args.no_cpu_baseline:
@@ -388,8 +396,35 @@ def run_ours(args, world, rank, local, pg):
             "clocks": clocks,
             "cpu_baseline": cb,
         }
+        if phases is not None:
+            line["phases_us"] = phases
         print(json.dumps(line), flush=True)
     layer.close()
+
+
+def phase_split(q, shape, args, xs, reps, dev, n, steps=50):
+    """Median over steps of the fused kernel's phase durations (us), each phase
+    taken as the latest CTA's timestamp minus the earliest start."""
+    import numpy as np
+    import torch
+    lay = q.MoeDecodeLayer(shape.E, shape.top_k, shape.D, shape.F, max_tokens=max(n, 1),
+                           act_dtype=shape.act_dtype, flags=q.MOE_FLAG_PHASE_TIMES)
+    out = torch.empty((n, shape.D), dtype=xs[0].dtype, device=dev)
+    per, cnt = [], []
+    for i in range(steps):
+        lay.forward(xs[i % len(xs)], reps[(i * 7) % len(reps)], out)
+        t = q.moe_get_phase_times(lay.plan)
+        t0 = t[:, 0].min()
+        per.append((t[:, :8] - t0).max(axis=0) / 1000.0)
+        cnt.append(np.concatenate([t[:, 8:13].mean(axis=0) / 1000.0, t[:, 13:15].mean(axis=0)]))
+    lay.close()
+    med = np.median(np.array(per), axis=0)
+    cm = np.median(np.array(cnt), axis=0)
+    names = q.PHASES
+    res = {f"{names[i]}_end": round(float(med[i]), 3) for i in range(1, 8)}
+    for j, nm in enumerate(names[8:15]):
+        res[nm] = round(float(cm[j]), 3)
+    return res
 
 
 def main():

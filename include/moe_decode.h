@@ -74,7 +74,14 @@ enum {
      * f32 accumulation throughout. Slower; used to check numerics. */
     MOE_FLAG_F32_DEBUG = 1u << 0,
     /* print the chosen path of each forward call to stderr */
-    MOE_FLAG_TRACE = 1u << 1
+    MOE_FLAG_TRACE = 1u << 1,
+    /* record per-CTA timestamps of the fused kernel's phases (see
+     * moe_get_phase_times); costs a few global stores per CTA */
+    MOE_FLAG_PHASE_TIMES = 1u << 2,
+    /* TEST ONLY: in the fused path, CTA 0 skips the first grid barrier, so
+     * every other CTA's bounded wait runs out (about 1 s) and the step ends
+     * with MOE_ERR_TIMEOUT reported by moe_plan_check. Output is garbage. */
+    MOE_FLAG_TEST_STALL = 1u << 8
 };
 
 typedef struct {
@@ -166,6 +173,17 @@ moe_status moe_plan_check(moe_plan *plan);
 moe_status moe_get_routing(moe_plan *plan, int32_t *topk_idx, float *topk_w,
                            int32_t *counts, int32_t *offsets, int32_t *slot_token,
                            int32_t *slot_k, int32_t *unique, int32_t *U);
+
+/* Phase timestamps (ns, %globaltimer) of the last fused step of a plan created
+ * with MOE_FLAG_PHASE_TIMES: for each CTA c, times[c*16 + i] with
+ *   i = 0 start, 1 router done, 2 after grid barrier 1, 3 routing and work
+ *   lists done, 4 gate/up done, 5 after grid barrier 2, 6 down done, 7 end;
+ *   8/9 gate/up ns spent waiting for data / computing (consumer warp 0),
+ *   10/11 the same for the down projection, 12 producer ns waiting for free
+ *   ring slots, 13 gate/up chunks, 14 down tiles of the CTA.
+ * Copies min(max_entries, ctas*16) entries to HOST memory, sets *ctas to the
+ * kernel's CTA count, and synchronises the plan's last stream. */
+moe_status moe_get_phase_times(moe_plan *plan, uint64_t *times, int max_entries, int *ctas);
 
 /* Number of CUDA kernels this plan has enqueued since creation (host
  * counter; forward calls captured into a CUDA graph count once, at capture). */

@@ -17,9 +17,12 @@ from ._abi import (  # noqa: F401
     MOE_ERR_TIMEOUT,
     MOE_ERR_UNSUPPORTED,
     MOE_FLAG_F32_DEBUG,
+    MOE_FLAG_PHASE_TIMES,
+    MOE_FLAG_TEST_STALL,
     MOE_FLAG_TRACE,
     MOE_OK,
     PLANE_FIELDS,
+    PHASES,
     MoeError,
     lib,
     make_config,
@@ -29,6 +32,7 @@ from ._abi import (  # noqa: F401
     moe_decode_forward,
     moe_decode_forward_host,
     moe_expert_planes,
+    moe_get_phase_times,
     moe_get_routing,
     moe_plan_check,
     moe_plan_create,

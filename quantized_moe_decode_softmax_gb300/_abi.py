@@ -20,11 +20,13 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_OOM, MOE
 MOE_DTYPE_F32, MOE_DTYPE_BF16 = 0, 1
 MOE_FLAG_F32_DEBUG = 1 << 0
 MOE_FLAG_TRACE = 1 << 1
+MOE_FLAG_PHASE_TIMES = 1 << 2
+MOE_FLAG_TEST_STALL = 1 << 8
 
 EXPORTED = (
     "moe_abi_version", "moe_status_str", "moe_plan_workspace_bytes", "moe_plan_create",
     "moe_decode_forward", "moe_decode_forward_host", "moe_plan_check", "moe_get_routing",
-    "moe_plan_launch_count", "moe_plan_free",
+    "moe_get_phase_times", "moe_plan_launch_count", "moe_plan_free",
 )
 
 
@@ -72,10 +74,11 @@ def lib():
         L.moe_plan_check.argtypes = [vp]
         L.moe_get_routing.argtypes = [vp] + [vp] * 8
         L.moe_plan_launch_count.argtypes = [vp, P(ctypes.c_uint64)]
+        L.moe_get_phase_times.argtypes = [vp, vp, i32, P(i32)]
         L.moe_plan_free.argtypes = [vp]
         for name in ("moe_plan_workspace_bytes", "moe_plan_create", "moe_decode_forward",
                      "moe_decode_forward_host", "moe_plan_check", "moe_get_routing", "moe_plan_launch_count",
-                     "moe_plan_free"):
+                     "moe_get_phase_times", "moe_plan_free"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -184,6 +187,20 @@ def moe_plan_launch_count(plan: int) -> int:
     c = ctypes.c_uint64(0)
     _check(lib().moe_plan_launch_count(plan, ctypes.byref(c)), "moe_plan_launch_count")
     return c.value
+
+
+PHASES = ("start", "router", "barrier1", "routing", "gate_up", "barrier2", "down", "end",
+          "a_wait", "a_compute", "b_wait", "b_compute", "producer_wait", "a_chunks", "b_tiles",
+          "reserved")
+
+
+def moe_get_phase_times(plan: int) -> np.ndarray:
+    """[ctas, 16] int64 of the plan's last fused step (see PHASES and the header)."""
+    buf = np.zeros(16 * 1024, np.uint64)
+    ctas = ctypes.c_int(0)
+    _check(lib().moe_get_phase_times(plan, buf.ctypes.data, buf.size, ctypes.byref(ctas)),
+           "moe_get_phase_times")
+    return buf[: 16 * ctas.value].reshape(ctas.value, 16).astype(np.int64)
 
 
 def moe_plan_free(plan: int) -> None:

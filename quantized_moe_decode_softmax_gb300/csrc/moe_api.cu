@@ -35,6 +35,9 @@ moe_status validate_config(const moe_config *c) {
     if (c->mma_min_tokens < 0) return MOE_ERR_INVALID_ARG;
     if (c->E > kMaxE || c->top_k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
     if (c->D % kGroup || c->Dff % kGroup) return MOE_ERR_UNSUPPORTED;
+    if (c->flags & ~(unsigned)(MOE_FLAG_F32_DEBUG | MOE_FLAG_TRACE | MOE_FLAG_PHASE_TIMES |
+                               MOE_FLAG_TEST_STALL))
+        return MOE_ERR_INVALID_ARG;
     if (c->Dff > kMaxDff || c->D > kMaxD) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
 }
@@ -60,11 +63,14 @@ size_t carve(const moe_config &c, char *base, Workspace *ws) {
     w.slot_of = (int *)take(S * 4);
     w.unique = (int *)take(E * 4);
     w.U = (int *)take(4);
-    w.h = (float *)take(S * F * 4);
+    // f32 h of the check path, or the fused path's bf16 h blocks:
+    // ceil(F / 256) K-slices x S slots x 512 bytes
+    const size_t h_blocks = ((F / 64 + 3) / 4) * S * 512;
+    w.h = (float *)take(S * F * 4 > h_blocks ? S * F * 4 : h_blocks);
     w.y = (float *)take(S * D * 4);
     w.status = (unsigned *)take(4 * 4);
     w.sync = (unsigned *)take(64 * 4);
-    w.phase_ns = (unsigned long long *)take(256 * 8);
+    w.phase_ns = (unsigned long long *)take(16 * 1024 * 8);
     w.x_stage = take(n * D * elem_size(c.x_dtype));
     w.out_stage = take(n * D * elem_size(c.out_dtype));
     if (ws) *ws = w;
@@ -153,6 +159,23 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan **out) {
         return err == cudaErrorMemoryAllocation ? MOE_ERR_OOM : MOE_ERR_CUDA;
     }
     carve(*cfg, (char *)p->ws_base, &p->ws);
+    p->fused_ok = false;
+    if (!(cfg->flags & MOE_FLAG_F32_DEBUG)) {
+        int max_smem = 0, per_sm = 0;
+        cudaError_t e2 = cudaSuccess;
+        if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device) ==
+                cudaSuccess &&
+            fused_layout(*cfg, p->num_sms, max_smem, &p->fused)) {
+            e2 = fused_prepare(p->fused, &per_sm);
+            // the cooperative launch needs every CTA resident at once
+            p->fused_ok = e2 == cudaSuccess && per_sm >= 1;
+        }
+        if (trace_enabled(p))
+            fprintf(stderr, "[moe] plan: fused=%d smem=%d slots=%d slot_bytes=%d ctas/sm=%d (%s)\n",
+                    (int)p->fused_ok, p->fused.smem_bytes, p->fused.NS, p->fused.slot_bytes, per_sm,
+                    cudaGetErrorString(e2));
+        cudaGetLastError();
+    }
     if (cudaMemset(p->ws_base, 0, p->ws_bytes) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
         cudaGetLastError();
@@ -181,24 +204,36 @@ moe_status moe_decode_forward(moe_plan *plan, const void *x, const void *router_
     cudaStream_t s = (cudaStream_t)stream;
     StepArgs a{};
     a.s = Shape{plan->cfg.E, plan->cfg.top_k, plan->cfg.D, plan->cfg.Dff, n_tokens,
-                plan->cfg.x_dtype, plan->cfg.router_dtype, plan->cfg.out_dtype};
+                plan->cfg.x_dtype, plan->cfg.router_dtype, plan->cfg.out_dtype,
+                plan->cfg.flags};
     a.x = x;
     a.router_w = router_w;
     a.router_bias = router_bias;
     a.planes = *planes;
     a.out = out;
 
+    const bool fused = plan->fused_ok && n_tokens <= fused_max_tokens();
     if (trace_enabled(plan))
         fprintf(stderr, "[moe] forward n=%d E=%d k=%d D=%d Dff=%d path=%s\n", n_tokens,
-                a.s.E, a.s.k, a.s.D, a.s.F, "f32-check");
+                a.s.E, a.s.k, a.s.D, a.s.F, fused ? "fused" : "f32-check");
     int launched = 0;
-    cudaError_t err = launch_router_logits(a, plan->ws, s, launched);
-    if (err == cudaSuccess) err = launch_topk_group(a, plan->ws, s, launched);
-    if (err == cudaSuccess) err = launch_experts_f32(a, plan->ws, s, launched);
+    cudaError_t err;
+    if (fused) {
+        err = launch_fused(a, plan->ws, plan->fused, s, launched);
+    } else {
+        err = launch_router_logits(a, plan->ws, s, launched);
+        if (err == cudaSuccess) err = launch_topk_group(a, plan->ws, s, launched);
+        if (err == cudaSuccess) err = launch_experts_f32(a, plan->ws, s, launched);
+    }
     plan->launches += launched;
     plan->last_stream = s;
     plan->last_n = n_tokens;
-    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    if (err != cudaSuccess) {
+        fprintf(stderr, "[moe] forward launch failed (%s path): %s\n", fused ? "fused" : "f32-check",
+                cudaGetErrorString(err));
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
     return MOE_OK;
 }
 
@@ -239,8 +274,11 @@ moe_status moe_plan_check(moe_plan *plan) {
         return MOE_ERR_CUDA;
     }
     if (status) {
-        unsigned zero = 0;
-        cudaMemcpy(plan->ws.status, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        // clear the status word and the grid-barrier counters a timed-out
+        // step may have left mid-way
+        cudaMemset(plan->ws.status, 0, 4 * sizeof(unsigned));
+        cudaMemset(plan->ws.sync, 0, 64 * sizeof(unsigned));
+        cudaDeviceSynchronize();
         return (status & kDevErrTimeout) ? MOE_ERR_TIMEOUT : MOE_ERR_CUDA;
     }
     return MOE_OK;
@@ -269,6 +307,24 @@ moe_status moe_get_routing(moe_plan *plan, int32_t *topk_idx, float *topk_w, int
             cudaGetLastError();
             return MOE_ERR_CUDA;
         }
+    return MOE_OK;
+}
+
+moe_status moe_get_phase_times(moe_plan *plan, uint64_t *times, int max_entries, int *ctas) {
+    if (!plan || !times || max_entries < 0 || !ctas) return MOE_ERR_INVALID_ARG;
+    if (!plan->fused_ok) return MOE_ERR_UNSUPPORTED;
+    DeviceGuard guard(plan->device);
+    if (cudaStreamSynchronize(plan->last_stream) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    *ctas = plan->fused.G;
+    size_t count = (size_t)plan->fused.G * 16;
+    if ((size_t)max_entries < count) count = (size_t)max_entries;
+    if (count && cudaMemcpy(times, plan->ws.phase_ns, count * 8, cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
     return MOE_OK;
 }
 

@@ -47,6 +47,7 @@ struct Workspace {
 struct Shape {
     int E, k, D, F, n;
     int x_dtype, w_dtype, out_dtype;
+    unsigned flags;  // MOE_FLAG_* of the plan
 };
 
 // Arguments of one step, device pointers.
@@ -57,6 +58,23 @@ struct StepArgs {
     const float *router_bias;
     moe_expert_planes planes;
     void *out;
+};
+
+// Shared-memory and work layout of the fused kernel (computed on the host).
+struct FusedLayout {
+    int G;            // CTAs (one per SM)
+    int NS;           // ring slots
+    int slot_bytes;   // bytes per ring slot
+    int nksA;         // gate/up K-slices (8 groups each) per 16-row tile
+    int nksB;         // down K-slices (4 groups each) per 16-row tile
+    int SA;           // gate/up row stride in a slot (bytes, padded)
+    int SB;           // down row stride in a slot (bytes, padded)
+    int hoff;         // offset of the h block area inside a down slot
+    int x_tokens;     // tokens the staged-activation area holds
+    int x_stride;     // bytes per token row of the staged activations
+    int part_bytes;   // gate/up partial-sum buffers (also the final reduction)
+    int off_bar, off_route, off_tiles, off_x, off_xsum, off_part, off_sbuf, off_ring;
+    int smem_bytes;
 };
 
 }  // namespace moe
@@ -72,6 +90,8 @@ struct moe_plan {
     int last_n;
     int mma_min_tokens;
     unsigned long long launches;  // kernels enqueued by this plan since creation
+    bool fused_ok;                // the fused kernel can run this shape
+    moe::FusedLayout fused;
 };
 
 namespace moe {
@@ -86,5 +106,12 @@ cudaError_t launch_topk_group(const StepArgs &a, const Workspace &ws, cudaStream
 // exact f32 expert path (expert_f32_kernels.cu)
 cudaError_t launch_experts_f32(const StepArgs &a, const Workspace &ws, cudaStream_t st,
                                int &launched);
+
+// fused single-launch path (fused_step.cu)
+bool fused_layout(const moe_config &c, int num_sms, int max_smem, FusedLayout *out);
+cudaError_t fused_prepare(const FusedLayout &L, int *blocks_per_sm);
+int fused_max_tokens();
+cudaError_t launch_fused(const StepArgs &a, const Workspace &ws, const FusedLayout &L,
+                         cudaStream_t st, int &launched);
 
 }  // namespace moe

@@ -53,9 +53,60 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Softmax + top-k + renormalisation of one token's logits held in registers:
+// lane l holds experts l + 32*i for i < NPL (entries past E are -inf).
+template <int NPL>
+__device__ __forceinline__ void warp_topk_token(const float *lt, int E, int k, int lane,
+                                                int *idx_out, float *w_out) {
+    float v[NPL];
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+        const int e = lane + 32 * i;
+        const float x = e < E ? __ldcg(lt + e) : -INFINITY;
+        v[i] = x == x ? x : -INFINITY;  // NaN ranks as -inf
+    }
+    float m = v[0];
+#pragma unroll
+    for (int i = 1; i < NPL; ++i) m = fmaxf(m, v[i]);
+    m = warp_max(m);
+    float z = 0.f;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i)
+        if (lane + 32 * i < E) z += expf(v[i] - m);
+    z = warp_sum(z);
+    // lane-local best of the untaken entries, refreshed only on the lane that
+    // loses its best to the warp-wide winner
+    ValIdx lb{-INFINITY, 0x7fffffff};
+#pragma unroll
+    for (int i = 0; i < NPL; ++i)
+        if (lane + 32 * i < E) lb = vi_better(lb, ValIdx{v[i], lane + 32 * i});
+    uint32_t taken = 0;
+    float psum = 0.f;
+    for (int j = 0; j < k; ++j) {
+        const ValIdx best = warp_argmax(lb);
+        if (lane == 0) {
+            const float p = expf(best.v - m) / z;
+            idx_out[j] = best.i;
+            w_out[j] = p;  // renormalised below
+            psum += p;
+        }
+        if ((best.i & 31) == lane) {
+            taken |= 1u << (best.i >> 5);
+            lb = ValIdx{-INFINITY, 0x7fffffff};
+#pragma unroll
+            for (int i = 0; i < NPL; ++i)
+                if (lane + 32 * i < E && !(taken & (1u << i)))
+                    lb = vi_better(lb, ValIdx{v[i], lane + 32 * i});
+        }
+    }
+    if (lane == 0)
+        for (int j = 0; j < k; ++j) w_out[j] = w_out[j] / psum;
+}
+
 // Softmax + top-k + renormalisation for tokens t = warp, warp + nwarps, ...
-// logits: [n, E] (global or shared). Writes s_idx / s_w [n*k] (shared).
-// Requires E <= 1024 (32 entries per lane) and k <= 16.
+// logits: [n, E] in global memory, read once through L2 (they may have been
+// written by other CTAs of the same kernel). Writes s_idx / s_w [n*k]
+// (shared). Requires E <= 1024 and k <= 16.
 __device__ inline void block_topk(const float *logits, int n, int E, int k, int *s_idx,
                                   float *s_w) {
     const int lane = threadIdx.x & 31;
@@ -63,49 +114,14 @@ __device__ inline void block_topk(const float *logits, int n, int E, int k, int 
     const int nwarps = blockDim.x >> 5;
     for (int t = warp; t < n; t += nwarps) {
         const float *lt = logits + (size_t)t * E;
-        float m = -INFINITY;
-        for (int e = lane; e < E; e += 32) m = fmaxf(m, lt[e]);
-        m = warp_max(m);
-        float z = 0.f;
-        for (int e = lane; e < E; e += 32) z += expf(lt[e] - m);
-        z = warp_sum(z);
-
-        uint32_t taken = 0;  // bit i: entry e = lane + 32*i already selected
-        float sel_v[16];
-        int sel_e[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            sel_v[j] = 0.f;
-            sel_e[j] = 0;
-            if (j < k) {
-                ValIdx best{-INFINITY, 0x7fffffff};
-                for (int i = 0, e = lane; e < E; ++i, e += 32) {
-                    if (taken & (1u << i)) continue;
-                    ValIdx c{lt[e], e};
-                    best = vi_better(best, c);
-                }
-                best = warp_argmax(best);
-                if ((best.i & 31) == lane) taken |= 1u << (best.i >> 5);
-                sel_v[j] = best.v;
-                sel_e[j] = best.i;
-            }
-        }
-        if (lane == 0) {
-            float p[16];
-            float psum = 0.f;
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-                if (j < k) {
-                    p[j] = expf(sel_v[j] - m) / z;
-                    psum += p[j];
-                }
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-                if (j < k) {
-                    s_idx[t * k + j] = sel_e[j];
-                    s_w[t * k + j] = p[j] / psum;
-                }
-        }
+        int *io = s_idx + t * k;
+        float *wo = s_w + t * k;
+        if (E <= 32) warp_topk_token<1>(lt, E, k, lane, io, wo);
+        else if (E <= 64) warp_topk_token<2>(lt, E, k, lane, io, wo);
+        else if (E <= 128) warp_topk_token<4>(lt, E, k, lane, io, wo);
+        else if (E <= 256) warp_topk_token<8>(lt, E, k, lane, io, wo);
+        else if (E <= 512) warp_topk_token<16>(lt, E, k, lane, io, wo);
+        else warp_topk_token<32>(lt, E, k, lane, io, wo);
     }
 }
 
@@ -120,8 +136,10 @@ __device__ inline void block_group(const int *s_idx, int n, int E, int k,
     const int S = n * k;
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_mask[e] = 0ull;
     __syncthreads();
-    for (int s = threadIdx.x; s < S; s += blockDim.x)
-        atomicOr(&s_mask[s_idx[s]], 1ull << (s / k));
+    for (int s = threadIdx.x; s < S; s += blockDim.x) {
+        const int e = s_idx[s];
+        if ((unsigned)e < (unsigned)E) atomicOr(&s_mask[e], 1ull << (s / k));
+    }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = __popcll(s_mask[e]);
     __syncthreads();
@@ -157,6 +175,7 @@ __device__ inline void block_group(const int *s_idx, int n, int E, int k,
     __syncthreads();
     for (int s = threadIdx.x; s < S; s += blockDim.x) {
         const int e = s_idx[s];
+        if ((unsigned)e >= (unsigned)E) continue;
         const int t = s / k;
         const unsigned long long below = (t == 0) ? 0ull : (s_mask[e] & ((1ull << t) - 1ull));
         const int pos = offsets[e] + __popcll(below);

@@ -38,7 +38,8 @@ def case(shape_name: str, seed: int, n: int, kind: str = "independent", cohort: 
         lay = full_layer(shape_name, seed)
         x = ms.draw_tokens(shape, lay.router_w, lay.router_bias, seed, 0, n, kind, cohort)
         return lay, x
-    return ms.make_case(shape_name, seed, n, kind, cohort=cohort, lazy=True, workers=1)
+    return ms.make_case(shape_name, seed, n, kind, cohort=cohort, lazy=True,
+                        workers=WORKERS if n * ms.SHAPES[shape_name].top_k > 16 else 1)
 
 
 def device_layer(lay):

@@ -1,0 +1,74 @@
+"""Which path runs, and the device-side timeout (GPU)."""
+import time
+
+import numpy as np
+import pytest
+
+import quantized_moe_decode_softmax_gb300 as q
+from gpu_cases import (TOL_BF16, assert_out_close, assert_routing_equal, case, device_layer,
+                       make_plan, run_gpu, run_oracle, x_tensor)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("n,launches", [(1, 1), (4, 1), (8, 1), (9, 5)])
+def test_launches_per_step(n, launches):
+    """Cohorts of up to 8 tokens run as one fused launch; larger cohorts take
+    the multi-kernel path."""
+    import torch
+    lay, x = case("qwen3", 2, n)
+    shape = lay.shape
+    dl = device_layer(lay)
+    plan = make_plan(shape)
+    c0 = q.moe_plan_launch_count(plan.plan)
+    plan.forward(x_tensor(shape, x), dl)
+    torch.cuda.synchronize()
+    assert q.moe_plan_launch_count(plan.plan) - c0 == launches
+
+
+def test_fused_matches_f32_check_path():
+    """The fused path and the f32 check path agree on one cohort."""
+    lay, x = case("qwen3", 2, 6)
+    shape = lay.shape
+    dl = device_layer(lay)
+    fast, r_fast = run_gpu(make_plan(shape, out_dtype="f32"), dl, shape, x)
+    slow, r_slow = run_gpu(make_plan(shape, flags=q.MOE_FLAG_F32_DEBUG, out_dtype="f32"), dl, shape, x)
+    assert_routing_equal(r_fast, r_slow)
+    assert_out_close(fast, slow, TOL_BF16)
+
+
+def test_device_wait_times_out_and_context_stays_usable():
+    """A grid barrier that one CTA never reaches: the other CTAs' bounded waits
+    give up, the host reads MOE_ERR_TIMEOUT, and the next step is correct."""
+    import torch
+    lay, x = case("qwen3", 2, 2)
+    shape = lay.shape
+    dl = device_layer(lay)
+    plan = make_plan(shape, flags=q.MOE_FLAG_TEST_STALL)
+    t0 = time.time()
+    plan.forward(x_tensor(shape, x), dl)
+    with pytest.raises(q.MoeError) as ei:
+        plan.check()
+    assert ei.value.status == q.MOE_ERR_TIMEOUT
+    assert time.time() - t0 < 30
+    # same device, a normal plan: correct results
+    ref = run_oracle(lay, x)
+    out, routing = run_gpu(make_plan(shape), dl, shape, x)
+    assert_routing_equal(routing, ref)
+    assert_out_close(out, ref["out"], TOL_BF16)
+    torch.cuda.synchronize()
+
+
+def test_phase_times_are_ordered():
+    """Per-CTA timestamps of the fused step's phases are non-decreasing."""
+    import torch
+    lay, x = case("qwen3", 2, 4)
+    shape = lay.shape
+    dl = device_layer(lay)
+    plan = make_plan(shape, flags=q.MOE_FLAG_PHASE_TIMES)
+    plan.forward(x_tensor(shape, x), dl)
+    torch.cuda.synchronize()
+    t = q.moe_get_phase_times(plan.plan)
+    assert t.shape[0] >= 1 and t.shape[1] == 16
+    assert np.all(np.diff(t[:, :8], axis=1) >= 0)
+    assert np.all(t[:, 0] > 0)
