@@ -1,0 +1,1141 @@
+// decode_step.cu -- the decode step for cohorts of up to 8 tokens as one
+// persistent kernel (one CTA per SM, cooperative launch).
+//
+// Phases inside one launch:
+//   R  router GEMV: logits[t, e] = x[t] . Wr[e] (+ bias). Each CTA owns at most
+//      two experts (e = cta, cta + G). Every CTA also stages x in shared memory
+//      as bf16 in the B-operand order of the tensor-core MMA, with per-group
+//      sums of x.                                            -> grid barrier 1
+//   T  every CTA reads the logits and computes softmax, top-k, renormalised
+//      weights and the grouping by expert itself (the same deterministic result
+//      in every CTA, so there is no second exchange).
+//   A  gate/up: the U * Dff (gate row, up row) pairs of the selected experts are
+//      split evenly over the CTAs; each CTA cuts its share into 16-row tiles.
+//      A producer warp streams each tile with two 3-D TMA copies (gate and up
+//      codes, 128-byte swizzle) and cp.async copies of the tile's scales and
+//      biases into a shared-memory ring. All 16 consumer warps work on every
+//      stage, each on its own share of the K (input) groups, running m16n8k16
+//      MMAs on the raw 4-bit codes; the last warp to finish a tile sums the 16
+//      partials in warp order and writes w * silu(g) * u as bf16 to global
+//      memory, one row per (token, expert) slot.            -> grid barrier 2
+//   B  down + combine: each CTA owns a slice of the D output rows for every
+//      selected expert. The down codes stream into the same ring (issued as soon
+//      as ring stages free up, before barrier 2); because the routing weight is
+//      folded into h, every warp accumulates its share of sum_e Wd[e] h_e and one
+//      fixed-order sum over warps gives the output with one final rounding.
+//
+// Sources (mlxcel GitHub issues):
+//   #1616 "perf(moe): batched decode scales 1.55x against 3.25x on dense":
+//     Proposed Solution - a token dimension for the fused decode kernel and one
+//     read of each selected expert plane per step (de-duplication across the
+//     cohort); Implementation Notes - f32 partials with a single final rounding,
+//     n_tokens as a runtime extent.
+//   #1859 "perf(moe): attribute the MoE decode gap at the M = 1 expert gather",
+//     Problem / Background - the per-(token, k) gather this replaces.
+//
+// Numerics. Codes enter the MMA as exact bf16 integers 128 + q (a magic-exponent
+// bit trick, two codes per logic op); products and sums are f32. Per group of 64
+// inputs, acc = sum (128 + q) v, and the row's contribution is
+// s * acc + (b - 128 s) * sum(v). For gate/up, sum(v) is the staged group sum of
+// x. For down, tile row 15 is fed zero codes, so its MMA row returns 128 * sum(h)
+// for free. Activations enter the MMA as bf16 (x, and w * silu(g) * u), so this
+// path is held to the bf16 tolerance; the f32 check path keeps every product in
+// f32. Every reduction has a fixed order: results are bitwise reproducible.
+//
+// MMA row mapping. Lane (g, c) of a warp holds MMA rows g and g + 8; they map to
+// tile rows 2g and 2g + 1, so the eight rows a warp reads at once sit in eight
+// different 16-byte columns of the 128-byte swizzle and the reads are free of
+// bank conflicts.
+//
+// Every wait is bounded (globaltimer, 1 s). A timeout sets a status bit and an
+// abort flag; the CTA then skips the remaining waits, still passes every barrier
+// it shares with its own threads, lets its copies in flight land and exits.
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include "moe_internal.h"
+#include "ptx.cuh"
+#include "routing.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kCW = 16;                      // warps per CTA (all consume; refills are issued
+                                             // by the last warp to release a ring stage)
+constexpr int kThreads = kCW * 32;
+constexpr int kNFast = 8;                    // cohort sizes 1..8 (one n8 MMA tile)
+constexpr int kMaxSlotsF = kNFast * kMaxTopK;
+constexpr int kMaxRing = 8;
+constexpr int kStageSlices = 8;              // K-slices (256 inputs each) per gate/up stage
+constexpr int kMaxTilesF = 160;
+constexpr int kStampsPerCta = 16;
+constexpr int kMaxDI = 4;                    // down items per warp per stage
+constexpr unsigned long long kWaitNs = 1000000000ull;  // 1 s bound on any wait
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// bf16 value `which` (0: low half, 1: high half) of a packed pair, widened to f32
+__device__ __forceinline__ float bf_half(uint32_t w, int which) {
+    return __uint_as_float(which ? (w & 0xFFFF0000u) : (w << 16));
+}
+
+__device__ __forceinline__ uint16_t f2bf(float f) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// codes of inputs p and p+4 of a packed word, as bf16x2 values 128 + q
+__device__ __forceinline__ uint32_t code_pair(uint32_t word, int p) {
+    return ((word >> (4 * p)) & 0x000F000Fu) | 0x43004300u;
+}
+
+// two k16 MMA steps over one packed word per MMA row (rows g and g+8) and the
+// matching activation word (4 bf16x2 pairs: (v0,v4) (v1,v5) (v2,v6) (v3,v7))
+__device__ __forceinline__ void mma_word(float (&acc)[4], uint32_t wg, uint32_t wg8, uint4 v) {
+    uint32_t a0[4] = {code_pair(wg, 0), code_pair(wg8, 0), code_pair(wg, 1), code_pair(wg8, 1)};
+    ptx::mma_bf16_16816(acc, a0, v.x, v.y);
+    uint32_t a1[4] = {code_pair(wg, 2), code_pair(wg8, 2), code_pair(wg, 3), code_pair(wg8, 3)};
+    ptx::mma_bf16_16816(acc, a1, v.z, v.w);
+}
+
+__device__ __forceinline__ float sum_bf16x8(uint4 v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s += __uint_as_float(w[i] << 16) + __uint_as_float(w[i] & 0xFFFF0000u);
+    return s;
+}
+
+__device__ __forceinline__ void load8f(const void *p, size_t i, int dtype, float (&v)[8]) {
+    if (dtype == MOE_DTYPE_F32) {
+        const float4 *q = reinterpret_cast<const float4 *>(static_cast<const float *>(p) + i);
+        const float4 a = __ldg(q), b = __ldg(q + 1);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+        const uint4 a = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p) + i));
+        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            v[2 * j] = __uint_as_float(w[j] << 16);
+            v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+    }
+}
+
+// byte offset of a swizzled shared-memory box element: TMA's 128/64/32-byte
+// swizzle XORs the 16-byte column (address bits 4..6) with bits 7..9 of the
+// offset from the 1024-byte aligned box base (mask 7, 3 or 1)
+__device__ __forceinline__ uint32_t swz(uint32_t off, uint32_t mask) {
+    return off ^ (((off >> 7) & mask) << 4);
+}
+
+// position of input f (within one expert's Dff) in the stored h row: each block
+// of 16 is stored as the pairs (0,4) (1,5) (2,6) (3,7) (8,12) ... of the MMA
+// B-operand order
+__device__ __forceinline__ int h_pos(int f) {
+    const int i = f & 15, lo = i & 7;
+    return (f & ~15) | (i & 8) | (2 * (lo & 3) + (lo >> 2));
+}
+
+struct Smem {
+    uint64_t *full;
+    int *misc;             // [0] abort [1] barrier ok [2] U [3] tiles [4] b0 [5] b1
+                           // [6] stages issued [8..9] red_cnt [10..11] red_gen
+                           // [16..23] stage release counts [24..39] grouping scans
+    unsigned long long *s_mask;
+    int *s_idx, *s_st, *s_sk, *s_of, *s_counts, *s_off, *s_unique;
+    float *s_w, *slot_w;
+    int4 *tiles;           // (u, f0 of the box within the expert, valid lo, valid hi)
+    unsigned char *xs;
+    float *xsum;
+    float *red;            // gate/up partials [2][kCW][32][8]; router / final scratch
+    unsigned char *ring;
+};
+
+__device__ __forceinline__ Smem carve_smem(unsigned char *base, const DecodeLayout &L, int E) {
+    Smem s;
+    s.full = reinterpret_cast<uint64_t *>(base + L.off_bar);
+    s.misc = reinterpret_cast<int *>(base + L.off_misc);
+    unsigned char *r = base + L.off_route;
+    s.s_mask = reinterpret_cast<unsigned long long *>(r);
+    int *ip = reinterpret_cast<int *>(r + 8 * (size_t)E);
+    s.s_idx = ip; ip += kMaxSlotsF;
+    s.s_w = reinterpret_cast<float *>(ip); ip += kMaxSlotsF;
+    s.s_st = ip; ip += kMaxSlotsF;
+    s.s_sk = ip; ip += kMaxSlotsF;
+    s.s_of = ip; ip += kMaxSlotsF;
+    s.slot_w = reinterpret_cast<float *>(ip); ip += kMaxSlotsF;
+    s.s_counts = ip; ip += E;
+    s.s_off = ip; ip += E + 1;
+    s.s_unique = ip;
+    s.tiles = reinterpret_cast<int4 *>(base + L.off_tiles);
+    s.xs = base + L.off_x;
+    s.xsum = reinterpret_cast<float *>(base + L.off_xsum);
+    s.red = reinterpret_cast<float *>(base + L.off_red);
+    s.ring = base + L.off_ring;
+    return s;
+}
+
+__device__ __forceinline__ void set_timeout(volatile int *abort_flag, unsigned *status) {
+    *abort_flag = 1;
+    atomicOr(status, kDevErrTimeout);
+}
+
+// bounded wait on an mbarrier phase; false on timeout or abort
+__device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                           unsigned *status) {
+#pragma unroll 1
+    for (int it = 0; it < 64; ++it)
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (unsigned it = 0;; ++it) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((it & 15) == 15) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > kWaitNs) {
+                set_timeout(abort_flag, status);
+                return false;
+            }
+        }
+    }
+}
+
+// bounded spin until *flag == want (shared memory, written by another warp)
+__device__ __forceinline__ bool wait_value(volatile int *flag, int want, volatile int *abort_flag,
+                                           unsigned *status) {
+    if (*flag == want) return true;
+    const unsigned long long t0 = globaltimer();
+    while (*flag != want) {
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > kWaitNs) {
+            set_timeout(abort_flag, status);
+            return false;
+        }
+        __nanosleep(32);
+    }
+    return true;
+}
+
+// Grid-wide barrier of all threads. The arrival counter only grows, by G per
+// barrier and 2G per launch; `target` is its value once every CTA has arrived
+// (the launch's base value plus G or 2G).
+__device__ __forceinline__ bool grid_barrier(unsigned long long *cnt, unsigned long long target,
+                                             volatile int *flag_ok, volatile int *abort_flag,
+                                             unsigned *status) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        __threadfence();
+        ptx::red_release_gpu_u64(cnt, 1ull);
+        if (ptx::ld_acquire_gpu_u64(cnt) < target) {
+            const unsigned long long t0 = globaltimer();
+            while (ptx::ld_acquire_gpu_u64(cnt) < target) {
+                if (*abort_flag || globaltimer() - t0 > kWaitNs) {
+                    ok = 0;
+                    set_timeout(abort_flag, status);
+                    break;
+                }
+            }
+        }
+        *flag_ok = ok;
+    }
+    __syncthreads();
+    return *flag_ok != 0;
+}
+
+__device__ __forceinline__ void stamp(unsigned long long *times, bool on, int i) {
+    if (on && threadIdx.x == 0) times[blockIdx.x * kStampsPerCta + i] = globaltimer();
+}
+
+struct DecodeArgs {
+    TMaps tm;  // first: 64-byte aligned members
+    StepArgs a;
+    Workspace ws;
+    DecodeLayout L;
+};
+
+// one gate/up tile: valid rows [v0, v1) of the concatenated U*Dff row space
+__device__ __forceinline__ int4 make_tile(int v0, int v1, int F) {
+    const int u = v0 / F, es = u * F;
+    const int r0 = min(v0, max(es, v1 - 16));  // 16-row box inside the expert, covering [v0, v1)
+    return make_int4(u, r0 - es, v0 - r0, v1 - r0);
+}
+
+// D-tile `dt` of a CTA's D rows [b0, b0 + 2 pp) (pp row pairs, ndt tiles):
+// first row and height (both even)
+__device__ __forceinline__ void d_tile(int b0, int pp, int ndt, int dt, int &start, int &h) {
+    const int s0 = pp * dt / ndt, s1 = pp * (dt + 1) / ndt;
+    start = b0 + 2 * s0;
+    h = 2 * (s1 - s0);
+}
+
+__device__ __forceinline__ uint32_t lds32(const unsigned char *p) {
+    return *reinterpret_cast<const uint32_t *>(p);
+}
+
+// order-preserving map of f32 to u32 (larger float -> larger key; NaN lowest)
+__device__ __forceinline__ uint32_t f2key(float f) {
+    const uint32_t u = __float_as_uint(f);
+    if (f != f) return 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key2f(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Top-k of one token's logits (warp-wide; lane l holds experts l + 32 i, i < 8):
+// the k largest in descending order, ties to the lower expert id, and their
+// renormalised softmax weights. The softmax denominator over all experts cancels
+// in the renormalisation, so only the k selected logits are exponentiated.
+__device__ __forceinline__ void warp_topk8(const float *lt, int E, int k, int lane, int *idx_out,
+                                           float *w_out) {
+    uint32_t key[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int e = lane + 32 * i;
+        key[i] = e < E ? f2key(__ldcg(lt + e)) : 0u;
+    }
+    uint32_t taken = 0;
+    float lsel = 0.f, lmax = 0.f;
+    for (int j = 0; j < k; ++j) {
+        uint32_t bk = 0;
+        int bi = 0;
+        bool have = false;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const bool cand = !((taken >> i) & 1u) && lane + 32 * i < E;
+            if (cand && (!have || key[i] > bk)) {
+                bk = key[i];
+                bi = i;
+                have = true;
+            }
+        }
+        const uint32_t wk = __reduce_max_sync(0xffffffffu, have ? bk : 0u);
+        const uint32_t ce = (have && bk == wk) ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu;
+        const uint32_t e = __reduce_min_sync(0xffffffffu, ce);
+        if ((int)(e & 31u) == lane) taken |= 1u << (e >> 5);
+        const float l = key2f(wk);
+        if (j == 0) lmax = l;
+        if (lane == j) {
+            lsel = l;
+            idx_out[j] = (int)e;
+        }
+    }
+    const float ev = lane < k ? expf(lsel - lmax) : 0.f;
+    const float z = warp_sum(ev);
+    if (lane < k) w_out[lane] = ev / z;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_constant__ DecodeArgs P) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *sbase = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const DecodeLayout &L = P.L;
+    const StepArgs &A = P.a;
+    const Workspace &W = P.ws;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int E = A.s.E, K = A.s.k, D = A.s.D, F = A.s.F, n = A.s.n;
+    const int GD = D / kGroup, GF = F / kGroup;
+    const unsigned G = gridDim.x;
+    const int cta = blockIdx.x;
+    Smem S = carve_smem(sbase, L, E);
+    volatile int *abort_flag = S.misc + 0;
+    volatile int *bar_ok = S.misc + 1;
+    volatile int *red_cnt = S.misc + 8;
+    volatile int *red_gen = S.misc + 10;
+    const bool timing = (A.s.flags & MOE_FLAG_PHASE_TIMES) != 0;
+    unsigned long long *gsync = reinterpret_cast<unsigned long long *>(W.sync);
+    uint16_t *Hg = reinterpret_cast<uint16_t *>(W.h);  // [slots][F] bf16, h_pos order
+
+    stamp(W.phase_ns, timing, 0);
+    // barrier epoch (thread 0 only): the counter grows by 2G per launch and no
+    // CTA of this launch can pass barrier 1 before this CTA arrives there
+    unsigned long long epoch = 0;
+    if (tid == 0) {
+        epoch = ptx::ld_acquire_gpu_u64(gsync);
+        for (int s = 0; s < L.NS; ++s) ptx::mbar_init(&S.full[s], 1);
+        for (int i = 0; i < 32; ++i) S.misc[i] = 0;
+        ptx::mbar_fence_init();
+    }
+    if (tid == 32) {
+        const CUtensorMap *maps[] = {&P.tm.gq, &P.tm.uq, &P.tm.gs, &P.tm.gb, &P.tm.us, &P.tm.ub,
+                                     &P.tm.dq[0], &P.tm.dq[1]};
+        for (const CUtensorMap *m : maps) ptx::prefetch_tensormap(m);
+    }
+    // zero the expert token masks (grouping below)
+    for (int e = tid; e < E; e += kThreads) S.s_mask[e] = 0ull;
+    __syncthreads();
+
+    // ---- phase R: router logits of this CTA's experts, x staging ----------------
+    {
+        const int nE = (cta < E ? 1 : 0) + (cta + (int)G < E ? 1 : 0);
+        float a0[kNFast], a1[kNFast];
+#pragma unroll
+        for (int t = 0; t < kNFast; ++t) a0[t] = a1[t] = 0.f;
+        const int chunks = D >> 3;
+        for (int i = tid; i < nE * chunks; i += kThreads) {
+            const int ei = i >= chunks ? 1 : 0;
+            const int ch = i - ei * chunks;
+            const int e = cta + ei * (int)G;
+            float wv[8];
+            load8f(A.router_w, (size_t)e * D + (size_t)ch * 8, A.s.w_dtype, wv);
+#pragma unroll
+            for (int t = 0; t < kNFast; ++t) {
+                if (t < n) {
+                    float xv[8];
+                    load8f(A.x, (size_t)t * D + (size_t)ch * 8, A.s.x_dtype, xv);
+                    float d = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) d = fmaf(xv[j], wv[j], d);
+                    if (ei) a1[t] += d; else a0[t] += d;
+                }
+            }
+        }
+        float *rs = S.red;  // [warps][2][8]
+#pragma unroll
+        for (int t = 0; t < kNFast; ++t) {
+            const float v0 = warp_sum(a0[t]), v1 = warp_sum(a1[t]);
+            if (lane == 0) {
+                rs[(warp * 2 + 0) * kNFast + t] = v0;
+                rs[(warp * 2 + 1) * kNFast + t] = v1;
+            }
+        }
+        // x -> bf16 in B-operand order (pairs (0,4) (1,5) (2,6) (3,7) per 8 inputs);
+        // rows of tokens >= n are zero
+        const int words = D / 8;
+        for (int i = tid; i < kNFast * words; i += kThreads) {
+            const int t = i / words, wd = i - t * words;
+            uint4 o = make_uint4(0, 0, 0, 0);
+            if (t < n) {
+                float v[8];
+                load8f(A.x, (size_t)t * D + (size_t)wd * 8, A.s.x_dtype, v);
+                uint16_t b[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) b[j] = f2bf(v[j]);
+                o.x = (uint32_t)b[0] | ((uint32_t)b[4] << 16);
+                o.y = (uint32_t)b[1] | ((uint32_t)b[5] << 16);
+                o.z = (uint32_t)b[2] | ((uint32_t)b[6] << 16);
+                o.w = (uint32_t)b[3] | ((uint32_t)b[7] << 16);
+            }
+            *reinterpret_cast<uint4 *>(S.xs + (size_t)t * L.x_stride + (size_t)wd * 16) = o;
+        }
+        __syncthreads();
+        if (tid < nE * n) {
+            const int ei = tid / n, t = tid - ei * n;
+            float l = 0.f;
+            for (int w = 0; w < kCW; ++w) l += rs[(w * 2 + ei) * kNFast + t];
+            const int e = cta + ei * (int)G;
+            if (A.router_bias) l += A.router_bias[e];
+            W.logits[(size_t)t * E + e] = l;
+        }
+        for (int i = tid; i < GD * kNFast; i += kThreads) {
+            const int gg = i / kNFast, t = i - gg * kNFast;
+            const unsigned char *row = S.xs + (size_t)t * L.x_stride + (size_t)gg * 128;
+            float s = 0.f;
+            for (int w = 0; w < 8; ++w) s += sum_bf16x8(*reinterpret_cast<const uint4 *>(row + w * 16));
+            S.xsum[gg * kNFast + t] = s;
+        }
+    }
+
+    // ---- grid barrier 1: all logits written -------------------------------------
+    stamp(W.phase_ns, timing, 1);
+    if (tid == 0) epoch = epoch / (2ull * G) * (2ull * G);
+    if (!((A.s.flags & MOE_FLAG_TEST_STALL) && cta == 0))
+        grid_barrier(gsync, epoch + G, bar_ok, abort_flag, W.status);
+    else
+        __syncthreads();  // test hook: CTA 0 never arrives; the others time out
+    stamp(W.phase_ns, timing, 2);
+
+    // ---- phase T: routing and grouping, redundantly in every CTA ---------------
+    if (warp < n) warp_topk8(W.logits + (size_t)warp * E, E, K, lane, S.s_idx + warp * K, S.s_w + warp * K);
+    __syncthreads();
+    const int Sl = n * K;
+    if (tid < Sl) atomicOr(reinterpret_cast<unsigned int *>(S.s_mask + S.s_idx[tid]), 1u << (tid / K));
+    __syncthreads();
+    // exclusive scans of counts and of (count > 0) over the experts, 32 per warp
+    int *wtot = S.misc + 24;  // [8] slot counts per warp of experts
+    int *utot = S.misc + 32;  // [8] selected experts per warp of experts
+    const int nwE = (E + 31) / 32;
+    int cnt = 0, incl = 0;
+    unsigned ub = 0;
+    if (warp < nwE) {
+        const int e = warp * 32 + lane;
+        cnt = e < E ? __popc((unsigned)S.s_mask[e]) : 0;
+        incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        ub = __ballot_sync(0xffffffffu, cnt > 0);
+        if (lane == 31) {
+            wtot[warp] = incl;
+            utot[warp] = __popc(ub);
+        }
+    }
+    __syncthreads();
+    if (warp < nwE) {
+        int base = 0, ubase = 0;
+        for (int w = 0; w < warp; ++w) {
+            base += wtot[w];
+            ubase += utot[w];
+        }
+        const int e = warp * 32 + lane;
+        if (e < E) {
+            S.s_off[e] = base + incl - cnt;
+            S.s_counts[e] = cnt;
+            if (cnt > 0) S.s_unique[ubase + __popc(ub & ((1u << lane) - 1u))] = e;
+            if (e == E - 1) {
+                S.s_off[E] = base + incl;
+                S.misc[2] = ubase + __popc(ub);
+            }
+        }
+    }
+    __syncthreads();
+    if (tid < Sl) {
+        const int t = tid / K, e = S.s_idx[tid];
+        const unsigned m = (unsigned)S.s_mask[e];
+        const int p = S.s_off[e] + __popc(m & ((1u << t) - 1u));
+        S.slot_w[p] = S.s_w[tid];
+        if (cta == 0) {
+            W.topk_idx[tid] = e;
+            W.topk_w[tid] = S.s_w[tid];
+            W.slot_token[p] = t;
+            W.slot_k[p] = tid - t * K;
+            W.slot_of[tid] = p;
+        }
+    }
+    if (cta == 0) {
+        const int U0 = S.misc[2];
+        for (int e = tid; e < E; e += kThreads) {
+            W.counts[e] = S.s_counts[e];
+            W.offsets[e] = S.s_off[e];
+            W.unique[e] = e < U0 ? S.s_unique[e] : -1;
+        }
+        if (tid == 0) {
+            W.offsets[E] = S.s_off[E];
+            *W.U = U0;
+        }
+    }
+    __syncthreads();
+    // gate/up tile list: this CTA's rows [R0, R1) of the U*F row space (even
+    // bounds), cut every 16 rows and at expert boundaries
+    if (warp == 0) {
+        const int U0 = S.misc[2];
+        const unsigned RP = (unsigned)U0 * (unsigned)F / 2u;
+        const int R0 = 2 * (int)(RP * (unsigned)cta / G), R1 = 2 * (int)(RP * (unsigned)(cta + 1) / G);
+        const int nsteps = (R1 - R0 + 15) / 16;
+        int tb = 0;
+        for (int m0 = 0; m0 < nsteps; m0 += 32) {
+            const int m = m0 + lane;
+            const bool valid = m < nsteps;
+            const int a = R0 + 16 * m, b = min(a + 16, R1);
+            const int eb = (a / F + 1) * F;
+            const bool split = valid && eb < b;
+            const int c2 = valid ? 1 + (split ? 1 : 0) : 0;
+            int inc = c2;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += v;
+            }
+            const int pos = tb + inc - c2;
+            if (valid && pos + c2 <= L.max_tiles) {
+                S.tiles[pos] = make_tile(a, split ? eb : b, F);
+                if (split) S.tiles[pos + 1] = make_tile(eb, b, F);
+            }
+            tb += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        if (lane == 0) {
+            if (tb > L.max_tiles) {
+                atomicOr(W.status, kDevErrInternal);  // the host bounds the count
+                tb = L.max_tiles;
+            }
+            S.misc[3] = tb;
+            // D rows of this CTA, in row pairs (even bounds)
+            S.misc[4] = 2 * (int)((unsigned)(D / 2) * (unsigned)cta / G);
+            S.misc[5] = 2 * (int)((unsigned)(D / 2) * (unsigned)(cta + 1) / G);
+        }
+    }
+    __syncthreads();
+    stamp(W.phase_ns, timing, 3);
+
+    const int U = S.misc[2];
+    const int nTiles = S.misc[3];
+    const int b0 = S.misc[4], rowsB = S.misc[5] - S.misc[4];
+    const int pp = rowsB / 2;                    // row pairs
+    const int ndt = (pp + 6) / 7;                // D-tiles of at most 14 rows (0, 1 or 2)
+    const int dsh = ndt > 1 ? 1 : 0;             // unit -> (expert index, D-tile) shift
+    int ds0 = b0, h0 = 0, ds1 = b0, h1 = 0;
+    if (ndt > 0) d_tile(b0, pp, ndt, 0, ds0, h0);
+    if (ndt > 1) d_tile(b0, pp, ndt, 1, ds1, h1);
+    const int nU = U * ndt;                      // down units of this CTA
+    const int tsh = L.NKC > 1 ? 1 : 0;           // gate/up stage -> (tile, K chunk) shift
+    const int nA = nTiles << tsh;                // gate/up stages
+    const int nB = (nU + L.P - 1) / L.P;         // down stages
+    const int total = nA + nB;
+
+    // ---- ring stages: issuing and release ----------------------------------------
+    // Stage st (gate/up tiles first, then down units) goes to ring slot st % NS.
+    // The first NS stages are issued here; after that the last warp to release a
+    // stage issues the stage NS further on into the freed slot. Called by a whole warp.
+    const uint64_t pol = ptx::policy_evict_first();
+    volatile int *rel_cnt = S.misc + 16;
+    auto issue_stage = [&](int st) {
+        const int slot = st % L.NS;
+        unsigned char *buf = S.ring + (size_t)slot * L.stage_bytes;
+        uint64_t *bar = &S.full[slot];
+        if (st < nA) {
+            if (lane == 0) {
+                const int4 tl = S.tiles[st >> tsh];
+                const int kc = st & tsh;
+                const int row0 = S.s_unique[tl.x] * F + tl.y;  // first row of the box (even)
+                ptx::mbar_arrive_expect_tx(bar, 2u * L.KS * 16u * 128u + 4u * 16u * L.sc_w);
+                ptx::tma_load_3d(buf, &P.tm.gq, 0, row0, kc * L.KS, bar, pol);
+                ptx::tma_load_3d(buf + L.off_up, &P.tm.uq, 0, row0, kc * L.KS, bar, pol);
+                const int gx = kc * L.GDc, py = row0 >> 1;
+                ptx::tma_load_3d(buf + L.off_sc, &P.tm.gs, gx, py, 0, bar, pol);
+                ptx::tma_load_3d(buf + L.off_sc + 1024, &P.tm.gb, gx, py, 0, bar, pol);
+                ptx::tma_load_3d(buf + L.off_sc + 2048, &P.tm.us, gx, py, 0, bar, pol);
+                ptx::tma_load_3d(buf + L.off_sc + 3072, &P.tm.ub, gx, py, 0, bar, pol);
+            }
+        } else {
+            const int jb = (st - nA) * L.P;
+            const int nu = min(L.P, nU - jb);
+            if (lane == 0) {
+                uint32_t bytes = 0;
+                for (int j = 0; j < nu; ++j)
+                    bytes += (uint32_t)(((jb + j) & dsh) ? h1 : h0) *
+                             (uint32_t)(L.sl_d * L.kw_d * 4 + 2 * L.rb_d);
+                ptx::mbar_arrive_expect_tx(bar, bytes);
+            }
+            __syncwarp();
+            if (lane < nu) {
+                const int unit = jb + lane;
+                const int e = S.s_unique[unit >> dsh];
+                const int dt = unit & dsh;
+                const int ds = dt ? ds1 : ds0, h = dt ? h1 : h0;
+                const int hi = h == L.Hd[0] ? 0 : 1;
+                unsigned char *ub = buf + (size_t)lane * L.unit_bytes;
+                const int row = e * D + ds;  // even
+                ptx::tma_load_3d(ub, &P.tm.dq[hi], 0, row, 0, bar, pol);
+                if (L.dmode) {
+                    ptx::tma_load_3d(ub + L.unit_sc, &P.tm.ds[hi], 0, row >> 1, 0, bar, pol);
+                    ptx::tma_load_3d(ub + L.unit_sc + L.unit_sc_stride, &P.tm.db[hi], 0, row >> 1, 0, bar, pol);
+                } else {
+                    const size_t off = (size_t)row * L.rb_d;  // 16-byte aligned: even row, rb_d = 8 mod 16
+                    const uint32_t nb = (uint32_t)h * L.rb_d;
+                    ptx::bulk_g2s(ub + L.unit_sc, reinterpret_cast<const unsigned char *>(A.planes.down_s) + off,
+                                  nb, bar, pol);
+                    ptx::bulk_g2s(ub + L.unit_sc + L.unit_sc_stride,
+                                  reinterpret_cast<const unsigned char *>(A.planes.down_b) + off, nb, bar, pol);
+                }
+            }
+        }
+        if (lane == 0) atomicMax(S.misc + 6, st + 1);
+    };
+    auto release_stage = [&](int st, int slot) {
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+            __threadfence_block();
+            last = atomicAdd(const_cast<int *>(rel_cnt + slot), 1) == kCW - 1;
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+            if (lane == 0) {
+                rel_cnt[slot] = 0;
+                __threadfence_block();
+                ptx::fence_proxy_async_shared();  // the stage's reads before the refill's async writes
+            }
+            __syncwarp();
+            if (st + L.NS < total && !*abort_flag) issue_stage(st + L.NS);
+        }
+    };
+    if (warp == 0)
+        for (int st = 0; st < min(total, L.NS); ++st) issue_stage(st);
+
+    const int g = lane >> 2, c = lane & 3;
+    const int r0 = 2 * g, r1 = 2 * g + 1;  // tile rows of MMA rows g and g + 8
+    unsigned long long ta_wait = 0, ta_comp = 0, tb_wait = 0, tb_comp = 0;
+    int slot = 0, par = 0;                 // ring position of the current stage
+
+    // ---- phase A: gate/up ---------------------------------------------------------
+    float tg[4] = {0.f, 0.f, 0.f, 0.f}, tu[4] = {0.f, 0.f, 0.f, 0.f};
+    // per-lane parts of the swizzled offsets: code rows 2g, 2g + 1 (the 16-byte
+    // column of group gi is (2 gi) ^ X), scale rows (parity, pair g)
+    const uint32_t X0 = (uint32_t)((c >> 1) ^ (r0 & 7)), X1 = (uint32_t)((c >> 1) ^ (r1 & 7));
+    const uint32_t rb0 = (uint32_t)(r0 * 128 + (c & 1) * 8), rb1 = (uint32_t)(r1 * 128 + (c & 1) * 8);
+    const uint32_t sco0 = (uint32_t)(g * L.sc_w), sco1 = (uint32_t)((8 + g) * L.sc_w);
+    const unsigned char *xlane = S.xs + (size_t)g * L.x_stride + c * 32;
+    for (int st = 0; st < nA; ++st) {
+        const unsigned long long tw0 = timing ? globaltimer() : 0ull;
+        const bool ok = __shfl_sync(0xffffffffu, (int)wait_phase(&S.full[slot], par, abort_flag, W.status), 0) != 0;
+        const unsigned long long tw1 = timing ? globaltimer() : 0ull;
+        const int t_idx = st >> tsh, kc = st & tsh;
+        const unsigned char *gb = S.ring + (size_t)slot * L.stage_bytes;
+        const unsigned char *ubx = gb + L.off_up;
+        const unsigned char *sc = gb + L.off_sc;
+        const int nP = (min(L.GDc, GD - kc * L.GDc)) >> 1;  // group pairs in this K chunk
+        const int pA = warp * nP / kCW, pB = (warp + 1) * nP / kCW;
+        if (ok) {
+#pragma unroll 1
+            for (int p = pA; p < pB; ++p) {
+                uint32_t sw[8];  // (gate s, gate b, up s, up b) of rows 2g, 2g + 1 for the pair
+                {
+                    const uint32_t a0 = swz(sco0 + 4u * p, (uint32_t)L.sc_m);
+                    const uint32_t a1 = swz(sco1 + 4u * p, (uint32_t)L.sc_m);
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) {
+                        sw[a] = lds32(sc + a * 1024 + a0);
+                        sw[4 + a] = lds32(sc + a * 1024 + a1);
+                    }
+                }
+                const uint32_t kb = (uint32_t)(p >> 1) * 2048u;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const uint32_t gi2 = (uint32_t)(((p & 1) * 2 + h2) * 2);
+                    const uint32_t o0 = kb + rb0 + ((gi2 ^ X0) << 4);
+                    const uint32_t o1 = kb + rb1 + ((gi2 ^ X1) << 4);
+                    const uint2 wg0 = *reinterpret_cast<const uint2 *>(gb + o0);
+                    const uint2 wg1 = *reinterpret_cast<const uint2 *>(gb + o1);
+                    const uint2 wu0 = *reinterpret_cast<const uint2 *>(ubx + o0);
+                    const uint2 wu1 = *reinterpret_cast<const uint2 *>(ubx + o1);
+                    const int gg = kc * L.GDc + 2 * p + h2;
+                    const uint4 xb0 = *reinterpret_cast<const uint4 *>(xlane + (size_t)gg * 128);
+                    const uint4 xb1 = *reinterpret_cast<const uint4 *>(xlane + (size_t)gg * 128 + 16);
+                    float cg[4] = {0.f, 0.f, 0.f, 0.f}, cu[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma_word(cg, wg0.x, wg1.x, xb0);
+                    mma_word(cu, wu0.x, wu1.x, xb0);
+                    mma_word(cg, wg0.y, wg1.y, xb1);
+                    mma_word(cu, wu0.y, wu1.y, xb1);
+                    const float2 xsm = *reinterpret_cast<const float2 *>(S.xsum + gg * kNFast + 2 * c);
+                    const float gs0 = bf_half(sw[0], h2), gb0 = bf_half(sw[1], h2);
+                    const float us0 = bf_half(sw[2], h2), ub0 = bf_half(sw[3], h2);
+                    const float gs1 = bf_half(sw[4], h2), gb1 = bf_half(sw[5], h2);
+                    const float us1 = bf_half(sw[6], h2), ub1 = bf_half(sw[7], h2);
+                    const float og0 = fmaf(-128.f, gs0, gb0), og1 = fmaf(-128.f, gs1, gb1);
+                    const float ou0 = fmaf(-128.f, us0, ub0), ou1 = fmaf(-128.f, us1, ub1);
+                    tg[0] = fmaf(gs0, cg[0], fmaf(og0, xsm.x, tg[0]));
+                    tg[1] = fmaf(gs0, cg[1], fmaf(og0, xsm.y, tg[1]));
+                    tg[2] = fmaf(gs1, cg[2], fmaf(og1, xsm.x, tg[2]));
+                    tg[3] = fmaf(gs1, cg[3], fmaf(og1, xsm.y, tg[3]));
+                    tu[0] = fmaf(us0, cu[0], fmaf(ou0, xsm.x, tu[0]));
+                    tu[1] = fmaf(us0, cu[1], fmaf(ou0, xsm.y, tu[1]));
+                    tu[2] = fmaf(us1, cu[2], fmaf(ou1, xsm.x, tu[2]));
+                    tu[3] = fmaf(us1, cu[3], fmaf(ou1, xsm.y, tu[3]));
+                }
+            }
+            // release the stage (after an abort the stage may still be in flight: keep it)
+            release_stage(st, slot);
+        }
+        if (++slot == L.NS) {
+            slot = 0;
+            par ^= 1;
+        }
+
+        if (kc == L.NKC - 1) {
+            // the tile's partial of this warp -> reduction buffer; the last warp reduces
+            const int b = t_idx & 1, round = t_idx >> 1;
+            if (lane == 0) wait_value(red_gen + b, round, abort_flag, W.status);
+            __syncwarp();
+            float *pp4 = S.red + ((size_t)(b * kCW + warp) * 32 + lane) * 8;
+            *reinterpret_cast<float4 *>(pp4) = make_float4(tg[0], tg[1], tg[2], tg[3]);
+            *reinterpret_cast<float4 *>(pp4 + 4) = make_float4(tu[0], tu[1], tu[2], tu[3]);
+            __syncwarp();
+            int prev = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                prev = atomicAdd(const_cast<int *>(red_cnt + b), 1);
+            }
+            prev = __shfl_sync(0xffffffffu, prev, 0);
+            if (prev == kCW - 1) {
+                __threadfence_block();
+                float gs[4] = {0.f, 0.f, 0.f, 0.f}, us[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int w2 = 0; w2 < kCW; ++w2) {
+                    const float *q = S.red + ((size_t)(b * kCW + w2) * 32 + lane) * 8;
+                    const float4 x0 = *reinterpret_cast<const float4 *>(q);
+                    const float4 x1 = *reinterpret_cast<const float4 *>(q + 4);
+                    gs[0] += x0.x; gs[1] += x0.y; gs[2] += x0.z; gs[3] += x0.w;
+                    us[0] += x1.x; us[1] += x1.y; us[2] += x1.z; us[3] += x1.w;
+                }
+                const int4 tl = S.tiles[t_idx];
+                const int e = S.s_unique[tl.x];
+                const unsigned m = (unsigned)S.s_mask[e];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int row = 2 * g + (i >> 1), tok = 2 * c + (i & 1);
+                    if (row >= tl.z && row < tl.w && ((m >> tok) & 1u)) {
+                        const int pslot = S.s_off[e] + __popc(m & ((1u << tok) - 1u));
+                        const float hv = S.slot_w[pslot] * (gs[i] / (1.0f + expf(-gs[i])) * us[i]);
+                        Hg[(size_t)pslot * F + h_pos(tl.y + row)] = f2bf(hv);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    red_cnt[b] = 0;
+                    __threadfence_block();
+                    red_gen[b] = round + 1;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) tg[i] = tu[i] = 0.f;
+        }
+        if (timing) {
+            ta_wait += tw1 - tw0;
+            ta_comp += globaltimer() - tw1;
+        }
+    }
+
+    // ---- grid barrier 2: every h row written ----------------------------------
+    stamp(W.phase_ns, timing, 4);
+    if (!((A.s.flags & MOE_FLAG_TEST_STALL) && cta == 0))
+        grid_barrier(gsync, epoch + 2ull * G, bar_ok, abort_flag, W.status);
+    stamp(W.phase_ns, timing, 5);
+
+    // ---- phase B: down, all experts summed per warp ----------------------------
+    float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+    // this warp's items of a down stage: item warp + 16 q is (unit j, group gm)
+    int itj[kMaxDI], itg[kMaxDI];
+#pragma unroll
+    for (int q = 0; q < kMaxDI; ++q) {
+        const int it = warp + q * kCW;
+        itj[q] = it / GF;
+        itg[q] = it - itj[q] * GF;
+    }
+    const int nItems = L.P * GF;
+    for (int st = nA; st < total; ++st) {
+        const int jb = (st - nA) * L.P;
+        const int nu = min(L.P, nU - jb);
+        // h of this warp's items (written by other CTAs before barrier 2): issue
+        // the loads before waiting for the stage's codes
+        uint4 hq[kMaxDI][2];
+#pragma unroll
+        for (int q = 0; q < kMaxDI; ++q) {
+            hq[q][0] = hq[q][1] = make_uint4(0, 0, 0, 0);
+            if (warp + q * kCW < nItems && itj[q] < nu) {
+                const int e = S.s_unique[(jb + itj[q]) >> dsh];
+                const unsigned m = (unsigned)S.s_mask[e];
+                if ((m >> g) & 1u) {
+                    const int ps = S.s_off[e] + __popc(m & ((1u << g) - 1u));
+                    const unsigned char *hp = reinterpret_cast<const unsigned char *>(Hg + (size_t)ps * F) +
+                                              (size_t)itg[q] * 128 + c * 32;
+                    hq[q][0] = ptx::ld_cg_v4(hp);
+                    hq[q][1] = ptx::ld_cg_v4(hp + 16);
+                }
+            }
+        }
+        const unsigned long long tw0 = timing ? globaltimer() : 0ull;
+        const bool ok = __shfl_sync(0xffffffffu, (int)wait_phase(&S.full[slot], par, abort_flag, W.status), 0) != 0;
+        const unsigned long long tw1 = timing ? globaltimer() : 0ull;
+        const unsigned char *buf = S.ring + (size_t)slot * L.stage_bytes;
+        if (ok) {
+#pragma unroll
+            for (int q = 0; q < kMaxDI; ++q) {
+                if (warp + q * kCW >= nItems || itj[q] >= nu) break;
+                const int j = itj[q], gm = itg[q];
+                const int dt = (jb + j) & dsh;
+                const int h = dt ? h1 : h0;
+                const unsigned char *ubase = buf + (size_t)j * L.unit_bytes;
+                const int ks = gm >> 2, chunk = 2 * (gm & 3) + (c >> 1);
+                const uint32_t oa = swz((uint32_t)((ks * h + r0) * 128 + chunk * 16 + (c & 1) * 8), 7u);
+                const uint32_t ob = swz((uint32_t)((ks * h + r1) * 128 + chunk * 16 + (c & 1) * 8), 7u);
+                const uint2 w0 = *reinterpret_cast<const uint2 *>(ubase + oa);
+                uint2 w1 = *reinterpret_cast<const uint2 *>(ubase + ob);
+                if (g == 7) w1 = make_uint2(0u, 0u);  // tile row 15: zero codes -> 128 * sum(h)
+                float cd[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_word(cd, w0.x, w1.x, hq[q][0]);
+                mma_word(cd, w0.y, w1.y, hq[q][1]);
+                const float hs0 = __shfl_sync(0xffffffffu, cd[2], 28 + c);
+                const float hs1 = __shfl_sync(0xffffffffu, cd[3], 28 + c);
+                // scales and biases of rows 2g and 2g + 1: [row parity][row pair][bytes]
+                const uint32_t ps = L.dmode ? (uint32_t)(h / 2 * L.rb_d) : (uint32_t)L.rb_d;
+                const uint32_t rs2 = L.dmode ? (uint32_t)L.rb_d : (uint32_t)(2 * L.rb_d);
+                const uint32_t cb = (uint32_t)((gm & ~1) * 2);
+                const uint32_t sa = swz(g * rs2 + cb, (uint32_t)L.sc_md);
+                const uint32_t sb = swz(ps + g * rs2 + cb, (uint32_t)L.sc_md);
+                const unsigned char *scs = ubase + L.unit_sc, *scb = scs + L.unit_sc_stride;
+                const int wh = gm & 1;
+                const float s0 = bf_half(lds32(scs + sa), wh), s1 = bf_half(lds32(scs + sb), wh);
+                const float o0 = fmaf(-128.f, s0, bf_half(lds32(scb + sa), wh)) * 0.0078125f;
+                const float o1 = fmaf(-128.f, s1, bf_half(lds32(scb + sb), wh)) * 0.0078125f;
+                const float v0 = fmaf(s0, cd[0], o0 * hs0), v1 = fmaf(s0, cd[1], o0 * hs1);
+                const float v2 = fmaf(s1, cd[2], o1 * hs0), v3 = fmaf(s1, cd[3], o1 * hs1);
+                if (dt == 0) {
+                    acc0[0] += v0; acc0[1] += v1; acc0[2] += v2; acc0[3] += v3;
+                } else {
+                    acc1[0] += v0; acc1[1] += v1; acc1[2] += v2; acc1[3] += v3;
+                }
+            }
+            release_stage(st, slot);
+        }
+        if (++slot == L.NS) {
+            slot = 0;
+            par ^= 1;
+        }
+        if (timing) {
+            tb_wait += tw1 - tw0;
+            tb_comp += globaltimer() - tw1;
+        }
+    }
+    if (timing && tid == 0) {
+        unsigned long long *tt = W.phase_ns + cta * kStampsPerCta;
+        tt[8] = ta_wait;
+        tt[9] = ta_comp;
+        tt[10] = tb_wait;
+        tt[11] = tb_comp;
+        tt[13] = (unsigned long long)nA;
+        tt[14] = (unsigned long long)(total - nA);
+    }
+
+    // ---- final: fixed-order sum over warps of their partial outputs -------------
+    {
+        float *red = S.red + ((size_t)warp * 32 + lane) * 8;
+        *reinterpret_cast<float4 *>(red) = make_float4(acc0[0], acc0[1], acc0[2], acc0[3]);
+        *reinterpret_cast<float4 *>(red + 4) = make_float4(acc1[0], acc1[1], acc1[2], acc1[3]);
+    }
+    __syncthreads();
+    stamp(W.phase_ns, timing, 6);
+    for (int o = tid; o < n * rowsB; o += kThreads) {
+        const int t = o / rowsB, r = o - t * rowsB;
+        const int dt = (ndt > 1 && b0 + r >= ds1) ? 1 : 0;
+        const int rt = b0 + r - (dt ? ds1 : ds0);
+        const int ln = (rt >> 1) * 4 + (t >> 1), idx = dt * 4 + (rt & 1) * 2 + (t & 1);
+        float v = 0.f;
+        for (int w = 0; w < kCW; ++w) v += S.red[((size_t)w * 32 + ln) * 8 + idx];
+        const size_t at = (size_t)t * D + b0 + r;
+        if (A.s.out_dtype == MOE_DTYPE_F32)
+            static_cast<float *>(A.out)[at] = v;
+        else
+            static_cast<uint16_t *>(A.out)[at] = f2bf(v);
+    }
+    if (timing) {
+        __syncthreads();
+        stamp(W.phase_ns, timing, 7);
+    }
+    // after an abort, stages may still be in flight: they must land before exit
+    if (*abort_flag && tid == 0) {
+        const int issued = S.misc[6];
+        for (int st = max(0, issued - L.NS); st < issued; ++st) {
+            const unsigned long long t0 = globaltimer();
+            while (!ptx::mbar_try_wait(&S.full[st % L.NS], (st / L.NS) & 1))
+                if (globaltimer() - t0 > kWaitNs) break;
+        }
+    }
+}
+
+}  // namespace
+
+// ---- host side -----------------------------------------------------------------
+
+static int round_up(int v, int m) { return (v + m - 1) / m * m; }
+
+bool fused_layout(const moe_config &c, int num_sms, int max_smem, DecodeLayout *out) {
+    DecodeLayout L{};
+    const int D = c.D, F = c.Dff, E = c.E, k = c.top_k, G = num_sms;
+    if (k * kNFast > kMaxSlotsF) return false;
+    // gate/up: K-slices of 256 inputs; scale row pairs with 16-byte aligned strides
+    if (D % 512 != 0) return false;
+    if (F % 256 != 0) return false;  // down K-slices of 256 inputs
+    if (E > 2 * G) return false;     // at most two router rows per CTA
+    if (E > 256) return false;       // top-k holds 8 logits per lane
+    if (D > 4096) return false;      // at most two K chunks per gate/up tile
+    L.G = G;
+    // gate/up stages
+    L.KS = D / 256 < kStageSlices ? D / 256 : kStageSlices;
+    L.NKC = (D / 256 + L.KS - 1) / L.KS;
+    L.GDc = 4 * L.KS;
+    L.off_up = L.KS * 16 * 128;
+    L.off_sc = 2 * L.off_up;
+    L.sc_w = 2 * L.GDc;  // 16, 32 or 64 bytes
+    L.sc_m = L.sc_w == 64 ? 3 : L.sc_w == 32 ? 1 : 0;
+    const int stage_a = L.off_sc + 4 * 1024;
+    // down units: D-tile heights of every CTA (even, at most 14; two distinct values)
+    int nh = 0;
+    L.Hd[0] = L.Hd[1] = 0;
+    for (int cta = 0; cta < G; ++cta) {
+        const int p0 = (int)((long long)(D / 2) * cta / G), p1 = (int)((long long)(D / 2) * (cta + 1) / G);
+        const int pairs = p1 - p0;
+        if (pairs == 0) continue;
+        const int ndt = (pairs + 6) / 7;
+        if (ndt > 2) return false;
+        for (int dt = 0; dt < ndt; ++dt) {
+            const int h = 2 * (pairs * (dt + 1) / ndt - pairs * dt / ndt);
+            if (h == L.Hd[0] || (nh > 1 && h == L.Hd[1])) continue;
+            if (nh == 2) return false;
+            L.Hd[nh++] = h;
+        }
+    }
+    if (nh == 0) return false;
+    if (nh == 1) L.Hd[1] = L.Hd[0];
+    const int Hmax = L.Hd[0] > L.Hd[1] ? L.Hd[0] : L.Hd[1];
+    L.kw_d = 32;
+    L.sl_d = F / 256;
+    L.swz_d = 7;
+    // down scales: rows of rb_d bytes; rb_d = 8 mod 16 keeps the rows of a bulk
+    // copy on distinct banks, 32/64/128 use row-pair boxes with swizzle
+    L.rb_d = F / 32;
+    if (L.rb_d % 16 == 8) {
+        L.dmode = 0;
+        L.sc_md = 0;
+        L.unit_sc_stride = round_up(Hmax * L.rb_d, 16);
+    } else if (L.rb_d == 32 || L.rb_d == 64 || L.rb_d == 128) {
+        L.dmode = 1;
+        L.sc_md = L.rb_d == 128 ? 7 : L.rb_d == 64 ? 3 : 1;
+        L.unit_sc_stride = round_up(Hmax * L.rb_d, 1024);
+    } else {
+        return false;
+    }
+    L.unit_w = round_up(L.sl_d * Hmax * L.kw_d * 4, 1024);
+    L.unit_sc = L.unit_w;
+    L.unit_bytes = round_up(L.unit_w + 2 * L.unit_sc_stride, 1024);
+    const int GF = F / kGroup;
+    L.P = stage_a / L.unit_bytes;
+    if (L.P < 1) L.P = 1;
+    while (L.P > 1 && L.P * GF > kMaxDI * kCW) --L.P;  // items of a stage: at most kMaxDI per warp
+    if (L.P * GF > kMaxDI * kCW) return false;
+    L.stage_bytes = round_up(stage_a > L.P * L.unit_bytes ? stage_a : L.P * L.unit_bytes, 1024);
+    // gate/up tiles per CTA: rows ceil(U*F/G) (+2 for even bounds) with U <= min(E, 8k)
+    const int Umax = E < kNFast * k ? E : kNFast * k;
+    const long long rows_cta = ((long long)Umax * F + G - 1) / G + 2;
+    const long long tiles = 2 * ((rows_cta + 15) / 16);
+    if (tiles > kMaxTilesF) return false;
+    L.max_tiles = kMaxTilesF;
+    L.x_stride = 2 * D + 16;
+    int off = 0;
+    L.off_bar = off;
+    off += 256;
+    L.off_misc = off;
+    off += 256;
+    L.off_route = off;
+    off += round_up(8 * E + 4 * (6 * kMaxSlotsF + E + (E + 1) + E), 128);
+    L.off_tiles = off;
+    off += round_up(16 * kMaxTilesF, 128);
+    L.off_x = off;
+    off += round_up(kNFast * L.x_stride, 128);
+    L.off_xsum = off;
+    off += round_up(4 * kNFast * (D / kGroup), 128);
+    L.off_red = off;
+    off += 2 * kCW * 32 * 8 * 4;
+    off = round_up(off, 1024);
+    L.off_ring = off;
+    const int tail = 2048 + 1024;  // over-read pad of the last stage + base alignment slack
+    const int room = max_smem - off - tail;
+    int ns = room / L.stage_bytes;
+    if (ns > kMaxRing) ns = kMaxRing;
+    if (ns < 2) return false;
+    L.NS = ns;
+    L.smem_bytes = off + ns * L.stage_bytes + tail;
+    *out = L;
+    return true;
+}
+
+cudaError_t fused_prepare(const DecodeLayout &L, int *blocks_per_sm) {
+    cudaError_t err = cudaFuncSetAttribute(decode_step_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem_bytes);
+    if (err != cudaSuccess) return err;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_step_kernel, kThreads,
+                                                         (size_t)L.smem_bytes);
+}
+
+int fused_max_tokens() { return kNFast; }
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        cudaGetLastError();
+    }
+    return fn;
+}
+
+CUtensorMapSwizzle swizzle_for(int inner_bytes) {
+    return inner_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+         : inner_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+         : inner_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE;
+}
+
+// 3-D view of a code plane [rows][words] as {inner words, rows, K-slices}: a box
+// of {inner, box_rows, box_slices} lands in shared memory as
+// [slice][row][inner * 4 bytes], swizzled
+bool encode_codes(CUtensorMap *m, const void *base, int words_per_row, long long rows, int inner,
+                  int box_rows, int box_slices) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)(words_per_row / inner)};
+    cuuint64_t strides[2] = {(cuuint64_t)words_per_row * 4u, (cuuint64_t)inner * 4u};
+    cuuint32_t box[3] = {(cuuint32_t)inner, (cuuint32_t)box_rows, (cuuint32_t)box_slices};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(inner * 4), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D view of a bf16 scale (or bias) array [rows][groups] as {groups, row pairs,
+// parity}: a box of {box_groups, box_pairs, 2} lands in shared memory as
+// [parity][row pair][box_groups * 2 bytes], swizzled, so rows 2i and 2i + 1 sit
+// in separate halves
+bool encode_scales(CUtensorMap *m, const void *base, int groups, long long rows, int box_groups,
+                   int box_pairs) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)groups, (cuuint64_t)(rows / 2), 2};
+    cuuint64_t strides[2] = {(cuuint64_t)groups * 4u, (cuuint64_t)groups * 2u};
+    cuuint32_t box[3] = {(cuuint32_t)box_groups, (cuuint32_t)box_pairs, 2};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(box_groups * 2), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool fused_encode_tmaps(const moe_config &c, const DecodeLayout &L, const moe_expert_planes &planes,
+                        TMaps *out) {
+    const long long E = c.E, D = c.D, F = c.Dff;
+    const int GD = (int)(D / kGroup), GF = (int)(F / kGroup);
+    bool ok = encode_codes(&out->gq, planes.gate_q, (int)(D / 8), E * F, 32, 16, L.KS) &&
+              encode_codes(&out->uq, planes.up_q, (int)(D / 8), E * F, 32, 16, L.KS) &&
+              encode_scales(&out->gs, planes.gate_s, GD, E * F, L.GDc, 8) &&
+              encode_scales(&out->gb, planes.gate_b, GD, E * F, L.GDc, 8) &&
+              encode_scales(&out->us, planes.up_s, GD, E * F, L.GDc, 8) &&
+              encode_scales(&out->ub, planes.up_b, GD, E * F, L.GDc, 8);
+    for (int i = 0; i < 2 && ok; ++i) {
+        ok = encode_codes(&out->dq[i], planes.down_q, (int)(F / 8), E * D, L.kw_d, L.Hd[i], L.sl_d);
+        if (ok && L.dmode)
+            ok = encode_scales(&out->ds[i], planes.down_s, GF, E * D, GF, L.Hd[i] / 2) &&
+                 encode_scales(&out->db[i], planes.down_b, GF, E * D, GF, L.Hd[i] / 2);
+    }
+    return ok;
+}
+
+cudaError_t launch_fused(const StepArgs &a, const Workspace &ws, const DecodeLayout &L,
+                         const TMaps &tm, cudaStream_t st, int &launched) {
+    DecodeArgs P;
+    P.tm = tm;
+    P.a = a;
+    P.ws = ws;
+    P.L = L;
+    void *args[] = {&P};
+    cudaError_t err = cudaLaunchCooperativeKernel((const void *)decode_step_kernel, dim3(L.G),
+                                                  dim3(kThreads), args, (size_t)L.smem_bytes, st);
+    if (err == cudaSuccess) launched += 1;
+    return err;
+}
+
+}  // namespace moe

@@ -137,8 +137,11 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan **out) {
     *out = nullptr;
     moe_status st = validate_config(cfg);
     if (st != MOE_OK) return st;
-    moe_plan *p = (moe_plan *)calloc(1, sizeof(moe_plan));
+    // the plan holds 64-byte aligned tensor maps
+    const size_t plan_bytes = (sizeof(moe_plan) + 63) / 64 * 64;
+    moe_plan *p = (moe_plan *)aligned_alloc(64, plan_bytes);
     if (!p) return MOE_ERR_OOM;
+    memset((void *)p, 0, plan_bytes);
     p->cfg = *cfg;
     p->mma_min_tokens = cfg->mma_min_tokens > 0 ? cfg->mma_min_tokens : 16;
     if (const char *env = getenv("MOE_MMA_MIN_TOKENS")) {
@@ -171,9 +174,10 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan **out) {
             p->fused_ok = e2 == cudaSuccess && per_sm >= 1;
         }
         if (trace_enabled(p))
-            fprintf(stderr, "[moe] plan: fused=%d smem=%d slots=%d slot_bytes=%d ctas/sm=%d (%s)\n",
-                    (int)p->fused_ok, p->fused.smem_bytes, p->fused.NS, p->fused.slot_bytes, per_sm,
-                    cudaGetErrorString(e2));
+            fprintf(stderr, "[moe] plan: fused=%d smem=%d stages=%d stage_bytes=%d down_units/stage=%d "
+                    "heights=%d,%d ctas/sm=%d (%s)\n",
+                    (int)p->fused_ok, p->fused.smem_bytes, p->fused.NS, p->fused.stage_bytes, p->fused.P,
+                    p->fused.Hd[0], p->fused.Hd[1], per_sm, cudaGetErrorString(e2));
         cudaGetLastError();
     }
     if (cudaMemset(p->ws_base, 0, p->ws_bytes) != cudaSuccess ||
@@ -212,14 +216,21 @@ moe_status moe_decode_forward(moe_plan *plan, const void *x, const void *router_
     a.planes = *planes;
     a.out = out;
 
-    const bool fused = plan->fused_ok && n_tokens <= fused_max_tokens();
+    bool fused = plan->fused_ok && n_tokens <= fused_max_tokens();
+    if (fused && (!plan->tm_valid || memcmp(&plan->tm_planes, planes, sizeof *planes) != 0)) {
+        // tensor maps describe the plane pointers: re-encode when they change
+        plan->tm_valid = fused_encode_tmaps(plan->cfg, plan->fused, *planes, &plan->tmaps);
+        if (plan->tm_valid) plan->tm_planes = *planes;
+        else if (trace_enabled(plan)) fprintf(stderr, "[moe] tensor map encoding failed\n");
+        fused = plan->tm_valid;
+    }
     if (trace_enabled(plan))
         fprintf(stderr, "[moe] forward n=%d E=%d k=%d D=%d Dff=%d path=%s\n", n_tokens,
                 a.s.E, a.s.k, a.s.D, a.s.F, fused ? "fused" : "f32-check");
     int launched = 0;
     cudaError_t err;
     if (fused) {
-        err = launch_fused(a, plan->ws, plan->fused, s, launched);
+        err = launch_fused(a, plan->ws, plan->fused, plan->tmaps, s, launched);
     } else {
         err = launch_router_logits(a, plan->ws, s, launched);
         if (err == cudaSuccess) err = launch_topk_group(a, plan->ws, s, launched);

@@ -2,6 +2,7 @@
 // translation units of the CUDA library. Not part of the public ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -60,21 +61,45 @@ struct StepArgs {
     void *out;
 };
 
-// Shared-memory and work layout of the fused kernel (computed on the host).
-struct FusedLayout {
+// Shared-memory and work layout of the single-launch decode step (host-computed).
+struct DecodeLayout {
     int G;            // CTAs (one per SM)
-    int NS;           // ring slots
-    int slot_bytes;   // bytes per ring slot
-    int nksA;         // gate/up K-slices (8 groups each) per 16-row tile
-    int nksB;         // down K-slices (4 groups each) per 16-row tile
-    int SA;           // gate/up row stride in a slot (bytes, padded)
-    int SB;           // down row stride in a slot (bytes, padded)
-    int hoff;         // offset of the h block area inside a down slot
-    int x_tokens;     // tokens the staged-activation area holds
-    int x_stride;     // bytes per token row of the staged activations
-    int part_bytes;   // gate/up partial-sum buffers (also the final reduction)
-    int off_bar, off_route, off_tiles, off_x, off_xsum, off_part, off_sbuf, off_ring;
-    int smem_bytes;
+    int NS;           // ring stages
+    int stage_bytes;  // bytes per ring stage (multiple of 1024)
+    // gate/up stages: one 16-row tile of gate and up rows x KS K-slices of 256 inputs
+    int KS;           // K-slices per gate/up stage
+    int NKC;          // gate/up stages per tile (K chunks)
+    int GDc;          // groups (64 inputs) per K chunk = 4 * KS
+    int off_up;       // byte offset of the up box inside a gate/up stage
+    int off_sc;       // byte offset of the four scale/bias boxes (1024 bytes apart)
+    int sc_w;         // bytes per row of a gate/up scale box (2 * GDc)
+    int sc_m;         // swizzle mask of the gate/up scale boxes
+    // down stages: P units, a unit = one expert x one D-tile (<= 15 rows) x all Dff
+    int kw_d;         // u32 words per down K-slice row (min(32, Dff/8))
+    int sl_d;         // down K-slices
+    int swz_d;        // swizzle mask of the down box (7: 128-byte rows, 3: 64-byte rows)
+    int Hd[2];        // down D-tile heights that occur (even; tensor map per height)
+    int dmode;        // down scale copies: 0 bulk rows as stored, 1 TMA row-pair boxes
+    int rb_d;         // bytes per row of down scales (Dff/32)
+    int sc_md;        // swizzle mask of the down scale boxes (mode 1)
+    int unit_w;       // bytes of a unit's weight box area (multiple of 1024)
+    int unit_sc;      // offset of a unit's scale block; its bias block follows at +unit_sc_stride
+    int unit_sc_stride;
+    int unit_bytes;   // bytes per unit (weights + scale/bias block, multiple of 1024)
+    int P;            // units per down stage
+    int max_tiles;    // gate/up tiles a CTA may own (bound of the tile list)
+    // shared memory carve (byte offsets from the 1024-aligned base)
+    int off_bar, off_misc, off_route, off_tiles, off_x, off_xsum, off_red, off_ring;
+    int x_stride;     // bytes per staged token row of x
+    int smem_bytes;   // dynamic shared memory requested (includes alignment slack)
+};
+
+// TMA descriptors of one forward call's expert planes (kernel parameters).
+struct TMaps {
+    CUtensorMap gq, uq;          // gate/up codes: 3-D {32 words, E*Dff rows, D/256 slices}
+    CUtensorMap gs, gb, us, ub;  // gate/up scales, biases: 3-D {D/64, E*Dff/2 row pairs, 2}
+    CUtensorMap dq[2];           // down codes per D-tile height: {kw_d, E*D rows, sl_d}
+    CUtensorMap ds[2], db[2];    // down scales, biases per height (scale mode 1)
 };
 
 }  // namespace moe
@@ -90,8 +115,11 @@ struct moe_plan {
     int last_n;
     int mma_min_tokens;
     unsigned long long launches;  // kernels enqueued by this plan since creation
-    bool fused_ok;                // the fused kernel can run this shape
-    moe::FusedLayout fused;
+    bool fused_ok;                // the single-launch kernel can run this shape
+    moe::DecodeLayout fused;
+    moe_expert_planes tm_planes;  // planes the cached tensor maps describe
+    bool tm_valid;
+    moe::TMaps tmaps;
 };
 
 namespace moe {
@@ -107,11 +135,14 @@ cudaError_t launch_topk_group(const StepArgs &a, const Workspace &ws, cudaStream
 cudaError_t launch_experts_f32(const StepArgs &a, const Workspace &ws, cudaStream_t st,
                                int &launched);
 
-// fused single-launch path (fused_step.cu)
-bool fused_layout(const moe_config &c, int num_sms, int max_smem, FusedLayout *out);
-cudaError_t fused_prepare(const FusedLayout &L, int *blocks_per_sm);
+// single-launch path (decode_step.cu)
+bool fused_layout(const moe_config &c, int num_sms, int max_smem, DecodeLayout *out);
+cudaError_t fused_prepare(const DecodeLayout &L, int *blocks_per_sm);
 int fused_max_tokens();
-cudaError_t launch_fused(const StepArgs &a, const Workspace &ws, const FusedLayout &L,
-                         cudaStream_t st, int &launched);
+// encode the tensor maps of `planes`; false if the driver rejects them
+bool fused_encode_tmaps(const moe_config &c, const DecodeLayout &L, const moe_expert_planes &planes,
+                        TMaps *out);
+cudaError_t launch_fused(const StepArgs &a, const Workspace &ws, const DecodeLayout &L,
+                         const TMaps &tm, cudaStream_t st, int &launched);
 
 }  // namespace moe

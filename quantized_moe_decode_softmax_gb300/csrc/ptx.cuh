@@ -78,6 +78,41 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+// 3-D tiled TMA load of one box of `tmap` at element coordinates (x, y, z)
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int x, int y, int z, uint64_t *bar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// fetch a tensor map (kernel parameter) into the TMA descriptor cache
+__device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// arrive on `bar` once every cp.async this thread issued before has landed
+// (the barrier's expected count includes this arrival)
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// fire-and-forget release add at gpu scope
+__device__ __forceinline__ void red_release_gpu_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// 16-byte load through L2 only (data written by other CTAs of the running grid)
+__device__ __forceinline__ uint4 ld_cg_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
 // ---- tensor core (legacy warp-level mma, f32 accumulate) -------------------------
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                                uint32_t b1) {
@@ -130,6 +165,12 @@ __device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned 
 
 // generic-proxy writes (by any CTA, made visible through an acquire) are
 // ordered before this thread's later async-proxy (bulk copy) reads
+// this thread's earlier generic-proxy shared-memory accesses (and those it has
+// observed) are ordered before its later async-proxy (TMA) writes
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
