@@ -145,7 +145,7 @@ __device__ __forceinline__ int h_pos(int f) {
 struct Smem {
     uint64_t *full;
     int *misc;             // [0] abort [1] barrier ok [2] U [3] tiles [4] b0 [5] b1
-                           // [6] stages issued [8..9] red_cnt [10..11] red_gen
+                           // [6] stages issued
                            // [16..23] stage release counts [24..39] grouping scans
     unsigned long long *s_mask;
     int *s_idx, *s_st, *s_sk, *s_of, *s_counts, *s_off, *s_unique;
@@ -203,22 +203,6 @@ __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, volat
             }
         }
     }
-}
-
-// bounded spin until *flag == want (shared memory, written by another warp)
-__device__ __forceinline__ bool wait_value(volatile int *flag, int want, volatile int *abort_flag,
-                                           unsigned *status) {
-    if (*flag == want) return true;
-    const unsigned long long t0 = globaltimer();
-    while (*flag != want) {
-        if (*abort_flag) return false;
-        if (globaltimer() - t0 > kWaitNs) {
-            set_timeout(abort_flag, status);
-            return false;
-        }
-        __nanosleep(32);
-    }
-    return true;
 }
 
 // Grid-wide barrier of all threads. The arrival counter only grows, by G per
@@ -332,6 +316,8 @@ __device__ __forceinline__ void warp_topk8(const float *lt, int E, int k, int la
     if (lane < k) w_out[lane] = ev / z;
 }
 
+// NKC: gate/up K chunks per tile (1 for D <= 2048, 2 for D <= 4096)
+template <int NKC>
 __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_constant__ DecodeArgs P) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sbase = reinterpret_cast<unsigned char *>(
@@ -347,8 +333,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     Smem S = carve_smem(sbase, L, E);
     volatile int *abort_flag = S.misc + 0;
     volatile int *bar_ok = S.misc + 1;
-    volatile int *red_cnt = S.misc + 8;
-    volatile int *red_gen = S.misc + 10;
     const bool timing = (A.s.flags & MOE_FLAG_PHASE_TIMES) != 0;
     unsigned long long *gsync = reinterpret_cast<unsigned long long *>(W.sync);
     uint16_t *Hg = reinterpret_cast<uint16_t *>(W.h);  // [slots][F] bf16, h_pos order
@@ -576,8 +560,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     if (ndt > 0) d_tile(b0, pp, ndt, 0, ds0, h0);
     if (ndt > 1) d_tile(b0, pp, ndt, 1, ds1, h1);
     const int nU = U * ndt;                      // down units of this CTA
-    const int tsh = L.NKC > 1 ? 1 : 0;           // gate/up stage -> (tile, K chunk) shift
-    const int nA = nTiles << tsh;                // gate/up stages
+    const int tsh = NKC > 1 ? 1 : 0;             // gate/up stage -> (tile, K chunk) shift
+    const int nA = nTiles * NKC;                 // gate/up stages
     const int nB = (nU + L.P - 1) / L.P;         // down stages
     const int total = nA + nB;
 
@@ -643,23 +627,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     auto release_stage = [&](int st, int slot) {
         __syncwarp();
         int last = 0;
-        if (lane == 0) {
-            __threadfence_block();
-            last = atomicAdd(const_cast<int *>(rel_cnt + slot), 1) == kCW - 1;
-        }
+        if (lane == 0)
+            last = ptx::atom_add_acqrel_cta_shared(const_cast<int *>(rel_cnt + slot), 1u) == kCW - 1;
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
             if (lane == 0) {
                 rel_cnt[slot] = 0;
-                __threadfence_block();
                 ptx::fence_proxy_async_shared();  // the stage's reads before the refill's async writes
             }
             __syncwarp();
             if (st + L.NS < total && !*abort_flag) issue_stage(st + L.NS);
         }
     };
-    if (warp == 0)
-        for (int st = 0; st < min(total, L.NS); ++st) issue_stage(st);
+    if (warp < min(total, L.NS)) issue_stage(warp);
 
     const int g = lane >> 2, c = lane & 3;
     const int r0 = 2 * g, r1 = 2 * g + 1;  // tile rows of MMA rows g and g + 8
@@ -667,129 +647,129 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     int slot = 0, par = 0;                 // ring position of the current stage
 
     // ---- phase A: gate/up ---------------------------------------------------------
-    float tg[4] = {0.f, 0.f, 0.f, 0.f}, tu[4] = {0.f, 0.f, 0.f, 0.f};
-    // per-lane parts of the swizzled offsets: code rows 2g, 2g + 1 (the 16-byte
-    // column of group gi is (2 gi) ^ X), scale rows (parity, pair g)
+    // A warp owns at most one pair of input groups per K chunk, the same pair in
+    // every tile, so its x fragments and group sums stay in registers.
     const uint32_t X0 = (uint32_t)((c >> 1) ^ (r0 & 7)), X1 = (uint32_t)((c >> 1) ^ (r1 & 7));
     const uint32_t rb0 = (uint32_t)(r0 * 128 + (c & 1) * 8), rb1 = (uint32_t)(r1 * 128 + (c & 1) * 8);
     const uint32_t sco0 = (uint32_t)(g * L.sc_w), sco1 = (uint32_t)((8 + g) * L.sc_w);
-    const unsigned char *xlane = S.xs + (size_t)g * L.x_stride + c * 32;
-    for (int st = 0; st < nA; ++st) {
-        const unsigned long long tw0 = timing ? globaltimer() : 0ull;
-        const bool ok = __shfl_sync(0xffffffffu, (int)wait_phase(&S.full[slot], par, abort_flag, W.status), 0) != 0;
-        const unsigned long long tw1 = timing ? globaltimer() : 0ull;
-        const int t_idx = st >> tsh, kc = st & tsh;
-        const unsigned char *gb = S.ring + (size_t)slot * L.stage_bytes;
-        const unsigned char *ubx = gb + L.off_up;
-        const unsigned char *sc = gb + L.off_sc;
-        const int nP = (min(L.GDc, GD - kc * L.GDc)) >> 1;  // group pairs in this K chunk
+    int pw[NKC];
+    uint4 xf[NKC][2][2];
+    float2 xsm[NKC][2];
+#pragma unroll
+    for (int kc = 0; kc < NKC; ++kc) {
+        const int nP = min(L.GDc, GD - kc * L.GDc) >> 1;  // group pairs in K chunk kc
         const int pA = warp * nP / kCW, pB = (warp + 1) * nP / kCW;
-        if (ok) {
-#pragma unroll 1
-            for (int p = pA; p < pB; ++p) {
-                uint32_t sw[8];  // (gate s, gate b, up s, up b) of rows 2g, 2g + 1 for the pair
-                {
-                    const uint32_t a0 = swz(sco0 + 4u * p, (uint32_t)L.sc_m);
-                    const uint32_t a1 = swz(sco1 + 4u * p, (uint32_t)L.sc_m);
+        pw[kc] = pB > pA ? pA : -1;
+        const int p0 = pB > pA ? pA : 0;
 #pragma unroll
-                    for (int a = 0; a < 4; ++a) {
-                        sw[a] = lds32(sc + a * 1024 + a0);
-                        sw[4 + a] = lds32(sc + a * 1024 + a1);
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int gg = kc * L.GDc + 2 * p0 + h2;
+            const unsigned char *xr = S.xs + (size_t)g * L.x_stride + (size_t)gg * 128 + c * 32;
+            xf[kc][h2][0] = *reinterpret_cast<const uint4 *>(xr);
+            xf[kc][h2][1] = *reinterpret_cast<const uint4 *>(xr + 16);
+            xsm[kc][h2] = *reinterpret_cast<const float2 *>(S.xsum + gg * kNFast + 2 * c);
+        }
+    }
+    float tg[4] = {0.f, 0.f, 0.f, 0.f}, tu[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int t_idx = 0; t_idx < nTiles; ++t_idx) {
+#pragma unroll
+        for (int kc = 0; kc < NKC; ++kc) {
+            const int st = t_idx * NKC + kc;
+            const unsigned long long tw0 = timing ? globaltimer() : 0ull;
+            const bool ok = __shfl_sync(0xffffffffu, (int)wait_phase(&S.full[slot], par, abort_flag, W.status), 0) != 0;
+            const unsigned long long tw1 = timing ? globaltimer() : 0ull;
+            if (ok) {
+                if (pw[kc] >= 0) {
+                    const int p = pw[kc];
+                    const unsigned char *gb = S.ring + (size_t)slot * L.stage_bytes;
+                    const unsigned char *ubx = gb + L.off_up;
+                    const unsigned char *sc = gb + L.off_sc;
+                    uint32_t sw[8];  // (gate s, gate b, up s, up b) of rows 2g, 2g + 1 for the pair
+                    {
+                        const uint32_t a0 = swz(sco0 + 4u * p, (uint32_t)L.sc_m);
+                        const uint32_t a1 = swz(sco1 + 4u * p, (uint32_t)L.sc_m);
+#pragma unroll
+                        for (int a = 0; a < 4; ++a) {
+                            sw[a] = lds32(sc + a * 1024 + a0);
+                            sw[4 + a] = lds32(sc + a * 1024 + a1);
+                        }
+                    }
+                    const uint32_t kb = (uint32_t)(p >> 1) * 2048u;
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const uint32_t gi2 = (uint32_t)(((p & 1) * 2 + h2) * 2);
+                        const uint32_t o0 = kb + rb0 + ((gi2 ^ X0) << 4);
+                        const uint32_t o1 = kb + rb1 + ((gi2 ^ X1) << 4);
+                        const uint2 wg0 = *reinterpret_cast<const uint2 *>(gb + o0);
+                        const uint2 wg1 = *reinterpret_cast<const uint2 *>(gb + o1);
+                        const uint2 wu0 = *reinterpret_cast<const uint2 *>(ubx + o0);
+                        const uint2 wu1 = *reinterpret_cast<const uint2 *>(ubx + o1);
+                        float cg[4] = {0.f, 0.f, 0.f, 0.f}, cu[4] = {0.f, 0.f, 0.f, 0.f};
+                        mma_word(cg, wg0.x, wg1.x, xf[kc][h2][0]);
+                        mma_word(cu, wu0.x, wu1.x, xf[kc][h2][0]);
+                        mma_word(cg, wg0.y, wg1.y, xf[kc][h2][1]);
+                        mma_word(cu, wu0.y, wu1.y, xf[kc][h2][1]);
+                        const float2 xs2 = xsm[kc][h2];
+                        const float gs0 = bf_half(sw[0], h2), gb0 = bf_half(sw[1], h2);
+                        const float us0 = bf_half(sw[2], h2), ub0 = bf_half(sw[3], h2);
+                        const float gs1 = bf_half(sw[4], h2), gb1 = bf_half(sw[5], h2);
+                        const float us1 = bf_half(sw[6], h2), ub1 = bf_half(sw[7], h2);
+                        const float og0 = fmaf(-128.f, gs0, gb0), og1 = fmaf(-128.f, gs1, gb1);
+                        const float ou0 = fmaf(-128.f, us0, ub0), ou1 = fmaf(-128.f, us1, ub1);
+                        tg[0] = fmaf(gs0, cg[0], fmaf(og0, xs2.x, tg[0]));
+                        tg[1] = fmaf(gs0, cg[1], fmaf(og0, xs2.y, tg[1]));
+                        tg[2] = fmaf(gs1, cg[2], fmaf(og1, xs2.x, tg[2]));
+                        tg[3] = fmaf(gs1, cg[3], fmaf(og1, xs2.y, tg[3]));
+                        tu[0] = fmaf(us0, cu[0], fmaf(ou0, xs2.x, tu[0]));
+                        tu[1] = fmaf(us0, cu[1], fmaf(ou0, xs2.y, tu[1]));
+                        tu[2] = fmaf(us1, cu[2], fmaf(ou1, xs2.x, tu[2]));
+                        tu[3] = fmaf(us1, cu[3], fmaf(ou1, xs2.y, tu[3]));
                     }
                 }
-                const uint32_t kb = (uint32_t)(p >> 1) * 2048u;
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const uint32_t gi2 = (uint32_t)(((p & 1) * 2 + h2) * 2);
-                    const uint32_t o0 = kb + rb0 + ((gi2 ^ X0) << 4);
-                    const uint32_t o1 = kb + rb1 + ((gi2 ^ X1) << 4);
-                    const uint2 wg0 = *reinterpret_cast<const uint2 *>(gb + o0);
-                    const uint2 wg1 = *reinterpret_cast<const uint2 *>(gb + o1);
-                    const uint2 wu0 = *reinterpret_cast<const uint2 *>(ubx + o0);
-                    const uint2 wu1 = *reinterpret_cast<const uint2 *>(ubx + o1);
-                    const int gg = kc * L.GDc + 2 * p + h2;
-                    const uint4 xb0 = *reinterpret_cast<const uint4 *>(xlane + (size_t)gg * 128);
-                    const uint4 xb1 = *reinterpret_cast<const uint4 *>(xlane + (size_t)gg * 128 + 16);
-                    float cg[4] = {0.f, 0.f, 0.f, 0.f}, cu[4] = {0.f, 0.f, 0.f, 0.f};
-                    mma_word(cg, wg0.x, wg1.x, xb0);
-                    mma_word(cu, wu0.x, wu1.x, xb0);
-                    mma_word(cg, wg0.y, wg1.y, xb1);
-                    mma_word(cu, wu0.y, wu1.y, xb1);
-                    const float2 xsm = *reinterpret_cast<const float2 *>(S.xsum + gg * kNFast + 2 * c);
-                    const float gs0 = bf_half(sw[0], h2), gb0 = bf_half(sw[1], h2);
-                    const float us0 = bf_half(sw[2], h2), ub0 = bf_half(sw[3], h2);
-                    const float gs1 = bf_half(sw[4], h2), gb1 = bf_half(sw[5], h2);
-                    const float us1 = bf_half(sw[6], h2), ub1 = bf_half(sw[7], h2);
-                    const float og0 = fmaf(-128.f, gs0, gb0), og1 = fmaf(-128.f, gs1, gb1);
-                    const float ou0 = fmaf(-128.f, us0, ub0), ou1 = fmaf(-128.f, us1, ub1);
-                    tg[0] = fmaf(gs0, cg[0], fmaf(og0, xsm.x, tg[0]));
-                    tg[1] = fmaf(gs0, cg[1], fmaf(og0, xsm.y, tg[1]));
-                    tg[2] = fmaf(gs1, cg[2], fmaf(og1, xsm.x, tg[2]));
-                    tg[3] = fmaf(gs1, cg[3], fmaf(og1, xsm.y, tg[3]));
-                    tu[0] = fmaf(us0, cu[0], fmaf(ou0, xsm.x, tu[0]));
-                    tu[1] = fmaf(us0, cu[1], fmaf(ou0, xsm.y, tu[1]));
-                    tu[2] = fmaf(us1, cu[2], fmaf(ou1, xsm.x, tu[2]));
-                    tu[3] = fmaf(us1, cu[3], fmaf(ou1, xsm.y, tu[3]));
-                }
+                // release the stage (after an abort the stage may still be in flight: keep it)
+                release_stage(st, slot);
             }
-            // release the stage (after an abort the stage may still be in flight: keep it)
-            release_stage(st, slot);
+            if (++slot == L.NS) {
+                slot = 0;
+                par ^= 1;
+            }
+            if (timing) {
+                ta_wait += tw1 - tw0;
+                ta_comp += globaltimer() - tw1;
+            }
         }
-        if (++slot == L.NS) {
-            slot = 0;
-            par ^= 1;
-        }
-
-        if (kc == L.NKC - 1) {
-            // the tile's partial of this warp -> reduction buffer; the last warp reduces
-            const int b = t_idx & 1, round = t_idx >> 1;
-            if (lane == 0) wait_value(red_gen + b, round, abort_flag, W.status);
-            __syncwarp();
-            float *pp4 = S.red + ((size_t)(b * kCW + warp) * 32 + lane) * 8;
+        // tile done: partials [warp][gate | up][lane][4] into buffer t & 1, then
+        // 128 threads (four warps, rotating) sum the 16 warps in order and write
+        // w * silu(g) * u for the tokens routed to the tile's expert. Buffer t & 1
+        // is written again only after the next tile's barrier, which the reducing
+        // threads reach after their sums.
+        {
+            float *pp4 = S.red + ((size_t)((t_idx & 1) * kCW + warp) * 64 + lane) * 4;
             *reinterpret_cast<float4 *>(pp4) = make_float4(tg[0], tg[1], tg[2], tg[3]);
-            *reinterpret_cast<float4 *>(pp4 + 4) = make_float4(tu[0], tu[1], tu[2], tu[3]);
-            __syncwarp();
-            int prev = 0;
-            if (lane == 0) {
-                __threadfence_block();
-                prev = atomicAdd(const_cast<int *>(red_cnt + b), 1);
-            }
-            prev = __shfl_sync(0xffffffffu, prev, 0);
-            if (prev == kCW - 1) {
-                __threadfence_block();
-                float gs[4] = {0.f, 0.f, 0.f, 0.f}, us[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int w2 = 0; w2 < kCW; ++w2) {
-                    const float *q = S.red + ((size_t)(b * kCW + w2) * 32 + lane) * 8;
-                    const float4 x0 = *reinterpret_cast<const float4 *>(q);
-                    const float4 x1 = *reinterpret_cast<const float4 *>(q + 4);
-                    gs[0] += x0.x; gs[1] += x0.y; gs[2] += x0.z; gs[3] += x0.w;
-                    us[0] += x1.x; us[1] += x1.y; us[2] += x1.z; us[3] += x1.w;
-                }
-                const int4 tl = S.tiles[t_idx];
-                const int e = S.s_unique[tl.x];
-                const unsigned m = (unsigned)S.s_mask[e];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int row = 2 * g + (i >> 1), tok = 2 * c + (i & 1);
-                    if (row >= tl.z && row < tl.w && ((m >> tok) & 1u)) {
-                        const int pslot = S.s_off[e] + __popc(m & ((1u << tok) - 1u));
-                        const float hv = S.slot_w[pslot] * (gs[i] / (1.0f + expf(-gs[i])) * us[i]);
-                        Hg[(size_t)pslot * F + h_pos(tl.y + row)] = f2bf(hv);
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) {
-                    red_cnt[b] = 0;
-                    __threadfence_block();
-                    red_gen[b] = round + 1;
-                }
-            }
+            *reinterpret_cast<float4 *>(pp4 + 128) = make_float4(tu[0], tu[1], tu[2], tu[3]);
 #pragma unroll
             for (int i = 0; i < 4; ++i) tg[i] = tu[i] = 0.f;
         }
-        if (timing) {
-            ta_wait += tw1 - tw0;
-            ta_comp += globaltimer() - tw1;
+        __syncthreads();
+        const int rt = tid - 128 * (t_idx & 3);
+        if (rt >= 0 && rt < 128) {
+            const int l = rt >> 2, i = rt & 3;  // fragment lane and element
+            const float *q = S.red + (size_t)(t_idx & 1) * kCW * 256 + l * 4 + i;
+            float gs = 0.f, us = 0.f;
+#pragma unroll 4
+            for (int w2 = 0; w2 < kCW; ++w2) {
+                gs += q[w2 * 256];
+                us += q[w2 * 256 + 128];
+            }
+            const int4 tl = S.tiles[t_idx];
+            const int e = S.s_unique[tl.x];
+            const unsigned m = (unsigned)S.s_mask[e];
+            const int row = 2 * (l >> 2) + (i >> 1), tok = 2 * (l & 3) + (i & 1);
+            if (row >= tl.z && row < tl.w && ((m >> tok) & 1u)) {
+                const int pslot = S.s_off[e] + __popc(m & ((1u << tok) - 1u));
+                const float sg = __fdividef(gs, 1.0f + __expf(-gs));
+                Hg[(size_t)pslot * F + h_pos(tl.y + row)] = f2bf(S.slot_w[pslot] * (sg * us));
+            }
         }
     }
 
@@ -810,27 +790,30 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
         itg[q] = it - itj[q] * GF;
     }
     const int nItems = L.P * GF;
+    // h of item q of down stage st (written by other CTAs before barrier 2), or 0
+    auto load_h = [&](int st, int q, uint4 (&hv)[2]) {
+        hv[0] = hv[1] = make_uint4(0, 0, 0, 0);
+        if (st >= total) return;
+        const int jb = (st - nA) * L.P;
+        if (warp + q * kCW < nItems && itj[q] < nU - jb) {
+            const int e = S.s_unique[(jb + itj[q]) >> dsh];
+            const unsigned m = (unsigned)S.s_mask[e];
+            if ((m >> g) & 1u) {
+                const int ps = S.s_off[e] + __popc(m & ((1u << g) - 1u));
+                const unsigned char *hp = reinterpret_cast<const unsigned char *>(Hg + (size_t)ps * F) +
+                                          (size_t)itg[q] * 128 + c * 32;
+                hv[0] = ptx::ld_cg_v4(hp);
+                hv[1] = ptx::ld_cg_v4(hp + 16);
+            }
+        }
+    };
+    // h fragments of this warp's items, loaded one stage ahead
+    uint4 hq[kMaxDI][2];
+#pragma unroll
+    for (int q = 0; q < kMaxDI; ++q) load_h(nA, q, hq[q]);
     for (int st = nA; st < total; ++st) {
         const int jb = (st - nA) * L.P;
         const int nu = min(L.P, nU - jb);
-        // h of this warp's items (written by other CTAs before barrier 2): issue
-        // the loads before waiting for the stage's codes
-        uint4 hq[kMaxDI][2];
-#pragma unroll
-        for (int q = 0; q < kMaxDI; ++q) {
-            hq[q][0] = hq[q][1] = make_uint4(0, 0, 0, 0);
-            if (warp + q * kCW < nItems && itj[q] < nu) {
-                const int e = S.s_unique[(jb + itj[q]) >> dsh];
-                const unsigned m = (unsigned)S.s_mask[e];
-                if ((m >> g) & 1u) {
-                    const int ps = S.s_off[e] + __popc(m & ((1u << g) - 1u));
-                    const unsigned char *hp = reinterpret_cast<const unsigned char *>(Hg + (size_t)ps * F) +
-                                              (size_t)itg[q] * 128 + c * 32;
-                    hq[q][0] = ptx::ld_cg_v4(hp);
-                    hq[q][1] = ptx::ld_cg_v4(hp + 16);
-                }
-            }
-        }
         const unsigned long long tw0 = timing ? globaltimer() : 0ull;
         const bool ok = __shfl_sync(0xffffffffu, (int)wait_phase(&S.full[slot], par, abort_flag, W.status), 0) != 0;
         const unsigned long long tw1 = timing ? globaltimer() : 0ull;
@@ -838,40 +821,42 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
         if (ok) {
 #pragma unroll
             for (int q = 0; q < kMaxDI; ++q) {
-                if (warp + q * kCW >= nItems || itj[q] >= nu) break;
-                const int j = itj[q], gm = itg[q];
-                const int dt = (jb + j) & dsh;
-                const int h = dt ? h1 : h0;
-                const unsigned char *ubase = buf + (size_t)j * L.unit_bytes;
-                const int ks = gm >> 2, chunk = 2 * (gm & 3) + (c >> 1);
-                const uint32_t oa = swz((uint32_t)((ks * h + r0) * 128 + chunk * 16 + (c & 1) * 8), 7u);
-                const uint32_t ob = swz((uint32_t)((ks * h + r1) * 128 + chunk * 16 + (c & 1) * 8), 7u);
-                const uint2 w0 = *reinterpret_cast<const uint2 *>(ubase + oa);
-                uint2 w1 = *reinterpret_cast<const uint2 *>(ubase + ob);
-                if (g == 7) w1 = make_uint2(0u, 0u);  // tile row 15: zero codes -> 128 * sum(h)
-                float cd[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_word(cd, w0.x, w1.x, hq[q][0]);
-                mma_word(cd, w0.y, w1.y, hq[q][1]);
-                const float hs0 = __shfl_sync(0xffffffffu, cd[2], 28 + c);
-                const float hs1 = __shfl_sync(0xffffffffu, cd[3], 28 + c);
-                // scales and biases of rows 2g and 2g + 1: [row parity][row pair][bytes]
-                const uint32_t ps = L.dmode ? (uint32_t)(h / 2 * L.rb_d) : (uint32_t)L.rb_d;
-                const uint32_t rs2 = L.dmode ? (uint32_t)L.rb_d : (uint32_t)(2 * L.rb_d);
-                const uint32_t cb = (uint32_t)((gm & ~1) * 2);
-                const uint32_t sa = swz(g * rs2 + cb, (uint32_t)L.sc_md);
-                const uint32_t sb = swz(ps + g * rs2 + cb, (uint32_t)L.sc_md);
-                const unsigned char *scs = ubase + L.unit_sc, *scb = scs + L.unit_sc_stride;
-                const int wh = gm & 1;
-                const float s0 = bf_half(lds32(scs + sa), wh), s1 = bf_half(lds32(scs + sb), wh);
-                const float o0 = fmaf(-128.f, s0, bf_half(lds32(scb + sa), wh)) * 0.0078125f;
-                const float o1 = fmaf(-128.f, s1, bf_half(lds32(scb + sb), wh)) * 0.0078125f;
-                const float v0 = fmaf(s0, cd[0], o0 * hs0), v1 = fmaf(s0, cd[1], o0 * hs1);
-                const float v2 = fmaf(s1, cd[2], o1 * hs0), v3 = fmaf(s1, cd[3], o1 * hs1);
-                if (dt == 0) {
-                    acc0[0] += v0; acc0[1] += v1; acc0[2] += v2; acc0[3] += v3;
-                } else {
-                    acc1[0] += v0; acc1[1] += v1; acc1[2] += v2; acc1[3] += v3;
+                if (warp + q * kCW < nItems && itj[q] < nu) {
+                    const int j = itj[q], gm = itg[q];
+                    const int dt = (jb + j) & dsh;
+                    const int h = dt ? h1 : h0;
+                    const unsigned char *ubase = buf + (size_t)j * L.unit_bytes;
+                    const int ks = gm >> 2, chunk = 2 * (gm & 3) + (c >> 1);
+                    const uint32_t oa = swz((uint32_t)((ks * h + r0) * 128 + chunk * 16 + (c & 1) * 8), 7u);
+                    const uint32_t ob = swz((uint32_t)((ks * h + r1) * 128 + chunk * 16 + (c & 1) * 8), 7u);
+                    const uint2 w0 = *reinterpret_cast<const uint2 *>(ubase + oa);
+                    uint2 w1 = *reinterpret_cast<const uint2 *>(ubase + ob);
+                    if (g == 7) w1 = make_uint2(0u, 0u);  // tile row 15: zero codes -> 128 * sum(h)
+                    float cd[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma_word(cd, w0.x, w1.x, hq[q][0]);
+                    mma_word(cd, w0.y, w1.y, hq[q][1]);
+                    const float hs0 = __shfl_sync(0xffffffffu, cd[2], 28 + c);
+                    const float hs1 = __shfl_sync(0xffffffffu, cd[3], 28 + c);
+                    // scales and biases of rows 2g and 2g + 1: [row parity][row pair][bytes]
+                    const uint32_t ps = L.dmode ? (uint32_t)(h / 2 * L.rb_d) : (uint32_t)L.rb_d;
+                    const uint32_t rs2 = L.dmode ? (uint32_t)L.rb_d : (uint32_t)(2 * L.rb_d);
+                    const uint32_t cb = (uint32_t)((gm & ~1) * 2);
+                    const uint32_t sa = swz(g * rs2 + cb, (uint32_t)L.sc_md);
+                    const uint32_t sb = swz(ps + g * rs2 + cb, (uint32_t)L.sc_md);
+                    const unsigned char *scs = ubase + L.unit_sc, *scb = scs + L.unit_sc_stride;
+                    const int wh = gm & 1;
+                    const float s0 = bf_half(lds32(scs + sa), wh), s1 = bf_half(lds32(scs + sb), wh);
+                    const float o0 = fmaf(-128.f, s0, bf_half(lds32(scb + sa), wh)) * 0.0078125f;
+                    const float o1 = fmaf(-128.f, s1, bf_half(lds32(scb + sb), wh)) * 0.0078125f;
+                    const float v0 = fmaf(s0, cd[0], o0 * hs0), v1 = fmaf(s0, cd[1], o0 * hs1);
+                    const float v2 = fmaf(s1, cd[2], o1 * hs0), v3 = fmaf(s1, cd[3], o1 * hs1);
+                    if (dt == 0) {
+                        acc0[0] += v0; acc0[1] += v1; acc0[2] += v2; acc0[3] += v3;
+                    } else {
+                        acc1[0] += v0; acc1[1] += v1; acc1[2] += v2; acc1[3] += v3;
+                    }
                 }
+                load_h(st + 1, q, hq[q]);
             }
             release_stage(st, slot);
         }
@@ -1036,12 +1021,15 @@ bool fused_layout(const moe_config &c, int num_sms, int max_smem, DecodeLayout *
     return true;
 }
 
+static const void *kernel_for(const DecodeLayout &L) {
+    return L.NKC == 1 ? (const void *)decode_step_kernel<1> : (const void *)decode_step_kernel<2>;
+}
+
 cudaError_t fused_prepare(const DecodeLayout &L, int *blocks_per_sm) {
-    cudaError_t err = cudaFuncSetAttribute(decode_step_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem_bytes);
+    const void *k = kernel_for(L);
+    cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem_bytes);
     if (err != cudaSuccess) return err;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_step_kernel, kThreads,
-                                                         (size_t)L.smem_bytes);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, kThreads, (size_t)L.smem_bytes);
 }
 
 int fused_max_tokens() { return kNFast; }
@@ -1132,7 +1120,7 @@ cudaError_t launch_fused(const StepArgs &a, const Workspace &ws, const DecodeLay
     P.ws = ws;
     P.L = L;
     void *args[] = {&P};
-    cudaError_t err = cudaLaunchCooperativeKernel((const void *)decode_step_kernel, dim3(L.G),
+    cudaError_t err = cudaLaunchCooperativeKernel(kernel_for(L), dim3(L.G),
                                                   dim3(kThreads), args, (size_t)L.smem_bytes, st);
     if (err == cudaSuccess) launched += 1;
     return err;

@@ -165,6 +165,29 @@ __device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned 
 
 // generic-proxy writes (by any CTA, made visible through an acquire) are
 // ordered before this thread's later async-proxy (bulk copy) reads
+// shared-memory counter add with acquire-release ordering at CTA scope; returns
+// the old value
+__device__ __forceinline__ uint32_t atom_add_acqrel_cta_shared(void *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "r"(smem_addr(p)), "r"(v)
+                 : "memory");
+    return old;
+}
+
+// shared-memory counter add with release ordering at CTA scope (no result)
+__device__ __forceinline__ void red_add_release_cta_shared(void *p, uint32_t v) {
+    asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+
+// shared-memory load with acquire ordering at CTA scope
+__device__ __forceinline__ uint32_t ld_acquire_cta_shared(const void *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+    return v;
+}
+
 // this thread's earlier generic-proxy shared-memory accesses (and those it has
 // observed) are ordered before its later async-proxy (TMA) writes
 __device__ __forceinline__ void fence_proxy_async_shared() {
