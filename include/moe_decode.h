@@ -158,6 +158,37 @@ moe_status moe_decode_forward_host(moe_plan *plan, const void *x_host, const voi
                                    const float *router_bias, const moe_expert_planes *planes,
                                    int n_tokens, int top_k, void *out_host, void *stream);
 
+/* The decode step without a plan and without any device allocation.
+ *
+ * For callers that cannot allocate device memory: for example code running
+ * while a CUDA graph is being captured, runtimes that forbid cudaMalloc, or
+ * processes whose device memory pool belongs to another framework. The pages
+ * this library follows have no counterpart of this call; it exists only for
+ * such callers.
+ *
+ * Runs the same single-launch kernel as moe_decode_forward, so it accepts what
+ * that kernel accepts: n_tokens 1..8, no MOE_FLAG_F32_DEBUG, and the shapes the
+ * kernel supports (otherwise MOE_ERR_UNSUPPORTED). cfg gives the layer shape
+ * and dtypes (max_tokens and flags are ignored; no phase timing, no routing
+ * copy-out). All other arguments are as for moe_decode_forward; the caller
+ * still owns x, router_w, router_bias, the planes and out.
+ *
+ * Scratch: one statically sized device array of 4 MiB inside the library,
+ * which every GPU that loads the library holds until the process exits. A call
+ * whose scratch would exceed it returns MOE_ERR_UNSUPPORTED before any launch.
+ * The call allocates nothing (no cudaMalloc, cudaFree or allocating library
+ * routine); it issues one cudaMemsetAsync that clears the array's status word
+ * and barrier counter, then the kernel, both on `stream`.
+ *
+ * The first call on a device looks up the array's device address on the
+ * current device (a one-time set-up); make that first call before any stream
+ * capture. Every call on a device shares the one array: calls that overlap on
+ * the GPU (different streams without ordering) race and give wrong results.
+ * Asynchronous; device-side timeouts are not reported by this call. */
+moe_status moe_decode_forward_noalloc(const moe_config *cfg, const void *x, const void *router_w,
+                                      const float *router_bias, const moe_expert_planes *planes,
+                                      int n_tokens, int top_k, void *out, void *stream);
+
 /* Synchronise the plan's last stream and report a device-side timeout or
  * internal error recorded by earlier calls (then clear it). */
 moe_status moe_plan_check(moe_plan *plan);

@@ -26,7 +26,7 @@ MOE_FLAG_TEST_STALL = 1 << 8
 EXPORTED = (
     "moe_abi_version", "moe_status_str", "moe_plan_workspace_bytes", "moe_plan_create",
     "moe_decode_forward", "moe_decode_forward_host", "moe_plan_check", "moe_get_routing",
-    "moe_get_phase_times", "moe_plan_launch_count", "moe_plan_free",
+    "moe_get_phase_times", "moe_plan_launch_count", "moe_plan_free", "moe_decode_forward_noalloc",
 )
 
 
@@ -163,6 +163,22 @@ def moe_decode_forward_host(plan: int, x_host, router_w, router_bias, planes, n_
                                        ctypes.byref(pl), int(n_tokens), int(top_k),
                                        _ptr(out_host), _stream(stream))
     _check(st, "moe_decode_forward_host")
+
+
+def moe_decode_forward_noalloc(cfg: moe_config, x, router_w, router_bias, planes, n_tokens: int,
+                               top_k: int, out, stream=None) -> None:
+    """The decode step without a plan and without device allocation (see the
+    header): scratch lives in a static device array of the library."""
+    L = lib()
+    fn = L.moe_decode_forward_noalloc
+    vp = ctypes.c_void_p
+    fn.argtypes = [ctypes.POINTER(moe_config), vp, vp, vp, ctypes.POINTER(moe_expert_planes),
+                   ctypes.c_int, ctypes.c_int, vp, vp]
+    fn.restype = ctypes.c_int
+    pl = planes if isinstance(planes, moe_expert_planes) else make_planes(planes)
+    st = fn(ctypes.byref(cfg), _ptr(x), _ptr(router_w), _ptr(router_bias), ctypes.byref(pl),
+            int(n_tokens), int(top_k), _ptr(out), _stream(stream))
+    _check(st, "moe_decode_forward_noalloc")
 
 
 def moe_plan_check(plan: int) -> None:

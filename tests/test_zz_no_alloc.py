@@ -1,0 +1,48 @@
+"""The allocation-free entry point (moe_decode_forward_noalloc) against the
+plan-based one, through the C ABI.
+
+Callers that cannot allocate device memory (for example code running during
+CUDA graph capture, or runtimes that own the device memory pool) use
+moe_decode_forward_noalloc, whose scratch is a static device array of the
+library. Its output must match moe_decode_forward's within the bf16 tolerance
+of the parity tests, on two calls in a row (the second call reuses the array
+the first one left behind). This file is collected last on purpose.
+"""
+import numpy as np
+import pytest
+
+import quantized_moe_decode_softmax_gb300 as q
+from gpu_cases import TOL_BF16, assert_out_close, case, device_layer, make_plan, run_gpu, x_tensor
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("n", [1, 4])
+def test_noalloc_matches_plan_entry_point_twice(n):
+    import torch
+    lay, x = case("qwen3", 2, n)
+    shape = lay.shape
+    dl = device_layer(lay)
+    ref, _ = run_gpu(make_plan(shape), dl, shape, x)
+    cfg = q.make_config(shape.E, shape.top_k, shape.D, shape.F, max_tokens=n)
+    xt = x_tensor(shape, x)
+    for _ in range(2):
+        out = torch.full((n, shape.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        q.moe_decode_forward_noalloc(cfg, xt, dl.router_w, dl.router_bias, dl.c_planes, n, shape.top_k, out)
+        torch.cuda.synchronize()
+        got = out.float().cpu().numpy()
+        assert np.all(np.isfinite(got))
+        assert_out_close(got, ref, TOL_BF16)
+
+
+def test_noalloc_declines_what_its_kernel_cannot_run():
+    import torch
+    lay, x = case("qwen3", 2, 1)
+    shape = lay.shape
+    dl = device_layer(lay)
+    xt = x_tensor(shape, np.repeat(x, 9, axis=0))
+    out = torch.empty((9, shape.D), dtype=torch.bfloat16, device="cuda")
+    cfg = q.make_config(shape.E, shape.top_k, shape.D, shape.F, max_tokens=9)
+    with pytest.raises(q.MoeError) as ei:  # more than 8 tokens
+        q.moe_decode_forward_noalloc(cfg, xt, dl.router_w, dl.router_bias, dl.c_planes, 9, shape.top_k, out)
+    assert ei.value.status == q.MOE_ERR_UNSUPPORTED
