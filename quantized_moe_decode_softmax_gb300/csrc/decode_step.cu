@@ -51,6 +51,7 @@
 // abort flag; the CTA then skips the remaining waits, still passes every barrier
 // it shares with its own threads, lets its copies in flight land and exits.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
 #include "moe_internal.h"
@@ -61,9 +62,14 @@ namespace moe {
 
 namespace {
 
-constexpr int kCW = 16;                      // warps per CTA (all consume; refills are issued
-                                             // by the last warp to release a ring stage)
-constexpr int kThreads = kCW * 32;
+constexpr int kCW = 16;                      // consumer warps (the MMA work)
+constexpr int kWarps = 20;                   // + one warpgroup: a producer warp and two reducer warps
+constexpr int kThreads = kWarps * 32;
+constexpr int kConsThreads = kCW * 32;
+constexpr int kProducer = kCW;               // streams every stage into the ring
+constexpr int kReducer0 = kCW + 1;           // warps kReducer0 + b reduce gate/up partial buffer b
+constexpr int kRegsConsumer = 112;           // register split after the routing phase:
+constexpr int kRegsProducer = 32;            // 512 * 112 + 128 * 32 = 640 * 96, the launch's registers
 constexpr int kNFast = 8;                    // cohort sizes 1..8 (one n8 MMA tile)
 constexpr int kMaxSlotsF = kNFast * kMaxTopK;
 constexpr int kMaxRing = 8;
@@ -71,6 +77,8 @@ constexpr int kStageSlices = 8;              // K-slices (256 inputs each) per g
 constexpr int kMaxTilesF = 160;
 constexpr int kStampsPerCta = 16;
 constexpr int kMaxDI = 4;                    // down items per warp per stage
+constexpr int kPartStride = 264;             // floats per warp partial (256 + 8: banks of the
+                                             // four warps a reducing lane sums do not collide)
 constexpr unsigned long long kWaitNs = 1000000000ull;  // 1 s bound on any wait
 
 __device__ __forceinline__ unsigned long long globaltimer() {
@@ -102,12 +110,21 @@ __device__ __forceinline__ void mma_word(float (&acc)[4], uint32_t wg, uint32_t 
     ptx::mma_bf16_16816(acc, a1, v.z, v.w);
 }
 
-__device__ __forceinline__ float sum_bf16x8(uint4 v) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    float s = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) s += __uint_as_float(w[i] << 16) + __uint_as_float(w[i] & 0xFFFF0000u);
-    return s;
+// f16 variant: f16 carries 10 mantissa bits, so both nibbles of a byte are
+// codes as they sit: OR-ing 0x6400 (1024.0) onto bits 0..3 gives 1024 + q and
+// onto bits 4..7 gives 1024 + 16 q. One shift by 8 brings the odd bytes down.
+// The activations of the 16 q positions (inputs 8i+1, 3, 5, 7) are staged
+// divided by 16, so every product is (1024 m + q) x / m with m = 1 or 16, and
+// per group sum((1024 + m q) x / m) = 1024 * sum(x / m) + sum(q x).
+__device__ __forceinline__ uint32_t code_lo(uint32_t w) { return (w & 0x000F000Fu) | 0x64006400u; }
+__device__ __forceinline__ uint32_t code_hi(uint32_t w) { return (w & 0x00F000F0u) | 0x64006400u; }
+
+__device__ __forceinline__ void mma_word_f16(float (&acc)[4], uint32_t wg, uint32_t wg8, uint4 v) {
+    uint32_t a0[4] = {code_lo(wg), code_lo(wg8), code_hi(wg), code_hi(wg8)};
+    ptx::mma_f16_16816(acc, a0, v.x, v.y);
+    const uint32_t s8 = wg >> 8, t8 = wg8 >> 8;
+    uint32_t a1[4] = {code_lo(s8), code_lo(t8), code_hi(s8), code_hi(t8)};
+    ptx::mma_f16_16816(acc, a1, v.z, v.w);
 }
 
 __device__ __forceinline__ void load8f(const void *p, size_t i, int dtype, float (&v)[8]) {
@@ -143,14 +160,16 @@ __device__ __forceinline__ int h_pos(int f) {
 }
 
 struct Smem {
-    uint64_t *full;
+    uint64_t *full, *empty;  // ring slots: data landed / consumed by every consumer warp
+    uint64_t *pfull, *pempty;  // gate/up partial buffers: all partials written / reduced
     int *misc;             // [0] abort [1] barrier ok [2] U [3] tiles [4] b0 [5] b1
-                           // [6] stages issued
+                           // [6] stages issued [8..9] partials written [10..11] shares reduced
                            // [16..23] stage release counts [24..39] grouping scans
     unsigned long long *s_mask;
     int *s_idx, *s_st, *s_sk, *s_of, *s_counts, *s_off, *s_unique;
     float *s_w, *slot_w;
-    int4 *tiles;           // (u, f0 of the box within the expert, valid lo, valid hi)
+    int4 *tiles;           // per tile: (u, f0 of the box within the expert, valid lo, valid hi),
+                           // then (expert, token mask, first slot, 0)
     unsigned char *xs;
     float *xsum;
     float *red;            // gate/up partials [2][kCW][32][8]; router / final scratch
@@ -160,6 +179,9 @@ struct Smem {
 __device__ __forceinline__ Smem carve_smem(unsigned char *base, const DecodeLayout &L, int E) {
     Smem s;
     s.full = reinterpret_cast<uint64_t *>(base + L.off_bar);
+    s.empty = s.full + kMaxRing;
+    s.pfull = s.full + 2 * kMaxRing;
+    s.pempty = s.pfull + 2;
     s.misc = reinterpret_cast<int *>(base + L.off_misc);
     unsigned char *r = base + L.off_route;
     s.s_mask = reinterpret_cast<unsigned long long *>(r);
@@ -208,10 +230,14 @@ __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, volat
 // Grid-wide barrier of all threads. The arrival counter only grows, by G per
 // barrier and 2G per launch; `target` is its value once every CTA has arrived
 // (the launch's base value plus G or 2G).
+__device__ __forceinline__ void cta_sync(bool consumers_only) {
+    if (consumers_only) ptx::named_bar(1, kConsThreads); else __syncthreads();
+}
+
 __device__ __forceinline__ bool grid_barrier(unsigned long long *cnt, unsigned long long target,
                                              volatile int *flag_ok, volatile int *abort_flag,
-                                             unsigned *status) {
-    __syncthreads();
+                                             unsigned *status, bool consumers_only = false) {
+    cta_sync(consumers_only);
     if (threadIdx.x == 0) {
         int ok = 1;
         __threadfence();
@@ -228,7 +254,7 @@ __device__ __forceinline__ bool grid_barrier(unsigned long long *cnt, unsigned l
         }
         *flag_ok = ok;
     }
-    __syncthreads();
+    cta_sync(consumers_only);
     return *flag_ok != 0;
 }
 
@@ -242,6 +268,12 @@ struct DecodeArgs {
     Workspace ws;
     DecodeLayout L;
 };
+
+// routing facts a tile's reduction needs: expert, token mask, first slot
+__device__ __forceinline__ int4 tile_route(const Smem &S, int u) {
+    const int e = S.s_unique[u];
+    return make_int4(e, (int)(unsigned)S.s_mask[e], S.s_off[e], 0);
+}
 
 // one gate/up tile: valid rows [v0, v1) of the concatenated U*Dff row space
 __device__ __forceinline__ int4 make_tile(int v0, int v1, int F) {
@@ -343,7 +375,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     unsigned long long epoch = 0;
     if (tid == 0) {
         epoch = ptx::ld_acquire_gpu_u64(gsync);
-        for (int s = 0; s < L.NS; ++s) ptx::mbar_init(&S.full[s], 1);
+        for (int s = 0; s < L.NS; ++s) {
+            ptx::mbar_init(&S.full[s], 1);
+            ptx::mbar_init(&S.empty[s], kCW);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&S.pfull[b], kCW);
+            ptx::mbar_init(&S.pempty[b], 1);
+        }
         for (int i = 0; i < 32; ++i) S.misc[i] = 0;
         ptx::mbar_fence_init();
     }
@@ -359,10 +398,53 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     // ---- phase R: router logits of this CTA's experts, x staging ----------------
     {
         const int nE = (cta < E ? 1 : 0) + (cta + (int)G < E ? 1 : 0);
+        const int chunks = D >> 3;  // 8-input chunks (a multiple of 32, at most kThreads)
         float a0[kNFast], a1[kNFast];
+        float2 xp[kNFast];
 #pragma unroll
-        for (int t = 0; t < kNFast; ++t) a0[t] = a1[t] = 0.f;
-        const int chunks = D >> 3;
+        for (int t = 0; t < kNFast; ++t) {
+            a0[t] = a1[t] = 0.f;
+            xp[t] = make_float2(0.f, 0.f);
+        }
+        // x -> f16 in B-operand order (pairs (0,4) (1,5) (2,6) (3,7) per 8 inputs),
+        // odd inputs divided by 16 (see mma_word_f16); returns the chunk's sums
+        // of x and of x / m as the MMA sees them. Rows of tokens >= n are zero.
+        auto stage = [&](int t, int ch, const float (&v)[8]) {
+            uint16_t b[8];
+            float sm = 0.f, smd = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const __half hv = __float2half_rn((j & 1) ? v[j] * 0.0625f : v[j]);
+                b[j] = __half_as_ushort(hv);
+                const float f = __half2float(hv);
+                smd += f;
+                sm += (j & 1) ? f * 16.f : f;
+            }
+            uint4 o;
+            o.x = (uint32_t)b[0] | ((uint32_t)b[4] << 16);
+            o.y = (uint32_t)b[1] | ((uint32_t)b[5] << 16);
+            o.z = (uint32_t)b[2] | ((uint32_t)b[6] << 16);
+            o.w = (uint32_t)b[3] | ((uint32_t)b[7] << 16);
+            *reinterpret_cast<uint4 *>(S.xs + (size_t)t * L.x_stride + (size_t)ch * 16) = o;
+            return make_float2(sm, smd);
+        };
+        auto stage_zero = [&](int t, int ch) {
+            *reinterpret_cast<uint4 *>(S.xs + (size_t)t * L.x_stride + (size_t)ch * 16) = make_uint4(0, 0, 0, 0);
+        };
+        if (nE == 0 && tid < chunks) {  // no router rows here: stage x on its own
+#pragma unroll
+            for (int t = 0; t < kNFast; ++t) {
+                if (t < n) {
+                    float xv[8];
+                    load8f(A.x, (size_t)t * D + (size_t)tid * 8, A.s.x_dtype, xv);
+                    xp[t] = stage(t, tid, xv);
+                } else {
+                    stage_zero(t, tid);
+                }
+            }
+        }
+        // item i: router row ei (0 or 1) of this CTA, chunk ch; thread tid < chunks
+        // gets chunk tid of row 0 first and stages x from the values it loads
         for (int i = tid; i < nE * chunks; i += kThreads) {
             const int ei = i >= chunks ? 1 : 0;
             const int ch = i - ei * chunks;
@@ -377,8 +459,28 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
                     float d = 0.f;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) d = fmaf(xv[j], wv[j], d);
-                    if (ei) a1[t] += d; else a0[t] += d;
+                    if (ei) {
+                        a1[t] += d;
+                    } else {
+                        a0[t] += d;
+                        xp[t] = stage(t, ch, xv);
+                    }
+                } else if (!ei) {
+                    stage_zero(t, ch);
                 }
+            }
+        }
+        // group sums of x and x/m: the 8 chunks of a group are 8 consecutive threads
+        if (tid < chunks) {
+#pragma unroll
+            for (int t = 0; t < kNFast; ++t) {
+                float2 v = xp[t];
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) {
+                    v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+                    v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+                }
+                if ((lane & 7) == 0) *reinterpret_cast<float2 *>(S.xsum + ((tid >> 3) * kNFast + t) * 2) = v;
             }
         }
         float *rs = S.red;  // [warps][2][8]
@@ -390,40 +492,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
                 rs[(warp * 2 + 1) * kNFast + t] = v1;
             }
         }
-        // x -> bf16 in B-operand order (pairs (0,4) (1,5) (2,6) (3,7) per 8 inputs);
-        // rows of tokens >= n are zero
-        const int words = D / 8;
-        for (int i = tid; i < kNFast * words; i += kThreads) {
-            const int t = i / words, wd = i - t * words;
-            uint4 o = make_uint4(0, 0, 0, 0);
-            if (t < n) {
-                float v[8];
-                load8f(A.x, (size_t)t * D + (size_t)wd * 8, A.s.x_dtype, v);
-                uint16_t b[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) b[j] = f2bf(v[j]);
-                o.x = (uint32_t)b[0] | ((uint32_t)b[4] << 16);
-                o.y = (uint32_t)b[1] | ((uint32_t)b[5] << 16);
-                o.z = (uint32_t)b[2] | ((uint32_t)b[6] << 16);
-                o.w = (uint32_t)b[3] | ((uint32_t)b[7] << 16);
-            }
-            *reinterpret_cast<uint4 *>(S.xs + (size_t)t * L.x_stride + (size_t)wd * 16) = o;
-        }
         __syncthreads();
         if (tid < nE * n) {
             const int ei = tid / n, t = tid - ei * n;
             float l = 0.f;
-            for (int w = 0; w < kCW; ++w) l += rs[(w * 2 + ei) * kNFast + t];
+            for (int w = 0; w < kWarps; ++w) l += rs[(w * 2 + ei) * kNFast + t];
             const int e = cta + ei * (int)G;
             if (A.router_bias) l += A.router_bias[e];
             W.logits[(size_t)t * E + e] = l;
-        }
-        for (int i = tid; i < GD * kNFast; i += kThreads) {
-            const int gg = i / kNFast, t = i - gg * kNFast;
-            const unsigned char *row = S.xs + (size_t)t * L.x_stride + (size_t)gg * 128;
-            float s = 0.f;
-            for (int w = 0; w < 8; ++w) s += sum_bf16x8(*reinterpret_cast<const uint4 *>(row + w * 16));
-            S.xsum[gg * kNFast + t] = s;
         }
     }
 
@@ -531,8 +607,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
             }
             const int pos = tb + inc - c2;
             if (valid && pos + c2 <= L.max_tiles) {
-                S.tiles[pos] = make_tile(a, split ? eb : b, F);
-                if (split) S.tiles[pos + 1] = make_tile(eb, b, F);
+                const int4 t0 = make_tile(a, split ? eb : b, F);
+                S.tiles[2 * pos] = t0;
+                S.tiles[2 * pos + 1] = tile_route(S, t0.x);
+                if (split) {
+                    const int4 t1 = make_tile(eb, b, F);
+                    S.tiles[2 * pos + 2] = t1;
+                    S.tiles[2 * pos + 3] = tile_route(S, t1.x);
+                }
             }
             tb += __shfl_sync(0xffffffffu, inc, 31);
         }
@@ -570,14 +652,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     // The first NS stages are issued here; after that the last warp to release a
     // stage issues the stage NS further on into the freed slot. Called by a whole warp.
     const uint64_t pol = ptx::policy_evict_first();
-    volatile int *rel_cnt = S.misc + 16;
     auto issue_stage = [&](int st) {
         const int slot = st % L.NS;
         unsigned char *buf = S.ring + (size_t)slot * L.stage_bytes;
         uint64_t *bar = &S.full[slot];
         if (st < nA) {
             if (lane == 0) {
-                const int4 tl = S.tiles[st >> tsh];
+                const int4 tl = S.tiles[2 * (st >> tsh)];
                 const int kc = st & tsh;
                 const int row0 = S.s_unique[tl.x] * F + tl.y;  // first row of the box (even)
                 ptx::mbar_arrive_expect_tx(bar, 2u * L.KS * 16u * 128u + 4u * 16u * L.sc_w);
@@ -622,24 +703,81 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
                 }
             }
         }
-        if (lane == 0) atomicMax(S.misc + 6, st + 1);
     };
-    auto release_stage = [&](int st, int slot) {
-        __syncwarp();
-        int last = 0;
-        if (lane == 0)
-            last = ptx::atom_add_acqrel_cta_shared(const_cast<int *>(rel_cnt + slot), 1u) == kCW - 1;
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-            if (lane == 0) {
-                rel_cnt[slot] = 0;
-                ptx::fence_proxy_async_shared();  // the stage's reads before the refill's async writes
+    if (warp >= kCW) {
+        // the fifth warpgroup hands most of its registers to the consumers; its
+        // first warp streams every stage into the ring as slots are released, the
+        // next two reduce the consumers' gate/up partials
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsProducer));
+        if (warp >= kReducer0 + 2) return;
+        if (warp != kProducer) {
+            // Reducer of partial buffer b = warp - kReducer0, i.e. of tiles b, b + 2, ...
+            // Lane l sums fragment lane l's four (row, token) values of the 16
+            // consumer warps in warp order, frees the buffer, then writes
+            // h = w * silu(g) * u as bf16 for the valid (row, token) pairs.
+            const int b = warp - kReducer0;
+            for (int t = b, r = 0; t < nTiles; t += 2, ++r) {
+                if (!__shfl_sync(0xffffffffu, (int)wait_phase(&S.pfull[b], (uint32_t)(r & 1), abort_flag, W.status), 0))
+                    break;
+                const float *q = S.red + (size_t)b * kCW * kPartStride + lane * 4;
+                float4 gs = *reinterpret_cast<const float4 *>(q);
+                float4 us = *reinterpret_cast<const float4 *>(q + 128);
+#pragma unroll
+                for (int w = 1; w < kCW; ++w) {
+                    const float4 a = *reinterpret_cast<const float4 *>(q + (size_t)w * kPartStride);
+                    const float4 u = *reinterpret_cast<const float4 *>(q + (size_t)w * kPartStride + 128);
+                    gs.x += a.x; gs.y += a.y; gs.z += a.z; gs.w += a.w;
+                    us.x += u.x; us.y += u.y; us.z += u.z; us.w += u.w;
+                }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&S.pempty[b], 1);
+                const int4 tl = S.tiles[2 * t], tr = S.tiles[2 * t + 1];
+                const unsigned m = (unsigned)tr.y;
+                const float gv[4] = {gs.x, gs.y, gs.z, gs.w}, uv[4] = {us.x, us.y, us.z, us.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int row = 2 * (lane >> 2) + (i >> 1), tok = 2 * (lane & 3) + (i & 1);
+                    if (row >= tl.z && row < tl.w && ((m >> tok) & 1u)) {
+                        const int pslot = tr.z + __popc(m & ((1u << tok) - 1u));
+                        const float sg = __fdividef(gv[i], 1.0f + __expf(-gv[i]));
+                        Hg[(size_t)pslot * F + h_pos(tl.y + row)] = f2bf(S.slot_w[pslot] * (sg * uv[i]));
+                    }
+                }
             }
-            __syncwarp();
-            if (st + L.NS < total && !*abort_flag) issue_stage(st + L.NS);
+            // every h row of this CTA written: the consumers pass grid barrier 2 after this
+            ptx::named_bar(2, kConsThreads + 64);
+            return;
         }
+        int issued = 0;
+        for (int st = 0; st < total; ++st) {
+            const int slot = st % L.NS, use = st / L.NS;
+            int ok = 1;
+            if (lane == 0 && use > 0) {
+                ok = wait_phase(&S.empty[slot], (use - 1) & 1, abort_flag, W.status);
+                ptx::fence_proxy_async_shared();  // the consumers' reads before the refill's async writes
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            issue_stage(st);
+            issued = st + 1;
+        }
+        if (lane == 0) {
+            // drain: every issued copy must land before the CTA may exit
+            for (int st = max(0, issued - L.NS); st < issued; ++st) {
+                const unsigned long long t0 = globaltimer();
+                while (!ptx::mbar_try_wait(&S.full[st % L.NS], (st / L.NS) & 1))
+                    if (globaltimer() - t0 > kWaitNs) break;
+            }
+        }
+        __syncwarp();
+        return;
+    }
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsConsumer));
+    // a consumer warp is done with a ring stage
+    auto release_stage = [&](int slot) {
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&S.empty[slot], 1);
     };
-    if (warp < min(total, L.NS)) issue_stage(warp);
 
     const int g = lane >> 2, c = lane & 3;
     const int r0 = 2 * g, r1 = 2 * g + 1;  // tile rows of MMA rows g and g + 8
@@ -654,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     const uint32_t sco0 = (uint32_t)(g * L.sc_w), sco1 = (uint32_t)((8 + g) * L.sc_w);
     int pw[NKC];
     uint4 xf[NKC][2][2];
-    float2 xsm[NKC][2];
+    float4 xsm[NKC][2];
 #pragma unroll
     for (int kc = 0; kc < NKC; ++kc) {
         const int nP = min(L.GDc, GD - kc * L.GDc) >> 1;  // group pairs in K chunk kc
@@ -667,14 +805,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
             const unsigned char *xr = S.xs + (size_t)g * L.x_stride + (size_t)gg * 128 + c * 32;
             xf[kc][h2][0] = *reinterpret_cast<const uint4 *>(xr);
             xf[kc][h2][1] = *reinterpret_cast<const uint4 *>(xr + 16);
-            xsm[kc][h2] = *reinterpret_cast<const float2 *>(S.xsum + gg * kNFast + 2 * c);
+            const float2 s0 = *reinterpret_cast<const float2 *>(S.xsum + (gg * kNFast + 2 * c) * 2);
+            const float2 s1 = *reinterpret_cast<const float2 *>(S.xsum + (gg * kNFast + 2 * c + 1) * 2);
+            xsm[kc][h2] = make_float4(s0.x, s1.x, s0.y, s1.y);
         }
     }
     float tg[4] = {0.f, 0.f, 0.f, 0.f}, tu[4] = {0.f, 0.f, 0.f, 0.f};
     for (int t_idx = 0; t_idx < nTiles; ++t_idx) {
 #pragma unroll
         for (int kc = 0; kc < NKC; ++kc) {
-            const int st = t_idx * NKC + kc;
             const unsigned long long tw0 = timing ? globaltimer() : 0ull;
             const bool ok = __shfl_sync(0xffffffffu, (int)wait_phase(&S.full[slot], par, abort_flag, W.status), 0) != 0;
             const unsigned long long tw1 = timing ? globaltimer() : 0ull;
@@ -705,29 +844,30 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
                         const uint2 wu0 = *reinterpret_cast<const uint2 *>(ubx + o0);
                         const uint2 wu1 = *reinterpret_cast<const uint2 *>(ubx + o1);
                         float cg[4] = {0.f, 0.f, 0.f, 0.f}, cu[4] = {0.f, 0.f, 0.f, 0.f};
-                        mma_word(cg, wg0.x, wg1.x, xf[kc][h2][0]);
-                        mma_word(cu, wu0.x, wu1.x, xf[kc][h2][0]);
-                        mma_word(cg, wg0.y, wg1.y, xf[kc][h2][1]);
-                        mma_word(cu, wu0.y, wu1.y, xf[kc][h2][1]);
-                        const float2 xs2 = xsm[kc][h2];
+                        mma_word_f16(cg, wg0.x, wg1.x, xf[kc][h2][0]);
+                        mma_word_f16(cu, wu0.x, wu1.x, xf[kc][h2][0]);
+                        mma_word_f16(cg, wg0.y, wg1.y, xf[kc][h2][1]);
+                        mma_word_f16(cu, wu0.y, wu1.y, xf[kc][h2][1]);
+                        const float4 xs4 = xsm[kc][h2];  // sum x, sum x/m of tokens 2c, 2c+1
                         const float gs0 = bf_half(sw[0], h2), gb0 = bf_half(sw[1], h2);
                         const float us0 = bf_half(sw[2], h2), ub0 = bf_half(sw[3], h2);
                         const float gs1 = bf_half(sw[4], h2), gb1 = bf_half(sw[5], h2);
                         const float us1 = bf_half(sw[6], h2), ub1 = bf_half(sw[7], h2);
-                        const float og0 = fmaf(-128.f, gs0, gb0), og1 = fmaf(-128.f, gs1, gb1);
-                        const float ou0 = fmaf(-128.f, us0, ub0), ou1 = fmaf(-128.f, us1, ub1);
-                        tg[0] = fmaf(gs0, cg[0], fmaf(og0, xs2.x, tg[0]));
-                        tg[1] = fmaf(gs0, cg[1], fmaf(og0, xs2.y, tg[1]));
-                        tg[2] = fmaf(gs1, cg[2], fmaf(og1, xs2.x, tg[2]));
-                        tg[3] = fmaf(gs1, cg[3], fmaf(og1, xs2.y, tg[3]));
-                        tu[0] = fmaf(us0, cu[0], fmaf(ou0, xs2.x, tu[0]));
-                        tu[1] = fmaf(us0, cu[1], fmaf(ou0, xs2.y, tu[1]));
-                        tu[2] = fmaf(us1, cu[2], fmaf(ou1, xs2.x, tu[2]));
-                        tu[3] = fmaf(us1, cu[3], fmaf(ou1, xs2.y, tu[3]));
+                        // row contribution: s * (acc - 1024 * sum(x/m)) + b * sum(x)
+                        const float ng0 = -1024.f * gs0, ng1 = -1024.f * gs1;
+                        const float nu0 = -1024.f * us0, nu1 = -1024.f * us1;
+                        tg[0] = fmaf(gs0, cg[0], fmaf(gb0, xs4.x, fmaf(ng0, xs4.z, tg[0])));
+                        tg[1] = fmaf(gs0, cg[1], fmaf(gb0, xs4.y, fmaf(ng0, xs4.w, tg[1])));
+                        tg[2] = fmaf(gs1, cg[2], fmaf(gb1, xs4.x, fmaf(ng1, xs4.z, tg[2])));
+                        tg[3] = fmaf(gs1, cg[3], fmaf(gb1, xs4.y, fmaf(ng1, xs4.w, tg[3])));
+                        tu[0] = fmaf(us0, cu[0], fmaf(ub0, xs4.x, fmaf(nu0, xs4.z, tu[0])));
+                        tu[1] = fmaf(us0, cu[1], fmaf(ub0, xs4.y, fmaf(nu0, xs4.w, tu[1])));
+                        tu[2] = fmaf(us1, cu[2], fmaf(ub1, xs4.x, fmaf(nu1, xs4.z, tu[2])));
+                        tu[3] = fmaf(us1, cu[3], fmaf(ub1, xs4.y, fmaf(nu1, xs4.w, tu[3])));
                     }
                 }
                 // release the stage (after an abort the stage may still be in flight: keep it)
-                release_stage(st, slot);
+                release_stage(slot);
             }
             if (++slot == L.NS) {
                 slot = 0;
@@ -738,45 +878,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
                 ta_comp += globaltimer() - tw1;
             }
         }
-        // tile done: partials [warp][gate | up][lane][4] into buffer t & 1, then
-        // 128 threads (four warps, rotating) sum the 16 warps in order and write
-        // w * silu(g) * u for the tokens routed to the tile's expert. Buffer t & 1
-        // is written again only after the next tile's barrier, which the reducing
-        // threads reach after their sums.
+        // tile done: this warp's partial [gate | up][lane][4] into buffer t & 1,
+        // once its reducer has read tile t - 2 out of it
         {
-            float *pp4 = S.red + ((size_t)((t_idx & 1) * kCW + warp) * 64 + lane) * 4;
+            const int b = t_idx & 1, r = t_idx >> 1;
+            if (r >= 1)
+                __shfl_sync(0xffffffffu, (int)wait_phase(&S.pempty[b], (uint32_t)((r - 1) & 1), abort_flag, W.status), 0);
+            float *pp4 = S.red + (size_t)(b * kCW + warp) * kPartStride + lane * 4;
             *reinterpret_cast<float4 *>(pp4) = make_float4(tg[0], tg[1], tg[2], tg[3]);
             *reinterpret_cast<float4 *>(pp4 + 128) = make_float4(tu[0], tu[1], tu[2], tu[3]);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&S.pfull[b], 1);
 #pragma unroll
             for (int i = 0; i < 4; ++i) tg[i] = tu[i] = 0.f;
-        }
-        __syncthreads();
-        const int rt = tid - 128 * (t_idx & 3);
-        if (rt >= 0 && rt < 128) {
-            const int l = rt >> 2, i = rt & 3;  // fragment lane and element
-            const float *q = S.red + (size_t)(t_idx & 1) * kCW * 256 + l * 4 + i;
-            float gs = 0.f, us = 0.f;
-#pragma unroll 4
-            for (int w2 = 0; w2 < kCW; ++w2) {
-                gs += q[w2 * 256];
-                us += q[w2 * 256 + 128];
-            }
-            const int4 tl = S.tiles[t_idx];
-            const int e = S.s_unique[tl.x];
-            const unsigned m = (unsigned)S.s_mask[e];
-            const int row = 2 * (l >> 2) + (i >> 1), tok = 2 * (l & 3) + (i & 1);
-            if (row >= tl.z && row < tl.w && ((m >> tok) & 1u)) {
-                const int pslot = S.s_off[e] + __popc(m & ((1u << tok) - 1u));
-                const float sg = __fdividef(gs, 1.0f + __expf(-gs));
-                Hg[(size_t)pslot * F + h_pos(tl.y + row)] = f2bf(S.slot_w[pslot] * (sg * us));
-            }
         }
     }
 
     // ---- grid barrier 2: every h row written ----------------------------------
     stamp(W.phase_ns, timing, 4);
+    ptx::named_bar(2, kConsThreads + 64);  // the reducers have written every h row of this CTA
     if (!((A.s.flags & MOE_FLAG_TEST_STALL) && cta == 0))
-        grid_barrier(gsync, epoch + 2ull * G, bar_ok, abort_flag, W.status);
+        grid_barrier(gsync, epoch + 2ull * G, bar_ok, abort_flag, W.status, true);
     stamp(W.phase_ns, timing, 5);
 
     // ---- phase B: down, all experts summed per warp ----------------------------
@@ -858,7 +980,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
                 }
                 load_h(st + 1, q, hq[q]);
             }
-            release_stage(st, slot);
+            release_stage(slot);
         }
         if (++slot == L.NS) {
             slot = 0;
@@ -885,9 +1007,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
         *reinterpret_cast<float4 *>(red) = make_float4(acc0[0], acc0[1], acc0[2], acc0[3]);
         *reinterpret_cast<float4 *>(red + 4) = make_float4(acc1[0], acc1[1], acc1[2], acc1[3]);
     }
-    __syncthreads();
+    cta_sync(true);
     stamp(W.phase_ns, timing, 6);
-    for (int o = tid; o < n * rowsB; o += kThreads) {
+    for (int o = tid; o < n * rowsB; o += kConsThreads) {
         const int t = o / rowsB, r = o - t * rowsB;
         const int dt = (ndt > 1 && b0 + r >= ds1) ? 1 : 0;
         const int rt = b0 + r - (dt ? ds1 : ds0);
@@ -901,17 +1023,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
             static_cast<uint16_t *>(A.out)[at] = f2bf(v);
     }
     if (timing) {
-        __syncthreads();
+        cta_sync(true);
         stamp(W.phase_ns, timing, 7);
-    }
-    // after an abort, stages may still be in flight: they must land before exit
-    if (*abort_flag && tid == 0) {
-        const int issued = S.misc[6];
-        for (int st = max(0, issued - L.NS); st < issued; ++st) {
-            const unsigned long long t0 = globaltimer();
-            while (!ptx::mbar_try_wait(&S.full[st % L.NS], (st / L.NS) & 1))
-                if (globaltimer() - t0 > kWaitNs) break;
-        }
     }
 }
 
@@ -1001,13 +1114,13 @@ bool fused_layout(const moe_config &c, int num_sms, int max_smem, DecodeLayout *
     L.off_route = off;
     off += round_up(8 * E + 4 * (6 * kMaxSlotsF + E + (E + 1) + E), 128);
     L.off_tiles = off;
-    off += round_up(16 * kMaxTilesF, 128);
+    off += round_up(32 * kMaxTilesF, 128);
     L.off_x = off;
     off += round_up(kNFast * L.x_stride, 128);
     L.off_xsum = off;
-    off += round_up(4 * kNFast * (D / kGroup), 128);
+    off += round_up(8 * kNFast * (D / kGroup), 128);
     L.off_red = off;
-    off += 2 * kCW * 32 * 8 * 4;
+    off += 2 * kCW * kPartStride * 4;
     off = round_up(off, 1024);
     L.off_ring = off;
     const int tail = 2048 + 1024;  // over-read pad of the last stage + base alignment slack
@@ -1027,7 +1140,18 @@ static const void *kernel_for(const DecodeLayout &L) {
 
 cudaError_t fused_prepare(const DecodeLayout &L, int *blocks_per_sm) {
     const void *k = kernel_for(L);
-    cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem_bytes);
+    // the register split inside the kernel hands exactly the launch's registers
+    // (640 threads x 96) from the fifth warpgroup to the consumers; any other
+    // per-thread count at launch would make the split wait forever, so such a
+    // build is declined here
+    cudaFuncAttributes fa{};
+    cudaError_t err = cudaFuncGetAttributes(&fa, k);
+    if (err != cudaSuccess) return err;
+    if (fa.numRegs * kThreads != kRegsConsumer * kConsThreads + kRegsProducer * (kThreads - kConsThreads)) {
+        *blocks_per_sm = 0;
+        return cudaSuccess;
+    }
+    err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem_bytes);
     if (err != cudaSuccess) return err;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, kThreads, (size_t)L.smem_bytes);
 }
