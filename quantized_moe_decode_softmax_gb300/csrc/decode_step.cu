@@ -76,7 +76,7 @@ constexpr int kMaxRing = 8;
 constexpr int kStageSlices = 8;              // K-slices (256 inputs each) per gate/up stage
 constexpr int kMaxTilesF = 160;
 constexpr int kStampsPerCta = 16;
-constexpr int kMaxDI = 4;                    // down items per warp per stage
+constexpr int kMaxDI = 2;                    // down items (unit, group pair) per warp per stage
 constexpr int kPartStride = 264;             // floats per warp partial (256 + 8: banks of the
                                              // four warps a reducing lane sums do not collide)
 constexpr unsigned long long kWaitNs = 1000000000ull;  // 1 s bound on any wait
@@ -168,6 +168,7 @@ struct Smem {
     unsigned long long *s_mask;
     int *s_idx, *s_st, *s_sk, *s_of, *s_counts, *s_off, *s_unique;
     float *s_w, *slot_w;
+    int4 *uroute;          // per selected expert u: (expert, token mask, first slot, 0)
     int4 *tiles;           // per tile: (u, f0 of the box within the expert, valid lo, valid hi),
                            // then (expert, token mask, first slot, 0)
     unsigned char *xs;
@@ -196,6 +197,7 @@ __device__ __forceinline__ Smem carve_smem(unsigned char *base, const DecodeLayo
     s.s_off = ip; ip += E + 1;
     s.s_unique = ip;
     s.tiles = reinterpret_cast<int4 *>(base + L.off_tiles);
+    s.uroute = s.tiles + 2 * kMaxTilesF;
     s.xs = base + L.off_x;
     s.xsum = reinterpret_cast<float *>(base + L.off_xsum);
     s.red = reinterpret_cast<float *>(base + L.off_red);
@@ -558,6 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
         }
     }
     __syncthreads();
+    if (tid < S.misc[2]) S.uroute[tid] = tile_route(S, tid);
     if (tid < Sl) {
         const int t = tid / K, e = S.s_idx[tid];
         const unsigned m = (unsigned)S.s_mask[e];
@@ -903,34 +906,40 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
 
     // ---- phase B: down, all experts summed per warp ----------------------------
     float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
-    // this warp's items of a down stage: item warp + 16 q is (unit j, group gm)
+    // this warp's items of a down stage: item warp + 16 q is (unit j, group pair gp)
+    const int GP = GF >> 1;
     int itj[kMaxDI], itg[kMaxDI];
 #pragma unroll
     for (int q = 0; q < kMaxDI; ++q) {
         const int it = warp + q * kCW;
-        itj[q] = it / GF;
-        itg[q] = it - itj[q] * GF;
+        itj[q] = it / GP;
+        itg[q] = it - itj[q] * GP;
     }
-    const int nItems = L.P * GF;
-    // h of item q of down stage st (written by other CTAs before barrier 2), or 0
-    auto load_h = [&](int st, int q, uint4 (&hv)[2]) {
-        hv[0] = hv[1] = make_uint4(0, 0, 0, 0);
+    const int nItems = L.P * GP;
+    // h of item q of down stage st (written by other CTAs before barrier 2), or 0:
+    // token g's 32 bytes of each group of the pair
+    auto load_h = [&](int st, int q, uint4 (&hv)[4]) {
+        hv[0] = hv[1] = hv[2] = hv[3] = make_uint4(0, 0, 0, 0);
         if (st >= total) return;
         const int jb = (st - nA) * L.P;
         if (warp + q * kCW < nItems && itj[q] < nU - jb) {
-            const int e = S.s_unique[(jb + itj[q]) >> dsh];
-            const unsigned m = (unsigned)S.s_mask[e];
+            const int4 ur = S.uroute[(jb + itj[q]) >> dsh];
+            const unsigned m = (unsigned)ur.y;
             if ((m >> g) & 1u) {
-                const int ps = S.s_off[e] + __popc(m & ((1u << g) - 1u));
+                const int ps = ur.z + __popc(m & ((1u << g) - 1u));
                 const unsigned char *hp = reinterpret_cast<const unsigned char *>(Hg + (size_t)ps * F) +
-                                          (size_t)itg[q] * 128 + c * 32;
+                                          (size_t)itg[q] * 256 + c * 32;
                 hv[0] = ptx::ld_cg_v4(hp);
                 hv[1] = ptx::ld_cg_v4(hp + 16);
+                hv[2] = ptx::ld_cg_v4(hp + 128);
+                hv[3] = ptx::ld_cg_v4(hp + 144);
             }
         }
     };
+    // scale/bias byte offsets of rows 2g and 2g + 1: [row parity][row pair][bytes]
+    const uint32_t rs2 = L.dmode ? (uint32_t)L.rb_d : (uint32_t)(2 * L.rb_d);
     // h fragments of this warp's items, loaded one stage ahead
-    uint4 hq[kMaxDI][2];
+    uint4 hq[kMaxDI][4];
 #pragma unroll
     for (int q = 0; q < kMaxDI; ++q) load_h(nA, q, hq[q]);
     for (int st = nA; st < total; ++st) {
@@ -944,38 +953,62 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
 #pragma unroll
             for (int q = 0; q < kMaxDI; ++q) {
                 if (warp + q * kCW < nItems && itj[q] < nu) {
-                    const int j = itj[q], gm = itg[q];
+                    const int j = itj[q], gp = itg[q];
                     const int dt = (jb + j) & dsh;
                     const int h = dt ? h1 : h0;
                     const unsigned char *ubase = buf + (size_t)j * L.unit_bytes;
-                    const int ks = gm >> 2, chunk = 2 * (gm & 3) + (c >> 1);
-                    const uint32_t oa = swz((uint32_t)((ks * h + r0) * 128 + chunk * 16 + (c & 1) * 8), 7u);
-                    const uint32_t ob = swz((uint32_t)((ks * h + r1) * 128 + chunk * 16 + (c & 1) * 8), 7u);
-                    const uint2 w0 = *reinterpret_cast<const uint2 *>(ubase + oa);
-                    uint2 w1 = *reinterpret_cast<const uint2 *>(ubase + ob);
-                    if (g == 7) w1 = make_uint2(0u, 0u);  // tile row 15: zero codes -> 128 * sum(h)
-                    float cd[4] = {0.f, 0.f, 0.f, 0.f};
-                    mma_word(cd, w0.x, w1.x, hq[q][0]);
-                    mma_word(cd, w0.y, w1.y, hq[q][1]);
-                    const float hs0 = __shfl_sync(0xffffffffu, cd[2], 28 + c);
-                    const float hs1 = __shfl_sync(0xffffffffu, cd[3], 28 + c);
-                    // scales and biases of rows 2g and 2g + 1: [row parity][row pair][bytes]
+                    // codes of rows 2g, 2g + 1 in the 256-input slice of the pair;
+                    // the pair's groups sit in 16-byte chunks ch0 and ch0 + 2
+                    const int rowA = (gp >> 1) * h + r0, rowB = rowA + 1;
+                    const uint32_t ch0 = (uint32_t)(4 * (gp & 1) + (c >> 1));
+                    const uint32_t la = (uint32_t)(rowA * 128 + (c & 1) * 8), lb = (uint32_t)(rowB * 128 + (c & 1) * 8);
+                    const uint32_t xa = (uint32_t)(rowA & 7), xb = (uint32_t)(rowB & 7);
+                    const uint2 wa0 = *reinterpret_cast<const uint2 *>(ubase + la + ((ch0 ^ xa) << 4));
+                    const uint2 wa1 = *reinterpret_cast<const uint2 *>(ubase + la + (((ch0 + 2) ^ xa) << 4));
+                    uint2 wb0 = *reinterpret_cast<const uint2 *>(ubase + lb + ((ch0 ^ xb) << 4));
+                    uint2 wb1 = *reinterpret_cast<const uint2 *>(ubase + lb + (((ch0 + 2) ^ xb) << 4));
+                    if (g == 7) wb0 = wb1 = make_uint2(0u, 0u);  // tile row 15: zero codes -> 128 * sum(h)
+                    float ca[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma_word(ca, wa0.x, wb0.x, hq[q][0]);
+                    mma_word(cb, wa1.x, wb1.x, hq[q][2]);
+                    mma_word(ca, wa0.y, wb0.y, hq[q][1]);
+                    mma_word(cb, wa1.y, wb1.y, hq[q][3]);
+                    const float ha0 = __shfl_sync(0xffffffffu, ca[2], 28 + c);
+                    const float ha1 = __shfl_sync(0xffffffffu, ca[3], 28 + c);
+                    const float hb0 = __shfl_sync(0xffffffffu, cb[2], 28 + c);
+                    const float hb1 = __shfl_sync(0xffffffffu, cb[3], 28 + c);
+                    // one 32-bit word holds the pair's two bf16 scales (or biases)
                     const uint32_t ps = L.dmode ? (uint32_t)(h / 2 * L.rb_d) : (uint32_t)L.rb_d;
-                    const uint32_t rs2 = L.dmode ? (uint32_t)L.rb_d : (uint32_t)(2 * L.rb_d);
-                    const uint32_t cb = (uint32_t)((gm & ~1) * 2);
-                    const uint32_t sa = swz(g * rs2 + cb, (uint32_t)L.sc_md);
-                    const uint32_t sb = swz(ps + g * rs2 + cb, (uint32_t)L.sc_md);
+                    const uint32_t cbo = (uint32_t)(gp * 4);
+                    const uint32_t sa = swz(g * rs2 + cbo, (uint32_t)L.sc_md);
+                    const uint32_t sb = swz(ps + g * rs2 + cbo, (uint32_t)L.sc_md);
                     const unsigned char *scs = ubase + L.unit_sc, *scb = scs + L.unit_sc_stride;
-                    const int wh = gm & 1;
-                    const float s0 = bf_half(lds32(scs + sa), wh), s1 = bf_half(lds32(scs + sb), wh);
-                    const float o0 = fmaf(-128.f, s0, bf_half(lds32(scb + sa), wh)) * 0.0078125f;
-                    const float o1 = fmaf(-128.f, s1, bf_half(lds32(scb + sb), wh)) * 0.0078125f;
-                    const float v0 = fmaf(s0, cd[0], o0 * hs0), v1 = fmaf(s0, cd[1], o0 * hs1);
-                    const float v2 = fmaf(s1, cd[2], o1 * hs0), v3 = fmaf(s1, cd[3], o1 * hs1);
+                    const uint32_t s0w = lds32(scs + sa), s1w = lds32(scs + sb);
+                    const uint32_t b0w = lds32(scb + sa), b1w = lds32(scb + sb);
+                    float v[4];
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const float *cd = hh ? cb : ca;
+                        const float hs0 = hh ? hb0 : ha0, hs1 = hh ? hb1 : ha1;
+                        const float s0 = bf_half(s0w, hh), s1 = bf_half(s1w, hh);
+                        const float o0 = fmaf(-128.f, s0, bf_half(b0w, hh)) * 0.0078125f;
+                        const float o1 = fmaf(-128.f, s1, bf_half(b1w, hh)) * 0.0078125f;
+                        if (hh == 0) {
+                            v[0] = fmaf(s0, cd[0], o0 * hs0);
+                            v[1] = fmaf(s0, cd[1], o0 * hs1);
+                            v[2] = fmaf(s1, cd[2], o1 * hs0);
+                            v[3] = fmaf(s1, cd[3], o1 * hs1);
+                        } else {
+                            v[0] += fmaf(s0, cd[0], o0 * hs0);
+                            v[1] += fmaf(s0, cd[1], o0 * hs1);
+                            v[2] += fmaf(s1, cd[2], o1 * hs0);
+                            v[3] += fmaf(s1, cd[3], o1 * hs1);
+                        }
+                    }
                     if (dt == 0) {
-                        acc0[0] += v0; acc0[1] += v1; acc0[2] += v2; acc0[3] += v3;
+                        acc0[0] += v[0]; acc0[1] += v[1]; acc0[2] += v[2]; acc0[3] += v[3];
                     } else {
-                        acc1[0] += v0; acc1[1] += v1; acc1[2] += v2; acc1[3] += v3;
+                        acc1[0] += v[0]; acc1[1] += v[1]; acc1[2] += v[2]; acc1[3] += v[3];
                     }
                 }
                 load_h(st + 1, q, hq[q]);
@@ -1096,8 +1129,10 @@ bool fused_layout(const moe_config &c, int num_sms, int max_smem, DecodeLayout *
     const int GF = F / kGroup;
     L.P = stage_a / L.unit_bytes;
     if (L.P < 1) L.P = 1;
-    while (L.P > 1 && L.P * GF > kMaxDI * kCW) --L.P;  // items of a stage: at most kMaxDI per warp
-    if (L.P * GF > kMaxDI * kCW) return false;
+    // items (unit, group pair) of a stage: at most kMaxDI per warp
+    if (GF / 2 > kMaxDI * kCW) return false;
+    while (L.P > 1 && L.P * (GF / 2) > kMaxDI * kCW) --L.P;
+    if (L.P * (GF / 2) > kMaxDI * kCW) return false;
     L.stage_bytes = round_up(stage_a > L.P * L.unit_bytes ? stage_a : L.P * L.unit_bytes, 1024);
     // gate/up tiles per CTA: rows ceil(U*F/G) (+2 for even bounds) with U <= min(E, 8k)
     const int Umax = E < kNFast * k ? E : kNFast * k;
@@ -1114,7 +1149,7 @@ bool fused_layout(const moe_config &c, int num_sms, int max_smem, DecodeLayout *
     L.off_route = off;
     off += round_up(8 * E + 4 * (6 * kMaxSlotsF + E + (E + 1) + E), 128);
     L.off_tiles = off;
-    off += round_up(32 * kMaxTilesF, 128);
+    off += round_up(32 * kMaxTilesF + 16 * kMaxSlotsF, 128);
     L.off_x = off;
     off += round_up(kNFast * L.x_stride, 128);
     L.off_xsum = off;
