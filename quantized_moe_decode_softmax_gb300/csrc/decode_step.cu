@@ -311,33 +311,48 @@ __device__ __forceinline__ float key2f(uint32_t k) {
 // the k largest in descending order, ties to the lower expert id, and their
 // renormalised softmax weights. The softmax denominator over all experts cancels
 // in the renormalisation, so only the k selected logits are exponentiated.
+// Each lane first sorts its eight (key, i) pairs (descending key, ascending i);
+// every round then takes the warp maximum of the lanes' heads, the lowest
+// expert id among the lanes holding it, and the winning lane drops its head.
 __device__ __forceinline__ void warp_topk8(const float *lt, int E, int k, int lane, int *idx_out,
                                            float *w_out) {
-    uint32_t key[8];
+    uint32_t key[8], ix[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int e = lane + 32 * i;
         key[i] = e < E ? f2key(__ldcg(lt + e)) : 0u;
+        ix[i] = (uint32_t)i;
     }
-    uint32_t taken = 0;
+    // Batcher's odd-even merge sort of 8 elements (19 compare-exchanges)
+    auto cx = [&](int a, int b) {
+        const bool sw = key[b] > key[a] || (key[b] == key[a] && ix[b] < ix[a]);
+        const uint32_t ka = key[a], ia = ix[a];
+        key[a] = sw ? key[b] : ka;
+        ix[a] = sw ? ix[b] : ia;
+        key[b] = sw ? ka : key[b];
+        ix[b] = sw ? ia : ix[b];
+    };
+    cx(0, 1); cx(2, 3); cx(4, 5); cx(6, 7);
+    cx(0, 2); cx(1, 3); cx(4, 6); cx(5, 7);
+    cx(1, 2); cx(5, 6);
+    cx(0, 4); cx(1, 5); cx(2, 6); cx(3, 7);
+    cx(2, 4); cx(3, 5);
+    cx(1, 2); cx(3, 4); cx(5, 6);
     float lsel = 0.f, lmax = 0.f;
     for (int j = 0; j < k; ++j) {
-        uint32_t bk = 0;
-        int bi = 0;
-        bool have = false;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const bool cand = !((taken >> i) & 1u) && lane + 32 * i < E;
-            if (cand && (!have || key[i] > bk)) {
-                bk = key[i];
-                bi = i;
-                have = true;
-            }
-        }
-        const uint32_t wk = __reduce_max_sync(0xffffffffu, have ? bk : 0u);
-        const uint32_t ce = (have && bk == wk) ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu;
+        const uint32_t wk = __reduce_max_sync(0xffffffffu, key[0]);
+        // a popped-out slot has i = 8: its id lane + 256 loses every tie
+        const uint32_t ce = key[0] == wk ? (uint32_t)lane + 32u * ix[0] : 0xFFFFFFFFu;
         const uint32_t e = __reduce_min_sync(0xffffffffu, ce);
-        if ((int)(e & 31u) == lane) taken |= 1u << (e >> 5);
+        if ((int)(e & 31u) == lane) {
+#pragma unroll
+            for (int i = 0; i < 7; ++i) {
+                key[i] = key[i + 1];
+                ix[i] = ix[i + 1];
+            }
+            key[7] = 0u;
+            ix[7] = 8u;
+        }
         const float l = key2f(wk);
         if (j == 0) lmax = l;
         if (lane == j) {
@@ -398,107 +413,75 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     __syncthreads();
 
     // ---- phase R: router logits of this CTA's experts, x staging ----------------
+    // Thread (token group tg, chunk ch) handles the 8-input chunk ch of tokens
+    // tg, tg + TG, ... : it stages x in shared memory (f16, B-operand order) with
+    // the chunk's sums, and dots the chunk with this CTA's router rows. A warp's
+    // 32 threads share the token, so the per-token sums over chunks are warp
+    // sums, combined over the chunk-warps in a fixed order.
     {
         const int nE = (cta < E ? 1 : 0) + (cta + (int)G < E ? 1 : 0);
-        const int chunks = D >> 3;  // 8-input chunks (a multiple of 32, at most kThreads)
-        float a0[kNFast], a1[kNFast];
-        float2 xp[kNFast];
+        const int chunks = D >> 3;                  // a multiple of 32, at most kThreads
+        const int NW = chunks >> 5;                 // chunk-warps per token
+        const int TG = min(kThreads / chunks, kNFast);
+        float *rs = S.red;                          // [token][router row][chunk-warp]
+        if (tid < TG * chunks) {
+            const int tg = tid / chunks, ch = tid - tg * chunks;
+            float w0[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, w1[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (nE > 0) load8f(A.router_w, (size_t)cta * D + (size_t)ch * 8, A.s.w_dtype, w0);
+            if (nE > 1) load8f(A.router_w, (size_t)(cta + (int)G) * D + (size_t)ch * 8, A.s.w_dtype, w1);
+#pragma unroll 1
+            for (int t = tg; t < n; t += TG) {
+                float xv[8];
+                load8f(A.x, (size_t)t * D + (size_t)ch * 8, A.s.x_dtype, xv);
+                // x -> f16 in B-operand order (pairs (0,4) (1,5) (2,6) (3,7)), odd
+                // inputs divided by 16 (see mma_word_f16); sums of x and of x / m
+                // as the MMA sees them
+                uint16_t b[8];
+                float sm = 0.f, smd = 0.f, d0 = 0.f, d1 = 0.f;
 #pragma unroll
-        for (int t = 0; t < kNFast; ++t) {
-            a0[t] = a1[t] = 0.f;
-            xp[t] = make_float2(0.f, 0.f);
-        }
-        // x -> f16 in B-operand order (pairs (0,4) (1,5) (2,6) (3,7) per 8 inputs),
-        // odd inputs divided by 16 (see mma_word_f16); returns the chunk's sums
-        // of x and of x / m as the MMA sees them. Rows of tokens >= n are zero.
-        auto stage = [&](int t, int ch, const float (&v)[8]) {
-            uint16_t b[8];
-            float sm = 0.f, smd = 0.f;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const __half hv = __float2half_rn((j & 1) ? v[j] * 0.0625f : v[j]);
-                b[j] = __half_as_ushort(hv);
-                const float f = __half2float(hv);
-                smd += f;
-                sm += (j & 1) ? f * 16.f : f;
-            }
-            uint4 o;
-            o.x = (uint32_t)b[0] | ((uint32_t)b[4] << 16);
-            o.y = (uint32_t)b[1] | ((uint32_t)b[5] << 16);
-            o.z = (uint32_t)b[2] | ((uint32_t)b[6] << 16);
-            o.w = (uint32_t)b[3] | ((uint32_t)b[7] << 16);
-            *reinterpret_cast<uint4 *>(S.xs + (size_t)t * L.x_stride + (size_t)ch * 16) = o;
-            return make_float2(sm, smd);
-        };
-        auto stage_zero = [&](int t, int ch) {
-            *reinterpret_cast<uint4 *>(S.xs + (size_t)t * L.x_stride + (size_t)ch * 16) = make_uint4(0, 0, 0, 0);
-        };
-        if (nE == 0 && tid < chunks) {  // no router rows here: stage x on its own
-#pragma unroll
-            for (int t = 0; t < kNFast; ++t) {
-                if (t < n) {
-                    float xv[8];
-                    load8f(A.x, (size_t)t * D + (size_t)tid * 8, A.s.x_dtype, xv);
-                    xp[t] = stage(t, tid, xv);
-                } else {
-                    stage_zero(t, tid);
+                for (int j = 0; j < 8; ++j) {
+                    const __half hv = __float2half_rn((j & 1) ? xv[j] * 0.0625f : xv[j]);
+                    b[j] = __half_as_ushort(hv);
+                    const float f = __half2float(hv);
+                    smd += f;
+                    sm += (j & 1) ? f * 16.f : f;
+                    d0 = fmaf(xv[j], w0[j], d0);
+                    d1 = fmaf(xv[j], w1[j], d1);
                 }
-            }
-        }
-        // item i: router row ei (0 or 1) of this CTA, chunk ch; thread tid < chunks
-        // gets chunk tid of row 0 first and stages x from the values it loads
-        for (int i = tid; i < nE * chunks; i += kThreads) {
-            const int ei = i >= chunks ? 1 : 0;
-            const int ch = i - ei * chunks;
-            const int e = cta + ei * (int)G;
-            float wv[8];
-            load8f(A.router_w, (size_t)e * D + (size_t)ch * 8, A.s.w_dtype, wv);
+                uint4 o;
+                o.x = (uint32_t)b[0] | ((uint32_t)b[4] << 16);
+                o.y = (uint32_t)b[1] | ((uint32_t)b[5] << 16);
+                o.z = (uint32_t)b[2] | ((uint32_t)b[6] << 16);
+                o.w = (uint32_t)b[3] | ((uint32_t)b[7] << 16);
+                *reinterpret_cast<uint4 *>(S.xs + (size_t)t * L.x_stride + (size_t)ch * 16) = o;
+                // group sums: the 8 chunks of a group are 8 consecutive threads
 #pragma unroll
-            for (int t = 0; t < kNFast; ++t) {
-                if (t < n) {
-                    float xv[8];
-                    load8f(A.x, (size_t)t * D + (size_t)ch * 8, A.s.x_dtype, xv);
-                    float d = 0.f;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) d = fmaf(xv[j], wv[j], d);
-                    if (ei) {
-                        a1[t] += d;
-                    } else {
-                        a0[t] += d;
-                        xp[t] = stage(t, ch, xv);
+                for (int off = 1; off < 8; off <<= 1) {
+                    sm += __shfl_xor_sync(0xffffffffu, sm, off);
+                    smd += __shfl_xor_sync(0xffffffffu, smd, off);
+                }
+                if ((lane & 7) == 0) *reinterpret_cast<float2 *>(S.xsum + ((ch >> 3) * kNFast + t) * 2) = make_float2(sm, smd);
+                if (nE > 0) {
+                    d0 = warp_sum(d0);
+                    d1 = warp_sum(d1);
+                    if (lane == 0) {
+                        rs[(t * 2 + 0) * NW + (ch >> 5)] = d0;
+                        rs[(t * 2 + 1) * NW + (ch >> 5)] = d1;
                     }
-                } else if (!ei) {
-                    stage_zero(t, ch);
                 }
             }
         }
-        // group sums of x and x/m: the 8 chunks of a group are 8 consecutive threads
-        if (tid < chunks) {
-#pragma unroll
-            for (int t = 0; t < kNFast; ++t) {
-                float2 v = xp[t];
-#pragma unroll
-                for (int o = 1; o < 8; o <<= 1) {
-                    v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
-                    v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
-                }
-                if ((lane & 7) == 0) *reinterpret_cast<float2 *>(S.xsum + ((tid >> 3) * kNFast + t) * 2) = v;
-            }
-        }
-        float *rs = S.red;  // [warps][2][8]
-#pragma unroll
-        for (int t = 0; t < kNFast; ++t) {
-            const float v0 = warp_sum(a0[t]), v1 = warp_sum(a1[t]);
-            if (lane == 0) {
-                rs[(warp * 2 + 0) * kNFast + t] = v0;
-                rs[(warp * 2 + 1) * kNFast + t] = v1;
-            }
+        // rows of tokens n..7 are zero (the MMA reads all eight token columns)
+        for (int i = tid; i < (kNFast - n) * chunks; i += kThreads) {
+            const int t = n + i / chunks, ch = i - (t - n) * chunks;
+            *reinterpret_cast<uint4 *>(S.xs + (size_t)t * L.x_stride + (size_t)ch * 16) = make_uint4(0, 0, 0, 0);
+            if ((ch & 7) == 0) *reinterpret_cast<float2 *>(S.xsum + ((ch >> 3) * kNFast + t) * 2) = make_float2(0.f, 0.f);
         }
         __syncthreads();
         if (tid < nE * n) {
             const int ei = tid / n, t = tid - ei * n;
             float l = 0.f;
-            for (int w = 0; w < kWarps; ++w) l += rs[(w * 2 + ei) * kNFast + t];
+            for (int w = 0; w < NW; ++w) l += rs[(t * 2 + ei) * NW + w];
             const int e = cta + ei * (int)G;
             if (A.router_bias) l += A.router_bias[e];
             W.logits[(size_t)t * E + e] = l;
@@ -518,79 +501,61 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     if (warp < n) warp_topk8(W.logits + (size_t)warp * E, E, K, lane, S.s_idx + warp * K, S.s_w + warp * K);
     __syncthreads();
     const int Sl = n * K;
-    if (tid < Sl) atomicOr(reinterpret_cast<unsigned int *>(S.s_mask + S.s_idx[tid]), 1u << (tid / K));
-    __syncthreads();
-    // exclusive scans of counts and of (count > 0) over the experts, 32 per warp
-    int *wtot = S.misc + 24;  // [8] slot counts per warp of experts
-    int *utot = S.misc + 32;  // [8] selected experts per warp of experts
-    const int nwE = (E + 31) / 32;
-    int cnt = 0, incl = 0;
-    unsigned ub = 0;
-    if (warp < nwE) {
-        const int e = warp * 32 + lane;
-        cnt = e < E ? __popc((unsigned)S.s_mask[e]) : 0;
-        incl = cnt;
+    // Grouping, slot table and tile list by warp 0 alone (no CTA barrier in
+    // between; __syncwarp orders the warp's shared-memory accesses).
+    if (warp == 0) {
+        for (int i = lane; i < Sl; i += 32)
+            ptx::red_or_shared(S.s_mask + S.s_idx[i], 1u << (i / K));
+        __syncwarp();
+        // counts and exclusive scans over the experts; lane l owns experts
+        // [8 l, 8 l + 8) (E <= 256), so the scans run in expert order
+        int cnt8[8], csum = 0, usum = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = lane * 8 + j;
+            cnt8[j] = e < E ? __popc((unsigned)S.s_mask[e]) : 0;
+            csum += cnt8[j];
+            usum += cnt8[j] > 0 ? 1 : 0;
+        }
+        int cinc = csum, uinc = usum;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        ub = __ballot_sync(0xffffffffu, cnt > 0);
-        if (lane == 31) {
-            wtot[warp] = incl;
-            utot[warp] = __popc(ub);
-        }
-    }
-    __syncthreads();
-    if (warp < nwE) {
-        int base = 0, ubase = 0;
-        for (int w = 0; w < warp; ++w) {
-            base += wtot[w];
-            ubase += utot[w];
-        }
-        const int e = warp * 32 + lane;
-        if (e < E) {
-            S.s_off[e] = base + incl - cnt;
-            S.s_counts[e] = cnt;
-            if (cnt > 0) S.s_unique[ubase + __popc(ub & ((1u << lane) - 1u))] = e;
-            if (e == E - 1) {
-                S.s_off[E] = base + incl;
-                S.misc[2] = ubase + __popc(ub);
+            const int v = __shfl_up_sync(0xffffffffu, cinc, o);
+            const int w = __shfl_up_sync(0xffffffffu, uinc, o);
+            if (lane >= o) {
+                cinc += v;
+                uinc += w;
             }
         }
-    }
-    __syncthreads();
-    if (tid < S.misc[2]) S.uroute[tid] = tile_route(S, tid);
-    if (tid < Sl) {
-        const int t = tid / K, e = S.s_idx[tid];
-        const unsigned m = (unsigned)S.s_mask[e];
-        const int p = S.s_off[e] + __popc(m & ((1u << t) - 1u));
-        S.slot_w[p] = S.s_w[tid];
-        if (cta == 0) {
-            W.topk_idx[tid] = e;
-            W.topk_w[tid] = S.s_w[tid];
-            W.slot_token[p] = t;
-            W.slot_k[p] = tid - t * K;
-            W.slot_of[tid] = p;
+        int cb = cinc - csum, ubs = uinc - usum;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = lane * 8 + j;
+            if (e < E) {
+                S.s_off[e] = cb;
+                S.s_counts[e] = cnt8[j];
+                if (cnt8[j] > 0) S.s_unique[ubs++] = e;
+                cb += cnt8[j];
+            }
         }
-    }
-    if (cta == 0) {
-        const int U0 = S.misc[2];
-        for (int e = tid; e < E; e += kThreads) {
-            W.counts[e] = S.s_counts[e];
-            W.offsets[e] = S.s_off[e];
-            W.unique[e] = e < U0 ? S.s_unique[e] : -1;
+        const int U0 = __shfl_sync(0xffffffffu, uinc, 31);
+        if (lane == 31) {
+            S.s_off[E] = cinc;
+            S.misc[2] = uinc;
         }
-        if (tid == 0) {
-            W.offsets[E] = S.s_off[E];
-            *W.U = U0;
+        __syncwarp();
+        for (int u = lane; u < U0; u += 32) S.uroute[u] = tile_route(S, u);
+        for (int i = lane; i < Sl; i += 32) {
+            const int t = i / K, e = S.s_idx[i];
+            const unsigned m = (unsigned)S.s_mask[e];
+            S.slot_w[S.s_off[e] + __popc(m & ((1u << t) - 1u))] = S.s_w[i];
         }
+        __syncwarp();
     }
-    __syncthreads();
     // gate/up tile list: this CTA's rows [R0, R1) of the U*F row space (even
     // bounds), cut every 16 rows and at expert boundaries
     if (warp == 0) {
-        const int U0 = S.misc[2];
+        const int U0 = S.misc[2];  // written by lane 31 before the __syncwarp above
         const unsigned RP = (unsigned)U0 * (unsigned)F / 2u;
         const int R0 = 2 * (int)(RP * (unsigned)cta / G), R1 = 2 * (int)(RP * (unsigned)(cta + 1) / G);
         const int nsteps = (R1 - R0 + 15) / 16;
@@ -612,11 +577,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
             if (valid && pos + c2 <= L.max_tiles) {
                 const int4 t0 = make_tile(a, split ? eb : b, F);
                 S.tiles[2 * pos] = t0;
-                S.tiles[2 * pos + 1] = tile_route(S, t0.x);
+                S.tiles[2 * pos + 1] = S.uroute[t0.x];
                 if (split) {
                     const int4 t1 = make_tile(eb, b, F);
                     S.tiles[2 * pos + 2] = t1;
-                    S.tiles[2 * pos + 3] = tile_route(S, t1.x);
+                    S.tiles[2 * pos + 3] = S.uroute[t1.x];
                 }
             }
             tb += __shfl_sync(0xffffffffu, inc, 31);
@@ -712,7 +677,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
         // first warp streams every stage into the ring as slots are released, the
         // next two reduce the consumers' gate/up partials
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsProducer));
-        if (warp >= kReducer0 + 2) return;
+        if (warp >= kReducer0 + 2) {
+            if (warp == kReducer0 + 2 && cta == 0) {
+                // the routing tables the host may read back (CTA 0's copy)
+                for (int i = lane; i < n * K; i += 32) {
+                    const int t = i / K, e = S.s_idx[i];
+                    const unsigned m = (unsigned)S.s_mask[e];
+                    const int p = S.s_off[e] + __popc(m & ((1u << t) - 1u));
+                    W.topk_idx[i] = e;
+                    W.topk_w[i] = S.s_w[i];
+                    W.slot_token[p] = t;
+                    W.slot_k[p] = i - t * K;
+                    W.slot_of[i] = p;
+                }
+                for (int e = lane; e < E; e += 32) {
+                    W.counts[e] = S.s_counts[e];
+                    W.offsets[e] = S.s_off[e];
+                    W.unique[e] = e < U ? S.s_unique[e] : -1;
+                }
+                if (lane == 0) {
+                    W.offsets[E] = S.s_off[E];
+                    *W.U = U;
+                }
+            }
+            return;
+        }
         if (warp != kProducer) {
             // Reducer of partial buffer b = warp - kReducer0, i.e. of tiles b, b + 2, ...
             // Lane l sums fragment lane l's four (row, token) values of the 16
@@ -938,6 +927,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     };
     // scale/bias byte offsets of rows 2g and 2g + 1: [row parity][row pair][bytes]
     const uint32_t rs2 = L.dmode ? (uint32_t)L.rb_d : (uint32_t)(2 * L.rb_d);
+    // shared-memory offsets of an item inside a unit of height h: codes of rows
+    // 2g and 2g + 1 for the pair's two groups (16-byte chunks ch0 and ch0 + 2 of
+    // the pair's 256-input slice), then the scale words of the two rows
+    auto item_offsets = [&](int gp, int h, uint32_t (&o)[6]) {
+        const int rowA = (gp >> 1) * h + r0, rowB = rowA + 1;
+        const uint32_t ch0 = (uint32_t)(4 * (gp & 1) + (c >> 1));
+        const uint32_t la = (uint32_t)(rowA * 128 + (c & 1) * 8), lb = (uint32_t)(rowB * 128 + (c & 1) * 8);
+        const uint32_t xa = (uint32_t)(rowA & 7), xb = (uint32_t)(rowB & 7);
+        o[0] = la + ((ch0 ^ xa) << 4);
+        o[1] = la + (((ch0 + 2) ^ xa) << 4);
+        o[2] = lb + ((ch0 ^ xb) << 4);
+        o[3] = lb + (((ch0 + 2) ^ xb) << 4);
+        const uint32_t ps = L.dmode ? (uint32_t)(h / 2 * L.rb_d) : (uint32_t)L.rb_d;
+        const uint32_t cbo = (uint32_t)(gp * 4);
+        o[4] = swz(g * rs2 + cbo, (uint32_t)L.sc_md);
+        o[5] = swz(ps + g * rs2 + cbo, (uint32_t)L.sc_md);
+    };
+    // the same for every stage when the unit is D-tile 0 (the only one for D <= 2048)
+    uint32_t io0[kMaxDI][6];
+#pragma unroll
+    for (int q = 0; q < kMaxDI; ++q) item_offsets(itg[q], h0, io0[q]);
     // h fragments of this warp's items, loaded one stage ahead
     uint4 hq[kMaxDI][4];
 #pragma unroll
@@ -953,20 +963,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
 #pragma unroll
             for (int q = 0; q < kMaxDI; ++q) {
                 if (warp + q * kCW < nItems && itj[q] < nu) {
-                    const int j = itj[q], gp = itg[q];
+                    const int j = itj[q];
                     const int dt = (jb + j) & dsh;
-                    const int h = dt ? h1 : h0;
+                    uint32_t o[6];
+                    if (dt == 0) {
+#pragma unroll
+                        for (int i = 0; i < 6; ++i) o[i] = io0[q][i];
+                    } else {
+                        item_offsets(itg[q], h1, o);
+                    }
                     const unsigned char *ubase = buf + (size_t)j * L.unit_bytes;
-                    // codes of rows 2g, 2g + 1 in the 256-input slice of the pair;
-                    // the pair's groups sit in 16-byte chunks ch0 and ch0 + 2
-                    const int rowA = (gp >> 1) * h + r0, rowB = rowA + 1;
-                    const uint32_t ch0 = (uint32_t)(4 * (gp & 1) + (c >> 1));
-                    const uint32_t la = (uint32_t)(rowA * 128 + (c & 1) * 8), lb = (uint32_t)(rowB * 128 + (c & 1) * 8);
-                    const uint32_t xa = (uint32_t)(rowA & 7), xb = (uint32_t)(rowB & 7);
-                    const uint2 wa0 = *reinterpret_cast<const uint2 *>(ubase + la + ((ch0 ^ xa) << 4));
-                    const uint2 wa1 = *reinterpret_cast<const uint2 *>(ubase + la + (((ch0 + 2) ^ xa) << 4));
-                    uint2 wb0 = *reinterpret_cast<const uint2 *>(ubase + lb + ((ch0 ^ xb) << 4));
-                    uint2 wb1 = *reinterpret_cast<const uint2 *>(ubase + lb + (((ch0 + 2) ^ xb) << 4));
+                    const uint2 wa0 = *reinterpret_cast<const uint2 *>(ubase + o[0]);
+                    const uint2 wa1 = *reinterpret_cast<const uint2 *>(ubase + o[1]);
+                    uint2 wb0 = *reinterpret_cast<const uint2 *>(ubase + o[2]);
+                    uint2 wb1 = *reinterpret_cast<const uint2 *>(ubase + o[3]);
                     if (g == 7) wb0 = wb1 = make_uint2(0u, 0u);  // tile row 15: zero codes -> 128 * sum(h)
                     float ca[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
                     mma_word(ca, wa0.x, wb0.x, hq[q][0]);
@@ -978,10 +988,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
                     const float hb0 = __shfl_sync(0xffffffffu, cb[2], 28 + c);
                     const float hb1 = __shfl_sync(0xffffffffu, cb[3], 28 + c);
                     // one 32-bit word holds the pair's two bf16 scales (or biases)
-                    const uint32_t ps = L.dmode ? (uint32_t)(h / 2 * L.rb_d) : (uint32_t)L.rb_d;
-                    const uint32_t cbo = (uint32_t)(gp * 4);
-                    const uint32_t sa = swz(g * rs2 + cbo, (uint32_t)L.sc_md);
-                    const uint32_t sb = swz(ps + g * rs2 + cbo, (uint32_t)L.sc_md);
+                    const uint32_t sa = o[4], sb = o[5];
                     const unsigned char *scs = ubase + L.unit_sc, *scb = scs + L.unit_sc_stride;
                     const uint32_t s0w = lds32(scs + sa), s1w = lds32(scs + sb);
                     const uint32_t b0w = lds32(scb + sa), b1w = lds32(scb + sb);

@@ -222,6 +222,11 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// 32-bit OR into shared memory (no return value)
+__device__ __forceinline__ void red_or_shared(void *p, uint32_t v) {
+    asm volatile("red.shared.or.b32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+
 // named barrier over `count` threads (a multiple of 32)
 __device__ __forceinline__ void named_bar(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
