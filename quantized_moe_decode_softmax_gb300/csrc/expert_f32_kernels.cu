@@ -49,8 +49,9 @@ __device__ __forceinline__ void deq8(uint32_t q, float s, float b, float (&w)[8]
 constexpr int kTok = 8;  // tokens per register tile
 
 // warp per gate/up row f of expert unique[blockIdx.y]
+// (experts with at least `thr` tokens are left to the tile kernels when thr > 0)
 template <int XT>
-__global__ void __launch_bounds__(256) gateup_f32_kernel(StepArgs a, Workspace ws) {
+__global__ void __launch_bounds__(256) gateup_f32_kernel(StepArgs a, Workspace ws, int thr) {
     const int lane = threadIdx.x & 31;
     const int f = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int u = blockIdx.y;
@@ -58,6 +59,7 @@ __global__ void __launch_bounds__(256) gateup_f32_kernel(StepArgs a, Workspace w
     if (u >= *ws.U || f >= F) return;
     const int e = ws.unique[u];
     const int p_begin = ws.offsets[e], p_end = ws.offsets[e + 1];
+    if (thr > 0 && p_end - p_begin >= thr) return;
     const size_t row = (size_t)e * F + f;
     const uint32_t *gq = a.planes.gate_q + row * (D / 8);
     const uint32_t *uq = a.planes.up_q + row * (D / 8);
@@ -100,7 +102,7 @@ __global__ void __launch_bounds__(256) gateup_f32_kernel(StepArgs a, Workspace w
 }
 
 // warp per down row d of expert unique[blockIdx.y]
-__global__ void __launch_bounds__(256) down_f32_kernel(StepArgs a, Workspace ws) {
+__global__ void __launch_bounds__(256) down_f32_kernel(StepArgs a, Workspace ws, int thr) {
     const int lane = threadIdx.x & 31;
     const int d = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int u = blockIdx.y;
@@ -108,6 +110,7 @@ __global__ void __launch_bounds__(256) down_f32_kernel(StepArgs a, Workspace ws)
     if (u >= *ws.U || d >= D) return;
     const int e = ws.unique[u];
     const int p_begin = ws.offsets[e], p_end = ws.offsets[e + 1];
+    if (thr > 0 && p_end - p_begin >= thr) return;
     const size_t row = (size_t)e * D + d;
     const uint32_t *dq = a.planes.down_q + row * (F / 8);
     const uint16_t *ds = a.planes.down_s + row * (F / kGroup);
@@ -157,20 +160,24 @@ __global__ void combine_kernel(StepArgs a, Workspace ws) {
 
 }  // namespace
 
-cudaError_t launch_experts_f32(const StepArgs &a, const Workspace &ws, cudaStream_t st,
+cudaError_t launch_experts_f32(const StepArgs &a, const Workspace &ws, int tile_thr, cudaStream_t st,
                                int &launched) {
     const int maxU = min(a.s.E, a.s.n * a.s.k);
+    const int thr = tile_thr > 0 && tile_variant_supported(a.s) ? tile_thr : 0;
     dim3 block(256);
+    cudaError_t err;
+    if (thr > 0 && (err = launch_expert_tiles(a, ws, thr, false, st, launched)) != cudaSuccess) return err;
     dim3 g1((a.s.F + 7) / 8, maxU);
     if (a.s.x_dtype == MOE_DTYPE_F32)
-        gateup_f32_kernel<MOE_DTYPE_F32><<<g1, block, 0, st>>>(a, ws);
+        gateup_f32_kernel<MOE_DTYPE_F32><<<g1, block, 0, st>>>(a, ws, thr);
     else
-        gateup_f32_kernel<MOE_DTYPE_BF16><<<g1, block, 0, st>>>(a, ws);
+        gateup_f32_kernel<MOE_DTYPE_BF16><<<g1, block, 0, st>>>(a, ws, thr);
     launched += 1;
-    cudaError_t err = cudaGetLastError();
+    err = cudaGetLastError();
     if (err != cudaSuccess) return err;
+    if (thr > 0 && (err = launch_expert_tiles(a, ws, thr, true, st, launched)) != cudaSuccess) return err;
     dim3 g2((a.s.D + 7) / 8, maxU);
-    down_f32_kernel<<<g2, block, 0, st>>>(a, ws);
+    down_f32_kernel<<<g2, block, 0, st>>>(a, ws, thr);
     launched += 1;
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;

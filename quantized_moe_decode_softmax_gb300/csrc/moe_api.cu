@@ -234,7 +234,9 @@ moe_status moe_decode_forward(moe_plan *plan, const void *x, const void *router_
     } else {
         err = launch_router_logits(a, plan->ws, s, launched);
         if (err == cudaSuccess) err = launch_topk_group(a, plan->ws, s, launched);
-        if (err == cudaSuccess) err = launch_experts_f32(a, plan->ws, s, launched);
+        // the f32 check path keeps every expert on the exact f32 kernels
+        const int thr = (plan->cfg.flags & MOE_FLAG_F32_DEBUG) ? 0 : plan->mma_min_tokens;
+        if (err == cudaSuccess) err = launch_experts_f32(a, plan->ws, thr, s, launched);
     }
     plan->launches += launched;
     plan->last_stream = s;

@@ -17,11 +17,11 @@ F32_DEBUG = 1
 
 
 def _check(shape_name, seed, n, kind="independent", full=False, flags=0, out_dtype=None,
-           tol=None):
+           tol=None, mma_min_tokens=0):
     lay, x = case(shape_name, seed, n, kind, full=full)
     shape = lay.shape
     ref = run_oracle(lay, x)
-    plan = make_plan(shape, flags=flags, out_dtype=out_dtype)
+    plan = make_plan(shape, flags=flags, out_dtype=out_dtype, mma_min_tokens=mma_min_tokens)
     out, routing = run_gpu(plan, device_layer(lay), shape, x)
     assert_routing_equal(routing, ref)
     if tol is None:
@@ -64,6 +64,20 @@ def test_qwen3_large_cohorts(n):
 def test_qwen3_shared_64_tokens_single_expert_set():
     # every token routes to the same 8 experts: per-expert count 64
     _check("qwen3", 2, 64, "shared")
+
+
+@pytest.mark.parametrize("shape_name,seed,n,full", [("qwen3", 2, 16, False), ("e256", 3, 16, False),
+                                                   ("tiny", 0, 12, True)])
+def test_tile_variant_for_every_expert(shape_name, seed, n, full):
+    # mma_min_tokens = 1: every selected expert takes the tile kernels (weights
+    # dequantised to bf16 in shared memory, tensor-core tiles over its tokens)
+    _check(shape_name, seed, n, full=full, mma_min_tokens=1)
+
+
+def test_tile_variant_with_mixed_counts():
+    # threshold 3 on a 64-token cohort: experts with at least 3 tokens take the
+    # tile kernels, the others the GEMV kernels, in the same step
+    _check("qwen3", 2, 64, mma_min_tokens=3)
 
 
 # ---- 256-expert top-6 layer (D=4096, Dff=2048, Zipf router bias) ------------------
