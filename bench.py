@@ -72,8 +72,8 @@ SEEDS = {"qwen3": 1, "e256": 3, "tiny": 0}
 # timed steps' mean unique-expert count (traffic grows with it).
 KERNEL_SOURCES = ("decode_step.cu", "ptx.cuh", "routing.cuh", "moe_internal.h")
 TRAFFIC = {
-    ("qwen3", 1): {"bytes": 22269696 + 1536, "unique": 8, "src": "d3d2e172fd6f51c7"},
-    ("qwen3", 8): {"bytes": 139172352 + 4851200, "unique": 52, "src": "d3d2e172fd6f51c7"},
+    ("qwen3", 1): {"bytes": 21904384 + 0, "unique": 8, "src": "9f497e0f4189a919"},
+    ("qwen3", 8): {"bytes": 138808576 + 4365824, "unique": 52, "src": "9f497e0f4189a919"},
 }
 
 

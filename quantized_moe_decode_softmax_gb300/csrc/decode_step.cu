@@ -1,23 +1,26 @@
 // decode_step.cu -- the decode step for cohorts of up to 8 tokens as one
-// persistent kernel (one CTA per SM, cooperative launch).
+// persistent kernel (one CTA per SM, cooperative launch, 20 warps: warps 0..15
+// consume, warp 16 produces, warps 17 and 18 reduce, warp 19 copies routing
+// tables out; after routing a setmaxnreg split gives the consumers 112 registers).
 //
 // Phases inside one launch:
 //   R  router GEMV: logits[t, e] = x[t] . Wr[e] (+ bias). Each CTA owns at most
 //      two experts (e = cta, cta + G). Every CTA also stages x in shared memory
-//      as bf16 in the B-operand order of the tensor-core MMA, with per-group
+//      as f16 in the B-operand order of the tensor-core MMA, with per-group
 //      sums of x.                                            -> grid barrier 1
 //   T  every CTA reads the logits and computes softmax, top-k, renormalised
 //      weights and the grouping by expert itself (the same deterministic result
-//      in every CTA, so there is no second exchange).
+//      in every CTA, so there is no second exchange); one warp builds the
+//      grouping, the slot table and the CTA's gate/up tile list.
 //   A  gate/up: the U * Dff (gate row, up row) pairs of the selected experts are
 //      split evenly over the CTAs; each CTA cuts its share into 16-row tiles.
-//      A producer warp streams each tile with two 3-D TMA copies (gate and up
-//      codes, 128-byte swizzle) and cp.async copies of the tile's scales and
-//      biases into a shared-memory ring. All 16 consumer warps work on every
-//      stage, each on its own share of the K (input) groups, running m16n8k16
-//      MMAs on the raw 4-bit codes; the last warp to finish a tile sums the 16
-//      partials in warp order and writes w * silu(g) * u as bf16 to global
-//      memory, one row per (token, expert) slot.            -> grid barrier 2
+//      The producer warp streams each tile (gate and up codes over all inputs,
+//      and the tile's scales and biases) with 3-D TMA copies (128-byte swizzle)
+//      into a shared-memory ring. All 16 consumer warps work on every stage,
+//      each on its own pair of input groups, running m16n8k16 MMAs on the raw
+//      4-bit codes; each warp writes its partial sums to one of two buffers and
+//      a reducer warp sums the 16 partials in warp order and writes
+//      w * silu(g) * u as bf16, one row per (token, expert) slot. -> barrier 2
 //   B  down + combine: each CTA owns a slice of the D output rows for every
 //      selected expert. The down codes stream into the same ring (issued as soon
 //      as ring stages free up, before barrier 2); because the routing weight is
@@ -33,14 +36,18 @@
 //   #1859 "perf(moe): attribute the MoE decode gap at the M = 1 expert gather",
 //     Problem / Background - the per-(token, k) gather this replaces.
 //
-// Numerics. Codes enter the MMA as exact bf16 integers 128 + q (a magic-exponent
-// bit trick, two codes per logic op); products and sums are f32. Per group of 64
-// inputs, acc = sum (128 + q) v, and the row's contribution is
-// s * acc + (b - 128 s) * sum(v). For gate/up, sum(v) is the staged group sum of
-// x. For down, tile row 15 is fed zero codes, so its MMA row returns 128 * sum(h)
-// for free. Activations enter the MMA as bf16 (x, and w * silu(g) * u), so this
-// path is held to the bf16 tolerance; the f32 check path keeps every product in
-// f32. Every reduction has a fixed order: results are bitwise reproducible.
+// Numerics. Codes enter the MMA as exact integers through magic-exponent bit
+// tricks, two codes per logic op; products and sums are f32.
+//   gate/up (f16): OR-ing 1024 onto a code nibble gives 1024 + q (low nibble) or
+//     1024 + 16 q (high nibble) with no shift; x is staged with the inputs of the
+//     high nibbles divided by 16, so per group sum((1024 + m q) x / m) =
+//     1024 sum(x / m) + sum(q x), and the row's contribution is
+//     s * (acc - 1024 sum(x / m)) + b * sum(x).
+//   down (bf16): 128 + q, row contribution s * acc + (b - 128 s) * sum(h); tile
+//     row 15 is fed zero codes, so its MMA row returns 128 * sum(h) for free.
+// x enters the MMA as f16 (|x| < 65504 is assumed) and h as bf16, so this path
+// is held to the bf16 tolerance; the f32 check path keeps every product in f32.
+// Every reduction has a fixed order: results are bitwise reproducible.
 //
 // MMA row mapping. Lane (g, c) of a warp holds MMA rows g and g + 8; they map to
 // tile rows 2g and 2g + 1, so the eight rows a warp reads at once sit in eight
