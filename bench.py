@@ -72,8 +72,8 @@ SEEDS = {"qwen3": 1, "e256": 3, "tiny": 0}
 # timed steps' mean unique-expert count (traffic grows with it).
 KERNEL_SOURCES = ("decode_step.cu", "ptx.cuh", "routing.cuh", "moe_internal.h")
 TRAFFIC = {
-    ("qwen3", 1): {"bytes": 21904384 + 0, "unique": 8, "src": "9f497e0f4189a919"},
-    ("qwen3", 8): {"bytes": 138808576 + 4365824, "unique": 52, "src": "9f497e0f4189a919"},
+    ("qwen3", 1): {"bytes": 22271744 + 0, "unique": 8, "src": "5ac8d54a51eae8b7"},
+    ("qwen3", 8): {"bytes": 139173888 + 4578304, "unique": 52, "src": "5ac8d54a51eae8b7"},
 }
 
 
