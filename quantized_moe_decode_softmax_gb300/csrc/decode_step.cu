@@ -223,9 +223,9 @@ __device__ __forceinline__ void set_timeout(volatile int *abort_flag, unsigned *
 // GB300: four polling warps slow sixteen MMA warps by ~40 %, suspended ones by
 // nothing).
 constexpr uint32_t kSuspendNs = 20000;
-__device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                           unsigned *status) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+// the slow path stays out of line, so the hot loops that wait keep a short body
+__device__ __noinline__ bool wait_phase_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                             unsigned *status) {
     const unsigned long long t0 = globaltimer();
     for (;;) {
         if (ptx::mbar_try_wait_hint(bar, parity, kSuspendNs)) return true;
@@ -235,6 +235,11 @@ __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, volat
             return false;
         }
     }
+}
+__device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                           unsigned *status) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    return wait_phase_slow(bar, parity, abort_flag, status);
 }
 
 // Grid-wide barrier of all threads. The arrival counter only grows, by G per
