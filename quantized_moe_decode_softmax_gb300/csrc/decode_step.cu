@@ -352,6 +352,7 @@ __device__ __forceinline__ void warp_topk8(const float *lt, int E, int k, int la
     cx(2, 4); cx(3, 5);
     cx(1, 2); cx(3, 4); cx(5, 6);
     float lsel = 0.f, lmax = 0.f;
+#pragma unroll 1
     for (int j = 0; j < k; ++j) {
         const uint32_t wk = __reduce_max_sync(0xffffffffu, key[0]);
         // a popped-out slot has i = 8: its id lane + 256 loses every tie
@@ -422,6 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
         for (const CUtensorMap *m : maps) ptx::prefetch_tensormap(m);
     }
     // zero the expert token masks (grouping below)
+#pragma unroll 1
     for (int e = tid; e < E; e += kThreads) S.s_mask[e] = 0ull;
     __syncthreads();
 
@@ -485,6 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
             }
         }
         // rows of tokens n..7 are zero (the MMA reads all eight token columns)
+#pragma unroll 1
         for (int i = tid; i < (kNFast - n) * chunks; i += kThreads) {
             const int t = n + i / chunks, ch = i - (t - n) * chunks;
             *reinterpret_cast<uint4 *>(S.xs + (size_t)t * L.x_stride + (size_t)ch * 16) = make_uint4(0, 0, 0, 0);
@@ -494,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
         if (tid < nE * n) {
             const int ei = tid / n, t = tid - ei * n;
             float l = 0.f;
+#pragma unroll 1
             for (int w = 0; w < NW; ++w) l += rs[(t * 2 + ei) * NW + w];
             const int e = cta + ei * (int)G;
             if (A.router_bias) l += A.router_bias[e];
@@ -517,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     // Grouping, slot table and tile list by warp 0 alone (no CTA barrier in
     // between; __syncwarp orders the warp's shared-memory accesses).
     if (warp == 0) {
+#pragma unroll 1
         for (int i = lane; i < Sl; i += 32)
             ptx::red_or_shared(S.s_mask + S.s_idx[i], 1u << (i / K));
         __syncwarp();
@@ -557,7 +562,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
             S.misc[2] = uinc;
         }
         __syncwarp();
+#pragma unroll 1
         for (int u = lane; u < U0; u += 32) S.uroute[u] = tile_route(S, u);
+#pragma unroll 1
         for (int i = lane; i < Sl; i += 32) {
             const int t = i / K, e = S.s_idx[i];
             const unsigned m = (unsigned)S.s_mask[e];
@@ -573,6 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
         const int R0 = 2 * (int)(RP * (unsigned)cta / G), R1 = 2 * (int)(RP * (unsigned)(cta + 1) / G);
         const int nsteps = (R1 - R0 + 15) / 16;
         int tb = 0;
+#pragma unroll 1
         for (int m0 = 0; m0 < nsteps; m0 += 32) {
             const int m = m0 + lane;
             const bool valid = m < nsteps;
@@ -656,6 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
             const int nu = min(L.P, nU - jb);
             if (lane == 0) {
                 uint32_t bytes = 0;
+#pragma unroll 1
                 for (int j = 0; j < nu; ++j)
                     bytes += (uint32_t)(((jb + j) & dsh) ? h1 : h0) *
                              (uint32_t)(L.sl_d * L.kw_d * 4 + 2 * L.rb_d);
@@ -693,6 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
         if (warp >= kReducer0 + 2) {
             if (warp == kReducer0 + 2 && cta == 0) {
                 // the routing tables the host may read back (CTA 0's copy)
+#pragma unroll 1
                 for (int i = lane; i < n * K; i += 32) {
                     const int t = i / K, e = S.s_idx[i];
                     const unsigned m = (unsigned)S.s_mask[e];
@@ -703,6 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
                     W.slot_k[p] = i - t * K;
                     W.slot_of[i] = p;
                 }
+#pragma unroll 1
                 for (int e = lane; e < E; e += 32) {
                     W.counts[e] = S.s_counts[e];
                     W.offsets[e] = S.s_off[e];
@@ -768,6 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
         }
         if (lane == 0) {
             // drain: every issued copy must land before the CTA may exit
+#pragma unroll 1
             for (int st = max(0, issued - L.NS); st < issued; ++st) {
                 const unsigned long long t0 = globaltimer();
                 while (!ptx::mbar_try_wait(&S.full[st % L.NS], (st / L.NS) & 1))
@@ -1062,6 +1074,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     }
     cta_sync(true);
     stamp(W.phase_ns, timing, 6);
+#pragma unroll 1
     for (int o = tid; o < n * rowsB; o += kConsThreads) {
         const int t = o / rowsB, r = o - t * rowsB;
         const int dt = (ndt > 1 && b0 + r >= ds1) ? 1 : 0;
