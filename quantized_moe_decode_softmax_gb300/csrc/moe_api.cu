@@ -217,12 +217,23 @@ moe_status moe_decode_forward(moe_plan *plan, const void *x, const void *router_
     a.out = out;
 
     bool fused = plan->fused_ok && n_tokens <= fused_max_tokens();
-    if (fused && (!plan->tm_valid || memcmp(&plan->tm_planes, planes, sizeof *planes) != 0)) {
-        // tensor maps describe the plane pointers: re-encode when they change
-        plan->tm_valid = fused_encode_tmaps(plan->cfg, plan->fused, *planes, &plan->tmaps);
-        if (plan->tm_valid) plan->tm_planes = *planes;
-        else if (trace_enabled(plan)) fprintf(stderr, "[moe] tensor map encoding failed\n");
-        fused = plan->tm_valid;
+    const moe::TMaps *tm = nullptr;
+    if (fused) {
+        // tensor maps describe the plane pointers: reuse the cached ones for
+        // these planes, else encode into the next cache entry
+        for (int i = 0; i < moe_plan::kTmCache && !tm; ++i) {
+            const moe_plan::TmEntry &en = plan->tm_cache[i];
+            if (en.valid && memcmp(&en.planes, planes, sizeof *planes) == 0) tm = &en.tmaps;
+        }
+        if (!tm) {
+            moe_plan::TmEntry &en = plan->tm_cache[plan->tm_next];
+            plan->tm_next = (plan->tm_next + 1) % moe_plan::kTmCache;
+            en.valid = fused_encode_tmaps(plan->cfg, plan->fused, *planes, &en.tmaps);
+            en.planes = *planes;
+            if (en.valid) tm = &en.tmaps;
+            else if (trace_enabled(plan)) fprintf(stderr, "[moe] tensor map encoding failed\n");
+        }
+        fused = tm != nullptr;
     }
     if (trace_enabled(plan))
         fprintf(stderr, "[moe] forward n=%d E=%d k=%d D=%d Dff=%d path=%s\n", n_tokens,
@@ -230,7 +241,7 @@ moe_status moe_decode_forward(moe_plan *plan, const void *x, const void *router_
     int launched = 0;
     cudaError_t err;
     if (fused) {
-        err = launch_fused(a, plan->ws, plan->fused, plan->tmaps, s, launched);
+        err = launch_fused(a, plan->ws, plan->fused, *tm, s, launched);
     } else {
         err = launch_router_logits(a, plan->ws, s, launched);
         if (err == cudaSuccess) err = launch_topk_group(a, plan->ws, s, launched);

@@ -117,9 +117,16 @@ struct moe_plan {
     unsigned long long launches;  // kernels enqueued by this plan since creation
     bool fused_ok;                // the single-launch kernel can run this shape
     moe::DecodeLayout fused;
-    moe_expert_planes tm_planes;  // planes the cached tensor maps describe
-    bool tm_valid;
-    moe::TMaps tmaps;
+    // tensor maps of recently used plane sets (a layer stack or replicas cycle
+    // through several), replaced round robin
+    struct TmEntry {
+        moe::TMaps tmaps;             // first: 64-byte aligned members
+        moe_expert_planes planes;     // the planes these maps describe
+        bool valid;
+    };
+    static constexpr int kTmCache = 64;
+    TmEntry tm_cache[kTmCache];
+    int tm_next;
 };
 
 namespace moe {
