@@ -290,13 +290,6 @@ __device__ __forceinline__ int4 tile_route(const Smem &S, int u) {
     return make_int4(e, (int)(unsigned)S.s_mask[e], S.s_off[e], 0);
 }
 
-// one gate/up tile: valid rows [v0, v1) of the concatenated U*Dff row space
-__device__ __forceinline__ int4 make_tile(int v0, int v1, int F) {
-    const int u = v0 / F, es = u * F;
-    const int r0 = min(v0, max(es, v1 - 16));  // 16-row box inside the expert, covering [v0, v1)
-    return make_int4(u, r0 - es, v0 - r0, v1 - r0);
-}
-
 // D-tile `dt` of a CTA's D rows [b0, b0 + 2 pp) (pp row pairs, ndt tiles):
 // first row and height (both even)
 __device__ __forceinline__ void d_tile(int b0, int pp, int ndt, int dt, int &start, int &h) {
@@ -572,40 +565,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
         }
         __syncwarp();
     }
-    // gate/up tile list: this CTA's rows [R0, R1) of the U*F row space (even
-    // bounds), cut every 16 rows and at expert boundaries
+    // gate/up tile list: the U*F rows of the selected experts in 16-row blocks
+    // (Dff is a multiple of 16, so no block straddles two experts), split evenly
+    // over the CTAs by whole blocks: every tile is a full 16 rows, and no CTA
+    // takes more than one block above the mean
     if (warp == 0) {
         const int U0 = S.misc[2];  // written by lane 31 before the __syncwarp above
-        const unsigned RP = (unsigned)U0 * (unsigned)F / 2u;
-        const int R0 = 2 * (int)(RP * (unsigned)cta / G), R1 = 2 * (int)(RP * (unsigned)(cta + 1) / G);
-        const int nsteps = (R1 - R0 + 15) / 16;
-        int tb = 0;
+        const unsigned NB = (unsigned)U0 * (unsigned)(F / 16);
+        const int B0 = (int)(NB * (unsigned)cta / G), B1 = (int)(NB * (unsigned)(cta + 1) / G);
+        int tb = B1 - B0;
 #pragma unroll 1
-        for (int m0 = 0; m0 < nsteps; m0 += 32) {
-            const int m = m0 + lane;
-            const bool valid = m < nsteps;
-            const int a = R0 + 16 * m, b = min(a + 16, R1);
-            const int eb = (a / F + 1) * F;
-            const bool split = valid && eb < b;
-            const int c2 = valid ? 1 + (split ? 1 : 0) : 0;
-            int inc = c2;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, inc, o);
-                if (lane >= o) inc += v;
-            }
-            const int pos = tb + inc - c2;
-            if (valid && pos + c2 <= L.max_tiles) {
-                const int4 t0 = make_tile(a, split ? eb : b, F);
-                S.tiles[2 * pos] = t0;
-                S.tiles[2 * pos + 1] = S.uroute[t0.x];
-                if (split) {
-                    const int4 t1 = make_tile(eb, b, F);
-                    S.tiles[2 * pos + 2] = t1;
-                    S.tiles[2 * pos + 3] = S.uroute[t1.x];
-                }
-            }
-            tb += __shfl_sync(0xffffffffu, inc, 31);
+        for (int b = lane; b < min(tb, L.max_tiles); b += 32) {
+            const int r = 16 * (B0 + b), u = r / F;
+            S.tiles[2 * b] = make_int4(u, r - u * F, 0, 16);
+            S.tiles[2 * b + 1] = S.uroute[u];
         }
         if (lane == 0) {
             if (tb > L.max_tiles) {
