@@ -21,6 +21,8 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libmoe_decode.so")
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
+# translation units whose kernels move registers between warpgroups (setmaxnreg)
+SPLIT_SOURCES = ("decode_step.cu",)
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE,
           "--expt-relaxed-constexpr"]
 
@@ -58,10 +60,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
 
     def compile_one(src):
         obj = os.path.join(BUILD_DIR, os.path.basename(src).replace(".cu", ".o"))
-        cmd = [nvcc, *flags, "-c", src, "-o", obj]
+        split = os.path.basename(src) in SPLIT_SOURCES
+        cmd = [nvcc, *flags, *(["-Xptxas", "-v"] if split else []), "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+        if split and "setmaxnreg' ignored" in r.stdout + r.stderr:
+            # the kernel would run, but every warp would keep the launch's
+            # register count instead of the consumer / producer split
+            raise RuntimeError(f"ptxas dropped the setmaxnreg register split of {src}")
         if verbose and (r.stdout or r.stderr):
             sys.stderr.write(r.stdout + r.stderr)
         return obj

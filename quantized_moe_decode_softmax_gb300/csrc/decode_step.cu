@@ -223,9 +223,8 @@ __device__ __forceinline__ void set_timeout(volatile int *abort_flag, unsigned *
 // GB300: four polling warps slow sixteen MMA warps by ~40 %, suspended ones by
 // nothing).
 constexpr uint32_t kSuspendNs = 20000;
-// the slow path stays out of line, so the hot loops that wait keep a short body
-__device__ __noinline__ bool wait_phase_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                             unsigned *status) {
+__device__ __forceinline__ bool wait_phase_loop(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                                unsigned *status) {
     const unsigned long long t0 = globaltimer();
     for (;;) {
         if (ptx::mbar_try_wait_hint(bar, parity, kSuspendNs)) return true;
@@ -236,10 +235,23 @@ __device__ __noinline__ bool wait_phase_slow(uint64_t *bar, uint32_t parity, vol
         }
     }
 }
+// Consumer warps: the slow path stays out of line, so the hot loops that wait
+// keep a short body.
+__device__ __noinline__ bool wait_phase_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                             unsigned *status) {
+    return wait_phase_loop(bar, parity, abort_flag, status);
+}
 __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                            unsigned *status) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     return wait_phase_slow(bar, parity, abort_flag, status);
+}
+// Producer and reducer warps (32 registers after the split) wait inline: a
+// function call made from that region leads ptxas to drop the setmaxnreg split
+// altogether (every warp then keeps 96 registers).
+__device__ __forceinline__ bool wait_phase_inl(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                               unsigned *status) {
+    return wait_phase_loop(bar, parity, abort_flag, status);
 }
 
 // Grid-wide barrier of all threads. The arrival counter only grows, by G per
@@ -706,7 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
             // h = w * silu(g) * u as bf16 for the valid (row, token) pairs.
             const int b = warp - kReducer0;
             for (int t = b, r = 0; t < nTiles; t += 2, ++r) {
-                if (!__shfl_sync(0xffffffffu, (int)wait_phase(&S.pfull[b], (uint32_t)(r & 1), abort_flag, W.status), 0))
+                if (!__shfl_sync(0xffffffffu, (int)wait_phase_inl(&S.pfull[b], (uint32_t)(r & 1), abort_flag, W.status), 0))
                     break;
                 const float *q = S.red + (size_t)b * kCW * kPartStride + lane * 4;
                 float4 gs = *reinterpret_cast<const float4 *>(q);
@@ -742,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
             const int slot = st % L.NS, use = st / L.NS;
             int ok = 1;
             if (lane == 0 && use > 0) {
-                ok = wait_phase(&S.empty[slot], (use - 1) & 1, abort_flag, W.status);
+                ok = wait_phase_inl(&S.empty[slot], (use - 1) & 1, abort_flag, W.status);
                 ptx::fence_proxy_async_shared();  // the consumers' reads before the refill's async writes
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
