@@ -4,7 +4,8 @@
  * One call runs one MoE layer's decode step for a cohort of 1..64 tokens:
  *   1. router GEMV, softmax over all experts, top-k, renormalise the k weights
  *   2. group the n*k (token, rank) slots by expert, de-duplicated, so every
- *      selected expert's planes are streamed from HBM once per step
+ *      selected expert's planes are streamed from HBM once per step (once
+ *      per chunk for cohorts that run in chunks; see moe_decode_forward)
  *   3. per selected expert: h = silu(Wg x) * (Wu x) on affine 4-bit weights
  *   4. y = Wd h, and out[t] = sum_j w[t,j] * y[t,j] in rank order j,
  *      f32 partials with a single final rounding
@@ -78,6 +79,11 @@ enum {
     /* record per-CTA timestamps of the fused kernel's phases (see
      * moe_get_phase_times); costs a few global stores per CTA */
     MOE_FLAG_PHASE_TIMES = 1u << 2,
+    /* cohorts of 9..32 tokens take the grouped multi-kernel path (every
+     * selected expert streamed once per step, tile kernels for experts with
+     * at least mma_min_tokens tokens) instead of chunks of the single-launch
+     * kernel; see moe_decode_forward */
+    MOE_FLAG_GROUPED_COHORTS = 1u << 3,
     /* TEST ONLY: in the fused path, CTA 0 skips the first grid barrier, so
      * every other CTA's bounded wait runs out (about 1 s) and the step ends
      * with MOE_ERR_TIMEOUT reported by moe_plan_check. Output is garbage. */
@@ -143,6 +149,17 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan **out);
  *   top_k       must equal cfg.top_k (checked, INVALID_ARG otherwise)
  *   out         [n_tokens, D] of cfg.out_dtype (device); must not alias x
  *   stream      cudaStream_t, or NULL for the legacy default stream
+ * Paths, chosen on the host from n_tokens and the plan:
+ *   n_tokens 1..8    one launch of the single-launch kernel;
+ *   n_tokens 9..32   balanced chunks of at most 8 tokens, each one launch of
+ *                    the single-launch kernel (an expert picked in several
+ *                    chunks is streamed once per chunk), then one grouping
+ *                    kernel that writes the whole cohort's routing tables;
+ *   n_tokens 33..64, or any n_tokens > 8 with MOE_FLAG_GROUPED_COHORTS:
+ *                    the grouped multi-kernel path (router, top-k and
+ *                    grouping, per-expert tile or GEMV kernels, combine);
+ *   MOE_FLAG_F32_DEBUG, or a shape the single-launch kernel declines:
+ *                    the grouped multi-kernel path with f32 GEMV kernels.
  * Asynchronous. Returns INVALID_ARG before any launch on a bad argument,
  * CUDA if a launch fails. A device-side timeout of the step's internal
  * waits is reported by the NEXT call on the plan, or by moe_plan_check. */

@@ -17,6 +17,7 @@ from ._abi import (  # noqa: F401
     MOE_ERR_TIMEOUT,
     MOE_ERR_UNSUPPORTED,
     MOE_FLAG_F32_DEBUG,
+    MOE_FLAG_GROUPED_COHORTS,
     MOE_FLAG_PHASE_TIMES,
     MOE_FLAG_TEST_STALL,
     MOE_FLAG_TRACE,

@@ -21,6 +21,7 @@ MOE_DTYPE_F32, MOE_DTYPE_BF16 = 0, 1
 MOE_FLAG_F32_DEBUG = 1 << 0
 MOE_FLAG_TRACE = 1 << 1
 MOE_FLAG_PHASE_TIMES = 1 << 2
+MOE_FLAG_GROUPED_COHORTS = 1 << 3
 MOE_FLAG_TEST_STALL = 1 << 8
 
 EXPORTED = (

@@ -36,7 +36,7 @@ moe_status validate_config(const moe_config *c) {
     if (c->E > kMaxE || c->top_k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
     if (c->D % kGroup || c->Dff % kGroup) return MOE_ERR_UNSUPPORTED;
     if (c->flags & ~(unsigned)(MOE_FLAG_F32_DEBUG | MOE_FLAG_TRACE | MOE_FLAG_PHASE_TIMES |
-                               MOE_FLAG_TEST_STALL))
+                               MOE_FLAG_GROUPED_COHORTS | MOE_FLAG_TEST_STALL))
         return MOE_ERR_INVALID_ARG;
     if (c->Dff > kMaxDff || c->D > kMaxD) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
@@ -216,7 +216,13 @@ moe_status moe_decode_forward(moe_plan *plan, const void *x, const void *router_
     a.planes = *planes;
     a.out = out;
 
-    bool fused = plan->fused_ok && n_tokens <= fused_max_tokens();
+    // n <= 8: one single-launch step; 9..kChunkMaxTokens: chunks of at most 8
+    // tokens through it (unless the plan asks for the grouped path); else the
+    // grouped multi-kernel path
+    const int fmax = fused_max_tokens();
+    const bool chunked = n_tokens > fmax && n_tokens <= kChunkMaxTokens &&
+                         !(plan->cfg.flags & MOE_FLAG_GROUPED_COHORTS);
+    bool fused = plan->fused_ok && (n_tokens <= fmax || chunked);
     const moe::TMaps *tm = nullptr;
     if (fused) {
         // tensor maps describe the plane pointers: reuse the cached ones for
@@ -235,13 +241,34 @@ moe_status moe_decode_forward(moe_plan *plan, const void *x, const void *router_
         }
         fused = tm != nullptr;
     }
+    const char *path = !fused ? "grouped" : n_tokens <= fmax ? "fused" : "fused-chunks";
     if (trace_enabled(plan))
         fprintf(stderr, "[moe] forward n=%d E=%d k=%d D=%d Dff=%d path=%s\n", n_tokens,
-                a.s.E, a.s.k, a.s.D, a.s.F, fused ? "fused" : "f32-check");
+                a.s.E, a.s.k, a.s.D, a.s.F, path);
     int launched = 0;
-    cudaError_t err;
-    if (fused) {
+    cudaError_t err = cudaSuccess;
+    if (fused && n_tokens <= fmax) {
         err = launch_fused(a, plan->ws, plan->fused, *tm, s, launched);
+    } else if (fused) {
+        // balanced chunks (sizes differ by at most one token); chunk c reads
+        // and writes its own rows of x, out and the logits, and the grouping
+        // kernel then routes the whole cohort from those logits for
+        // moe_get_routing (the same decisions each chunk took on the device)
+        const int nch = (n_tokens + fmax - 1) / fmax;
+        const size_t xrow = (size_t)a.s.D * elem_size(plan->cfg.x_dtype);
+        const size_t orow = (size_t)a.s.D * elem_size(plan->cfg.out_dtype);
+        for (int c = 0, t0 = 0; c < nch && err == cudaSuccess; ++c) {
+            const int nc = (int)((long long)n_tokens * (c + 1) / nch) - t0;
+            StepArgs ac = a;
+            ac.s.n = nc;
+            ac.x = static_cast<const char *>(x) + (size_t)t0 * xrow;
+            ac.out = static_cast<char *>(out) + (size_t)t0 * orow;
+            Workspace wc = plan->ws;
+            wc.logits = plan->ws.logits + (size_t)t0 * a.s.E;
+            err = launch_fused(ac, wc, plan->fused, *tm, s, launched);
+            t0 += nc;
+        }
+        if (err == cudaSuccess) err = launch_topk_group(a, plan->ws, s, launched);
     } else {
         err = launch_router_logits(a, plan->ws, s, launched);
         if (err == cudaSuccess) err = launch_topk_group(a, plan->ws, s, launched);
@@ -253,8 +280,7 @@ moe_status moe_decode_forward(moe_plan *plan, const void *x, const void *router_
     plan->last_stream = s;
     plan->last_n = n_tokens;
     if (err != cudaSuccess) {
-        fprintf(stderr, "[moe] forward launch failed (%s path): %s\n", fused ? "fused" : "f32-check",
-                cudaGetErrorString(err));
+        fprintf(stderr, "[moe] forward launch failed (%s path): %s\n", path, cudaGetErrorString(err));
         cudaGetLastError();
         return MOE_ERR_CUDA;
     }

@@ -17,6 +17,9 @@ constexpr int kMaxTopK = 16;
 constexpr int kMaxDff = 8192;
 constexpr int kMaxD = 16384;
 constexpr int kMaxSlots = kMaxTokens * kMaxTopK;
+// largest cohort that runs as chunks of the single-launch kernel by default
+// (larger ones take the grouped multi-kernel path)
+constexpr int kChunkMaxTokens = 32;
 
 // status word bits written by device code (ws.status[0])
 enum : unsigned {

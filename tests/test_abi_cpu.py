@@ -96,3 +96,21 @@ def test_missing_library_fails_loudly(monkeypatch):
     monkeypatch.setattr(_abi, "_lib", None)
     with pytest.raises(RuntimeError, match="no fallback"):
         _abi.lib()
+
+
+def test_flag_values_match_the_header():
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    found = {name: 1 << int(bit) for name, bit in re.findall(r"(MOE_FLAG_\w+)\s*=\s*1u\s*<<\s*(\d+)", text)}
+    assert found == {name: getattr(q, name) for name in found}
+    assert set(found) == {n for n in dir(q) if n.startswith("MOE_FLAG_")}
+
+
+@pytest.mark.parametrize("flags,status", [
+    (q.MOE_FLAG_GROUPED_COHORTS, q.MOE_OK),
+    (q.MOE_FLAG_GROUPED_COHORTS | q.MOE_FLAG_F32_DEBUG | q.MOE_FLAG_TRACE, q.MOE_OK),
+    (1 << 4, q.MOE_ERR_INVALID_ARG),
+])
+def test_plan_flags_validated(libpath, flags, status):
+    cfg = q.make_config(**GOOD, flags=flags)
+    n = ctypes.c_size_t(0)
+    assert q.lib().moe_plan_workspace_bytes(ctypes.byref(cfg), ctypes.byref(n)) == status

@@ -14,6 +14,7 @@ from gpu_cases import (TOL_BF16, TOL_F32, assert_out_close, assert_routing_equal
 pytestmark = pytest.mark.gpu
 
 F32_DEBUG = 1
+GROUPED = 1 << 3  # MOE_FLAG_GROUPED_COHORTS
 
 
 def _check(shape_name, seed, n, kind="independent", full=False, flags=0, out_dtype=None,
@@ -56,9 +57,15 @@ def test_qwen3_ladder(n, kind):
     _check("qwen3", 2, n, kind)
 
 
-@pytest.mark.parametrize("n", [16, 64])
+@pytest.mark.parametrize("n", [9, 16, 17, 32, 33, 64])
 def test_qwen3_large_cohorts(n):
+    # 9..32: chunks of the single-launch kernel; 33 and 64: the grouped path
     _check("qwen3", 2, n)
+
+
+@pytest.mark.parametrize("n,kind", [(12, "independent"), (24, "shared")])
+def test_qwen3_grouped_path_below_the_chunk_limit(n, kind):
+    _check("qwen3", 2, n, kind, flags=GROUPED)
 
 
 def test_qwen3_shared_64_tokens_single_expert_set():
@@ -69,9 +76,10 @@ def test_qwen3_shared_64_tokens_single_expert_set():
 @pytest.mark.parametrize("shape_name,seed,n,full", [("qwen3", 2, 16, False), ("e256", 3, 16, False),
                                                    ("tiny", 0, 12, True)])
 def test_tile_variant_for_every_expert(shape_name, seed, n, full):
-    # mma_min_tokens = 1: every selected expert takes the tile kernels (weights
-    # dequantised to bf16 in shared memory, tensor-core tiles over its tokens)
-    _check(shape_name, seed, n, full=full, mma_min_tokens=1)
+    # mma_min_tokens = 1 on the grouped path: every selected expert takes the
+    # tile kernels (weights dequantised in shared memory, tensor-core tiles over
+    # its tokens)
+    _check(shape_name, seed, n, full=full, flags=GROUPED, mma_min_tokens=1)
 
 
 def test_tile_variant_with_mixed_counts():
@@ -84,6 +92,11 @@ def test_tile_variant_with_mixed_counts():
 @pytest.mark.parametrize("n", [1, 4, 16])
 def test_e256(n):
     _check("e256", 3, n)
+
+
+def test_e256_chunks_of_unequal_size():
+    # 20 tokens run as chunks of 6, 7 and 7 tokens
+    _check("e256", 3, 20)
 
 
 def test_e256_f32_check_path():

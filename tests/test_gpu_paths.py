@@ -11,20 +11,36 @@ from gpu_cases import (TOL_BF16, assert_out_close, assert_routing_equal, case, d
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("n,launches", [(1, 1), (4, 1), (8, 1), (9, 7)])
-def test_launches_per_step(n, launches):
-    """Cohorts of up to 8 tokens run as one fused launch; larger cohorts take
-    the multi-kernel path (router, grouping, tile and GEMV gate/up, tile and
-    GEMV down, combine)."""
+@pytest.mark.parametrize("n,flags,launches", [(1, 0, 1), (4, 0, 1), (8, 0, 1), (9, 0, 3), (16, 0, 3),
+                                               (17, 0, 4), (32, 0, 5), (33, 0, 7),
+                                               (9, q.MOE_FLAG_GROUPED_COHORTS, 7)])
+def test_launches_per_step(n, flags, launches):
+    """Cohorts of up to 8 tokens run as one fused launch; 9..32 tokens as
+    chunks of at most 8 plus one grouping kernel; larger cohorts (or any
+    cohort above 8 with the grouped flag) take the multi-kernel path (router,
+    grouping, tile and GEMV gate/up, tile and GEMV down, combine)."""
     import torch
     lay, x = case("qwen3", 2, n)
     shape = lay.shape
     dl = device_layer(lay)
-    plan = make_plan(shape)
+    plan = make_plan(shape, flags=flags)
     c0 = q.moe_plan_launch_count(plan.plan)
     plan.forward(x_tensor(shape, x), dl)
     torch.cuda.synchronize()
     assert q.moe_plan_launch_count(plan.plan) - c0 == launches
+
+
+def test_chunked_matches_grouped_path():
+    """The same 20-token cohort through chunks of the single-launch kernel and
+    through the grouped path: identical routing tables, outputs within the
+    bf16 tolerance."""
+    lay, x = case("qwen3", 2, 20)
+    shape = lay.shape
+    dl = device_layer(lay)
+    a, r_a = run_gpu(make_plan(shape, out_dtype="f32"), dl, shape, x)
+    b, r_b = run_gpu(make_plan(shape, flags=q.MOE_FLAG_GROUPED_COHORTS, out_dtype="f32"), dl, shape, x)
+    assert_routing_equal(r_a, r_b)
+    assert_out_close(a, b, TOL_BF16)
 
 
 def test_fused_matches_f32_check_path():
