@@ -55,6 +55,11 @@ def parse_args():
                     help="CPU work of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--stack", type=int, default=0,
+                    help="time a stack of this many distinct layers (one step = one forward "
+                         "per layer) and print one line per --sweep cohort size")
+    ap.add_argument("--sweep", default="1,2,4,8,16,32,64",
+                    help="cohort sizes of the --stack run")
     ap.add_argument("--phases", action="store_true",
                     help="also time the fused kernel's phases (router / gate-up / down)")
     ap.add_argument("--sustain-seconds", type=float, default=1.5,
@@ -462,11 +467,148 @@ def phase_split(q, shape, args, xs, reps, dev, n, steps=50):
     return res
 
 
+# ----------------------------------------------------------------------------
+# layer stack: L distinct layers, one forward per layer per step
+# ----------------------------------------------------------------------------
+def run_stack(args, world, rank, local, pg):
+    """A stack of `args.stack` layers of one shape, each with its own seeded
+    weights and router (about 14.5 GB of expert planes for 48 Qwen3-shaped
+    layers). A step runs one forward per layer, in layer order, each on a cohort
+    drawn for that layer's router (so routing keeps its per-layer diversity; no
+    attention or residual kernels run between layers). One JSON line per cohort
+    size of --sweep: tokens/s through the whole stack, the per-layer time, and
+    the unique-expert bytes against the HBM peak."""
+    import numpy as np
+    import torch
+
+    import moe_synth as ms
+    import quantized_moe_decode_softmax_gb300 as q
+
+    shape = ms.SHAPES[args.shape]
+    seed = SEEDS[args.shape]
+    L = args.stack
+    sizes = [int(v) for v in args.sweep.split(",") if v.strip()]
+    workers = max(1, min(16, os.cpu_count() or 1))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    act = torch.bfloat16 if shape.act_dtype == "bf16" else torch.float32
+    t_gen = time.perf_counter()
+    layers, routers = [], []
+    for l in range(L):
+        lay = ms.make_layer(shape, seed, l, workers=workers)
+        layers.append(q.DeviceLayer.from_host(ms.router_storage(shape, lay.router_w), lay.router_bias,
+                                              lay.planes, shape.top_k, device=dev))
+        routers.append((lay.router_w, lay.router_bias))
+        del lay
+    t_gen = time.perf_counter() - t_gen
+    P = 4  # cohorts per layer, cycled over the steps
+    peak, peak_kind = load_peaks()
+    esize = 2 if shape.act_dtype == "bf16" else 4
+
+    def to_dev(x):
+        st = ms.x_storage(shape, x)
+        t = torch.from_numpy(st.view(np.int16) if st.dtype == np.uint16 else st)
+        return t.to(dev).view(act) if st.dtype == np.uint16 else t.to(dev)
+
+    for n in sizes:
+        xs, U_of = [], []
+        for l in range(L):
+            rw, rb = routers[l]
+            cs = [ms.draw_tokens(shape, rw, rb, seed, l, n, args.kind, cohort=c) for c in range(P)]
+            xs.append([to_dev(x) for x in cs])
+            U_of.append([len(ms.routed_experts(x, rw, rb, shape.top_k)) for x in cs])
+        outs = [torch.empty((n, shape.D), dtype=act, device=dev) for _ in range(2)]
+        layer = q.MoeDecodeLayer(shape.E, shape.top_k, shape.D, shape.F, max_tokens=n,
+                                 act_dtype=shape.act_dtype, flags=args.flags,
+                                 mma_min_tokens=args.mma_min_tokens)
+        stream = torch.cuda.Stream(device=dev)
+        # a step is L forwards: at most 20 steps per graph (the graph holds K * L
+        # forwards), at least 3 warm-up steps
+        K, W = max(1, min(args.steps, 20)), max(3, min(args.warmup, 5))
+
+        def step(i):
+            for l in range(L):
+                layer.forward(xs[l][i % P], layers[l], outs[l % 2], stream=stream)
+
+        c0 = q.moe_plan_launch_count(layer.plan)
+        with torch.cuda.stream(stream):
+            for i in range(W):
+                step(i)
+        stream.synchronize()
+        layer.check()
+        launches_per_step = (q.moe_plan_launch_count(layer.plan) - c0) / max(W, 1)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(K):
+                step(W + i)
+        sampler = None if args.no_clocks else ClockSampler(local)
+        with torch.cuda.stream(stream):
+            graph.replay()
+            stream.synchronize()
+            if sampler:
+                sampler.start()
+            t_end = time.perf_counter() + args.sustain_seconds
+            while time.perf_counter() < t_end:
+                graph.replay()
+                stream.synchronize()
+            barrier(pg, local)
+            torch.cuda.synchronize()
+            start = torch.cuda.Event(enable_timing=True)
+            stop = torch.cuda.Event(enable_timing=True)
+            start.record(stream)
+            graph.replay()
+            stop.record(stream)
+            stop.synchronize()
+            torch.cuda.synchronize()
+            barrier(pg, local)
+            clocks = sampler.stop() if sampler else None
+        layer.check()
+        elapsed_ms = max_over_ranks(pg, start.elapsed_time(stop), dev)
+        ms_per_step = elapsed_ms / K
+        # phase split of one layer's single-launch step (fused cohorts only)
+        phases = (phase_split(q, shape, args, xs[0], [layers[0]], dev, n)
+                  if args.phases and n <= 8 else None)
+        avg_U = sum(U_of[l][(W + i) % P] for i in range(K) for l in range(L)) / K
+        bytes_per_step = avg_U * shape.plane_bytes + L * n * shape.D * esize * 2
+        achieved = bytes_per_step / (ms_per_step / 1000.0) / 1e9
+        if rank == 0:
+            line = {
+                "metric": METRIC, "value": world * n * K / (elapsed_ms / 1000.0), "unit": "tokens/s",
+                "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": ms_per_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic (seeded; random-init weights of the layer shape)",
+                "config": {"workload": f"{L}-layer stack of {shape.E}-expert top-{shape.top_k} "
+                                       f"D={shape.D} Dff={shape.F} MoE layers, n_tokens={n}",
+                           "layers": L, "n_tokens": n, "cohorts": args.kind,
+                           "expert_plane_bytes": L * shape.E * shape.plane_bytes,
+                           "l2": "every layer's planes are read once per step (stack >> L2)",
+                           "parallelism": f"replicas x{world}"},
+                "per_layer_us": ms_per_step * 1000.0 / L,
+                "layer_tokens_per_s": world * n * K * L / (elapsed_ms / 1000.0),
+                "unique_experts_per_layer": avg_U / L,
+                "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                             "frac": achieved / peak, "traffic": None,
+                             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                             if peak_kind == "measured" else "fallback",
+                             "timing": "CUDA events around the K-step graph replay"},
+                "gpu_launches": int(round(K * launches_per_step)),
+                "launches_per_layer": launches_per_step / L,
+                "clocks": clocks,
+                "phases_us": phases,
+                "stack_build_s": t_gen,
+            }
+            print(json.dumps(line), flush=True)
+        layer.close()
+        del xs, outs, graph
+
+
 def main():
     args = parse_args()
     world, rank, local, pg = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank, pg)
+    elif args.stack > 0:
+        run_stack(args, world, rank, local, pg)
     else:
         run_ours(args, world, rank, local, pg)
     if pg is not None:

@@ -1,7 +1,8 @@
-// expert_f32_kernels.cu -- the f32 check path of the expert half of the step.
+// expert_f32_kernels.cu -- the GEMV variant of the grouped path's expert half.
 // Every weight is dequantised exactly to f32 (w = s*q + b) and every product
-// is accumulated in f32 on the CUDA cores. Slow by design; it is the path that
-// MOE_FLAG_F32_DEBUG selects, held to 1e-4 of RMS(out) against the oracle.
+// is accumulated in f32 on the CUDA cores. It serves the experts below the
+// tile threshold on the grouped path, and every expert under MOE_FLAG_F32_DEBUG,
+// where it is held to 1e-4 of RMS(out) against the oracle.
 //
 // Stages (one launch each), over the de-duplicated expert list:
 //   gate/up : h[p, f] = silu(sum_d Wg[e,f,d] x[t,d]) * sum_d Wu[e,f,d] x[t,d]
@@ -41,104 +42,163 @@ __device__ __forceinline__ void ld8(const void *p, size_t i, float (&v)[8]) {
     }
 }
 
-__device__ __forceinline__ void deq8(uint32_t q, float s, float b, float (&w)[8]) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) w[j] = fmaf(s, (float)((q >> (4 * j)) & 0xFu), b);
+// exact f32 value of a 4-bit code: the code ORed into the mantissa of 2^23,
+// minus 2^23
+__device__ __forceinline__ float code_f32(uint32_t word, int j) {
+    return __uint_as_float(0x4B000000u | ((word >> (4 * j)) & 0xFu)) - 8388608.0f;
 }
 
-constexpr int kTok = 8;  // tokens per register tile
+// w[j] = s * q_j + b for the 8 codes of one packed word
+__device__ __forceinline__ void deq8(uint32_t q, float s, float b, float (&w)[8]) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) w[j] = fmaf(s, code_f32(q, j), b);
+}
 
-// warp per gate/up row f of expert unique[blockIdx.y]
-// (experts with at least `thr` tokens are left to the tile kernels when thr > 0)
+constexpr int kTok = 8;             // tokens per pass (accumulators per thread and matrix)
+constexpr int kRowThreads = 256;    // one thread per weight row
+constexpr int kStageBytes = 65536;  // activations of one pass in shared memory, at most
+
+// tokens per pass for a K-long activation row staged as f32
+__host__ __device__ inline int pass_tokens(int K) {
+    const int t = kStageBytes / (K * 4);
+    return t < 1 ? 1 : t > kTok ? kTok : t;
+}
+
+// Thread per gate/up row f of expert unique[blockIdx.y] (experts with at
+// least `thr` tokens are left to the tile kernels when thr > 0). Per pass of up
+// to T of the expert's slots, the block stages their activations as f32 in
+// shared memory; every thread then walks its two rows (gate and up) in 16-byte
+// code loads, dequantises each weight exactly and accumulates its products
+// with every staged token (the warp's threads read the same activation, so the
+// shared-memory reads are broadcasts and no cross-thread sum is needed).
 template <int XT>
-__global__ void __launch_bounds__(256) gateup_f32_kernel(StepArgs a, Workspace ws, int thr) {
-    const int lane = threadIdx.x & 31;
-    const int f = blockIdx.x * 8 + (threadIdx.x >> 5);
+__global__ void __launch_bounds__(kRowThreads) gateup_f32_kernel(StepArgs a, Workspace ws, int thr, int T) {
+    extern __shared__ float4 xs4[];
+    float *xs = reinterpret_cast<float *>(xs4);  // [T][D]
     const int u = blockIdx.y;
     const int D = a.s.D, F = a.s.F;
-    if (u >= *ws.U || f >= F) return;
+    if (u >= *ws.U) return;
     const int e = ws.unique[u];
     const int p_begin = ws.offsets[e], p_end = ws.offsets[e + 1];
     if (thr > 0 && p_end - p_begin >= thr) return;
-    const size_t row = (size_t)e * F + f;
-    const uint32_t *gq = a.planes.gate_q + row * (D / 8);
-    const uint32_t *uq = a.planes.up_q + row * (D / 8);
+    const int f = blockIdx.x * kRowThreads + threadIdx.x;
+    const bool has_row = f < F;
+    const size_t row = (size_t)e * F + (has_row ? f : F - 1);
+    const uint4 *gq = reinterpret_cast<const uint4 *>(a.planes.gate_q + row * (D / 8));
+    const uint4 *uq = reinterpret_cast<const uint4 *>(a.planes.up_q + row * (D / 8));
     const uint16_t *gs = a.planes.gate_s + row * (D / kGroup);
     const uint16_t *gb = a.planes.gate_b + row * (D / kGroup);
     const uint16_t *us = a.planes.up_s + row * (D / kGroup);
     const uint16_t *ub = a.planes.up_b + row * (D / kGroup);
-    for (int p0 = p_begin; p0 < p_end; p0 += kTok) {
-        const int cnt = min(kTok, p_end - p0);
-        int tok[kTok];
-#pragma unroll
-        for (int i = 0; i < kTok; ++i) tok[i] = i < cnt ? ws.slot_token[p0 + i] : 0;
+    for (int p0 = p_begin; p0 < p_end; p0 += T) {
+        const int cnt = min(T, p_end - p0);
+        __syncthreads();  // the previous pass is done with xs
+        for (int i = threadIdx.x; i < cnt * (D / 8); i += kRowThreads) {
+            const int t = i / (D / 8), c8 = i - t * (D / 8);
+            float v[8];
+            ld8<XT>(a.x, (size_t)ws.slot_token[p0 + t] * D + (size_t)c8 * 8, v);
+            float4 *dst = reinterpret_cast<float4 *>(xs + (size_t)t * D + c8 * 8);
+            dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+            dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+        }
+        __syncthreads();
+        if (!has_row) continue;
         float ag[kTok], au[kTok];
 #pragma unroll
-        for (int i = 0; i < kTok; ++i) ag[i] = au[i] = 0.f;
-        for (int wi = lane; wi < D / 8; wi += 32) {
-            float wg[8], wu[8];
-            deq8(__ldg(gq + wi), bf16f(gs[wi / 8]), bf16f(gb[wi / 8]), wg);
-            deq8(__ldg(uq + wi), bf16f(us[wi / 8]), bf16f(ub[wi / 8]), wu);
+        for (int t = 0; t < kTok; ++t) ag[t] = au[t] = 0.f;
+#pragma unroll 1
+        for (int g = 0; g < D / kGroup; ++g) {
+            const float sg = bf16f(gs[g]), bg = bf16f(gb[g]), su = bf16f(us[g]), bu = bf16f(ub[g]);
 #pragma unroll
-            for (int i = 0; i < kTok; ++i) {
-                if (i < cnt) {
-                    float xv[8];
-                    ld8<XT>(a.x, (size_t)tok[i] * D + (size_t)wi * 8, xv);
+            for (int hq = 0; hq < 2; ++hq) {
+                const uint4 cg = __ldg(gq + 2 * g + hq), cu = __ldg(uq + 2 * g + hq);
+                const uint32_t wg4[4] = {cg.x, cg.y, cg.z, cg.w}, wu4[4] = {cu.x, cu.y, cu.z, cu.w};
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        ag[i] = fmaf(wg[j], xv[j], ag[i]);
-                        au[i] = fmaf(wu[j], xv[j], au[i]);
+                for (int w = 0; w < 4; ++w) {
+                    float wg[8], wu[8];
+                    deq8(wg4[w], sg, bg, wg);
+                    deq8(wu4[w], su, bu, wu);
+                    const int k0 = g * kGroup + hq * 32 + w * 8;
+#pragma unroll
+                    for (int t = 0; t < kTok; ++t) {
+                        if (t < cnt) {
+                            const float4 x0 = *reinterpret_cast<const float4 *>(xs + (size_t)t * D + k0);
+                            const float4 x1 = *reinterpret_cast<const float4 *>(xs + (size_t)t * D + k0 + 4);
+                            const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                ag[t] = fmaf(wg[j], xv[j], ag[t]);
+                                au[t] = fmaf(wu[j], xv[j], au[t]);
+                            }
+                        }
                     }
                 }
             }
         }
 #pragma unroll
-        for (int i = 0; i < kTok; ++i) {
-            const float g = warp_sum(ag[i]);
-            const float uu = warp_sum(au[i]);
-            if (lane == 0 && i < cnt) ws.h[(size_t)(p0 + i) * F + f] = g / (1.0f + expf(-g)) * uu;
-        }
+        for (int t = 0; t < kTok; ++t)
+            if (t < cnt) ws.h[(size_t)(p0 + t) * F + f] = ag[t] / (1.0f + expf(-ag[t])) * au[t];
     }
 }
 
-// warp per down row d of expert unique[blockIdx.y]
-__global__ void __launch_bounds__(256) down_f32_kernel(StepArgs a, Workspace ws, int thr) {
-    const int lane = threadIdx.x & 31;
-    const int d = blockIdx.x * 8 + (threadIdx.x >> 5);
+// Thread per down row d of expert unique[blockIdx.y]: the same scheme over the
+// f32 h rows of the expert's slots.
+__global__ void __launch_bounds__(kRowThreads) down_f32_kernel(StepArgs a, Workspace ws, int thr, int T) {
+    extern __shared__ float4 hs4[];
+    float *hs = reinterpret_cast<float *>(hs4);  // [T][F]
     const int u = blockIdx.y;
     const int D = a.s.D, F = a.s.F;
-    if (u >= *ws.U || d >= D) return;
+    if (u >= *ws.U) return;
     const int e = ws.unique[u];
     const int p_begin = ws.offsets[e], p_end = ws.offsets[e + 1];
     if (thr > 0 && p_end - p_begin >= thr) return;
-    const size_t row = (size_t)e * D + d;
-    const uint32_t *dq = a.planes.down_q + row * (F / 8);
+    const int d = blockIdx.x * kRowThreads + threadIdx.x;
+    const bool has_row = d < D;
+    const size_t row = (size_t)e * D + (has_row ? d : D - 1);
+    const uint4 *dq = reinterpret_cast<const uint4 *>(a.planes.down_q + row * (F / 8));
     const uint16_t *ds = a.planes.down_s + row * (F / kGroup);
     const uint16_t *db = a.planes.down_b + row * (F / kGroup);
-    for (int p0 = p_begin; p0 < p_end; p0 += kTok) {
-        const int cnt = min(kTok, p_end - p0);
+    for (int p0 = p_begin; p0 < p_end; p0 += T) {
+        const int cnt = min(T, p_end - p0);
+        __syncthreads();
+        for (int i = threadIdx.x; i < cnt * (F / 4); i += kRowThreads) {
+            const int t = i / (F / 4), c4 = i - t * (F / 4);
+            hs4[(size_t)t * (F / 4) + c4] =
+                *reinterpret_cast<const float4 *>(ws.h + (size_t)(p0 + t) * F + (size_t)c4 * 4);
+        }
+        __syncthreads();
+        if (!has_row) continue;
         float acc[kTok];
 #pragma unroll
-        for (int i = 0; i < kTok; ++i) acc[i] = 0.f;
-        for (int wi = lane; wi < F / 8; wi += 32) {
-            float wd[8];
-            deq8(__ldg(dq + wi), bf16f(ds[wi / 8]), bf16f(db[wi / 8]), wd);
+        for (int t = 0; t < kTok; ++t) acc[t] = 0.f;
+#pragma unroll 1
+        for (int g = 0; g < F / kGroup; ++g) {
+            const float sd = bf16f(ds[g]), bd = bf16f(db[g]);
 #pragma unroll
-            for (int i = 0; i < kTok; ++i) {
-                if (i < cnt) {
-                    const float4 *hp = reinterpret_cast<const float4 *>(ws.h + (size_t)(p0 + i) * F + wi * 8);
-                    const float4 h0 = hp[0], h1 = hp[1];
-                    const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+            for (int hq = 0; hq < 2; ++hq) {
+                const uint4 c = __ldg(dq + 2 * g + hq);
+                const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[i] = fmaf(wd[j], hv[j], acc[i]);
+                for (int w = 0; w < 4; ++w) {
+                    float wd[8];
+                    deq8(w4[w], sd, bd, wd);
+                    const int k0 = g * kGroup + hq * 32 + w * 8;
+#pragma unroll
+                    for (int t = 0; t < kTok; ++t) {
+                        if (t < cnt) {
+                            const float4 h0 = *reinterpret_cast<const float4 *>(hs + (size_t)t * F + k0);
+                            const float4 h1 = *reinterpret_cast<const float4 *>(hs + (size_t)t * F + k0 + 4);
+                            const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) acc[t] = fmaf(wd[j], hv[j], acc[t]);
+                        }
+                    }
                 }
             }
         }
 #pragma unroll
-        for (int i = 0; i < kTok; ++i) {
-            const float v = warp_sum(acc[i]);
-            if (lane == 0 && i < cnt) ws.y[(size_t)(p0 + i) * D + d] = v;
-        }
+        for (int t = 0; t < kTok; ++t)
+            if (t < cnt) ws.y[(size_t)(p0 + t) * D + d] = acc[t];
     }
 }
 
@@ -167,17 +227,29 @@ cudaError_t launch_experts_f32(const StepArgs &a, const Workspace &ws, int tile_
     dim3 block(256);
     cudaError_t err;
     if (thr > 0 && (err = launch_expert_tiles(a, ws, thr, false, st, launched)) != cudaSuccess) return err;
-    dim3 g1((a.s.F + 7) / 8, maxU);
-    if (a.s.x_dtype == MOE_DTYPE_F32)
-        gateup_f32_kernel<MOE_DTYPE_F32><<<g1, block, 0, st>>>(a, ws, thr);
-    else
-        gateup_f32_kernel<MOE_DTYPE_BF16><<<g1, block, 0, st>>>(a, ws, thr);
+    const int T1 = pass_tokens(a.s.D), T2 = pass_tokens(a.s.F);
+    const int sm1 = T1 * a.s.D * 4, sm2 = T2 * a.s.F * 4;
+    dim3 g1((a.s.F + kRowThreads - 1) / kRowThreads, maxU);
+    if (a.s.x_dtype == MOE_DTYPE_F32) {
+        if ((err = cudaFuncSetAttribute(gateup_f32_kernel<MOE_DTYPE_F32>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, sm1)) != cudaSuccess)
+            return err;
+        gateup_f32_kernel<MOE_DTYPE_F32><<<g1, kRowThreads, sm1, st>>>(a, ws, thr, T1);
+    } else {
+        if ((err = cudaFuncSetAttribute(gateup_f32_kernel<MOE_DTYPE_BF16>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, sm1)) != cudaSuccess)
+            return err;
+        gateup_f32_kernel<MOE_DTYPE_BF16><<<g1, kRowThreads, sm1, st>>>(a, ws, thr, T1);
+    }
     launched += 1;
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     if (thr > 0 && (err = launch_expert_tiles(a, ws, thr, true, st, launched)) != cudaSuccess) return err;
-    dim3 g2((a.s.D + 7) / 8, maxU);
-    down_f32_kernel<<<g2, block, 0, st>>>(a, ws, thr);
+    if ((err = cudaFuncSetAttribute(down_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sm2)) !=
+        cudaSuccess)
+        return err;
+    dim3 g2((a.s.D + kRowThreads - 1) / kRowThreads, maxU);
+    down_f32_kernel<<<g2, kRowThreads, sm2, st>>>(a, ws, thr, T2);
     launched += 1;
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
