@@ -79,7 +79,7 @@ enum {
     /* record per-CTA timestamps of the fused kernel's phases (see
      * moe_get_phase_times); costs a few global stores per CTA */
     MOE_FLAG_PHASE_TIMES = 1u << 2,
-    /* cohorts of 9..32 tokens take the grouped multi-kernel path (every
+    /* cohorts of 9..16 tokens take the grouped multi-kernel path (every
      * selected expert streamed once per step, tile kernels for experts with
      * at least mma_min_tokens tokens) instead of chunks of the single-launch
      * kernel; see moe_decode_forward */
@@ -151,11 +151,11 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan **out);
  *   stream      cudaStream_t, or NULL for the legacy default stream
  * Paths, chosen on the host from n_tokens and the plan:
  *   n_tokens 1..8    one launch of the single-launch kernel;
- *   n_tokens 9..32   balanced chunks of at most 8 tokens, each one launch of
+ *   n_tokens 9..16   balanced chunks of at most 8 tokens, each one launch of
  *                    the single-launch kernel (an expert picked in several
  *                    chunks is streamed once per chunk), then one grouping
  *                    kernel that writes the whole cohort's routing tables;
- *   n_tokens 33..64, or any n_tokens > 8 with MOE_FLAG_GROUPED_COHORTS:
+ *   n_tokens 17..64, or any n_tokens > 8 with MOE_FLAG_GROUPED_COHORTS:
  *                    the grouped multi-kernel path (router, top-k and
  *                    grouping, per-expert tile or GEMV kernels, combine);
  *   MOE_FLAG_F32_DEBUG, or a shape the single-launch kernel declines:

@@ -64,13 +64,68 @@ __host__ __device__ inline int pass_tokens(int K) {
     return t < 1 ? 1 : t > kTok ? kTok : t;
 }
 
+// One thread's gate and up rows against NT staged tokens (cnt <= NT of them
+// real): accumulators ag/au per token. The next group's codes and scales are
+// loaded before the current group is computed.
+template <int NT>
+__device__ __forceinline__ void gateup_row(const uint4 *gq, const uint4 *uq, const uint16_t *gs,
+                                           const uint16_t *gb, const uint16_t *us, const uint16_t *ub,
+                                           const float *xs, int D, int cnt, float (&ag)[kTok],
+                                           float (&au)[kTok]) {
+    const int G = D / kGroup;
+    uint4 ng0 = __ldg(gq), ng1 = __ldg(gq + 1), nu0 = __ldg(uq), nu1 = __ldg(uq + 1);
+    uint16_t nsg = gs[0], nbg = gb[0], nsu = us[0], nbu = ub[0];
+#pragma unroll 1
+    for (int g = 0; g < G; ++g) {
+        const uint4 cg[2] = {ng0, ng1}, cu[2] = {nu0, nu1};
+        const float sg = bf16f(nsg), bg = bf16f(nbg), su = bf16f(nsu), bu = bf16f(nbu);
+        if (g + 1 < G) {
+            ng0 = __ldg(gq + 2 * g + 2);
+            ng1 = __ldg(gq + 2 * g + 3);
+            nu0 = __ldg(uq + 2 * g + 2);
+            nu1 = __ldg(uq + 2 * g + 3);
+            nsg = gs[g + 1];
+            nbg = gb[g + 1];
+            nsu = us[g + 1];
+            nbu = ub[g + 1];
+        }
+#pragma unroll
+        for (int hq = 0; hq < 2; ++hq) {
+            const uint32_t wg4[4] = {cg[hq].x, cg[hq].y, cg[hq].z, cg[hq].w};
+            const uint32_t wu4[4] = {cu[hq].x, cu[hq].y, cu[hq].z, cu[hq].w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                float wg[8], wu[8];
+                deq8(wg4[w], sg, bg, wg);
+                deq8(wu4[w], su, bu, wu);
+                const int k0 = g * kGroup + hq * 32 + w * 8;
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    if (NT == 1 || t < cnt) {
+                        const float4 x0 = *reinterpret_cast<const float4 *>(xs + (size_t)t * D + k0);
+                        const float4 x1 = *reinterpret_cast<const float4 *>(xs + (size_t)t * D + k0 + 4);
+                        const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            ag[t] = fmaf(wg[j], xv[j], ag[t]);
+                            au[t] = fmaf(wu[j], xv[j], au[t]);
+                        }
+                    }
+                }
+            }
+        }
+    }
+}
+
 // Thread per gate/up row f of expert unique[blockIdx.y] (experts with at
 // least `thr` tokens are left to the tile kernels when thr > 0). Per pass of up
 // to T of the expert's slots, the block stages their activations as f32 in
 // shared memory; every thread then walks its two rows (gate and up) in 16-byte
 // code loads, dequantises each weight exactly and accumulates its products
 // with every staged token (the warp's threads read the same activation, so the
-// shared-memory reads are broadcasts and no cross-thread sum is needed).
+// shared-memory reads are broadcasts and no cross-thread sum is needed). The
+// token loop is specialised for 1, 2, 4 or 8 tokens, so a pass issues work for
+// at most twice its tokens.
 template <int XT>
 __global__ void __launch_bounds__(kRowThreads) gateup_f32_kernel(StepArgs a, Workspace ws, int thr, int T) {
     extern __shared__ float4 xs4[];
@@ -106,38 +161,57 @@ __global__ void __launch_bounds__(kRowThreads) gateup_f32_kernel(StepArgs a, Wor
         float ag[kTok], au[kTok];
 #pragma unroll
         for (int t = 0; t < kTok; ++t) ag[t] = au[t] = 0.f;
+        if (cnt == 1)
+            gateup_row<1>(gq, uq, gs, gb, us, ub, xs, D, cnt, ag, au);
+        else if (cnt == 2)
+            gateup_row<2>(gq, uq, gs, gb, us, ub, xs, D, cnt, ag, au);
+        else if (cnt <= 4)
+            gateup_row<4>(gq, uq, gs, gb, us, ub, xs, D, cnt, ag, au);
+        else
+            gateup_row<kTok>(gq, uq, gs, gb, us, ub, xs, D, cnt, ag, au);
+#pragma unroll
+        for (int t = 0; t < kTok; ++t)
+            if (t < cnt) ws.h[(size_t)(p0 + t) * F + f] = ag[t] / (1.0f + expf(-ag[t])) * au[t];
+    }
+}
+
+// One thread's down row against NT staged h rows (cnt <= NT of them real).
+template <int NT>
+__device__ __forceinline__ void down_row(const uint4 *dq, const uint16_t *ds, const uint16_t *db,
+                                         const float *hs, int F, int cnt, float (&acc)[kTok]) {
+    const int G = F / kGroup;
+    uint4 n0 = __ldg(dq), n1 = __ldg(dq + 1);
+    uint16_t ns = ds[0], nb = db[0];
 #pragma unroll 1
-        for (int g = 0; g < D / kGroup; ++g) {
-            const float sg = bf16f(gs[g]), bg = bf16f(gb[g]), su = bf16f(us[g]), bu = bf16f(ub[g]);
+    for (int g = 0; g < G; ++g) {
+        const uint4 c[2] = {n0, n1};
+        const float sd = bf16f(ns), bd = bf16f(nb);
+        if (g + 1 < G) {
+            n0 = __ldg(dq + 2 * g + 2);
+            n1 = __ldg(dq + 2 * g + 3);
+            ns = ds[g + 1];
+            nb = db[g + 1];
+        }
 #pragma unroll
-            for (int hq = 0; hq < 2; ++hq) {
-                const uint4 cg = __ldg(gq + 2 * g + hq), cu = __ldg(uq + 2 * g + hq);
-                const uint32_t wg4[4] = {cg.x, cg.y, cg.z, cg.w}, wu4[4] = {cu.x, cu.y, cu.z, cu.w};
+        for (int hq = 0; hq < 2; ++hq) {
+            const uint32_t w4[4] = {c[hq].x, c[hq].y, c[hq].z, c[hq].w};
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    float wg[8], wu[8];
-                    deq8(wg4[w], sg, bg, wg);
-                    deq8(wu4[w], su, bu, wu);
-                    const int k0 = g * kGroup + hq * 32 + w * 8;
+            for (int w = 0; w < 4; ++w) {
+                float wd[8];
+                deq8(w4[w], sd, bd, wd);
+                const int k0 = g * kGroup + hq * 32 + w * 8;
 #pragma unroll
-                    for (int t = 0; t < kTok; ++t) {
-                        if (t < cnt) {
-                            const float4 x0 = *reinterpret_cast<const float4 *>(xs + (size_t)t * D + k0);
-                            const float4 x1 = *reinterpret_cast<const float4 *>(xs + (size_t)t * D + k0 + 4);
-                            const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                for (int t = 0; t < NT; ++t) {
+                    if (NT == 1 || t < cnt) {
+                        const float4 h0 = *reinterpret_cast<const float4 *>(hs + (size_t)t * F + k0);
+                        const float4 h1 = *reinterpret_cast<const float4 *>(hs + (size_t)t * F + k0 + 4);
+                        const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
 #pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                ag[t] = fmaf(wg[j], xv[j], ag[t]);
-                                au[t] = fmaf(wu[j], xv[j], au[t]);
-                            }
-                        }
+                        for (int j = 0; j < 8; ++j) acc[t] = fmaf(wd[j], hv[j], acc[t]);
                     }
                 }
             }
         }
-#pragma unroll
-        for (int t = 0; t < kTok; ++t)
-            if (t < cnt) ws.h[(size_t)(p0 + t) * F + f] = ag[t] / (1.0f + expf(-ag[t])) * au[t];
     }
 }
 
@@ -171,31 +245,14 @@ __global__ void __launch_bounds__(kRowThreads) down_f32_kernel(StepArgs a, Works
         float acc[kTok];
 #pragma unroll
         for (int t = 0; t < kTok; ++t) acc[t] = 0.f;
-#pragma unroll 1
-        for (int g = 0; g < F / kGroup; ++g) {
-            const float sd = bf16f(ds[g]), bd = bf16f(db[g]);
-#pragma unroll
-            for (int hq = 0; hq < 2; ++hq) {
-                const uint4 c = __ldg(dq + 2 * g + hq);
-                const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    float wd[8];
-                    deq8(w4[w], sd, bd, wd);
-                    const int k0 = g * kGroup + hq * 32 + w * 8;
-#pragma unroll
-                    for (int t = 0; t < kTok; ++t) {
-                        if (t < cnt) {
-                            const float4 h0 = *reinterpret_cast<const float4 *>(hs + (size_t)t * F + k0);
-                            const float4 h1 = *reinterpret_cast<const float4 *>(hs + (size_t)t * F + k0 + 4);
-                            const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) acc[t] = fmaf(wd[j], hv[j], acc[t]);
-                        }
-                    }
-                }
-            }
-        }
+        if (cnt == 1)
+            down_row<1>(dq, ds, db, hs, F, cnt, acc);
+        else if (cnt == 2)
+            down_row<2>(dq, ds, db, hs, F, cnt, acc);
+        else if (cnt <= 4)
+            down_row<4>(dq, ds, db, hs, F, cnt, acc);
+        else
+            down_row<kTok>(dq, ds, db, hs, F, cnt, acc);
 #pragma unroll
         for (int t = 0; t < kTok; ++t)
             if (t < cnt) ws.y[(size_t)(p0 + t) * D + d] = acc[t];

@@ -19,7 +19,7 @@ constexpr int kMaxD = 16384;
 constexpr int kMaxSlots = kMaxTokens * kMaxTopK;
 // largest cohort that runs as chunks of the single-launch kernel by default
 // (larger ones take the grouped multi-kernel path)
-constexpr int kChunkMaxTokens = 32;
+constexpr int kChunkMaxTokens = 16;
 
 // status word bits written by device code (ws.status[0])
 enum : unsigned {
