@@ -405,12 +405,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     unsigned long long *gsync = reinterpret_cast<unsigned long long *>(W.sync);
     uint16_t *Hg = reinterpret_cast<uint16_t *>(W.h);  // [slots][F] bf16, h_pos order
 
-    stamp(W.phase_ns, timing, 0);
-    // barrier epoch (thread 0 only): the counter grows by 2G per launch and no
-    // CTA of this launch can pass barrier 1 before this CTA arrives there
+    // Prologue on shared memory and kernel parameters only: it may overlap the
+    // tail of the previous kernel in the stream (programmatic dependent launch).
     unsigned long long epoch = 0;
     if (tid == 0) {
-        epoch = ptx::ld_acquire_gpu_u64(gsync);
         for (int s = 0; s < L.NS; ++s) {
             ptx::mbar_init(&S.full[s], 1);
             ptx::mbar_init(&S.empty[s], kCW);
@@ -430,6 +428,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     // zero the expert token masks (grouping below)
 #pragma unroll 1
     for (int e = tid; e < E; e += kThreads) S.s_mask[e] = 0ull;
+    // the next kernel may start its own prologue as this grid's CTAs exit; every
+    // global memory access below waits for the previous kernel to complete
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
+    stamp(W.phase_ns, timing, 0);
+    // barrier epoch (thread 0 only): the counter grows by 2G per launch and no
+    // CTA of this launch can pass barrier 1 before this CTA arrives there
+    if (tid == 0) epoch = ptx::ld_acquire_gpu_u64(gsync);
     __syncthreads();
 
     // ---- phase R: router logits of this CTA's experts, x staging ----------------
@@ -1297,8 +1303,31 @@ cudaError_t launch_fused(const StepArgs &a, const Workspace &ws, const DecodeLay
     P.ws = ws;
     P.L = L;
     void *args[] = {&P};
-    cudaError_t err = cudaLaunchCooperativeKernel(kernel_for(L), dim3(L.G),
-                                                  dim3(kThreads), args, (size_t)L.smem_bytes, st);
+    // cooperative (every CTA resident at once, which the grid barriers need),
+    // and with programmatic stream serialization: the launch may begin while
+    // the previous kernel of the stream finishes; the kernel's prologue touches
+    // shared memory only and then waits for that kernel (griddepcontrol.wait).
+    // A driver that declines the combination gets the plain cooperative launch.
+    static bool pdl_ok = true;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(L.G);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)L.smem_bytes;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_ok ? 2 : 1;
+    cudaError_t err = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(kernel_for(L)), args);
+    if (err != cudaSuccess && pdl_ok) {
+        cudaGetLastError();
+        pdl_ok = false;
+        cfg.numAttrs = 1;
+        err = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(kernel_for(L)), args);
+    }
     if (err == cudaSuccess) launched += 1;
     return err;
 }

@@ -107,6 +107,20 @@ __device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// programmatic dependent launch: let the next kernel of the stream (launched
+// with programmatic stream serialization) start as this grid's CTAs signal
+// or exit; a no-op when no such kernel follows
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// wait until the grids this one depends on have completed and their memory
+// operations are visible; returns at once when the launch had no such
+// dependency
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // arrive on `bar` once every cp.async this thread issued before has landed
 // (the barrier's expected count includes this arrival)
 __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t *bar) {
