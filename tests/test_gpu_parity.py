@@ -152,6 +152,22 @@ def test_host_entry_point_matches_device_entry_point():
     assert torch.equal(out_host.view(torch.int16), dev.cpu().view(torch.int16))
 
 
+def test_host_entry_point_for_a_chunked_cohort():
+    """12 tokens through the host entry point (chunks of the single launch):
+    the same bits as the device entry point."""
+    import torch
+    lay, x = case("qwen3", 2, 12)
+    shape = lay.shape
+    dl = device_layer(lay)
+    plan = make_plan(shape)
+    xt = x_tensor(shape, x)
+    dev = plan.forward(xt, dl)
+    torch.cuda.synchronize()
+    out_host = torch.empty((12, shape.D), dtype=torch.bfloat16).pin_memory()
+    plan.forward_host(xt.cpu().pin_memory(), dl, out_host)
+    assert torch.equal(out_host.view(torch.int16), dev.cpu().view(torch.int16))
+
+
 def test_zero_input():
     import torch
     lay, _ = case("qwen3", 2, 2)
