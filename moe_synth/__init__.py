@@ -84,7 +84,17 @@ QWEN3 = LayerShape(E=128, top_k=8, D=2048, F=768, act_dtype="bf16", router_std=0
 E256 = LayerShape(E=256, top_k=6, D=4096, F=2048, act_dtype="bf16",
                   router_std=1.0 / 64.0, zipf_s=1.1)
 
-SHAPES: Dict[str, LayerShape] = {"tiny": TINY, "qwen3": QWEN3, "e256": E256}
+# edge shapes for parity tests: the largest top-k (16) on the single-launch
+# path, the largest expert count (1024, multi-kernel path), top-k equal to the
+# expert count, and top-1 with f32 activations. Router deviations put the
+# logits' standard deviation near 1-2 so the margin rule is met quickly.
+K16 = LayerShape(E=64, top_k=16, D=512, F=256, act_dtype="bf16", router_std=2.0 / 512 ** 0.5)
+E1024 = LayerShape(E=1024, top_k=16, D=256, F=128, act_dtype="bf16", router_std=2.0 / 256 ** 0.5)
+KALL = LayerShape(E=8, top_k=8, D=512, F=256, act_dtype="bf16", router_std=1.0 / 512 ** 0.5)
+K1 = LayerShape(E=16, top_k=1, D=512, F=256, act_dtype="f32", router_std=1.0 / 512 ** 0.5)
+
+SHAPES: Dict[str, LayerShape] = {"tiny": TINY, "qwen3": QWEN3, "e256": E256, "k16": K16,
+                                 "e1024": E1024, "kall": KALL, "k1": K1}
 
 # named workloads: shape, seed, cohort sizes and cohort kinds
 WORKLOADS = {

@@ -103,6 +103,26 @@ def test_e256_f32_check_path():
     _check("e256", 3, 4, flags=F32_DEBUG, out_dtype="f32")
 
 
+# ---- edge shapes -------------------------------------------------------------------
+@pytest.mark.parametrize("shape_name,n,flags", [
+    ("k16", 1, 0),           # top-16 on the single launch
+    ("k16", 8, 0),           # 128 slots, the single launch's maximum
+    ("k16", 12, 0),          # chunks of 6 and 6
+    ("k16", 12, GROUPED),
+    ("kall", 3, 0),          # top-k = E: every expert selected, weights = softmax
+    ("k1", 5, 0),            # top-1, f32 activations on the single launch
+    ("e1024", 4, 0),         # 1024 experts (multi-kernel path), top-16
+    ("e1024", 64, 0),        # 64 tokens x top-16 = 1024 slots, the largest cohort
+])
+def test_edge_shapes(shape_name, n, flags):
+    _check(shape_name, 5, n, full=True, flags=flags)
+
+
+def test_edge_shapes_f32_check_path():
+    _check("k16", 5, 8, full=True, flags=F32_DEBUG, out_dtype="f32")
+    _check("e1024", 5, 16, full=True, flags=F32_DEBUG, out_dtype="f32")
+
+
 # ---- properties --------------------------------------------------------------------
 def test_deterministic_and_identical_tokens():
     import torch
