@@ -31,13 +31,15 @@
 namespace moe {
 namespace {
 
-constexpr int kTT = 256;               // threads per block (8 warps, 16 rows each)
+constexpr int kTR = 64;                // weight-tile rows per block (one MMA row tile per warp)
+constexpr int kTT = 2 * kTR;           // threads per block: two per tile row (4 warps)
 constexpr int kKC = 128;               // inputs per K chunk (two groups)
 constexpr int kRowB = kKC * 2 + 16;    // shared row stride in bytes (ldmatrix without bank conflicts)
 constexpr int kMaxNT = kMaxTokens / 8; // token tiles
-constexpr int kSmemA = 128 * kRowB;    // weights: 128 rows x kKC f16
+constexpr int kSmemA = kTR * kRowB;    // weights: kTR rows x kKC f16
 constexpr int kSmemX = kMaxTokens * kRowB;
 constexpr int kSmem = kSmemA + kSmemX;
+static_assert(kTR * 65 * 4 <= kSmem, "the gate/up epilogue reuses the tile's shared memory");
 
 __device__ __forceinline__ float bf16f(uint16_t h) { return __uint_as_float(((uint32_t)h) << 16); }
 
@@ -85,7 +87,7 @@ __device__ __forceinline__ uint4 load8_f16(const void *p, size_t i, int dtype) {
 }
 
 // The shared K-chunk loop of both kernels: rows [16 w, 16 w + 16) of the
-// 128-row weight tile against the expert's NT token tiles.
+// kTR-row weight tile against the expert's NT token tiles.
 //   load_w(r, half, dst): dequantise group `half` of the chunk for tile row r
 //   load_x(j, piece, dst): 8 inputs (piece of the chunk) of the expert's j-th token
 template <typename LW, typename LX>
@@ -119,7 +121,8 @@ __device__ __forceinline__ void tile_product(unsigned char *As, unsigned char *X
     }
 }
 
-// block (64 rows f of expert unique[blockIdx.y]): tile rows 0..63 gate, 64..127 up
+// block (kTR / 2 rows f of expert unique[blockIdx.y]): tile rows [0, kTR / 2) gate,
+// [kTR / 2, kTR) up
 __global__ void __launch_bounds__(kTT) gateup_tile_kernel(StepArgs a, Workspace ws, int thr) {
     extern __shared__ __align__(16) unsigned char sm[];
     const int u = blockIdx.y;
@@ -127,15 +130,15 @@ __global__ void __launch_bounds__(kTT) gateup_tile_kernel(StepArgs a, Workspace 
     const int e = ws.unique[u];
     const int off = ws.offsets[e], cnt = ws.offsets[e + 1] - off;
     if (cnt < thr) return;
-    const int D = a.s.D, F = a.s.F, f0 = blockIdx.x * 64;
+    const int D = a.s.D, F = a.s.F, f0 = blockIdx.x * (kTR / 2);
     const int NT = (cnt + 7) / 8;
     unsigned char *As = sm, *Xs = sm + kSmemA;
     float acc[kMaxNT][4];
 #pragma unroll
     for (int nt = 0; nt < kMaxNT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
     auto load_w = [&](int r, int k, unsigned char *dst) {
-        const size_t row = (size_t)e * F + f0 + (r & 63);
-        const bool up = r >= 64;
+        const size_t row = (size_t)e * F + f0 + (r % (kTR / 2));
+        const bool up = r >= kTR / 2;
         const uint32_t *q = (up ? a.planes.up_q : a.planes.gate_q) + row * (D / 8) + k / 8;
         const size_t gi = row * (D / kGroup) + k / kGroup;
         const float s = bf16f((up ? a.planes.up_s : a.planes.gate_s)[gi]);
@@ -147,7 +150,7 @@ __global__ void __launch_bounds__(kTT) gateup_tile_kernel(StepArgs a, Workspace 
         return load8_f16(a.x, (size_t)ws.slot_token[off + j] * D + k, a.s.x_dtype);
     };
     tile_product(As, Xs, D, NT, load_w, load_x, acc);
-    // accumulators -> shared [128 rows][65] f32, then h = silu(gate) * up per (slot, f)
+    // accumulators -> shared [kTR rows][65] f32, then h = silu(gate) * up per (slot, f)
     float *E = reinterpret_cast<float *>(sm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
 #pragma unroll
@@ -161,14 +164,14 @@ __global__ void __launch_bounds__(kTT) gateup_tile_kernel(StepArgs a, Workspace 
         }
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < cnt * 64; i += kTT) {
-        const int j = i >> 6, fr = i & 63;
-        const float gv = E[fr * 65 + j], uv = E[(64 + fr) * 65 + j];
+    for (int i = threadIdx.x; i < cnt * (kTR / 2); i += kTT) {
+        const int j = i / (kTR / 2), fr = i % (kTR / 2);
+        const float gv = E[fr * 65 + j], uv = E[(kTR / 2 + fr) * 65 + j];
         ws.h[(size_t)(off + j) * F + f0 + fr] = gv / (1.0f + expf(-gv)) * uv;
     }
 }
 
-// block (128 rows d of expert unique[blockIdx.y])
+// block (kTR rows d of expert unique[blockIdx.y])
 __global__ void __launch_bounds__(kTT) down_tile_kernel(StepArgs a, Workspace ws, int thr) {
     extern __shared__ __align__(16) unsigned char sm[];
     const int u = blockIdx.y;
@@ -176,7 +179,7 @@ __global__ void __launch_bounds__(kTT) down_tile_kernel(StepArgs a, Workspace ws
     const int e = ws.unique[u];
     const int off = ws.offsets[e], cnt = ws.offsets[e + 1] - off;
     if (cnt < thr) return;
-    const int D = a.s.D, F = a.s.F, d0 = blockIdx.x * 128;
+    const int D = a.s.D, F = a.s.F, d0 = blockIdx.x * kTR;
     const int NT = (cnt + 7) / 8;
     unsigned char *As = sm, *Xs = sm + kSmemA;
     float acc[kMaxNT][4];
@@ -221,9 +224,9 @@ cudaError_t launch_expert_tiles(const StepArgs &a, const Workspace &ws, int thr,
     if (err != cudaSuccess) return err;
     const int maxU = min(a.s.E, a.s.n * a.s.k);
     if (!down) {
-        gateup_tile_kernel<<<dim3(a.s.F / 64, maxU), kTT, kSmem, st>>>(a, ws, thr);
+        gateup_tile_kernel<<<dim3(a.s.F / (kTR / 2), maxU), kTT, kSmem, st>>>(a, ws, thr);
     } else {
-        down_tile_kernel<<<dim3(a.s.D / 128, maxU), kTT, kSmem, st>>>(a, ws, thr);
+        down_tile_kernel<<<dim3(a.s.D / kTR, maxU), kTT, kSmem, st>>>(a, ws, thr);
     }
     launched += 1;
     return cudaGetLastError();
