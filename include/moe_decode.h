@@ -227,8 +227,8 @@ moe_status moe_get_routing(moe_plan *plan, int32_t *topk_idx, float *topk_w,
  *   i = 0 start, 1 router done, 2 after grid barrier 1, 3 routing and work
  *   lists done, 4 gate/up done, 5 after grid barrier 2, 6 down done, 7 end;
  *   8/9 gate/up ns spent waiting for data / computing (consumer warp 0),
- *   10/11 the same for the down projection, 12 producer ns waiting for free
- *   ring slots, 13 gate/up chunks, 14 down tiles of the CTA.
+ *   10/11 the same for the down projection, 12 reserved (0), 13 gate/up
+ *   chunks, 14 down tiles of the CTA.
  * Copies min(max_entries, ctas*16) entries to HOST memory, sets *ctas to the
  * kernel's CTA count, and synchronises the plan's last stream. */
 moe_status moe_get_phase_times(moe_plan *plan, uint64_t *times, int max_entries, int *ctas);

@@ -207,7 +207,7 @@ def moe_plan_launch_count(plan: int) -> int:
 
 
 PHASES = ("start", "router", "barrier1", "routing", "gate_up", "barrier2", "down", "end",
-          "a_wait", "a_compute", "b_wait", "b_compute", "producer_wait", "a_chunks", "b_tiles",
+          "a_wait", "a_compute", "b_wait", "b_compute", "reserved", "a_chunks", "b_tiles",
           "reserved")
 
 

@@ -285,6 +285,34 @@ def check_invariants():
     assert np.array_equal(base["out_bf16"], ms.bf16_bits(base["out"]))
 
 
+def check_expert_shards_sum_to_the_step():
+    """Expert-parallel split, done with virtual shards on the CPU: shard g keeps the
+    planes of its experts and zeroes the scales and biases of all others. All
+    weights of a zeroed expert are then 0, so its SwiGLU output is exactly 0 while
+    routing is unchanged. The shards' f32 outputs must sum to the unsharded output
+    (up to f32 rounding of the two summation orders), for 2 and 3 shards."""
+    lay = ms.make_layer(SMALL, 13, 0)
+    x = ms.draw_tokens(SMALL, lay.router_w, None, 13, 0, 6)
+    k = SMALL.top_k
+    full = oracle.moe_forward(x, lay.router_w, None, lay.planes, k)
+    owner = np.random.default_rng(4).permutation(SMALL.E)
+    for G in (2, 3):
+        total = np.zeros_like(full["out"], dtype=np.float64)
+        for g in range(G):
+            mine = np.zeros(SMALL.E, bool)
+            mine[owner[g::G]] = True
+            arrs = []
+            for name, a in zip(ms.ExpertPlanes.FIELDS, lay.planes.arrays()):
+                a = a.copy()
+                if not name.endswith("_q"):
+                    a[~mine] = 0  # bf16 +0
+                arrs.append(a)
+            part = oracle.moe_forward(x, lay.router_w, None, ms.ExpertPlanes(*arrs), k)
+            assert np.array_equal(part["topk_idx"], full["topk_idx"])
+            total += part["out"]
+        assert np.abs(total - full["out"]).max() <= 1e-6 * _rms(full["out"]), G
+
+
 ALL_CHECKS = [
     check_quant_roundtrip,
     check_dequant_known_codes,
@@ -297,4 +325,5 @@ ALL_CHECKS = [
     check_brute_force_dense,
     check_closed_form_golden,
     check_invariants,
+    check_expert_shards_sum_to_the_step,
 ]
