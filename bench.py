@@ -18,6 +18,10 @@ timed K steps, which run as a captured CUDA graph; `e2e` is the same metric
 through the host-buffer entry point, with the H2D and D2H copies inside the
 timed region; `roofline` relates the unique expert bytes per step to the
 measured HBM peak.
+
+`--stack L --sweep 1,2,...` instead times a stack of L distinct layers (one
+forward per layer per step, e.g. 48 layers and 16 GB of planes) and prints one
+line per cohort size of the sweep.
 """
 from __future__ import annotations
 
