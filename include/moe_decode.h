@@ -93,7 +93,7 @@ enum {
 typedef struct {
     int E;              /* experts, 1..1024 */
     int top_k;          /* experts per token, 1..min(E, 16) */
-    int D;              /* hidden size; multiple of 64 */
+    int D;              /* hidden size; multiple of 64, <= 16384 */
     int Dff;            /* expert intermediate size; multiple of 64, <= 8192 */
     int bits;           /* must be 4 */
     int group_size;     /* must be 64 */
@@ -132,9 +132,10 @@ moe_status moe_plan_workspace_bytes(const moe_config *cfg, size_t *bytes);
 
 /* Validate cfg and allocate the plan's workspace on the current device.
  * The plan is bound to that device. Decline (UNSUPPORTED): bits != 4,
- * group_size != 64, D or Dff not a multiple of 64, Dff > 8192, E > 1024,
- * top_k > 16. INVALID_ARG: null pointers, non-positive sizes,
- * top_k > E, max_tokens outside 1..64, unknown dtypes. OOM / CUDA: the
+ * group_size != 64, D or Dff not a multiple of 64, D > 16384, Dff > 8192,
+ * E > 1024, top_k > 16. INVALID_ARG: null pointers, non-positive sizes,
+ * top_k > E, max_tokens outside 1..64, unknown dtypes, negative
+ * mma_min_tokens, unknown flags. OOM / CUDA: the
  * allocation failed (nothing leaks). On success *out owns the workspace
  * until moe_plan_free. */
 moe_status moe_plan_create(const moe_config *cfg, moe_plan **out);

@@ -114,3 +114,57 @@ def test_plan_flags_validated(libpath, flags, status):
     cfg = q.make_config(**GOOD, flags=flags)
     n = ctypes.c_size_t(0)
     assert q.lib().moe_plan_workspace_bytes(ctypes.byref(cfg), ctypes.byref(n)) == status
+
+
+# one documented rule broken at a time, from a valid configuration
+_SINGLE_VIOLATIONS = [
+    ("bits", 8, q.MOE_ERR_UNSUPPORTED), ("group_size", 128, q.MOE_ERR_UNSUPPORTED),
+    ("D", 2048 + 32, q.MOE_ERR_UNSUPPORTED), ("Dff", 768 + 8, q.MOE_ERR_UNSUPPORTED),
+    ("D", 16384 + 64, q.MOE_ERR_UNSUPPORTED), ("Dff", 8192 + 64, q.MOE_ERR_UNSUPPORTED),
+    ("E", 1025, q.MOE_ERR_UNSUPPORTED), ("top_k", 17, q.MOE_ERR_UNSUPPORTED),
+    ("E", 0, q.MOE_ERR_INVALID_ARG), ("top_k", 0, q.MOE_ERR_INVALID_ARG),
+    ("D", 0, q.MOE_ERR_INVALID_ARG), ("Dff", -64, q.MOE_ERR_INVALID_ARG),
+    ("max_tokens", 0, q.MOE_ERR_INVALID_ARG), ("max_tokens", 65, q.MOE_ERR_INVALID_ARG),
+    ("x_dtype", 2, q.MOE_ERR_INVALID_ARG), ("router_dtype", -1, q.MOE_ERR_INVALID_ARG),
+    ("out_dtype", 9, q.MOE_ERR_INVALID_ARG), ("mma_min_tokens", -3, q.MOE_ERR_INVALID_ARG),
+    ("flags", 1 << 5, q.MOE_ERR_INVALID_ARG),
+]
+
+
+def _status(**over):
+    base = dict(E=128, top_k=8, D=2048, Dff=768, bits=4, group_size=64, max_tokens=64,
+                x_dtype=q.MOE_DTYPE_BF16, router_dtype=q.MOE_DTYPE_BF16,
+                out_dtype=q.MOE_DTYPE_BF16, flags=0, mma_min_tokens=0)
+    base.update(over)
+    cfg = q.moe_config(base["E"], base["top_k"], base["D"], base["Dff"], base["bits"],
+                       base["group_size"], base["max_tokens"], base["x_dtype"],
+                       base["router_dtype"], base["out_dtype"], base["flags"],
+                       base["mma_min_tokens"])
+    n = ctypes.c_size_t(0)
+    return q.lib().moe_plan_workspace_bytes(ctypes.byref(cfg), ctypes.byref(n)), n.value
+
+
+@pytest.mark.parametrize("field,value,status", _SINGLE_VIOLATIONS,
+                         ids=[f"{f}={v}" for f, v, _ in _SINGLE_VIOLATIONS])
+def test_each_documented_rule_alone(libpath, field, value, status):
+    assert _status(**{field: value})[0] == status
+
+
+def test_random_valid_configs_are_accepted_and_sized(libpath):
+    import random
+    r = random.Random(7)
+    for _ in range(300):
+        E = r.randint(1, 1024)
+        cfg = dict(E=E, top_k=r.randint(1, min(E, 16)), D=64 * r.randint(1, 256),
+                   Dff=64 * r.randint(1, 128), max_tokens=r.randint(1, 64),
+                   x_dtype=r.choice([q.MOE_DTYPE_F32, q.MOE_DTYPE_BF16]),
+                   out_dtype=r.choice([q.MOE_DTYPE_F32, q.MOE_DTYPE_BF16]),
+                   mma_min_tokens=r.randint(0, 64))
+        st, nbytes = _status(**cfg)
+        assert st == q.MOE_OK, cfg
+        # the workspace holds at least h and y in f32 for every slot
+        S = cfg["max_tokens"] * cfg["top_k"]
+        assert nbytes >= 4 * S * (cfg["Dff"] + cfg["D"]), cfg
+        # and grows with the largest cohort
+        if cfg["max_tokens"] < 64:
+            assert _status(**dict(cfg, max_tokens=cfg["max_tokens"] + 1))[1] > nbytes, cfg
