@@ -37,8 +37,10 @@
  * round-trip bound on the original weights, a float64 brute-force dense
  * formulation built from library routines (numpy matmul, scipy softmax),
  * the E=1 and k=1 and k=E special cases, x=0, routing-weight sums, expert
- * storage-order and token-order permutations, identical tokens, and a stable
- * sort for the grouping.
+ * storage-order and token-order permutations, identical tokens, a stable
+ * sort for the grouping, and, for the final rounding, PyTorch's float32 to
+ * bfloat16 cast plus round-to-nearest-even taken from its definition on
+ * exact rational distances (ties, carries, subnormals, overflow, NaN).
  */
 #include <math.h>
 #include <stdint.h>

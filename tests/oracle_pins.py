@@ -313,6 +313,73 @@ def check_expert_shards_sum_to_the_step():
         assert np.abs(total - full["out"]).max() <= 1e-6 * _rms(full["out"]), G
 
 
+def _bf16_by_definition(u: int) -> int:
+    """bf16 bits of the f32 with bits u, rounded to nearest with ties to an even
+    last mantissa bit (IEEE 754 roundTiesToEven), taken from the definition: the
+    two bf16 values that bracket the input are compared by exact rational
+    distance. A magnitude that rounds past the largest finite bf16 goes to
+    infinity, as if the exponent range were unbounded (IEEE overflow rule)."""
+    from fractions import Fraction
+
+    def value(bits32):
+        sign = -1 if bits32 >> 31 else 1
+        exp = (bits32 >> 23) & 0xFF
+        man = bits32 & 0x7FFFFF
+        if exp == 0:
+            return sign * Fraction(man, 1 << 149)
+        return sign * Fraction((1 << 23) | man, 1 << 23) * Fraction(2) ** (exp - 127)
+
+    sign = u & 0x80000000
+    mag = u & 0x7FFFFFFF
+    if mag >= 0x7F800000:
+        return (u >> 16) & 0xFFFF  # infinities pass through (NaN is checked apart)
+    lo = mag & 0xFFFF0000          # the bf16 at or below |v|
+    hi = lo + 0x10000              # the next bf16 up (0x7F800000 is infinity)
+    v = value(mag)
+    d_lo = v - value(lo)
+    d_hi = (Fraction(2) ** 128 if hi == 0x7F800000 else value(hi)) - v
+    if d_lo < d_hi:
+        pick = lo
+    elif d_hi < d_lo:
+        pick = hi
+    else:
+        pick = lo if ((lo >> 16) & 1) == 0 else hi
+    return ((sign | pick) >> 16) & 0xFFFF
+
+
+def check_final_rounding_vs_library():
+    """The single final rounding (f32 -> bf16, round to nearest even) against two
+    references that do not share the oracle's bit formula: PyTorch's CPU
+    float32 -> bfloat16 conversion, and the definition above on exact rational
+    distances. Cases: exact ties with an even and with an odd lower neighbour,
+    one ulp either side of a tie, carries into the exponent, +-0, subnormals,
+    the largest finite values (overflow to infinity), infinities, NaN, and
+    random bit patterns."""
+    import torch
+    rng = np.random.default_rng(23)
+    special_u = [0x00000000, 0x80000000, 0x00000001, 0x80000001, 0x00008000, 0x00018000,
+                 0x00007FFF, 0x00008001, 0x007FFFFF, 0x807FFFFF, 0x00800000, 0x3F7FFFFF,
+                 0x3FFFFFFF, 0xBFFFFFFF, 0x3F808000, 0x3F818000, 0x3F807FFF, 0x3F808001,
+                 0x7F7FFFFF, 0xFF7FFFFF, 0x7F7F7FFF, 0x7F7F8000, 0x7F7E8000, 0x7F800000,
+                 0xFF800000, 0x7FC00000, 0x7F800001, 0xFFFFFFFF, 0x7F7F0000]
+    ties = [(int(b) << 16) | 0x8000 for b in rng.integers(0, 0x7F7F, 64)]
+    near = [t + d for t in ties[:16] for d in (-1, 1)]
+    rand = [int(v) for v in rng.integers(0, 1 << 32, 4096, dtype=np.uint64)]
+    normals = [int(v) for v in (rng.standard_normal(2048).astype(np.float32) *
+                                np.float32(3.0)).view(np.uint32)]
+    u = np.array(special_u + ties + near + rand + normals, dtype=np.uint64).astype(np.uint32)
+    f = u.view(np.float32)
+    got = oracle.round_bf16(f)
+    lib_bits = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    nan = np.isnan(f)
+    got_nan = (got & 0x7F80) == 0x7F80
+    got_nan &= (got & 0x7F) != 0
+    assert np.array_equal(got_nan, nan), "NaN inputs must give NaN, and only they"
+    assert np.array_equal(got[~nan], lib_bits[~nan]), "final rounding differs from torch's bf16 cast"
+    by_def = np.array([_bf16_by_definition(int(v)) for v in u[~nan]], dtype=np.uint16)
+    assert np.array_equal(got[~nan], by_def), "final rounding differs from round-to-nearest-even"
+
+
 ALL_CHECKS = [
     check_quant_roundtrip,
     check_dequant_known_codes,
@@ -326,4 +393,5 @@ ALL_CHECKS = [
     check_closed_form_golden,
     check_invariants,
     check_expert_shards_sum_to_the_step,
+    check_final_rounding_vs_library,
 ]

@@ -36,6 +36,9 @@ MUTANTS = {
     "offsets_inclusive": ("offsets[e + 1] = offsets[e] + counts[e];",
                           "offsets[e + 1] = offsets[e] + counts[e] + (e == 0);"),
     "final_round_truncates": ("u += 0x7FFFu + ((u >> 16) & 1u);", ""),
+    "final_round_ties_to_odd": ("u += 0x7FFFu + ((u >> 16) & 1u);",
+                                "u += 0x7FFFu + (((u >> 16) & 1u) ^ 1u);"),
+    "final_round_ties_away": ("u += 0x7FFFu + ((u >> 16) & 1u);", "u += 0x8000u;"),
 }
 
 
