@@ -84,9 +84,10 @@ enum {
      * at least mma_min_tokens tokens) instead of chunks of the single-launch
      * kernel; see moe_decode_forward */
     MOE_FLAG_GROUPED_COHORTS = 1u << 3,
-    /* TEST ONLY: in the fused path, CTA 0 skips the first grid barrier, so
-     * every other CTA's bounded wait runs out (about 1 s) and the step ends
-     * with MOE_ERR_TIMEOUT reported by moe_plan_check. Output is garbage. */
+    /* TEST ONLY: in the plan's first forward call on the fused path, CTA 0
+     * reaches the first grid barrier only after another CTA's bounded wait has
+     * run out (about 1 s), so that step ends with a recorded timeout and
+     * garbage output; later calls of the plan run normally. */
     MOE_FLAG_TEST_STALL = 1u << 8
 };
 
@@ -120,17 +121,23 @@ typedef struct {
 
 typedef struct moe_plan moe_plan;
 
-/* Library ABI version (MOE_ABI_VERSION of the build). */
+/* Library ABI version (MOE_ABI_VERSION of the build). No counterpart on the
+ * pages (a library utility). */
 int moe_abi_version(void);
 
-/* Human-readable name of a status code (static string). */
+/* Human-readable name of a status code (static string). Source: #1616
+ * Implementation Notes (errors are returned so the caller can fall back). */
 const char *moe_status_str(moe_status s);
 
 /* Device bytes a plan for cfg would allocate. Host-only; no CUDA call.
- * Returns INVALID_ARG / UNSUPPORTED exactly as moe_plan_create would. */
+ * Returns INVALID_ARG / UNSUPPORTED exactly as moe_plan_create would.
+ * Source: #1616 Implementation Notes (validate shapes before dispatch). */
 moe_status moe_plan_workspace_bytes(const moe_config *cfg, size_t *bytes);
 
 /* Validate cfg and allocate the plan's workspace on the current device.
+ * Source: #1616 Implementation Notes -- templating on k / Din / Dff / bits /
+ * group size with n_tokens a runtime extent, a decline for configurations the
+ * kernels do not cover, validation before any dispatch.
  * The plan is bound to that device. Decline (UNSUPPORTED): bits != 4,
  * group_size != 64, D or Dff not a multiple of 64, D > 16384, Dff > 8192,
  * E > 1024, top_k > 16. INVALID_ARG: null pointers, non-positive sizes,
@@ -140,7 +147,10 @@ moe_status moe_plan_workspace_bytes(const moe_config *cfg, size_t *bytes);
  * until moe_plan_free. */
 moe_status moe_plan_create(const moe_config *cfg, moe_plan **out);
 
-/* One decode step.
+/* One decode step. Source: #1616 Current Behavior (the routed decode block:
+ * router, SwitchGLU experts, moe_weighted_sum) and Proposed Solution (a token
+ * dimension and one read of each selected expert plane per step); #1859
+ * Problem / Background (the per-(token, k) gather this replaces).
  *   x           [n_tokens, D] of cfg.x_dtype (device)
  *   router_w    [E, D] of cfg.router_dtype (device)
  *   router_bias [E] f32 added to the logits, or NULL (device)
@@ -162,13 +172,22 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan **out);
  *   MOE_FLAG_F32_DEBUG, or a shape the single-launch kernel declines:
  *                    the grouped multi-kernel path with f32 GEMV kernels.
  * Asynchronous. Returns INVALID_ARG before any launch on a bad argument,
- * CUDA if a launch fails. A device-side timeout of the step's internal
- * waits is reported by the NEXT call on the plan, or by moe_plan_check. */
+ * CUDA if a launch fails.
+ * Device-side errors. Every wait inside a step is bounded (about 1 s); a wait
+ * that gives up records MOE_ERR_TIMEOUT in the plan and the step's output is
+ * garbage. Once that step has finished on the device, the next call on the
+ * plan (this one, moe_decode_forward_host, or moe_plan_check) returns
+ * MOE_ERR_TIMEOUT (MOE_ERR_CUDA for an internal error) and clears it; a
+ * forward call that reports it launches nothing and only enqueues two small
+ * memsets that reset the plan's error state on `stream`. A step that was
+ * still running at the time is reported by a later call. The steps after a
+ * timed-out one run normally: the grid-barrier counters stay consistent. */
 moe_status moe_decode_forward(moe_plan *plan, const void *x, const void *router_w,
                               const float *router_bias, const moe_expert_planes *planes,
                               int n_tokens, int top_k, void *out, void *stream);
 
-/* The same step with x and out in HOST memory: copies x to the plan's device
+/* The same step with x and out in HOST memory (#1616 Current Behavior: the
+ * decode tick of a serving loop hands activations in and out): copies x to the plan's device
  * staging buffer, runs moe_decode_forward, copies out back and synchronises
  * the stream before returning. Pinned host memory gives asynchronous copies;
  * pageable memory works but is slower. */
@@ -185,11 +204,13 @@ moe_status moe_decode_forward_host(moe_plan *plan, const void *x_host, const voi
  * such callers.
  *
  * Runs the same single-launch kernel as moe_decode_forward, so it accepts what
- * that kernel accepts: n_tokens 1..8, no MOE_FLAG_F32_DEBUG, and the shapes the
- * kernel supports (otherwise MOE_ERR_UNSUPPORTED). cfg gives the layer shape
- * and dtypes (max_tokens and flags are ignored; no phase timing, no routing
- * copy-out). All other arguments are as for moe_decode_forward; the caller
- * still owns x, router_w, router_bias, the planes and out.
+ * that kernel accepts: n_tokens 1..8 and the shapes the kernel supports
+ * (otherwise MOE_ERR_UNSUPPORTED). cfg gives the layer shape and dtypes.
+ * MOE_FLAG_F32_DEBUG in cfg.flags is declined (MOE_ERR_UNSUPPORTED); every
+ * other flag, and max_tokens, is ignored (no phase timing, no trace, no test
+ * hook, no routing copy-out). All other arguments are as for
+ * moe_decode_forward; the caller still owns x, router_w, router_bias, the
+ * planes and out.
  *
  * Scratch: one statically sized device array of 4 MiB inside the library,
  * which every GPU that loads the library holds until the process exits. A call
@@ -200,7 +221,9 @@ moe_status moe_decode_forward_host(moe_plan *plan, const void *x_host, const voi
  *
  * The first call on a device looks up the array's device address on the
  * current device (a one-time set-up); make that first call before any stream
- * capture. Every call on a device shares the one array: calls that overlap on
+ * capture. The address is kept per device ordinal for the life of the
+ * process: after cudaDeviceReset, or with a context other than the device's
+ * primary context current, it is stale and this call must not be used. Every call on a device shares the one array: calls that overlap on
  * the GPU (different streams without ordering) race and give wrong results.
  * Asynchronous; device-side timeouts are not reported by this call. */
 moe_status moe_decode_forward_noalloc(const moe_config *cfg, const void *x, const void *router_w,
@@ -208,11 +231,14 @@ moe_status moe_decode_forward_noalloc(const moe_config *cfg, const void *x, cons
                                       int n_tokens, int top_k, void *out, void *stream);
 
 /* Synchronise the plan's last stream and report a device-side timeout or
- * internal error recorded by earlier calls (then clear it). */
+ * internal error recorded by earlier calls (then clear it). Source: #1616
+ * Implementation Notes (errors are returned, never a terminate). */
 moe_status moe_plan_check(moe_plan *plan);
 
 /* Copy the routing and grouping of the plan's last forward call to HOST
  * arrays (any pointer may be NULL to skip it). Synchronises the last stream.
+ * Source: #1616 Leading hypothesis (slots sorted by expert id) and Proposed
+ * Solution (de-duplicated expert ids across the cohort).
  *   topk_idx [n,k] int32, topk_w [n,k] f32   (rank order: descending logit,
  *                                             ties to the lower expert id)
  *   counts [E], offsets [E+1]                (exclusive scan of counts)
@@ -224,7 +250,9 @@ moe_status moe_get_routing(moe_plan *plan, int32_t *topk_idx, float *topk_w,
                            int32_t *slot_k, int32_t *unique, int32_t *U);
 
 /* Phase timestamps (ns, %globaltimer) of the last fused step of a plan created
- * with MOE_FLAG_PHASE_TIMES: for each CTA c, times[c*16 + i] with
+ * with MOE_FLAG_PHASE_TIMES. Source: #1859 Proposed Solution step 2 (split the
+ * step into router, expert gather and combine and attribute the time): for
+ * each CTA c, times[c*16 + i] with
  *   i = 0 start, 1 router done, 2 after grid barrier 1, 3 routing and work
  *   lists done, 4 gate/up done, 5 after grid barrier 2, 6 down done, 7 end;
  *   8/9 gate/up ns spent waiting for data / computing (consumer warp 0),
@@ -235,10 +263,12 @@ moe_status moe_get_routing(moe_plan *plan, int32_t *topk_idx, float *topk_w,
 moe_status moe_get_phase_times(moe_plan *plan, uint64_t *times, int max_entries, int *ctas);
 
 /* Number of CUDA kernels this plan has enqueued since creation (host
- * counter; forward calls captured into a CUDA graph count once, at capture). */
+ * counter; forward calls captured into a CUDA graph count once, at capture).
+ * Source: #1859 Proposed Solution step 2 (attribute time per kernel). */
 moe_status moe_plan_launch_count(const moe_plan *plan, uint64_t *count);
 
-/* Free the plan's workspace (synchronises its last stream). NULL is a no-op. */
+/* Free the plan's workspace (synchronises its last stream). NULL is a no-op.
+ * No counterpart on the pages (a library utility). */
 moe_status moe_plan_free(moe_plan *plan);
 
 #ifdef __cplusplus

@@ -212,9 +212,19 @@ __device__ __forceinline__ Smem carve_smem(unsigned char *base, const DecodeLayo
     return s;
 }
 
+// Record a device-side error: the bit in the plan's status word, and a 1 in the
+// host-mapped words whose device address the host stored in status words 2..3
+// (word 0 for a timeout, word 1 for an internal error; address 0 when the host
+// has none), so that the next forward call can report it without synchronising.
+__device__ __forceinline__ void report_error(unsigned *status, unsigned bit) {
+    atomicOr(status, bit);
+    const unsigned long long host = *reinterpret_cast<volatile unsigned long long *>(status + 2);
+    if (host) reinterpret_cast<volatile unsigned *>(host)[bit == kDevErrTimeout ? 0 : 1] = 1u;
+}
+
 __device__ __forceinline__ void set_timeout(volatile int *abort_flag, unsigned *status) {
     *abort_flag = 1;
-    atomicOr(status, kDevErrTimeout);
+    report_error(status, kDevErrTimeout);
 }
 
 // Bounded wait on an mbarrier phase; false on timeout or abort. The waiting
@@ -517,12 +527,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     }
 
     // ---- grid barrier 1: all logits written -------------------------------------
+    // Every CTA arrives at both grid barriers exactly once on every path (after
+    // a timeout too), so the counter is base + 2G when a launch ends and the
+    // next launch starts from a multiple of 2G; the rounding below only guards
+    // against a counter corrupted from outside.
     stamp(W.phase_ns, timing, 1);
     if (tid == 0) epoch = epoch / (2ull * G) * (2ull * G);
-    if (!((A.s.flags & MOE_FLAG_TEST_STALL) && cta == 0))
-        grid_barrier(gsync, epoch + G, bar_ok, abort_flag, W.status);
-    else
-        __syncthreads();  // test hook: CTA 0 never arrives; the others time out
+    if ((A.s.flags & MOE_FLAG_TEST_STALL) && cta == 0) {
+        // test hook: CTA 0 arrives late, only once another CTA's bounded wait has
+        // given up (or after 2 s), so the others time out while the counter still
+        // ends the launch consistent
+        if (tid == 0) {
+            const unsigned long long t0 = globaltimer();
+            while (!(*reinterpret_cast<volatile unsigned *>(W.status) & kDevErrTimeout) &&
+                   globaltimer() - t0 < 2 * kWaitNs) {
+            }
+        }
+        __syncthreads();
+    }
+    grid_barrier(gsync, epoch + G, bar_ok, abort_flag, W.status);
     stamp(W.phase_ns, timing, 2);
 
     // ---- phase T: routing and grouping, redundantly in every CTA ---------------
@@ -600,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
         }
         if (lane == 0) {
             if (tb > L.max_tiles) {
-                atomicOr(W.status, kDevErrInternal);  // the host bounds the count
+                report_error(W.status, kDevErrInternal);  // the host bounds the count
                 tb = L.max_tiles;
             }
             S.misc[3] = tb;
@@ -905,8 +928,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     // ---- grid barrier 2: every h row written ----------------------------------
     stamp(W.phase_ns, timing, 4);
     ptx::named_bar(2, kConsThreads + 64);  // the reducers have written every h row of this CTA
-    if (!((A.s.flags & MOE_FLAG_TEST_STALL) && cta == 0))
-        grid_barrier(gsync, epoch + 2ull * G, bar_ok, abort_flag, W.status, true);
+    grid_barrier(gsync, epoch + 2ull * G, bar_ok, abort_flag, W.status, true);
     stamp(W.phase_ns, timing, 5);
 
     // ---- phase B: down, all experts summed per warp ----------------------------

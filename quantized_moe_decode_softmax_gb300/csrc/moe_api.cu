@@ -187,6 +187,25 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan **out) {
         free(p);
         return MOE_ERR_CUDA;
     }
+    // the host-mapped error word: the device writes it on a timeout, so the next
+    // forward call can report the error without a synchronisation. Without
+    // mapped host memory, errors are reported by moe_plan_check only.
+    p->host_err = nullptr;
+    {
+        void *h = nullptr, *d = nullptr;
+        if (cudaHostAlloc(&h, 64, cudaHostAllocMapped) == cudaSuccess) {
+            memset(h, 0, 64);
+            unsigned long long dev_addr = 0;
+            if (cudaHostGetDevicePointer(&d, h, 0) == cudaSuccess && d) {
+                dev_addr = (unsigned long long)(uintptr_t)d;
+                if (cudaMemcpy(p->ws.status + 2, &dev_addr, sizeof dev_addr, cudaMemcpyHostToDevice) ==
+                    cudaSuccess)
+                    p->host_err = static_cast<volatile unsigned *>(h);
+            }
+            if (!p->host_err) cudaFreeHost(h);
+        }
+        cudaGetLastError();
+    }
     p->last_stream = nullptr;
     *out = p;
     return MOE_OK;
@@ -206,10 +225,24 @@ moe_status moe_decode_forward(moe_plan *plan, const void *x, const void *router_
 
     DeviceGuard guard(plan->device);
     cudaStream_t s = (cudaStream_t)stream;
+    // an error a finished earlier step recorded on the device: report it, clear
+    // the plan's error state on this stream, and run nothing
+    if (plan->host_err && (plan->host_err[0] || plan->host_err[1])) {
+        const bool timeout = plan->host_err[0] != 0u;
+        plan->host_err[0] = plan->host_err[1] = 0u;
+        if (cudaMemsetAsync(plan->ws.status, 0, sizeof(unsigned), s) != cudaSuccess ||
+            cudaMemsetAsync(plan->ws.sync, 0, 64 * sizeof(unsigned), s) != cudaSuccess) {
+            cudaGetLastError();
+            return MOE_ERR_CUDA;
+        }
+        return timeout ? MOE_ERR_TIMEOUT : MOE_ERR_CUDA;
+    }
     StepArgs a{};
+    // the test hook stalls only the plan's first step
+    const unsigned step_flags = plan->forwards == 0 ? plan->cfg.flags : plan->cfg.flags & ~(unsigned)MOE_FLAG_TEST_STALL;
     a.s = Shape{plan->cfg.E, plan->cfg.top_k, plan->cfg.D, plan->cfg.Dff, n_tokens,
                 plan->cfg.x_dtype, plan->cfg.router_dtype, plan->cfg.out_dtype,
-                plan->cfg.flags};
+                step_flags};
     a.x = x;
     a.router_w = router_w;
     a.router_bias = router_bias;
@@ -277,6 +310,7 @@ moe_status moe_decode_forward(moe_plan *plan, const void *x, const void *router_
         if (err == cudaSuccess) err = launch_experts_f32(a, plan->ws, thr, s, launched);
     }
     plan->launches += launched;
+    plan->forwards += 1;
     plan->last_stream = s;
     plan->last_n = n_tokens;
     if (err != cudaSuccess) {
@@ -323,10 +357,11 @@ moe_status moe_plan_check(moe_plan *plan) {
         cudaGetLastError();
         return MOE_ERR_CUDA;
     }
+    if (plan->host_err) plan->host_err[0] = plan->host_err[1] = 0u;
     if (status) {
-        // clear the status word and the grid-barrier counters a timed-out
-        // step may have left mid-way
-        cudaMemset(plan->ws.status, 0, 4 * sizeof(unsigned));
+        // clear the error bits (words 2..3 keep the host word's address) and the
+        // grid-barrier counters
+        cudaMemset(plan->ws.status, 0, sizeof(unsigned));
         cudaMemset(plan->ws.sync, 0, 64 * sizeof(unsigned));
         cudaDeviceSynchronize();
         return (status & kDevErrTimeout) ? MOE_ERR_TIMEOUT : MOE_ERR_CUDA;
@@ -394,6 +429,10 @@ moe_status moe_plan_free(moe_plan *plan) {
             st = MOE_ERR_CUDA;
         }
         if (cudaFree(plan->ws_base) != cudaSuccess) {
+            cudaGetLastError();
+            st = MOE_ERR_CUDA;
+        }
+        if (plan->host_err && cudaFreeHost((void *)plan->host_err) != cudaSuccess) {
             cudaGetLastError();
             st = MOE_ERR_CUDA;
         }

@@ -41,7 +41,8 @@ struct Workspace {
     int *U;             // [1]
     float *h;           // [max_n * k, Dff]  grouped position major
     float *y;           // [max_n * k, D]    grouped position major
-    unsigned *status;   // [4]   device error bits
+    unsigned *status;   // [4]   [0] device error bits; [2..3] device address of the
+                        //       plan's host-mapped error word (0: none)
     unsigned *sync;     // [64]  barrier counters (zeroed at plan creation)
     unsigned long long *phase_ns;  // [256] optional phase timestamps
     void *x_stage;      // [max_n, D] host-call staging for x
@@ -118,6 +119,10 @@ struct moe_plan {
     int last_n;
     int mma_min_tokens;
     unsigned long long launches;  // kernels enqueued by this plan since creation
+    unsigned long long forwards;  // moe_decode_forward calls that launched
+    // pinned, device-mapped word set by the device on a timeout or internal
+    // error (null if the driver could not map host memory)
+    volatile unsigned *host_err;
     bool fused_ok;                // the single-launch kernel can run this shape
     moe::DecodeLayout fused;
     // tensor maps of recently used plane sets (a layer stack or replicas cycle

@@ -55,8 +55,10 @@ def test_fused_matches_f32_check_path():
 
 
 def test_device_wait_times_out_and_context_stays_usable():
-    """A grid barrier that one CTA never reaches: the other CTAs' bounded waits
-    give up, the host reads MOE_ERR_TIMEOUT, and the next step is correct."""
+    """A grid barrier that one CTA reaches only after the others' bounded waits
+    gave up: moe_plan_check reports MOE_ERR_TIMEOUT, and the NEXT step on the
+    SAME plan (whose barrier counter the stalled step left behind) matches the
+    oracle. No GPU fault or hang is involved: every wait is bounded."""
     import torch
     lay, x = case("qwen3", 2, 2)
     shape = lay.shape
@@ -68,12 +70,35 @@ def test_device_wait_times_out_and_context_stays_usable():
         plan.check()
     assert ei.value.status == q.MOE_ERR_TIMEOUT
     assert time.time() - t0 < 30
-    # same device, a normal plan: correct results
     ref = run_oracle(lay, x)
-    out, routing = run_gpu(make_plan(shape), dl, shape, x)
+    for _ in range(2):  # the same plan, twice
+        out, routing = run_gpu(plan, dl, shape, x)
+        assert_routing_equal(routing, ref)
+        assert_out_close(out, ref["out"], TOL_BF16)
+    torch.cuda.synchronize()
+
+
+def test_timeout_is_reported_by_the_next_forward_call():
+    """The stalled step has finished on the device: the next forward call on the
+    plan returns MOE_ERR_TIMEOUT without launching, and the call after it runs
+    normally and matches the oracle (no moe_plan_check in between)."""
+    import torch
+    lay, x = case("qwen3", 2, 3)
+    shape = lay.shape
+    dl = device_layer(lay)
+    plan = make_plan(shape, flags=q.MOE_FLAG_TEST_STALL)
+    xt = x_tensor(shape, x)
+    plan.forward(xt, dl)
+    torch.cuda.synchronize()
+    c0 = q.moe_plan_launch_count(plan.plan)
+    with pytest.raises(q.MoeError) as ei:
+        plan.forward(xt, dl)
+    assert ei.value.status == q.MOE_ERR_TIMEOUT
+    assert q.moe_plan_launch_count(plan.plan) == c0
+    ref = run_oracle(lay, x)
+    out, routing = run_gpu(plan, dl, shape, x)  # also runs moe_plan_check: clear
     assert_routing_equal(routing, ref)
     assert_out_close(out, ref["out"], TOL_BF16)
-    torch.cuda.synchronize()
 
 
 def test_phase_times_are_ordered():

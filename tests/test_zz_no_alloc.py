@@ -4,9 +4,11 @@ plan-based one, through the C ABI.
 Callers that cannot allocate device memory (for example code running during
 CUDA graph capture, or runtimes that own the device memory pool) use
 moe_decode_forward_noalloc, whose scratch is a static device array of the
-library. Its output must match moe_decode_forward's within the bf16 tolerance
-of the parity tests, on two calls in a row (the second call reuses the array
-the first one left behind). This file is collected last on purpose.
+library. It runs the same kernel on the same inputs as moe_decode_forward, so
+its output must equal that entry point's output bit for bit (which is within
+the bf16 tolerance of the parity tests), on two calls in a row (the second
+call reuses the array the first one left behind). This file is collected last
+on purpose.
 """
 import numpy as np
 import pytest
@@ -33,6 +35,7 @@ def test_noalloc_matches_plan_entry_point_twice(n):
         got = out.float().cpu().numpy()
         assert np.all(np.isfinite(got))
         assert_out_close(got, ref, TOL_BF16)
+        assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), "bits differ from the plan path" 
 
 
 def test_noalloc_declines_what_its_kernel_cannot_run():
