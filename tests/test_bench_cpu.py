@@ -7,7 +7,8 @@ import bench
 
 def test_traffic_is_reported_only_for_the_captured_sources(monkeypatch):
     t = bench.TRAFFIC[("qwen3", 1)]
-    assert t["src"] == bench.kernel_src_hash(), "re-capture the ncu traffic after a kernel change"
+    # as if the sources were the captured ones
+    monkeypatch.setattr(bench, "kernel_src_hash", lambda: t["src"])
     # scaled to the timed steps' mean unique-expert count
     assert bench.traffic_per_launch("qwen3", 1, t["unique"]) == t["bytes"]
     assert bench.traffic_per_launch("qwen3", 1, 2 * t["unique"]) == 2 * t["bytes"]
