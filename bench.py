@@ -67,7 +67,9 @@ def parse_args():
     ap.add_argument("--phases", action="store_true",
                     help="also time the fused kernel's phases (router / gate-up / down)")
     ap.add_argument("--sustain-seconds", type=float, default=1.5,
-                    help="graph replays before the timed one, while clocks are sampled")
+                    help="graph replays before the timed ones, while clocks are sampled")
+    ap.add_argument("--runs", type=int, default=7,
+                    help="timed replays of the K-step graph (value = the median run)")
     return ap.parse_args()
 
 
@@ -206,8 +208,29 @@ def max_over_ranks(pg, value: float, device=None) -> float:
 # ----------------------------------------------------------------------------
 # oracle (CPU) timing: the reference arm and the cpu_baseline key
 # ----------------------------------------------------------------------------
-def oracle_sample(shape_name, n, kind, cohorts, seconds):
-    """Time the CPU oracle on cohorts of the workload for about `seconds`."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name:"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def oracle_sample(shape_name, n, kind, cohorts, seconds, threads=None):
+    """Time the CPU oracle on cohorts of the workload for about `seconds`, on
+    `threads` OpenMP threads (default: every host core)."""
     import numpy as np
 
     import moe_synth as ms
@@ -218,7 +241,7 @@ def oracle_sample(shape_name, n, kind, cohorts, seconds):
     xs = [ms.draw_tokens(shape, router_w, bias, seed, 0, n, kind, cohort=c) for c in range(cohorts)]
     experts = sorted({e for x in xs for e in ms.routed_experts(x, router_w, bias, shape.top_k)})
     lay = ms.make_layer(shape, seed, 0, experts)
-    threads = oracle.set_threads(os.cpu_count() or 1)
+    threads = oracle.set_threads(threads or os.cpu_count() or 1)
     oracle.moe_forward(xs[0], router_w, bias, lay.planes, shape.top_k)  # warm
     steps, t0 = 0, time.perf_counter()
     while True:
@@ -228,8 +251,20 @@ def oracle_sample(shape_name, n, kind, cohorts, seconds):
         if el >= seconds:
             break
     return {"value": n * steps / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "cpu_model": cpu_model(),
             "sample": f"{steps} steps of n_tokens={n} ({kind} cohorts), {el:.1f} s, "
                       f"OpenMP over (token, expert) slots"}, steps, el
+
+
+def cpu_baseline(args):
+    """The oracle on all host cores, plus its single-thread leg."""
+    seconds = max(1.0, min(30.0, args.cpu_seconds))
+    cohorts = min(args.cohorts, 16)
+    cb, _, _ = oracle_sample(args.shape, args.n_tokens, args.kind, cohorts, seconds)
+    one, _, _ = oracle_sample(args.shape, args.n_tokens, args.kind, cohorts, seconds, threads=1)
+    cb["single_thread"] = {"value": one["value"], "unit": one["unit"], "cores": one["cores"],
+                           "sample": one["sample"]}
+    return cb
 
 
 def run_reference(args, world, rank, pg):
@@ -239,6 +274,10 @@ def run_reference(args, world, rank, pg):
     shape_name, n = args.shape, args.n_tokens
     seconds = max(1.0, min(30.0, args.cpu_seconds))
     cb, steps, el = oracle_sample(shape_name, n, args.kind, min(args.cohorts, 16), seconds)
+    one, _, _ = oracle_sample(shape_name, n, args.kind, min(args.cohorts, 16), min(seconds, 5.0),
+                              threads=1)
+    cb["single_thread"] = {"value": one["value"], "unit": one["unit"], "cores": one["cores"],
+                           "sample": one["sample"]}
     line = {
         "impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": steps, "warmup": 1, "ms_per_step": 1000.0 * el / steps,
@@ -351,20 +390,24 @@ def run_ours(args, world, rank, local, pg):
         while time.perf_counter() < t_end:
             graph.replay()
             stream.synchronize()
-        barrier(pg, local)
-        torch.cuda.synchronize()
-        start = torch.cuda.Event(enable_timing=True)
-        stop = torch.cuda.Event(enable_timing=True)
-        start.record(stream)
-        graph.replay()
-        stop.record(stream)
-        stop.synchronize()
-        torch.cuda.synchronize()
-        barrier(pg, local)
+        # R timed replays of the K-step graph, each bracketed by a barrier and a
+        # synchronize; the line reports the median run and the range
+        run_ms = []
+        for _ in range(max(1, args.runs)):
+            barrier(pg, local)
+            torch.cuda.synchronize()
+            start = torch.cuda.Event(enable_timing=True)
+            stop = torch.cuda.Event(enable_timing=True)
+            start.record(stream)
+            graph.replay()
+            stop.record(stream)
+            stop.synchronize()
+            torch.cuda.synchronize()
+            barrier(pg, local)
+            run_ms.append(max_over_ranks(pg, start.elapsed_time(stop), dev))
         clocks = sampler.stop() if sampler else None
-    elapsed_ms = start.elapsed_time(stop)
     layer.check()
-    elapsed_ms = max_over_ranks(pg, elapsed_ms, dev)
+    elapsed_ms = statistics.median(run_ms)
     ms_per_step = elapsed_ms / K
 
     # per-step device time (each step's events), same inputs
@@ -408,13 +451,15 @@ def run_ours(args, world, rank, local, pg):
         phases = phase_split(q, shape, args, xs, reps, dev, n)
 
     if rank == 0:
-        cb = None
-        if not args.no_cpu_baseline:
-            cb, _, _ = oracle_sample(args.shape, n, args.kind, min(args.cohorts, 16),
-                                     max(1.0, min(30.0, args.cpu_seconds)))
+        cb = None if args.no_cpu_baseline else cpu_baseline(args)
+        tok = sorted(world * n * K / (m / 1000.0) for m in run_ms)
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": K, "warmup": W, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "runs": {"n": len(run_ms), "value_is": "median run",
+                     "ms_per_step": {"min": min(run_ms) / K, "median": ms_per_step,
+                                     "max": max(run_ms) / K},
+                     "tokens_per_s": {"min": tok[0], "median": value, "max": tok[-1]}},
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded; random-init weights of the layer shape)",
             "config": workload_config(args),

@@ -63,12 +63,38 @@ def make_plan(shape, flags=0, out_dtype=None, max_tokens=64, mma_min_tokens=0):
                           mma_min_tokens=mma_min_tokens)
 
 
-def run_gpu(plan, dl, shape, x):
+# measured parity margins of this session: one dict per compared output
+MARGINS: list = []
+
+
+def path_name(n, launches, flags=0):
+    """Which path a forward call took, from the kernels it launched."""
+    if flags & 1:
+        return "grouped, f32 check path"
+    if launches == 1:
+        return "single launch"
+    if 9 <= n <= 16 and launches == (n + 7) // 8 + 1:
+        return f"chunks of the single launch ({(n + 7) // 8})"
+    return "grouped multi-kernel"
+
+
+def record_margin(test, shape_name, n, kind, path, out_dtype, tol, err_rel):
+    MARGINS.append(dict(test=test, shape=shape_name, n=int(n), kind=kind, path=path,
+                        out=out_dtype or "act", tol=tol, err_rel=err_rel,
+                        used=err_rel / tol if tol else None))
+
+
+def run_gpu(plan, dl, shape, x, launches=None):
+    """Forward through the C ABI; `launches` (a list) receives the kernel count."""
     import torch
+    from quantized_moe_decode_softmax_gb300 import moe_plan_launch_count
     xt = x_tensor(shape, x)
+    c0 = moe_plan_launch_count(plan.plan)
     out = plan.forward(xt, dl)
     torch.cuda.synchronize()
     plan.check()
+    if launches is not None:
+        launches.append(moe_plan_launch_count(plan.plan) - c0)
     return out.float().cpu().numpy(), plan.routing(x.shape[0])
 
 

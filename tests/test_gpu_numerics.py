@@ -1,0 +1,107 @@
+"""Numerics of the tensor-core paths beyond the bf16 tolerance (GPU).
+
+1. Cohort order. A row permutation of x permutes the output rows bit for bit,
+   on the single launch, the chunks of it and the grouped path (tile and GEMV
+   variants): every token's result is computed independently of its position.
+
+2. A derived error model for the single-launch kernel with f32 output. The
+   kernel rounds three things the oracle keeps in f32:
+     - h' = w * silu(g) * u is stored as bf16 (round to nearest even): an
+       absolute error uniform in +-ulp(h')/2, variance ulp(h')^2 / 12;
+     - gate/up accumulate (1024 m + q) x / m and subtract 1024 sum(x / m) per
+       group (and the down projection 128 + q against h): f32 cancellation of
+       a few ulps of 1024 sum|x|, below 2^-13 of h' (taken as a relative error
+       of that size);
+     - x enters the MMA as f16: exact for bf16 x inside f16's range, a relative
+       error of at most 2^-11 for f32 x (taken as that relative error on h').
+   Each output element is out[t, d] = sum_j sum_f Wd_j[d, f] h'_jf, so its error
+   is a sum of independent terms with variance
+     var[t, d] = sum_j sum_f Wd_j[d, f]^2 (ulp(h'_jf)^2 / 12 + (c h'_jf)^2),
+   c^2 = 2^-26 (+ 2^-22 / 3 for f32 x). The test requires every element within
+   6 standard deviations (one element of a few ten thousand exceeds 6 sigma
+   with probability below 1e-4 under the model), with an absolute floor of
+   1e-6 RMS(out).
+"""
+import numpy as np
+import pytest
+
+import moe_synth as ms
+import oracle
+from gpu_cases import (TOL_BF16, assert_out_close, case, device_layer, make_plan, path_name,
+                       record_margin, rms, run_gpu, run_oracle, x_tensor)
+
+pytestmark = pytest.mark.gpu
+
+GROUPED = 1 << 3  # MOE_FLAG_GROUPED_COHORTS
+
+
+@pytest.mark.parametrize("shape_name,n,kind,flags,mma_min", [
+    ("qwen3", 8, "independent", 0, 0),        # single launch
+    ("qwen3", 12, "independent", 0, 0),       # two chunks of the single launch
+    ("qwen3", 24, "independent", 0, 0),       # grouped: GEMV variant
+    ("qwen3", 24, "shared", GROUPED, 0),      # grouped: tile variant (24 tokens per expert)
+    ("tiny", 5, "independent", 0, 0),         # grouped (shape the single launch declines)
+])
+def test_row_permutation_permutes_output_rows_bitwise(shape_name, n, kind, flags, mma_min):
+    import torch
+    lay, x = case(shape_name, 2 if shape_name == "qwen3" else 0, n, kind,
+                  full=shape_name == "tiny")
+    shape = lay.shape
+    dl = device_layer(lay)
+    plan = make_plan(shape, flags=flags, mma_min_tokens=mma_min)
+    perm = np.random.default_rng(n).permutation(n)
+    xt = x_tensor(shape, x)
+    a = plan.forward(xt, dl).clone()
+    b = plan.forward(x_tensor(shape, x[perm]), dl).clone()
+    torch.cuda.synchronize()
+    plan.check()
+    bits = torch.int16 if a.dtype == torch.bfloat16 else torch.int32
+    assert torch.equal(b.view(bits).cpu(), a.view(bits).cpu()[torch.from_numpy(perm)])
+
+
+def _error_sigma(lay, x, ref):
+    """Per-element standard deviation of the single-launch kernel's f32 output
+    error under the model in the module docstring."""
+    shape = lay.shape
+    n, D = x.shape
+    c2 = 2.0 ** -26 + (2.0 ** -22 / 3.0 if shape.act_dtype == "f32" else 0.0)
+    var = np.zeros((n, D), np.float64)
+    deq = {}
+    for t in range(n):
+        for j in range(shape.top_k):
+            e = int(ref["topk_idx"][t, j])
+            if e not in deq:
+                p = lay.planes
+                deq[e] = oracle.dequant(p.down_q[e], p.down_s[e], p.down_b[e]).astype(np.float64)
+            h, _ = oracle.expert_mlp(x[t], lay.planes, e)
+            hp = float(ref["topk_w"][t, j]) * h.astype(np.float64)
+            _, ex = np.frexp(hp)  # |hp| in [2^(ex-1), 2^ex)
+            ulp = np.where(hp != 0.0, np.ldexp(1.0, ex - 1 - 7), 0.0)
+            per_f = ulp ** 2 / 12.0 + c2 * hp ** 2
+            var[t] += np.square(deq[e]) @ per_f
+    return np.sqrt(var)
+
+
+@pytest.mark.parametrize("shape_name,seed,n,kind", [
+    ("qwen3", 2, 1, "independent"),
+    ("qwen3", 2, 4, "independent"),
+    ("qwen3", 2, 8, "shared"),
+    ("k1", 5, 5, "independent"),   # f32 activations on the single launch
+    ("e256", 3, 1, "independent"),
+])
+def test_single_launch_f32_output_within_the_derived_error_model(shape_name, seed, n, kind):
+    lay, x = case(shape_name, seed, n, kind, full=shape_name == "k1")
+    shape = lay.shape
+    ref = run_oracle(lay, x)
+    plan = make_plan(shape, out_dtype="f32")
+    launches = []
+    out, _ = run_gpu(plan, device_layer(lay), shape, x, launches)
+    assert launches[0] == 1, "this case must run on the single launch"
+    sigma = _error_sigma(lay, x, ref)
+    r = rms(ref["out"])
+    err = np.abs(out.astype(np.float64) - ref["out"].astype(np.float64))
+    z = err / np.maximum(sigma, 1e-6 * r)
+    record_margin(f"model z max {z.max():.2f} (bound 6)", shape_name, n, kind,
+                  path_name(n, launches[0]), "f32", TOL_BF16, float(err.max()) / r)
+    assert z.max() <= 6.0, f"max |err| / sigma = {z.max():.2f}"
+    assert_out_close(out, ref["out"], TOL_BF16)

@@ -9,7 +9,8 @@ import pytest
 
 import moe_synth as ms
 from gpu_cases import (TOL_BF16, TOL_F32, assert_out_close, assert_routing_equal, case,
-                       device_layer, make_plan, run_gpu, run_oracle, x_tensor)
+                       device_layer, make_plan, path_name, record_margin, run_gpu, run_oracle,
+                       x_tensor)
 
 pytestmark = pytest.mark.gpu
 
@@ -19,14 +20,23 @@ GROUPED = 1 << 3  # MOE_FLAG_GROUPED_COHORTS
 
 def _check(shape_name, seed, n, kind="independent", full=False, flags=0, out_dtype=None,
            tol=None, mma_min_tokens=0):
+    import os
     lay, x = case(shape_name, seed, n, kind, full=full)
     shape = lay.shape
     ref = run_oracle(lay, x)
     plan = make_plan(shape, flags=flags, out_dtype=out_dtype, mma_min_tokens=mma_min_tokens)
-    out, routing = run_gpu(plan, device_layer(lay), shape, x)
+    launches = []
+    out, routing = run_gpu(plan, device_layer(lay), shape, x, launches)
     assert_routing_equal(routing, ref)
     if tol is None:
         tol = TOL_F32 if flags & F32_DEBUG else TOL_BF16
+    err = float(np.abs(out.astype(np.float64) - ref["out"].astype(np.float64)).max())
+    err_rel = err / max(float(np.sqrt(np.mean(np.square(ref["out"].astype(np.float64))))), 1e-30)
+    path = path_name(n, launches[0], flags)
+    if mma_min_tokens:
+        path += f", tile threshold {mma_min_tokens}"
+    record_margin(os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0], shape_name, n, kind,
+                  path, out_dtype, tol, err_rel)
     return assert_out_close(out, ref["out"], tol)
 
 
