@@ -1,8 +1,10 @@
 """Numerics of the tensor-core paths beyond the bf16 tolerance (GPU).
 
 1. Cohort order. A row permutation of x permutes the output rows bit for bit,
-   on the single launch, the chunks of it and the grouped path (tile and GEMV
-   variants): every token's result is computed independently of its position.
+   on the single launch and the grouped path (tile and GEMV variants): every
+   token's result is computed independently of its position. On the chunks of
+   the single launch (9..16 tokens) this holds for permutations inside each
+   chunk; across chunks the rows agree within the bf16 tolerance.
 
 2. A derived error model for the single-launch kernel with f32 output. The
    kernel rounds three things the oracle keeps in f32:
@@ -49,13 +51,31 @@ def test_row_permutation_permutes_output_rows_bitwise(shape_name, n, kind, flags
     shape = lay.shape
     dl = device_layer(lay)
     plan = make_plan(shape, flags=flags, mma_min_tokens=mma_min)
-    perm = np.random.default_rng(n).permutation(n)
     xt = x_tensor(shape, x)
     a = plan.forward(xt, dl).clone()
+    bits = torch.int16 if a.dtype == torch.bfloat16 else torch.int32
+    rng = np.random.default_rng(n)
+    chunked = shape_name == "qwen3" and 9 <= n <= 16 and not flags
+    if chunked:
+        # Chunks of the single launch: a token's result depends, at the rounding
+        # level, on which experts share its chunk (the down projection's sum
+        # order over a chunk's expert set). A permutation inside each chunk
+        # keeps every chunk's token set and must permute rows bit for bit; a
+        # permutation across chunks stays within the bf16 tolerance.
+        half = n // 2  # two chunks of n/2 tokens (n even here)
+        inside = np.concatenate([rng.permutation(half), half + rng.permutation(n - half)])
+        b = plan.forward(x_tensor(shape, x[inside]), dl).clone()
+        across = rng.permutation(n)
+        c = plan.forward(x_tensor(shape, x[across]), dl).clone()
+        torch.cuda.synchronize()
+        plan.check()
+        assert torch.equal(b.view(bits).cpu(), a.view(bits).cpu()[torch.from_numpy(inside)])
+        assert_out_close(c.float().cpu().numpy(), a.float().cpu().numpy()[across], TOL_BF16)
+        return
+    perm = rng.permutation(n)
     b = plan.forward(x_tensor(shape, x[perm]), dl).clone()
     torch.cuda.synchronize()
     plan.check()
-    bits = torch.int16 if a.dtype == torch.bfloat16 else torch.int32
     assert torch.equal(b.view(bits).cpu(), a.view(bits).cpu()[torch.from_numpy(perm)])
 
 
