@@ -71,12 +71,13 @@ class LayerShape:
     router_std: float
     expert_std: float = 0.02
     zipf_s: float = 0.0  # >0: add a Zipf log-prior router bias
+    down_bits: int = 4   # 4: down codes as uint32 words; 6: a byte stream of 6-bit codes
 
     @property
     def plane_bytes(self) -> int:
         """HBM bytes of one expert's three planes with scales and biases."""
-        per = self.D * self.F // 2 + 4 * self.D * self.F // GROUP
-        return 3 * per
+        sb = 4 * self.D * self.F // GROUP
+        return 2 * (self.D * self.F // 2 + sb) + self.D * self.F * self.down_bits // 8 + sb
 
 
 TINY = LayerShape(E=8, top_k=2, D=256, F=128, act_dtype="f32", router_std=0.05)
@@ -92,9 +93,15 @@ K16 = LayerShape(E=64, top_k=16, D=512, F=256, act_dtype="bf16", router_std=2.0 
 E1024 = LayerShape(E=1024, top_k=16, D=256, F=128, act_dtype="bf16", router_std=2.0 / 256 ** 0.5)
 KALL = LayerShape(E=8, top_k=8, D=512, F=256, act_dtype="bf16", router_std=1.0 / 512 ** 0.5)
 K1 = LayerShape(E=16, top_k=1, D=512, F=256, act_dtype="f32", router_std=1.0 / 512 ** 0.5)
+# mixed widths: 4-bit gate/up with 6-bit down (a small layer, and the
+# 128-expert top-8 shape with 6-bit down)
+DOTS = LayerShape(E=16, top_k=4, D=512, F=256, act_dtype="bf16", router_std=1.0 / 512 ** 0.5,
+                  down_bits=6)
+QWEN3_D6 = LayerShape(E=128, top_k=8, D=2048, F=768, act_dtype="bf16", router_std=0.02, down_bits=6)
 
 SHAPES: Dict[str, LayerShape] = {"tiny": TINY, "qwen3": QWEN3, "e256": E256, "k16": K16,
-                                 "e1024": E1024, "kall": KALL, "k1": K1}
+                                 "e1024": E1024, "kall": KALL, "k1": K1, "dots": DOTS,
+                                 "qwen3_d6": QWEN3_D6}
 
 # named workloads: shape, seed, cohort sizes and cohort kinds
 WORKLOADS = {
@@ -121,20 +128,43 @@ def quantize_affine4(w: np.ndarray):
     (q = 0 where s == 0). Returns (q_packed uint32 [rows, cols/8],
     s_bits uint16 [rows, cols/64], b_bits uint16 [rows, cols/64]).
     """
+    q, s_bits, b_bits = _quantize_codes(w, 15)
+    return pack_nibbles(q), s_bits, b_bits
+
+
+def quantize_affine6(w: np.ndarray):
+    """The same affine rule with 6-bit codes (63 steps per group). Returns
+    (q_packed uint8 [rows, 3*cols/4], s_bits, b_bits); see pack_6bit."""
+    q, s_bits, b_bits = _quantize_codes(w, 63)
+    return pack_6bit(q), s_bits, b_bits
+
+
+def _quantize_codes(w: np.ndarray, qmax: int):
     rows, cols = w.shape
     assert cols % GROUP == 0
     g = w.reshape(rows, cols // GROUP, GROUP).astype(np.float32)
     lo = g.min(axis=2)
     hi = g.max(axis=2)
-    s_bits = bf16_bits((hi - lo) / np.float32(15.0))
+    s_bits = bf16_bits((hi - lo) / np.float32(qmax))
     b_bits = bf16_bits(lo)
     s = bf16_to_f32(s_bits)[..., None]
     b = bf16_to_f32(b_bits)[..., None]
     with np.errstate(divide="ignore", invalid="ignore"):
         qf = np.rint((g - b) / np.where(s == 0, np.float32(1.0), s))
     qf = np.where(s == 0, 0.0, qf)
-    q = np.clip(qf, 0, 15).astype(np.uint32).reshape(rows, cols)
-    return pack_nibbles(q), s_bits, b_bits
+    q = np.clip(qf, 0, qmax).astype(np.uint32).reshape(rows, cols)
+    return q, s_bits, b_bits
+
+
+def pack_6bit(q: np.ndarray) -> np.ndarray:
+    """Pack 6-bit codes [rows, cols] as one little-endian bit stream per row:
+    code j occupies bits 6j..6j+5, so four codes fill three bytes. Returns
+    uint8 [rows, 3*cols/4]."""
+    rows, cols = q.shape
+    q4 = q.reshape(rows, cols // 4, 4).astype(np.uint32)
+    v = q4[..., 0] | (q4[..., 1] << 6) | (q4[..., 2] << 12) | (q4[..., 3] << 18)
+    out = np.stack([v & 0xFF, (v >> 8) & 0xFF, (v >> 16) & 0xFF], axis=-1).astype(np.uint8)
+    return out.reshape(rows, 3 * cols // 4)
 
 
 def pack_nibbles(q: np.ndarray) -> np.ndarray:
@@ -164,7 +194,7 @@ class ExpertPlanes:
     up_q: np.ndarray     # uint32 [E, F, D/8]
     up_s: np.ndarray
     up_b: np.ndarray
-    down_q: np.ndarray   # uint32 [E, D, F/8]
+    down_q: np.ndarray   # uint32 [E, D, F/8] (4-bit), or uint8 [E, D, 3F/4] (6-bit)
     down_s: np.ndarray   # uint16 [E, D, F/64]
     down_b: np.ndarray
 
@@ -212,7 +242,8 @@ def draw_router(shape: LayerShape, seed: int, layer: int):
 def expert_planes(shape: LayerShape, seed: int, layer: int, e: int):
     """The nine quantised arrays of expert e (gate q/s/b, up q/s/b, down q/s/b)."""
     gate, up, down = draw_expert_weights(shape, seed, layer, e)
-    return (*quantize_affine4(gate), *quantize_affine4(up), *quantize_affine4(down))
+    qd = quantize_affine6 if shape.down_bits == 6 else quantize_affine4
+    return (*quantize_affine4(gate), *quantize_affine4(up), *qd(down))
 
 
 def _expert_planes_job(args):
@@ -234,7 +265,8 @@ def make_layer(shape: LayerShape, seed: int, layer: int = 0,
         up_q=np.zeros((E, F, D // 8), np.uint32),
         up_s=np.zeros((E, F, D // GROUP), np.uint16),
         up_b=np.zeros((E, F, D // GROUP), np.uint16),
-        down_q=np.zeros((E, D, F // 8), np.uint32),
+        down_q=(np.zeros((E, D, 3 * F // 4), np.uint8) if shape.down_bits == 6
+                else np.zeros((E, D, F // 8), np.uint32)),
         down_s=np.zeros((E, D, F // GROUP), np.uint16),
         down_b=np.zeros((E, D, F // GROUP), np.uint16),
     )

@@ -35,6 +35,14 @@ def build(force: bool = False) -> str:
     return _LIB
 
 
+# activation kinds (moe_oracle.c oracle_options)
+ACT_SWIGLU, ACT_GEGLU, ACT_GEGLU_TANH, ACT_SWIGLU_CLAMPED = 0, 1, 2, 3
+
+
+class _Options(ctypes.Structure):
+    _fields_ = [("activation", ctypes.c_int), ("limit", ctypes.c_float), ("down_bits", ctypes.c_int)]
+
+
 class _Planes(ctypes.Structure):
     _fields_ = [(name, ctypes.c_void_p) for name in (
         "gate_q", "gate_s", "gate_b", "up_q", "up_s", "up_b", "down_q", "down_s", "down_b")]
@@ -48,9 +56,14 @@ def _load(path: str):
     L.oracle_dequant.argtypes = [vp, vp, vp, i32, i32, vp]
     L.oracle_route.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
     L.oracle_group.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
+    L.oracle_dequant6.argtypes = [vp, vp, vp, i32, i32, vp]
     L.oracle_expert_mlp.argtypes = [i32, i32, vp] + [vp] * 9 + [vp, vp]
+    L.oracle_expert_mlp_opt.argtypes = [i32, i32, vp] + [vp] * 9 + [ctypes.POINTER(_Options), vp, vp]
     L.oracle_moe_forward.argtypes = [i32] * 5 + [vp, vp, vp, ctypes.POINTER(_Planes)] + [vp] * 10
     L.oracle_moe_forward.restype = i32
+    L.oracle_moe_forward_opt.argtypes = [i32] * 5 + [vp, vp, vp, ctypes.POINTER(_Planes),
+                                                     ctypes.POINTER(_Options)] + [vp] * 10
+    L.oracle_moe_forward_opt.restype = i32
     L.oracle_round_bf16.argtypes = [vp, vp, ctypes.c_size_t]
     return L
 
@@ -96,6 +109,20 @@ def dequant(q, s, b) -> np.ndarray:
     return out
 
 
+def dequant6(q, s, b) -> np.ndarray:
+    """Dequantise one 6-bit plane [rows, cols]: q uint8 [rows, 3*cols/4] (bit
+    stream, code j at bits 6j..6j+5), s/b uint16 bits [rows, cols/64]."""
+    q, s, b = _c(q, np.uint8), _c(s, np.uint16), _c(b, np.uint16)
+    rows, cols = q.shape[0], q.shape[1] * 4 // 3
+    out = np.empty((rows, cols), np.float32)
+    lib().oracle_dequant6(_p(q), _p(s), _p(b), rows, cols, _p(out))
+    return out
+
+
+def _options(activation=ACT_SWIGLU, limit=0.0, down_bits=4):
+    return _Options(int(activation), float(limit), int(down_bits))
+
+
 def route(x, router_w, bias, k):
     """-> (topk_idx [n,k] int32, topk_w [n,k] f32, logits [n,E] f32, probs [n,E] f32)."""
     x, wr = _c(x, np.float32), _c(router_w, np.float32)
@@ -125,20 +152,25 @@ def group(topk_idx, E):
     return dict(counts=counts, offsets=offsets, slot_token=st, slot_k=sk, unique=uq[:u].copy(), U=u)
 
 
-def expert_mlp(x_t, planes, e):
-    """One expert's SwiGLU MLP on one token -> (h [F], y [D])."""
+def expert_mlp(x_t, planes, e, activation=ACT_SWIGLU, limit=0.0, down_bits=4):
+    """One expert's gated MLP on one token -> (h [F], y [D]). The default is
+    SwiGLU with 4-bit down planes; down_bits=6 takes uint8 down codes."""
     x_t = _c(x_t, np.float32)
     D = x_t.shape[0]
     F = planes.gate_q.shape[1]
     arrs = [_c(a[e], a.dtype) for a in planes.arrays()]
     h = np.empty(F, np.float32)
     y = np.empty(D, np.float32)
-    lib().oracle_expert_mlp(D, F, _p(x_t), *[_p(a) for a in arrs], _p(h), _p(y))
+    opt = _options(activation, limit, down_bits)
+    lib().oracle_expert_mlp_opt(D, F, _p(x_t), *[_p(a) for a in arrs], ctypes.byref(opt), _p(h), _p(y))
     return h, y
 
 
-def moe_forward(x, router_w, bias, planes, k, want_bf16: bool = False):
-    """The whole decode step. Returns a dict with routing, grouping and out."""
+def moe_forward(x, router_w, bias, planes, k, want_bf16: bool = False, activation=ACT_SWIGLU,
+                limit=0.0, down_bits=4):
+    """The whole decode step. Returns a dict with routing, grouping and out.
+    activation / limit / down_bits select the layer variant (moe_oracle.c
+    oracle_options); the default is SwiGLU with 4-bit down planes."""
     x, wr = _c(x, np.float32), _c(router_w, np.float32)
     bias = None if bias is None else _c(bias, np.float32)
     n, D = x.shape
@@ -156,9 +188,10 @@ def moe_forward(x, router_w, bias, planes, k, want_bf16: bool = False):
     U = np.zeros(1, np.int32)
     out = np.empty((n, D), np.float32)
     out16 = np.empty((n, D), np.uint16) if want_bf16 else None
-    rc = lib().oracle_moe_forward(E, k, D, F, n, _p(x), _p(wr), _p(bias), ctypes.byref(pl),
-                                  _p(idx), _p(w), _p(counts), _p(offsets), _p(st), _p(sk),
-                                  _p(uq), _p(U), _p(out), _p(out16))
+    opt = _options(activation, limit, down_bits)
+    rc = lib().oracle_moe_forward_opt(E, k, D, F, n, _p(x), _p(wr), _p(bias), ctypes.byref(pl),
+                                      ctypes.byref(opt), _p(idx), _p(w), _p(counts), _p(offsets),
+                                      _p(st), _p(sk), _p(uq), _p(U), _p(out), _p(out16))
     if rc != 0:
         raise ValueError("oracle_moe_forward rejected its arguments")
     u = int(U[0])

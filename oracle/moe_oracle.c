@@ -89,6 +89,30 @@ static float dequant_at(const uint32_t *qrow, const uint16_t *srow,
     return fmaf(s, q, b);
 }
 
+/* Weight of input column j of one 6-bit row. The row's codes form one
+ * little-endian bit stream of bytes: code j occupies bits 6j .. 6j+5 (four codes
+ * in three bytes); w = s*q + b with q in 0..63 and the bf16 pair of group j/64. */
+static float dequant6_at(const uint8_t *qrow, const uint16_t *srow, const uint16_t *brow, int j) {
+    int bit = 6 * j, byte = bit >> 3, sh = bit & 7;
+    uint32_t v = qrow[byte];
+    if (sh > 2) v |= (uint32_t)qrow[byte + 1] << 8;  /* the code spans two bytes */
+    float q = (float)((v >> sh) & 0x3Fu);
+    float s = bf16_widen(srow[j / ORACLE_GROUP]);
+    float b = bf16_widen(brow[j / ORACLE_GROUP]);
+    return fmaf(s, q, b);
+}
+
+/* Dequantise a [rows, cols] 6-bit plane (rows of 3*cols/4 bytes) to f32. */
+void oracle_dequant6(const uint8_t *q, const uint16_t *s, const uint16_t *b,
+                     int rows, int cols, float *out) {
+    for (int r = 0; r < rows; ++r) {
+        const uint8_t *qr = q + (size_t)r * (3 * cols / 4);
+        const uint16_t *sr = s + (size_t)r * (cols / ORACLE_GROUP);
+        const uint16_t *br = b + (size_t)r * (cols / ORACLE_GROUP);
+        for (int j = 0; j < cols; ++j) out[(size_t)r * cols + j] = dequant6_at(qr, sr, br, j);
+    }
+}
+
 /* Dequantise a [rows, cols] plane to f32. */
 void oracle_dequant(const uint32_t *q, const uint16_t *s, const uint16_t *b,
                     int rows, int cols, float *out) {
@@ -171,15 +195,60 @@ void oracle_group(int n, int E, int k, const int32_t *topk_idx, int32_t *counts,
     *U = u;
 }
 
-/* One expert's SwiGLU MLP on one token:
+/* Layer options beyond the default (SwiGLU, 4-bit down planes).
+ * Activations (h = act(g, u)):
+ *   ORACLE_ACT_SWIGLU         silu(g) * u, silu(z) = z / (1 + exp(-z))
+ *   ORACLE_ACT_GEGLU          gelu(g) * u, gelu(z) = z * Phi(z) = z/2 (1 + erf(z / sqrt 2))
+ *   ORACLE_ACT_GEGLU_TANH     gelu's tanh form: z/2 (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3)))
+ *   ORACLE_ACT_SWIGLU_CLAMPED silu(min(g, L)) * min(max(u, -L), L), L = limit
+ * Sources: #1616 Implementation Notes names the GeGLU variant of the fused
+ * kernel (gemma4); #1859 Problem / Background names the clamp stage of
+ * deepseek_v4's limited SwiGLU. Neither page gives the formulas or the bounds:
+ * GeGLU is read as the GLU with GELU (exact, and the tanh approximation as a
+ * second kind), the clamp as bounding the gate from above and the up
+ * projection on both sides at one limit L.
+ * down_bits: 4 (uint32 words of eight codes) or 6 (#1616 Implementation Notes:
+ * dots.llm1 has 4-bit gate/up with 6-bit down; the byte stream of
+ * dequant6_at). */
+typedef struct {
+    int activation;
+    float limit;
+    int down_bits;
+} oracle_options;
+
+enum { ORACLE_ACT_SWIGLU = 0, ORACLE_ACT_GEGLU = 1, ORACLE_ACT_GEGLU_TANH = 2,
+       ORACLE_ACT_SWIGLU_CLAMPED = 3 };
+
+static float silu(float z) { return z / (1.0f + expf(-z)); }
+
+static float glu_activation(const oracle_options *o, float g, float u) {
+    switch (o->activation) {
+        case ORACLE_ACT_GEGLU:
+            return 0.5f * g * (1.0f + erff(g * 0.70710678118654752f)) * u;
+        case ORACLE_ACT_GEGLU_TANH: {
+            float inner = 0.79788456080286536f * (g + 0.044715f * g * g * g);
+            return 0.5f * g * (1.0f + tanhf(inner)) * u;
+        }
+        case ORACLE_ACT_SWIGLU_CLAMPED: {
+            float gc = fminf(g, o->limit);
+            float uc = fminf(fmaxf(u, -o->limit), o->limit);
+            return silu(gc) * uc;
+        }
+        default:
+            return silu(g) * u;
+    }
+}
+
+/* One expert's gated MLP on one token (options as above):
  *   g_f = sum_d Wg[f,d] x[d],  u_f = sum_d Wu[f,d] x[d],
- *   h_f = silu(g_f) * u_f,     y_d = sum_f Wd[d,f] h_f.
- * Planes are those of a single expert (no E stride). h is caller scratch [F]. */
-void oracle_expert_mlp(int D, int F, const float *x,
-                       const uint32_t *gq, const uint16_t *gs, const uint16_t *gb,
-                       const uint32_t *uq, const uint16_t *us, const uint16_t *ub,
-                       const uint32_t *dq, const uint16_t *ds, const uint16_t *db,
-                       float *h, float *y) {
+ *   h_f = act(g_f, u_f),       y_d = sum_f Wd[d,f] h_f.
+ * Planes are those of a single expert (no E stride); dq holds uint32 words
+ * (4-bit) or bytes (6-bit). h is caller scratch [F]. */
+void oracle_expert_mlp_opt(int D, int F, const float *x,
+                           const uint32_t *gq, const uint16_t *gs, const uint16_t *gb,
+                           const uint32_t *uq, const uint16_t *us, const uint16_t *ub,
+                           const void *dq, const uint16_t *ds, const uint16_t *db,
+                           const oracle_options *opt, float *h, float *y) {
     for (int f = 0; f < F; ++f) {
         const uint32_t *gqr = gq + (size_t)f * (D / 8);
         const uint16_t *gsr = gs + (size_t)f * (D / ORACLE_GROUP);
@@ -192,23 +261,38 @@ void oracle_expert_mlp(int D, int F, const float *x,
             g = fmaf(dequant_at(gqr, gsr, gbr, d), x[d], g);
             u = fmaf(dequant_at(uqr, usr, ubr, d), x[d], u);
         }
-        float silu = g / (1.0f + expf(-g));
-        h[f] = silu * u;
+        h[f] = glu_activation(opt, g, u);
     }
     for (int d = 0; d < D; ++d) {
-        const uint32_t *dqr = dq + (size_t)d * (F / 8);
         const uint16_t *dsr = ds + (size_t)d * (F / ORACLE_GROUP);
         const uint16_t *dbr = db + (size_t)d * (F / ORACLE_GROUP);
         float acc = 0.0f;
-        for (int f = 0; f < F; ++f) acc = fmaf(dequant_at(dqr, dsr, dbr, f), h[f], acc);
+        if (opt->down_bits == 6) {
+            const uint8_t *dqr = (const uint8_t *)dq + (size_t)d * (3 * F / 4);
+            for (int f = 0; f < F; ++f) acc = fmaf(dequant6_at(dqr, dsr, dbr, f), h[f], acc);
+        } else {
+            const uint32_t *dqr = (const uint32_t *)dq + (size_t)d * (F / 8);
+            for (int f = 0; f < F; ++f) acc = fmaf(dequant_at(dqr, dsr, dbr, f), h[f], acc);
+        }
         y[d] = acc;
     }
+}
+
+static const oracle_options kDefaultOptions = {ORACLE_ACT_SWIGLU, 0.0f, 4};
+
+/* The default layer: SwiGLU with 4-bit down planes. */
+void oracle_expert_mlp(int D, int F, const float *x,
+                       const uint32_t *gq, const uint16_t *gs, const uint16_t *gb,
+                       const uint32_t *uq, const uint16_t *us, const uint16_t *ub,
+                       const uint32_t *dq, const uint16_t *ds, const uint16_t *db,
+                       float *h, float *y) {
+    oracle_expert_mlp_opt(D, F, x, gq, gs, gb, uq, us, ub, dq, ds, db, &kDefaultOptions, h, y);
 }
 
 typedef struct {
     const uint32_t *gate_q; const uint16_t *gate_s; const uint16_t *gate_b;
     const uint32_t *up_q;   const uint16_t *up_s;   const uint16_t *up_b;
-    const uint32_t *down_q; const uint16_t *down_s; const uint16_t *down_b;
+    const void *down_q;     const uint16_t *down_s; const uint16_t *down_b;  /* words or bytes */
 } oracle_planes;
 
 /* The whole decode step. Planes are stacked [E, ...] (see oracle_planes).
@@ -216,14 +300,15 @@ typedef struct {
  * slot_k, unique, U), out_f32 [n,D] before rounding and, when out_bf16 is not
  * NULL, out rounded once to bf16 (round to nearest even). Returns 0, or -1 on
  * bad arguments or allocation failure. */
-int oracle_moe_forward(int E, int k, int D, int F, int n,
-                       const float *x, const float *router_w, const float *router_bias,
-                       const oracle_planes *pl,
-                       int32_t *topk_idx, float *topk_w,
-                       int32_t *counts, int32_t *offsets, int32_t *slot_token,
-                       int32_t *slot_k, int32_t *unique, int32_t *U,
-                       float *out_f32, uint16_t *out_bf16) {
+int oracle_moe_forward_opt(int E, int k, int D, int F, int n,
+                           const float *x, const float *router_w, const float *router_bias,
+                           const oracle_planes *pl, const oracle_options *opt,
+                           int32_t *topk_idx, float *topk_w,
+                           int32_t *counts, int32_t *offsets, int32_t *slot_token,
+                           int32_t *slot_k, int32_t *unique, int32_t *U,
+                           float *out_f32, uint16_t *out_bf16) {
     if (E < 1 || k < 1 || k > E || n < 1 || D % ORACLE_GROUP || F % ORACLE_GROUP) return -1;
+    if (opt->down_bits != 4 && opt->down_bits != 6) return -1;
     oracle_route(n, E, D, k, x, router_w, router_bias, topk_idx, topk_w, NULL, NULL);
     oracle_group(n, E, k, topk_idx, counts, offsets, slot_token, slot_k, unique, U);
 
@@ -231,7 +316,9 @@ int oracle_moe_forward(int E, int k, int D, int F, int n,
     float *y = (float *)malloc(sizeof(float) * (size_t)S * D);  /* y per slot, slot = t*k + j */
     if (!y) return -1;
     const size_t gstride = (size_t)F * (D / 8), gsstride = (size_t)F * (D / ORACLE_GROUP);
-    const size_t dstride = (size_t)D * (F / 8), dsstride = (size_t)D * (F / ORACLE_GROUP);
+    /* bytes of one expert's down codes */
+    const size_t dstride = (size_t)D * (opt->down_bits == 6 ? 3 * F / 4 : F / 2);
+    const size_t dsstride = (size_t)D * (F / ORACLE_GROUP);
     int failed = 0;
 #pragma omp parallel
     {
@@ -244,11 +331,11 @@ int oracle_moe_forward(int E, int k, int D, int F, int n,
         for (int slot = 0; slot < S; ++slot) {
             if (!h) continue;
             int t = slot / k, e = topk_idx[slot];
-            oracle_expert_mlp(D, F, x + (size_t)t * D,
-                              pl->gate_q + e * gstride, pl->gate_s + e * gsstride, pl->gate_b + e * gsstride,
-                              pl->up_q + e * gstride, pl->up_s + e * gsstride, pl->up_b + e * gsstride,
-                              pl->down_q + e * dstride, pl->down_s + e * dsstride, pl->down_b + e * dsstride,
-                              h, y + (size_t)slot * D);
+            oracle_expert_mlp_opt(D, F, x + (size_t)t * D,
+                                  pl->gate_q + e * gstride, pl->gate_s + e * gsstride, pl->gate_b + e * gsstride,
+                                  pl->up_q + e * gstride, pl->up_s + e * gsstride, pl->up_b + e * gsstride,
+                                  (const uint8_t *)pl->down_q + e * dstride, pl->down_s + e * dsstride,
+                                  pl->down_b + e * dsstride, opt, h, y + (size_t)slot * D);
         }
         free(h);
     }
@@ -265,6 +352,19 @@ int oracle_moe_forward(int E, int k, int D, int F, int n,
         for (size_t i = 0; i < (size_t)n * D; ++i) out_bf16[i] = bf16_round_rne(out_f32[i]);
     free(y);
     return 0;
+}
+
+/* The default layer (SwiGLU, 4-bit down planes). */
+int oracle_moe_forward(int E, int k, int D, int F, int n,
+                       const float *x, const float *router_w, const float *router_bias,
+                       const oracle_planes *pl,
+                       int32_t *topk_idx, float *topk_w,
+                       int32_t *counts, int32_t *offsets, int32_t *slot_token,
+                       int32_t *slot_k, int32_t *unique, int32_t *U,
+                       float *out_f32, uint16_t *out_bf16) {
+    return oracle_moe_forward_opt(E, k, D, F, n, x, router_w, router_bias, pl, &kDefaultOptions,
+                                  topk_idx, topk_w, counts, offsets, slot_token, slot_k, unique, U,
+                                  out_f32, out_bf16);
 }
 
 /* The single final rounding, exposed for tests. */

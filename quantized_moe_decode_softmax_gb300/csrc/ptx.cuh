@@ -110,6 +110,12 @@ __device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
 // programmatic dependent launch: let the next kernel of the stream (launched
 // with programmatic stream serialization) start as this grid's CTAs signal
 // or exit; a no-op when no such kernel follows
+// bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16); it
+// returns no data, so it is safe at any point, before griddep_wait too
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

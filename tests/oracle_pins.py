@@ -380,6 +380,130 @@ def check_final_rounding_vs_library():
     assert np.array_equal(got[~nan], by_def), "final rounding differs from round-to-nearest-even"
 
 
+# ---------------------------------------------------------------------------
+# layer variants: GeGLU, clamped SwiGLU, 6-bit down planes
+# ---------------------------------------------------------------------------
+def _act64(kind, g, u, limit):
+    """The activations in float64 from library routines (scipy erf and expit,
+    numpy tanh and clip)."""
+    if kind == oracle.ACT_GEGLU:
+        return 0.5 * g * (1.0 + special.erf(g / np.sqrt(2.0))) * u
+    if kind == oracle.ACT_GEGLU_TANH:
+        return 0.5 * g * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * (g + 0.044715 * g ** 3))) * u
+    if kind == oracle.ACT_SWIGLU_CLAMPED:
+        gc = np.minimum(g, limit)
+        return gc * special.expit(gc) * np.clip(u, -limit, limit)
+    return g * special.expit(g) * u
+
+
+def check_activation_variants_vs_library():
+    """Each activation kind of the oracle's expert MLP against a float64 dense
+    formulation from library routines, on one expert; for the clamp, a limit
+    below the largest |gate| and |up| so that both bounds act. Then the whole
+    step with GeGLU against the brute-force dense gate formulation, and the
+    clamp with a limit above every |gate| and |up| equal to SwiGLU bit for bit."""
+    shp = ms.LayerShape(E=1, top_k=1, D=256, F=192, act_dtype="f32", router_std=0.05,
+                        expert_std=0.08)
+    lay = ms.make_layer(shp, 31, 0)
+    x = np.random.default_rng(31).standard_normal((2, shp.D)).astype(np.float32)
+    wg, wu, wd = _dense_f64(lay.planes, 0)
+    for t in range(2):
+        x64 = x[t].astype(np.float64)
+        g, u = wg @ x64, wu @ x64
+        limit = float(np.quantile(np.abs(np.concatenate([g, u])), 0.6))
+        assert (g > limit).any() and (g < -limit).any() and (np.abs(u) > limit).any()
+        for kind in (oracle.ACT_SWIGLU, oracle.ACT_GEGLU, oracle.ACT_GEGLU_TANH,
+                     oracle.ACT_SWIGLU_CLAMPED):
+            h, y = oracle.expert_mlp(x[t], lay.planes, 0, activation=kind, limit=limit)
+            h64 = _act64(kind, g, u, limit)
+            y64 = wd @ h64
+            assert np.abs(h - h64).max() <= 1e-5 * _rms(h64), kind
+            assert np.abs(y - y64).max() <= 1e-5 * _rms(y64), kind
+
+    lay = ms.make_layer(SMALL, 4, 0)
+    xs = ms.draw_tokens(SMALL, lay.router_w, None, 4, 0, 4)
+    k = SMALL.top_k
+    r = oracle.moe_forward(xs, lay.router_w, None, lay.planes, k, activation=oracle.ACT_GEGLU)
+    x64 = xs.astype(np.float64)
+    lg = x64 @ lay.router_w.astype(np.float64).T
+    order = np.argsort(-lg, axis=1, kind="stable")[:, :k]
+    G = np.zeros((xs.shape[0], SMALL.E))
+    np.put_along_axis(G, order, special.softmax(np.take_along_axis(lg, order, axis=1), axis=1), axis=1)
+    out = np.zeros((xs.shape[0], SMALL.D))
+    for e in range(SMALL.E):
+        wg, wu, wd = _dense_f64(lay.planes, e)
+        out += G[:, e:e + 1] * (_act64(oracle.ACT_GEGLU, x64 @ wg.T, x64 @ wu.T, 0.0) @ wd.T)
+    assert np.abs(r["out"] - out).max() <= 1e-5 * _rms(out)
+
+    base = oracle.moe_forward(xs, lay.router_w, None, lay.planes, k)
+    wide = oracle.moe_forward(xs, lay.router_w, None, lay.planes, k,
+                              activation=oracle.ACT_SWIGLU_CLAMPED, limit=1e30)
+    assert np.array_equal(wide["out"], base["out"])
+
+
+def _pack6_by_int(codes):
+    """6-bit codes of one row packed through a Python integer: code j shifted
+    to bit 6j, written out as little-endian bytes."""
+    v = 0
+    for j, c in enumerate(codes):
+        v |= int(c) << (6 * j)
+    return np.frombuffer(v.to_bytes(3 * len(codes) // 4, "little"), dtype=np.uint8)
+
+
+def check_dequant6_known_codes():
+    """A 6-bit row with known codes, packed through a Python integer (not the
+    generator's packer), dequantises to s*q + b exactly; the generator's packer
+    gives the same bytes."""
+    cols = 256
+    rows = 3
+    codes = np.array([[(7 * j + 3 * r + 1) % 64 for j in range(cols)] for r in range(rows)], np.uint32)
+    q = np.stack([_pack6_by_int(codes[r]) for r in range(rows)])
+    assert np.array_equal(q, ms.pack_6bit(codes))
+    s = np.array([[0.5, 0.25, 2.0, 1.0]] * rows, np.float32)
+    b = np.array([[-3.0, 1.0, -0.5, 0.0]] * rows, np.float32)
+    got = oracle.dequant6(q, ms.bf16_bits(s), ms.bf16_bits(b))
+    want = np.repeat(s, 64, axis=1) * codes.astype(np.float32) + np.repeat(b, 64, axis=1)
+    assert np.array_equal(got, want)
+
+
+def check_quant6_roundtrip():
+    """6-bit codes dequantise to within half a step of the original weights."""
+    rng = np.random.default_rng(12)
+    w = (rng.standard_normal((8, 256)) * 0.02).astype(np.float32)
+    q, sb, bb = ms.quantize_affine6(w)
+    deq = oracle.dequant6(q, sb, bb).astype(np.float64)
+    step = np.repeat(ms.bf16_to_f32(sb).astype(np.float64), 64, axis=1)
+    bias = np.repeat(ms.bf16_to_f32(bb).astype(np.float64), 64, axis=1)
+    # half a step, plus the rounding of the bias to bf16 (2^-8 relative)
+    assert np.all(np.abs(deq - w) <= 0.5 * step + np.abs(bias) * 2.0 ** -8 + 1e-9)
+    assert np.abs(deq - w).max() < np.abs(w).max() / 40
+
+
+def check_down6_layer_vs_dense():
+    """A layer with 4-bit gate/up and 6-bit down planes: the whole step against
+    the brute-force dense formulation (every expert, dense gate from a full
+    sort, float64), the 6-bit planes dequantised through the pinned routine."""
+    shp = ms.SHAPES["dots"]
+    lay = ms.make_layer(shp, 7, 0)
+    x = ms.draw_tokens(shp, lay.router_w, None, 7, 0, 3)
+    k = shp.top_k
+    r = oracle.moe_forward(x, lay.router_w, None, lay.planes, k, down_bits=6)
+    x64 = x.astype(np.float64)
+    lg = x64 @ lay.router_w.astype(np.float64).T
+    order = np.argsort(-lg, axis=1, kind="stable")[:, :k]
+    G = np.zeros((x.shape[0], shp.E))
+    np.put_along_axis(G, order, special.softmax(np.take_along_axis(lg, order, axis=1), axis=1), axis=1)
+    out = np.zeros((x.shape[0], shp.D))
+    p = lay.planes
+    for e in range(shp.E):
+        wg = oracle.dequant(p.gate_q[e], p.gate_s[e], p.gate_b[e]).astype(np.float64)
+        wu = oracle.dequant(p.up_q[e], p.up_s[e], p.up_b[e]).astype(np.float64)
+        wd = oracle.dequant6(p.down_q[e], p.down_s[e], p.down_b[e]).astype(np.float64)
+        out += G[:, e:e + 1] * _swiglu64(wg, wu, wd, x64)
+    assert np.array_equal(r["topk_idx"], order)
+    assert np.abs(r["out"] - out).max() <= 1e-5 * _rms(out)
+
+
 ALL_CHECKS = [
     check_quant_roundtrip,
     check_dequant_known_codes,
@@ -394,4 +518,8 @@ ALL_CHECKS = [
     check_invariants,
     check_expert_shards_sum_to_the_step,
     check_final_rounding_vs_library,
+    check_activation_variants_vs_library,
+    check_dequant6_known_codes,
+    check_quant6_roundtrip,
+    check_down6_layer_vs_dense,
 ]

@@ -18,16 +18,24 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.c")
 
 MUTANTS = {
     "nibble_order_reversed": ("(word >> (4 * (j % 8)))", "(word >> (4 * (7 - j % 8)))"),
-    "scale_bias_swapped": ("return fmaf(s, q, b);", "return fmaf(b, q, s);"),
-    "bias_dropped": ("return fmaf(s, q, b);", "return s * q;"),
-    "group_index_ignored": ("float s = bf16_widen(srow[j / ORACLE_GROUP]);", "float s = bf16_widen(srow[0]);"),
+    "scale_bias_swapped": ("return fmaf(s, q, b);\n}\n\n/* Weight of input column j of one 6-bit",
+                           "return fmaf(b, q, s);\n}\n\n/* Weight of input column j of one 6-bit"),
+    "bias_dropped": ("return fmaf(s, q, b);\n}\n\n/* Weight of input column j of one 6-bit",
+                     "return s * q;\n}\n\n/* Weight of input column j of one 6-bit"),
+    "group_index_ignored": ("& 0xFu);\n    float s = bf16_widen(srow[j / ORACLE_GROUP]);",
+                            "& 0xFu);\n    float s = bf16_widen(srow[0]);"),
+    "six_bit_scale_bias_swapped": ("& 0x3Fu);\n    float s = bf16_widen(srow[j / ORACLE_GROUP]);\n"
+                                   "    float b = bf16_widen(brow[j / ORACLE_GROUP]);",
+                                   "& 0x3Fu);\n    float b = bf16_widen(srow[j / ORACLE_GROUP]);\n"
+                                   "    float s = bf16_widen(brow[j / ORACLE_GROUP]);"),
+    "six_bit_group_index_ignored": ("& 0x3Fu);\n    float s = bf16_widen(srow[j / ORACLE_GROUP]);",
+                                    "& 0x3Fu);\n    float s = bf16_widen(srow[0]);"),
     "router_bias_dropped": ("if (bias) acc += bias[e];", ""),
     "no_renormalise": ("topk_w[(size_t)t * k + j] = p[topk_idx[(size_t)t * k + j]] / psum;",
                        "topk_w[(size_t)t * k + j] = p[topk_idx[(size_t)t * k + j]];"),
     "tie_to_higher_index": ("if (best < 0 || l[e] > l[best])", "if (best < 0 || l[e] >= l[best])"),
-    "silu_sign": ("float silu = g / (1.0f + expf(-g));", "float silu = g / (1.0f + expf(g));"),
-    "gate_up_swapped": ("float silu = g / (1.0f + expf(-g));\n        h[f] = silu * u;",
-                        "float silu = u / (1.0f + expf(-u));\n        h[f] = silu * g;"),
+    "silu_sign": ("return z / (1.0f + expf(-z));", "return z / (1.0f + expf(z));"),
+    "gate_up_swapped": ("            return silu(g) * u;", "            return silu(u) * g;"),
     "x_index_reversed": ("g = fmaf(dequant_at(gqr, gsr, gbr, d), x[d], g);",
                          "g = fmaf(dequant_at(gqr, gsr, gbr, d), x[D - 1 - d], g);"),
     "combine_rank0_weight": ("acc = fmaf(topk_w[(size_t)t * k + j], y[",
@@ -39,6 +47,16 @@ MUTANTS = {
     "final_round_ties_to_odd": ("u += 0x7FFFu + ((u >> 16) & 1u);",
                                 "u += 0x7FFFu + (((u >> 16) & 1u) ^ 1u);"),
     "final_round_ties_away": ("u += 0x7FFFu + ((u >> 16) & 1u);", "u += 0x8000u;"),
+    "gelu_erf_unscaled": ("erff(g * 0.70710678118654752f)", "erff(g)"),
+    "gelu_tanh_no_cubic": ("(g + 0.044715f * g * g * g)", "(g + 0.044715f * g * g)"),
+    "clamp_gate_below_too": ("float gc = fminf(g, o->limit);",
+                             "float gc = fminf(fmaxf(g, -o->limit), o->limit);"),
+    "clamp_up_dropped": ("float uc = fminf(fmaxf(u, -o->limit), o->limit);", "float uc = u;"),
+    "six_bit_byte_order": ("if (sh > 2) v |= (uint32_t)qrow[byte + 1] << 8;",
+                           "if (sh > 2) v = (v << 8) | qrow[byte + 1];"),
+    "six_bit_mask": ("float q = (float)((v >> sh) & 0x3Fu);", "float q = (float)((v >> sh) & 0x1Fu);"),
+    "six_bit_row_stride": ("const uint8_t *dqr = (const uint8_t *)dq + (size_t)d * (3 * F / 4);",
+                           "const uint8_t *dqr = (const uint8_t *)dq + (size_t)d * (F / 2);"),
 }
 
 
