@@ -6,7 +6,8 @@
  *   2. group the n*k (token, rank) slots by expert, de-duplicated, so every
  *      selected expert's planes are streamed from HBM once per step (once
  *      per chunk for cohorts that run in chunks; see moe_decode_forward)
- *   3. per selected expert: h = silu(Wg x) * (Wu x) on affine 4-bit weights
+ *   3. per selected expert: h = act(Wg x, Wu x) on affine 4-bit weights
+ *      (SwiGLU silu(g) * u by default; GeGLU and a clamped SwiGLU as options)
  *   4. y = Wd h, and out[t] = sum_j w[t,j] * y[t,j] in rank order j,
  *      f32 partials with a single final rounding
  *
@@ -40,6 +41,9 @@
  * Data formats (MLX-style affine 4-bit quantisation, group 64)
  *   plane q : uint32 [E, rows, cols/8]; nibble j (bits 4j..4j+3) of word i
  *             is the code (0..15) of input column 8*i + j
+ *   6-bit down planes (cfg.down_bits = 6): bytes [E, D, 3*Dff/4]; the codes
+ *             (0..63) of a row form one little-endian bit stream, code j in
+ *             bits 6j..6j+5 (four codes in three bytes)
  *   scale s : bf16 [E, rows, cols/64]; bias b : bf16 [E, rows, cols/64]
  *   weight  : w = s * q + b, groups of 64 consecutive input columns
  *   gate, up: rows = Dff, cols = D;  down: rows = D, cols = Dff
@@ -55,7 +59,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 typedef enum {
     MOE_OK = 0,
@@ -91,6 +95,19 @@ enum {
     MOE_FLAG_TEST_STALL = 1u << 8
 };
 
+/* expert activation h = act(g, u), g = Wg x, u = Wu x. The pages name the
+ * variants without formulas (#1616 Implementation Notes: the GeGLU variant of
+ * the fused kernel; #1859 Problem / Background: deepseek_v4's clamp stage);
+ * the readings below are the plainest ones. */
+enum {
+    MOE_ACT_SWIGLU = 0,          /* silu(g) * u, silu(z) = z / (1 + exp(-z)) */
+    MOE_ACT_GEGLU = 1,           /* gelu(g) * u, gelu(z) = z/2 (1 + erf(z / sqrt 2)) */
+    MOE_ACT_GEGLU_TANH = 2,      /* gelu in its tanh form:
+                                    z/2 (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3))) */
+    MOE_ACT_SWIGLU_CLAMPED = 3   /* silu(min(g, L)) * min(max(u, -L), L),
+                                    L = act_limit */
+};
+
 typedef struct {
     int E;              /* experts, 1..1024 */
     int top_k;          /* experts per token, 1..min(E, 16) */
@@ -105,6 +122,16 @@ typedef struct {
     unsigned flags;     /* MOE_FLAG_* */
     int mma_min_tokens; /* per-expert token count from which an expert takes
                            the tensor-core tile path; 0 = library default */
+    /* ABI version 2 */
+    int activation;     /* MOE_ACT_* */
+    float act_limit;    /* the clamp bound L of MOE_ACT_SWIGLU_CLAMPED (finite,
+                           > 0); ignored by the other activations */
+    int down_bits;      /* bits of the down codes: 0 or 4 (uint32 words), 6
+                           (the byte stream above; Dff must be a multiple of 64) */
+    int expert_begin;   /* the experts this plan owns, [expert_begin, expert_end):
+                           routing still ranks all E experts, but only owned */
+    int expert_end;     /* experts are streamed and summed (expert-parallel
+                           shard); both 0 = all E experts */
 } moe_config;
 
 typedef struct {
@@ -114,7 +141,8 @@ typedef struct {
     const uint32_t *up_q;   /* [E, Dff, D/8]  */
     const uint16_t *up_s;   /* [E, Dff, D/64] bf16 */
     const uint16_t *up_b;   /* [E, Dff, D/64] bf16 */
-    const uint32_t *down_q; /* [E, D, Dff/8]  */
+    const uint32_t *down_q; /* [E, D, Dff/8]; bytes [E, D, 3*Dff/4] when
+                               cfg.down_bits = 6 (16-byte aligned) */
     const uint16_t *down_s; /* [E, D, Dff/64] bf16 */
     const uint16_t *down_b; /* [E, D, Dff/64] bf16 */
 } moe_expert_planes;
@@ -140,9 +168,15 @@ moe_status moe_plan_workspace_bytes(const moe_config *cfg, size_t *bytes);
  * kernels do not cover, validation before any dispatch.
  * The plan is bound to that device. Decline (UNSUPPORTED): bits != 4,
  * group_size != 64, D or Dff not a multiple of 64, D > 16384, Dff > 8192,
- * E > 1024, top_k > 16. INVALID_ARG: null pointers, non-positive sizes,
- * top_k > E, max_tokens outside 1..64, unknown dtypes, negative
- * mma_min_tokens, unknown flags. OOM / CUDA: the
+ * E > 1024, top_k > 16, activation not a MOE_ACT_*, down_bits not 0, 4 or 6.
+ * INVALID_ARG: null pointers, non-positive sizes, top_k > E, max_tokens
+ * outside 1..64, unknown dtypes, negative mma_min_tokens, unknown flags, a
+ * clamp bound that is not finite and positive (MOE_ACT_SWIGLU_CLAMPED), an
+ * expert range other than 0 <= expert_begin < expert_end <= E (or 0, 0).
+ * A plan with 6-bit down planes runs every cohort on the grouped path.
+ * Source of the expert range: #1616 Proposed Solution (one read of each
+ * expert plane per step, which an expert-parallel split keeps per GPU).
+ * OOM / CUDA: the
  * allocation failed (nothing leaks). On success *out owns the workspace
  * until moe_plan_free. */
 moe_status moe_plan_create(const moe_config *cfg, moe_plan **out);
@@ -171,6 +205,12 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan **out);
  *                    grouping, per-expert tile or GEMV kernels, combine);
  *   MOE_FLAG_F32_DEBUG, or a shape the single-launch kernel declines:
  *                    the grouped multi-kernel path with f32 GEMV kernels.
+ * Expert range. A plan that owns the experts [expert_begin, expert_end)
+ * writes out[t] = sum over the ranks j whose expert it owns of w[t,j] *
+ * y[t,j] (0 where it owns none): the plans of a partition of the experts
+ * produce partial outputs that sum to the whole step (use out_dtype f32 for
+ * partials that are summed afterwards). Routing (top-k and weights over all
+ * E experts) is the same in every shard.
  * Asynchronous. Returns INVALID_ARG before any launch on a bad argument,
  * CUDA if a launch fails.
  * Device-side errors. Every wait inside a step is bounded (about 1 s); a wait
@@ -244,7 +284,10 @@ moe_status moe_plan_check(moe_plan *plan);
  *   counts [E], offsets [E+1]                (exclusive scan of counts)
  *   slot_token [n*k], slot_k [n*k]           (slots grouped by expert
  *                                             ascending, token ascending)
- *   unique [E] (first *U entries valid), U   (experts with count > 0) */
+ *   unique [E] (first *U entries valid), U   (experts with count > 0)
+ * With an expert range, topk_idx / topk_w cover every expert and the grouping
+ * arrays cover the owned experts only (counts of the others are 0; the first
+ * offsets[E] entries of slot_token / slot_k are valid). */
 moe_status moe_get_routing(moe_plan *plan, int32_t *topk_idx, float *topk_w,
                            int32_t *counts, int32_t *offsets, int32_t *slot_token,
                            int32_t *slot_k, int32_t *unique, int32_t *U);

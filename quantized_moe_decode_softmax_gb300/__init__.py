@@ -9,6 +9,10 @@ streams only.
 from ._abi import (  # noqa: F401
     EXPORTED,
     LIB_PATH,
+    MOE_ACT_GEGLU,
+    MOE_ACT_GEGLU_TANH,
+    MOE_ACT_SWIGLU,
+    MOE_ACT_SWIGLU_CLAMPED,
     MOE_DTYPE_BF16,
     MOE_DTYPE_F32,
     MOE_ERR_CUDA,

@@ -23,6 +23,7 @@ MOE_FLAG_TRACE = 1 << 1
 MOE_FLAG_PHASE_TIMES = 1 << 2
 MOE_FLAG_GROUPED_COHORTS = 1 << 3
 MOE_FLAG_TEST_STALL = 1 << 8
+MOE_ACT_SWIGLU, MOE_ACT_GEGLU, MOE_ACT_GEGLU_TANH, MOE_ACT_SWIGLU_CLAMPED = range(4)
 
 EXPORTED = (
     "moe_abi_version", "moe_status_str", "moe_plan_workspace_bytes", "moe_plan_create",
@@ -42,7 +43,10 @@ class moe_config(ctypes.Structure):
                 ("Dff", ctypes.c_int), ("bits", ctypes.c_int), ("group_size", ctypes.c_int),
                 ("max_tokens", ctypes.c_int), ("x_dtype", ctypes.c_int),
                 ("router_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
-                ("flags", ctypes.c_uint), ("mma_min_tokens", ctypes.c_int)]
+                ("flags", ctypes.c_uint), ("mma_min_tokens", ctypes.c_int),
+                ("activation", ctypes.c_int), ("act_limit", ctypes.c_float),
+                ("down_bits", ctypes.c_int), ("expert_begin", ctypes.c_int),
+                ("expert_end", ctypes.c_int)]
 
 
 PLANE_FIELDS = ("gate_q", "gate_s", "gate_b", "up_q", "up_s", "up_b", "down_q", "down_s", "down_b")
@@ -113,11 +117,14 @@ def _check(st: int, what: str):
 
 
 def make_config(E, top_k, D, Dff, max_tokens, x_dtype=MOE_DTYPE_BF16, router_dtype=None,
-                out_dtype=None, flags=0, mma_min_tokens=0, bits=4, group_size=64) -> moe_config:
+                out_dtype=None, flags=0, mma_min_tokens=0, bits=4, group_size=64,
+                activation=MOE_ACT_SWIGLU, act_limit=0.0, down_bits=0, expert_begin=0,
+                expert_end=0) -> moe_config:
     router_dtype = x_dtype if router_dtype is None else router_dtype
     out_dtype = x_dtype if out_dtype is None else out_dtype
     return moe_config(E, top_k, D, Dff, bits, group_size, max_tokens, x_dtype, router_dtype,
-                      out_dtype, flags, mma_min_tokens)
+                      out_dtype, flags, mma_min_tokens, activation, act_limit, down_bits,
+                      expert_begin, expert_end)
 
 
 def make_planes(planes: Any) -> moe_expert_planes:

@@ -61,6 +61,7 @@
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
+#include "activation.cuh"
 #include "moe_internal.h"
 #include "ptx.cuh"
 #include "routing.cuh"
@@ -277,7 +278,8 @@ __device__ __forceinline__ bool grid_barrier(unsigned long long *cnt, unsigned l
     cta_sync(consumers_only);
     if (threadIdx.x == 0) {
         int ok = 1;
-        __threadfence();
+        // the release add orders every write of this CTA before it (the CTA
+        // barrier above, then release cumulativity); no separate fence
         ptx::red_release_gpu_u64(cnt, 1ull);
         if (ptx::ld_acquire_gpu_u64(cnt) < target) {
             const unsigned long long t0 = globaltimer();
@@ -554,10 +556,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     const int Sl = n * K;
     // Grouping, slot table and tile list by warp 0 alone (no CTA barrier in
     // between; __syncwarp orders the warp's shared-memory accesses).
+    // only the experts this plan owns ([e_lo, e_hi), all by default) are
+    // grouped, streamed and summed
+    const int e_lo = A.s.e_lo, e_hi = A.s.e_hi;
     if (warp == 0) {
 #pragma unroll 1
-        for (int i = lane; i < Sl; i += 32)
-            ptx::red_or_shared(S.s_mask + S.s_idx[i], 1u << (i / K));
+        for (int i = lane; i < Sl; i += 32) {
+            const int e = S.s_idx[i];
+            if (e >= e_lo && e < e_hi) ptx::red_or_shared(S.s_mask + e, 1u << (i / K));
+        }
         __syncwarp();
         // counts and exclusive scans over the experts; lane l owns experts
         // [8 l, 8 l + 8) (E <= 256), so the scans run in expert order
@@ -601,6 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
 #pragma unroll 1
         for (int i = lane; i < Sl; i += 32) {
             const int t = i / K, e = S.s_idx[i];
+            if (e < e_lo || e >= e_hi) continue;
             const unsigned m = (unsigned)S.s_mask[e];
             S.slot_w[S.s_off[e] + __popc(m & ((1u << t) - 1u))] = S.s_w[i];
         }
@@ -719,10 +727,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
 #pragma unroll 1
                 for (int i = lane; i < n * K; i += 32) {
                     const int t = i / K, e = S.s_idx[i];
-                    const unsigned m = (unsigned)S.s_mask[e];
-                    const int p = S.s_off[e] + __popc(m & ((1u << t) - 1u));
                     W.topk_idx[i] = e;
                     W.topk_w[i] = S.s_w[i];
+                    if (e < A.s.e_lo || e >= A.s.e_hi) {
+                        W.slot_of[i] = -1;  // an expert this plan does not own
+                        continue;
+                    }
+                    const unsigned m = (unsigned)S.s_mask[e];
+                    const int p = S.s_off[e] + __popc(m & ((1u << t) - 1u));
                     W.slot_token[p] = t;
                     W.slot_k[p] = i - t * K;
                     W.slot_of[i] = p;
@@ -769,8 +781,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
                     const int row = 2 * (lane >> 2) + (i >> 1), tok = 2 * (lane & 3) + (i & 1);
                     if (row >= tl.z && row < tl.w && ((m >> tok) & 1u)) {
                         const int pslot = tr.z + __popc(m & ((1u << tok) - 1u));
-                        const float sg = __fdividef(gv[i], 1.0f + __expf(-gv[i]));
-                        Hg[(size_t)pslot * F + h_pos(tl.y + row)] = f2bf(S.slot_w[pslot] * (sg * uv[i]));
+                        Hg[(size_t)pslot * F + h_pos(tl.y + row)] =
+                            f2bf(S.slot_w[pslot] * glu_act<false>(A.s.act, A.s.act_limit, gv[i], uv[i]));
                     }
                 }
             }

@@ -5,7 +5,8 @@
 // where it is held to 1e-4 of RMS(out) against the oracle.
 //
 // Stages (one launch each), over the de-duplicated expert list:
-//   gate/up : h[p, f] = silu(sum_d Wg[e,f,d] x[t,d]) * sum_d Wu[e,f,d] x[t,d]
+//   gate/up : h[p, f] = act(sum_d Wg[e,f,d] x[t,d], sum_d Wu[e,f,d] x[t,d])
+//             (activation.cuh; SwiGLU by default)
 //   down    : y[p, d] = sum_f Wd[e,d,f] h[p,f]
 //   combine : out[t, d] = sum_{j<k} w[t,j] * y[slot_of(t,j), d], j ascending
 // where p runs over the slots grouped under expert e and t = slot_token[p].
@@ -16,6 +17,7 @@
 // rounding, parity against an all-f32 dense reference).
 #include <cuda_bf16.h>
 
+#include "activation.cuh"
 #include "moe_internal.h"
 #include "routing.cuh"
 
@@ -171,7 +173,7 @@ __global__ void __launch_bounds__(kRowThreads) gateup_f32_kernel(StepArgs a, Wor
             gateup_row<kTok>(gq, uq, gs, gb, us, ub, xs, D, cnt, ag, au);
 #pragma unroll
         for (int t = 0; t < kTok; ++t)
-            if (t < cnt) ws.h[(size_t)(p0 + t) * F + f] = ag[t] / (1.0f + expf(-ag[t])) * au[t];
+            if (t < cnt) ws.h[(size_t)(p0 + t) * F + f] = glu_act<true>(a.s.act, a.s.act_limit, ag[t], au[t]);
     }
 }
 
@@ -215,8 +217,49 @@ __device__ __forceinline__ void down_row(const uint4 *dq, const uint16_t *ds, co
     }
 }
 
+// 6-bit down rows: one group of 64 codes is 48 bytes of a little-endian bit
+// stream (code j at bits 6j..6j+5); w = s * q + b exactly in f32.
+__device__ __forceinline__ void deq64_6bit(const uint4 (&c)[3], float s, float b, float (&w)[64]) {
+    const uint32_t v[12] = {c[0].x, c[0].y, c[0].z, c[0].w, c[1].x, c[1].y,
+                            c[1].z, c[1].w, c[2].x, c[2].y, c[2].z, c[2].w};
+#pragma unroll
+    for (int j = 0; j < 64; ++j) {
+        const int bit = 6 * j, wi = bit >> 5, sh = bit & 31;
+        const uint32_t lo = v[wi], hi = wi + 1 < 12 ? v[wi + 1] : 0u;
+        const uint32_t q = __funnelshift_r(lo, hi, sh) & 0x3Fu;
+        w[j] = fmaf(s, __uint_as_float(0x4B000000u | q) - 8388608.0f, b);
+    }
+}
+
+template <int NT>
+__device__ __forceinline__ void down_row6(const unsigned char *dq, const uint16_t *ds, const uint16_t *db,
+                                          const float *hs, int F, int cnt, float (&acc)[kTok]) {
+    const int G = F / kGroup;
+#pragma unroll 1
+    for (int g = 0; g < G; ++g) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(dq + (size_t)g * 48);
+        const uint4 c[3] = {__ldg(p), __ldg(p + 1), __ldg(p + 2)};
+        float wd[64];
+        deq64_6bit(c, bf16f(ds[g]), bf16f(db[g]), wd);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            if (NT == 1 || t < cnt) {
+                const float *hr = hs + (size_t)t * F + g * kGroup;
+#pragma unroll
+                for (int j = 0; j < 64; j += 4) {
+                    const float4 h4 = *reinterpret_cast<const float4 *>(hr + j);
+                    acc[t] = fmaf(wd[j], h4.x, acc[t]);
+                    acc[t] = fmaf(wd[j + 1], h4.y, acc[t]);
+                    acc[t] = fmaf(wd[j + 2], h4.z, acc[t]);
+                    acc[t] = fmaf(wd[j + 3], h4.w, acc[t]);
+                }
+            }
+        }
+    }
+}
+
 // Thread per down row d of expert unique[blockIdx.y]: the same scheme over the
-// f32 h rows of the expert's slots.
+// f32 h rows of the expert's slots (4-bit or 6-bit down codes).
 __global__ void __launch_bounds__(kRowThreads) down_f32_kernel(StepArgs a, Workspace ws, int thr, int T) {
     extern __shared__ float4 hs4[];
     float *hs = reinterpret_cast<float *>(hs4);  // [T][F]
@@ -230,6 +273,8 @@ __global__ void __launch_bounds__(kRowThreads) down_f32_kernel(StepArgs a, Works
     const bool has_row = d < D;
     const size_t row = (size_t)e * D + (has_row ? d : D - 1);
     const uint4 *dq = reinterpret_cast<const uint4 *>(a.planes.down_q + row * (F / 8));
+    const unsigned char *dq6 = reinterpret_cast<const unsigned char *>(a.planes.down_q) + row * (3 * F / 4);
+    const bool six = a.s.down_bits == 6;
     const uint16_t *ds = a.planes.down_s + row * (F / kGroup);
     const uint16_t *db = a.planes.down_b + row * (F / kGroup);
     for (int p0 = p_begin; p0 < p_end; p0 += T) {
@@ -245,7 +290,12 @@ __global__ void __launch_bounds__(kRowThreads) down_f32_kernel(StepArgs a, Works
         float acc[kTok];
 #pragma unroll
         for (int t = 0; t < kTok; ++t) acc[t] = 0.f;
-        if (cnt == 1)
+        if (six) {
+            if (cnt == 1)
+                down_row6<1>(dq6, ds, db, hs, F, cnt, acc);
+            else
+                down_row6<kTok>(dq6, ds, db, hs, F, cnt, acc);
+        } else if (cnt == 1)
             down_row<1>(dq, ds, db, hs, F, cnt, acc);
         else if (cnt == 2)
             down_row<2>(dq, ds, db, hs, F, cnt, acc);
@@ -267,8 +317,11 @@ __global__ void combine_kernel(StepArgs a, Workspace ws) {
     if (i >= a.s.n * D) return;
     const int t = i / D, d = i - t * D;
     float acc = 0.f;
-    for (int j = 0; j < k; ++j)
-        acc = fmaf(ws.topk_w[t * k + j], ws.y[(size_t)ws.slot_of[t * k + j] * D + d], acc);
+    for (int j = 0; j < k; ++j) {
+        const int p = ws.slot_of[t * k + j];
+        if (p < 0) continue;  // an expert this plan does not own
+        acc = fmaf(ws.topk_w[t * k + j], ws.y[(size_t)p * D + d], acc);
+    }
     if (OT == MOE_DTYPE_F32)
         static_cast<float *>(a.out)[i] = acc;
     else

@@ -24,6 +24,7 @@
 // sorted matrix path, taken here per expert instead of per call).
 #include <cuda_fp16.h>
 
+#include "activation.cuh"
 #include "moe_internal.h"
 #include "ptx.cuh"
 #include "routing.cuh"
@@ -61,6 +62,31 @@ __device__ __forceinline__ void dequant_group(const uint32_t *q, float s, float 
             const float lo = fmaf(s, (float)((w[i] >> (8 * j)) & 0xFu), b);
             const float hi = fmaf(s, (float)((w[i] >> (8 * j + 4)) & 0xFu), b);
             o[j] = pack_f16(lo, hi);
+        }
+        *reinterpret_cast<uint4 *>(dst + i * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// one group of one 6-bit row (48 bytes, a little-endian bit stream of 64
+// codes) dequantised to f16 at dst
+__device__ __forceinline__ void dequant_group6(const unsigned char *q, float s, float b, unsigned char *dst) {
+    const uint4 c0 = __ldg(reinterpret_cast<const uint4 *>(q));
+    const uint4 c1 = __ldg(reinterpret_cast<const uint4 *>(q) + 1);
+    const uint4 c2 = __ldg(reinterpret_cast<const uint4 *>(q) + 2);
+    const uint32_t v[12] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w, c2.x, c2.y, c2.z, c2.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float w2[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int bit = 6 * (8 * i + 2 * j + h), wi = bit >> 5, sh = bit & 31;
+                const uint32_t code = __funnelshift_r(v[wi], wi + 1 < 12 ? v[wi + 1] : 0u, sh) & 0x3Fu;
+                w2[h] = fmaf(s, (float)code, b);
+            }
+            o[j] = pack_f16(w2[0], w2[1]);
         }
         *reinterpret_cast<uint4 *>(dst + i * 16) = make_uint4(o[0], o[1], o[2], o[3]);
     }
@@ -167,7 +193,7 @@ __global__ void __launch_bounds__(kTT) gateup_tile_kernel(StepArgs a, Workspace 
     for (int i = threadIdx.x; i < cnt * (kTR / 2); i += kTT) {
         const int j = i / (kTR / 2), fr = i % (kTR / 2);
         const float gv = E[fr * 65 + j], uv = E[(kTR / 2 + fr) * 65 + j];
-        ws.h[(size_t)(off + j) * F + f0 + fr] = gv / (1.0f + expf(-gv)) * uv;
+        ws.h[(size_t)(off + j) * F + f0 + fr] = glu_act<true>(a.s.act, a.s.act_limit, gv, uv);
     }
 }
 
@@ -188,8 +214,12 @@ __global__ void __launch_bounds__(kTT) down_tile_kernel(StepArgs a, Workspace ws
     auto load_w = [&](int r, int k, unsigned char *dst) {
         const size_t row = (size_t)e * D + d0 + r;
         const size_t gi = row * (F / kGroup) + k / kGroup;
-        dequant_group(a.planes.down_q + row * (F / 8) + k / 8, bf16f(a.planes.down_s[gi]),
-                      bf16f(a.planes.down_b[gi]), dst);
+        if (a.s.down_bits == 6)
+            dequant_group6(reinterpret_cast<const unsigned char *>(a.planes.down_q) + row * (3 * F / 4) + k / 64 * 48,
+                           bf16f(a.planes.down_s[gi]), bf16f(a.planes.down_b[gi]), dst);
+        else
+            dequant_group(a.planes.down_q + row * (F / 8) + k / 8, bf16f(a.planes.down_s[gi]),
+                          bf16f(a.planes.down_b[gi]), dst);
     };
     auto load_x = [&](int j, int k) -> uint4 {
         if (j >= cnt) return make_uint4(0, 0, 0, 0);

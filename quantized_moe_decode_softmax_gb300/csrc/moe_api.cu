@@ -39,6 +39,15 @@ moe_status validate_config(const moe_config *c) {
                                MOE_FLAG_GROUPED_COHORTS | MOE_FLAG_TEST_STALL))
         return MOE_ERR_INVALID_ARG;
     if (c->Dff > kMaxDff || c->D > kMaxD) return MOE_ERR_UNSUPPORTED;
+    if (c->activation < MOE_ACT_SWIGLU || c->activation > MOE_ACT_SWIGLU_CLAMPED) return MOE_ERR_UNSUPPORTED;
+    if (c->activation == MOE_ACT_SWIGLU_CLAMPED &&
+        !(c->act_limit > 0.0f && c->act_limit <= 3.0e38f))  // finite and positive (NaN fails)
+        return MOE_ERR_INVALID_ARG;
+    if (c->down_bits != 0 && c->down_bits != 4 && c->down_bits != 6) return MOE_ERR_UNSUPPORTED;
+    if (c->expert_begin != 0 || c->expert_end != 0) {
+        if (c->expert_begin < 0 || c->expert_begin >= c->expert_end || c->expert_end > c->E)
+            return MOE_ERR_INVALID_ARG;
+    }
     return MOE_OK;
 }
 
@@ -163,7 +172,8 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan **out) {
     }
     carve(*cfg, (char *)p->ws_base, &p->ws);
     p->fused_ok = false;
-    if (!(cfg->flags & MOE_FLAG_F32_DEBUG)) {
+    // the single-launch kernel reads 4-bit down planes only
+    if (!(cfg->flags & MOE_FLAG_F32_DEBUG) && cfg->down_bits != 6) {
         int max_smem = 0, per_sm = 0;
         cudaError_t e2 = cudaSuccess;
         if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device) ==
@@ -240,9 +250,7 @@ moe_status moe_decode_forward(moe_plan *plan, const void *x, const void *router_
     StepArgs a{};
     // the test hook stalls only the plan's first step
     const unsigned step_flags = plan->forwards == 0 ? plan->cfg.flags : plan->cfg.flags & ~(unsigned)MOE_FLAG_TEST_STALL;
-    a.s = Shape{plan->cfg.E, plan->cfg.top_k, plan->cfg.D, plan->cfg.Dff, n_tokens,
-                plan->cfg.x_dtype, plan->cfg.router_dtype, plan->cfg.out_dtype,
-                step_flags};
+    a.s = shape_of(plan->cfg, n_tokens, step_flags);
     a.x = x;
     a.router_w = router_w;
     a.router_bias = router_bias;

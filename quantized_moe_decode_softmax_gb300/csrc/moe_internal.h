@@ -53,7 +53,22 @@ struct Shape {
     int E, k, D, F, n;
     int x_dtype, w_dtype, out_dtype;
     unsigned flags;  // MOE_FLAG_* of the plan
+    int act;         // MOE_ACT_*
+    float act_limit; // clamp bound of MOE_ACT_SWIGLU_CLAMPED
+    int down_bits;   // 4 or 6
+    int e_lo, e_hi;  // owned experts [e_lo, e_hi)
 };
+
+// the Shape of a plan's config for a cohort of n tokens
+inline Shape shape_of(const moe_config &c, int n, unsigned flags) {
+    Shape s{c.E, c.top_k, c.D, c.Dff, n, c.x_dtype, c.router_dtype, c.out_dtype, flags,
+            c.activation, c.act_limit, c.down_bits == 6 ? 6 : 4, 0, c.E};
+    if (c.expert_begin != 0 || c.expert_end != 0) {
+        s.e_lo = c.expert_begin;
+        s.e_hi = c.expert_end;
+    }
+    return s;
+}
 
 // Arguments of one step, device pointers.
 struct StepArgs {

@@ -95,6 +95,16 @@ extern "C" moe_status moe_decode_forward_noalloc(const moe_config *cfg, const vo
     if (cfg->E > kMaxE || cfg->top_k > kMaxTopK || cfg->D > kMaxD || cfg->Dff > kMaxDff ||
         cfg->D % kGroup || cfg->Dff % kGroup)
         return MOE_ERR_UNSUPPORTED;
+    // the layer variants: activations and the expert range as for a plan; the
+    // single-launch kernel reads 4-bit down planes only
+    if (cfg->activation < MOE_ACT_SWIGLU || cfg->activation > MOE_ACT_SWIGLU_CLAMPED) return MOE_ERR_UNSUPPORTED;
+    if (cfg->activation == MOE_ACT_SWIGLU_CLAMPED && !(cfg->act_limit > 0.0f && cfg->act_limit <= 3.0e38f))
+        return MOE_ERR_INVALID_ARG;
+    if (cfg->down_bits == 6) return MOE_ERR_UNSUPPORTED;
+    if (cfg->down_bits != 0 && cfg->down_bits != 4) return MOE_ERR_UNSUPPORTED;
+    if ((cfg->expert_begin != 0 || cfg->expert_end != 0) &&
+        (cfg->expert_begin < 0 || cfg->expert_begin >= cfg->expert_end || cfg->expert_end > cfg->E))
+        return MOE_ERR_INVALID_ARG;
     // the scratch this call needs must fit the static array
     if (carve_noalloc(*cfg, n_tokens, nullptr, nullptr) > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED;
 
@@ -147,7 +157,7 @@ extern "C" moe_status moe_decode_forward_noalloc(const moe_config *cfg, const vo
         return MOE_ERR_CUDA;
     }
     StepArgs a{};
-    a.s = Shape{c.E, c.top_k, c.D, c.Dff, n_tokens, c.x_dtype, c.router_dtype, c.out_dtype, 0u};
+    a.s = shape_of(c, n_tokens, 0u);
     a.x = x;
     a.router_w = router_w;
     a.router_bias = router_bias;

@@ -59,7 +59,8 @@ __global__ void router_logits_kernel(const void *__restrict__ x, const void *__r
 }
 
 // one CTA: softmax, top-k, renormalise, then group; writes the workspace
-__global__ void __launch_bounds__(1024) topk_group_kernel(Workspace ws, int n, int E, int k) {
+__global__ void __launch_bounds__(1024) topk_group_kernel(Workspace ws, int n, int E, int k, int e_lo,
+                                                          int e_hi) {
     __shared__ int s_idx[kMaxSlots];
     __shared__ float s_w[kMaxSlots];
     __shared__ unsigned long long s_mask[kMaxE];
@@ -70,7 +71,7 @@ __global__ void __launch_bounds__(1024) topk_group_kernel(Workspace ws, int n, i
     __shared__ int s_U;
     block_topk(ws.logits, n, E, k, s_idx, s_w);
     __syncthreads();
-    block_group(s_idx, n, E, k, s_mask, s_counts, s_off, s_st, s_sk, s_of, s_unique, &s_U);
+    block_group(s_idx, n, E, k, e_lo, e_hi, s_mask, s_counts, s_off, s_st, s_sk, s_of, s_unique, &s_U);
     const int S = n * k;
     for (int s = threadIdx.x; s < S; s += blockDim.x) {
         ws.topk_idx[s] = s_idx[s];
@@ -116,7 +117,7 @@ cudaError_t launch_router_logits(const StepArgs &a, const Workspace &ws, cudaStr
 
 cudaError_t launch_topk_group(const StepArgs &a, const Workspace &ws, cudaStream_t st,
                               int &launched) {
-    topk_group_kernel<<<1, 1024, 0, st>>>(ws, a.s.n, a.s.E, a.s.k);
+    topk_group_kernel<<<1, 1024, 0, st>>>(ws, a.s.n, a.s.E, a.s.k, a.s.e_lo, a.s.e_hi);
     launched += 1;
     return cudaGetLastError();
 }

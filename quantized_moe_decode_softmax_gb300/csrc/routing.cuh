@@ -125,11 +125,13 @@ __device__ inline void block_topk(const float *logits, int n, int E, int k, int 
     }
 }
 
-// Grouping of the n*k slots by expert (block-cooperative, all threads).
+// Grouping of the n*k slots by expert (block-cooperative, all threads), over
+// the experts [e_lo, e_hi) only (an expert-parallel shard; the other slots get
+// slot_of = -1 and no grouped position).
 // s_mask: [E] u64 scratch (token bitmask per expert, n <= 64).
 // Outputs (shared): counts[E], offsets[E+1], slot_token/slot_k[n*k] in grouped
 // order, slot_of[n*k] (t*k + j -> grouped position), unique[E], *U.
-__device__ inline void block_group(const int *s_idx, int n, int E, int k,
+__device__ inline void block_group(const int *s_idx, int n, int E, int k, int e_lo, int e_hi,
                                    unsigned long long *s_mask, int *counts, int *offsets,
                                    int *slot_token, int *slot_k, int *slot_of, int *unique,
                                    int *U) {
@@ -138,7 +140,7 @@ __device__ inline void block_group(const int *s_idx, int n, int E, int k,
     __syncthreads();
     for (int s = threadIdx.x; s < S; s += blockDim.x) {
         const int e = s_idx[s];
-        if ((unsigned)e < (unsigned)E) atomicOr(&s_mask[e], 1ull << (s / k));
+        if ((unsigned)e < (unsigned)E && e >= e_lo && e < e_hi) atomicOr(&s_mask[e], 1ull << (s / k));
     }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = __popcll(s_mask[e]);
@@ -175,7 +177,10 @@ __device__ inline void block_group(const int *s_idx, int n, int E, int k,
     __syncthreads();
     for (int s = threadIdx.x; s < S; s += blockDim.x) {
         const int e = s_idx[s];
-        if ((unsigned)e >= (unsigned)E) continue;
+        if ((unsigned)e >= (unsigned)E || e < e_lo || e >= e_hi) {
+            slot_of[s] = -1;
+            continue;
+        }
         const int t = s / k;
         const unsigned long long below = (t == 0) ? 0ull : (s_mask[e] & ((1ull << t) - 1ull));
         const int pos = offsets[e] + __popcll(below);

@@ -13,10 +13,13 @@ _DT = {"f32": _abi.MOE_DTYPE_F32, "bf16": _abi.MOE_DTYPE_BF16}
 
 def _to_torch(a: np.ndarray, device, torch):
     """numpy storage array -> device tensor with the same bytes.
-    uint32 -> int32, uint16 (bf16 bits) -> bfloat16, float32 -> float32."""
+    uint32 -> int32, uint16 (bf16 bits) -> bfloat16, uint8 -> uint8 (6-bit
+    down codes), float32 -> float32."""
     a = np.ascontiguousarray(a)
     if a.dtype == np.uint32:
         return torch.from_numpy(a.view(np.int32)).to(device)
+    if a.dtype == np.uint8:
+        return torch.from_numpy(a).to(device)
     if a.dtype == np.uint16:
         return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
     if a.dtype == np.float32:
@@ -49,8 +52,7 @@ class DeviceLayer:
 
     @property
     def plane_bytes_per_expert(self) -> int:
-        per = self.D * self.Dff // 2 + 4 * self.D * self.Dff // 64
-        return 3 * per
+        return sum(t.numel() * t.element_size() for t in self.planes.values()) // self.E
 
 
 class MoeDecodeLayer:
@@ -58,11 +60,17 @@ class MoeDecodeLayer:
 
     def __init__(self, E: int, top_k: int, D: int, Dff: int, max_tokens: int = 64,
                  act_dtype: str = "bf16", out_dtype: Optional[str] = None, flags: int = 0,
-                 mma_min_tokens: int = 0):
+                 mma_min_tokens: int = 0, activation: int = _abi.MOE_ACT_SWIGLU,
+                 act_limit: float = 0.0, down_bits: int = 0, experts=None):
+        """experts: (begin, end) of the experts this plan owns (an expert-parallel
+        shard), or None for all of them."""
+        eb, ee = (0, 0) if experts is None else (int(experts[0]), int(experts[1]))
         self.cfg = _abi.make_config(E, top_k, D, Dff, max_tokens, x_dtype=_DT[act_dtype],
                                     router_dtype=_DT[act_dtype],
                                     out_dtype=_DT[out_dtype or act_dtype], flags=flags,
-                                    mma_min_tokens=mma_min_tokens)
+                                    mma_min_tokens=mma_min_tokens, activation=activation,
+                                    act_limit=act_limit, down_bits=down_bits,
+                                    expert_begin=eb, expert_end=ee)
         self.act_dtype = act_dtype
         self.out_dtype = out_dtype or act_dtype
         self.plan = _abi.moe_plan_create(self.cfg)

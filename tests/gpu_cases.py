@@ -56,11 +56,13 @@ def x_tensor(shape, x):
     return torch.from_numpy(st).cuda()
 
 
-def make_plan(shape, flags=0, out_dtype=None, max_tokens=64, mma_min_tokens=0):
+def make_plan(shape, flags=0, out_dtype=None, max_tokens=64, mma_min_tokens=0, activation=0,
+              act_limit=0.0, experts=None):
     from quantized_moe_decode_softmax_gb300 import MoeDecodeLayer
     return MoeDecodeLayer(shape.E, shape.top_k, shape.D, shape.F, max_tokens=max_tokens,
                           act_dtype=shape.act_dtype, out_dtype=out_dtype, flags=flags,
-                          mma_min_tokens=mma_min_tokens)
+                          mma_min_tokens=mma_min_tokens, activation=activation,
+                          act_limit=act_limit, down_bits=shape.down_bits, experts=experts)
 
 
 # measured parity margins of this session: one dict per compared output
@@ -98,9 +100,24 @@ def run_gpu(plan, dl, shape, x, launches=None):
     return out.float().cpu().numpy(), plan.routing(x.shape[0])
 
 
-def run_oracle(lay, x):
-    return oracle.moe_forward(x, lay.router_w, lay.router_bias, lay.planes, lay.shape.top_k,
-                              want_bf16=True)
+def run_oracle(lay, x, activation=0, limit=0.0, planes=None):
+    return oracle.moe_forward(x, lay.router_w, lay.router_bias, lay.planes if planes is None else planes,
+                              lay.shape.top_k, want_bf16=True, activation=activation, limit=limit,
+                              down_bits=lay.shape.down_bits)
+
+
+def planes_owned(lay, lo, hi):
+    """The layer's planes with the scales and biases of every expert outside
+    [lo, hi) zeroed: those experts' weights are all 0, so their outputs are
+    exactly 0 and the oracle step is the shard's partial (routing unchanged)."""
+    arrs = []
+    for name, a in zip(ms.ExpertPlanes.FIELDS, lay.planes.arrays()):
+        a = a.copy()
+        if not name.endswith("_q"):
+            a[:lo] = 0
+            a[hi:] = 0
+        arrs.append(a)
+    return ms.ExpertPlanes(*arrs)
 
 
 def assert_routing_equal(r, ref):

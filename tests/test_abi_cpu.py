@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(libpath):
 
 
 def test_abi_version_and_status_strings(libpath):
-    assert q.moe_abi_version() == 1
+    assert q.moe_abi_version() == 2
     assert q.moe_status_str(q.MOE_OK) == "MOE_OK"
     assert q.moe_status_str(q.MOE_ERR_UNSUPPORTED) == "MOE_ERR_UNSUPPORTED"
     assert q.moe_status_str(99) == "MOE_ERR_UNKNOWN"
@@ -128,18 +128,40 @@ _SINGLE_VIOLATIONS = [
     ("x_dtype", 2, q.MOE_ERR_INVALID_ARG), ("router_dtype", -1, q.MOE_ERR_INVALID_ARG),
     ("out_dtype", 9, q.MOE_ERR_INVALID_ARG), ("mma_min_tokens", -3, q.MOE_ERR_INVALID_ARG),
     ("flags", 1 << 5, q.MOE_ERR_INVALID_ARG),
+    ("activation", 4, q.MOE_ERR_UNSUPPORTED), ("activation", -1, q.MOE_ERR_UNSUPPORTED),
+    ("down_bits", 5, q.MOE_ERR_UNSUPPORTED), ("down_bits", 8, q.MOE_ERR_UNSUPPORTED),
+]
+
+# the clamp bound and the expert range (each broken alone)
+_PAIR_VIOLATIONS = [
+    (dict(activation=3, act_limit=0.0), q.MOE_ERR_INVALID_ARG),
+    (dict(activation=3, act_limit=-1.0), q.MOE_ERR_INVALID_ARG),
+    (dict(activation=3, act_limit=float("nan")), q.MOE_ERR_INVALID_ARG),
+    (dict(activation=3, act_limit=float("inf")), q.MOE_ERR_INVALID_ARG),
+    (dict(activation=3, act_limit=7.0), q.MOE_OK),
+    (dict(activation=1, act_limit=0.0), q.MOE_OK),   # the bound is ignored elsewhere
+    (dict(expert_begin=5, expert_end=3), q.MOE_ERR_INVALID_ARG),
+    (dict(expert_begin=4, expert_end=4), q.MOE_ERR_INVALID_ARG),
+    (dict(expert_begin=-1, expert_end=5), q.MOE_ERR_INVALID_ARG),
+    (dict(expert_begin=0, expert_end=129), q.MOE_ERR_INVALID_ARG),
+    (dict(expert_begin=0, expert_end=128), q.MOE_OK),
+    (dict(expert_begin=64, expert_end=128), q.MOE_OK),
+    (dict(down_bits=6), q.MOE_OK),
+    (dict(down_bits=4), q.MOE_OK),
 ]
 
 
 def _status(**over):
     base = dict(E=128, top_k=8, D=2048, Dff=768, bits=4, group_size=64, max_tokens=64,
                 x_dtype=q.MOE_DTYPE_BF16, router_dtype=q.MOE_DTYPE_BF16,
-                out_dtype=q.MOE_DTYPE_BF16, flags=0, mma_min_tokens=0)
+                out_dtype=q.MOE_DTYPE_BF16, flags=0, mma_min_tokens=0, activation=0,
+                act_limit=0.0, down_bits=0, expert_begin=0, expert_end=0)
     base.update(over)
     cfg = q.moe_config(base["E"], base["top_k"], base["D"], base["Dff"], base["bits"],
                        base["group_size"], base["max_tokens"], base["x_dtype"],
                        base["router_dtype"], base["out_dtype"], base["flags"],
-                       base["mma_min_tokens"])
+                       base["mma_min_tokens"], base["activation"], base["act_limit"],
+                       base["down_bits"], base["expert_begin"], base["expert_end"])
     n = ctypes.c_size_t(0)
     return q.lib().moe_plan_workspace_bytes(ctypes.byref(cfg), ctypes.byref(n)), n.value
 
@@ -148,6 +170,19 @@ def _status(**over):
                          ids=[f"{f}={v}" for f, v, _ in _SINGLE_VIOLATIONS])
 def test_each_documented_rule_alone(libpath, field, value, status):
     assert _status(**{field: value})[0] == status
+
+
+@pytest.mark.parametrize("over,status", _PAIR_VIOLATIONS, ids=[str(o) for o, _ in _PAIR_VIOLATIONS])
+def test_layer_variant_and_expert_range_rules(libpath, over, status):
+    assert _status(**over)[0] == status
+
+
+def test_config_struct_matches_the_header():
+    """The ctypes struct lists the header's moe_config fields in order."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(r"typedef struct \{([^}]*)\}\s*moe_config;", text).group(1)
+    fields = re.findall(r"(\w+)\s*;", body)
+    assert fields == [f for f, _ in q.moe_config._fields_]
 
 
 def test_random_valid_configs_are_accepted_and_sized(libpath):
@@ -159,7 +194,11 @@ def test_random_valid_configs_are_accepted_and_sized(libpath):
                    Dff=64 * r.randint(1, 128), max_tokens=r.randint(1, 64),
                    x_dtype=r.choice([q.MOE_DTYPE_F32, q.MOE_DTYPE_BF16]),
                    out_dtype=r.choice([q.MOE_DTYPE_F32, q.MOE_DTYPE_BF16]),
-                   mma_min_tokens=r.randint(0, 64))
+                   mma_min_tokens=r.randint(0, 64), activation=r.randint(0, 3),
+                   act_limit=r.uniform(0.5, 50.0), down_bits=r.choice([0, 4, 6]))
+        if r.random() < 0.5:
+            b = r.randint(0, E - 1)
+            cfg.update(expert_begin=b, expert_end=r.randint(b + 1, E))
         st, nbytes = _status(**cfg)
         assert st == q.MOE_OK, cfg
         # the workspace holds at least h and y in f32 for every slot

@@ -49,3 +49,21 @@ def test_noalloc_declines_what_its_kernel_cannot_run():
     with pytest.raises(q.MoeError) as ei:  # more than 8 tokens
         q.moe_decode_forward_noalloc(cfg, xt, dl.router_w, dl.router_bias, dl.c_planes, 9, shape.top_k, out)
     assert ei.value.status == q.MOE_ERR_UNSUPPORTED
+
+
+def test_noalloc_with_a_layer_variant_and_an_expert_range():
+    """The allocation-free entry point takes the same variant fields."""
+    import torch
+    lay, x = case("qwen3", 2, 3)
+    shape = lay.shape
+    dl = device_layer(lay)
+    xt = x_tensor(shape, x)
+    ref_plan = make_plan(shape, activation=q.MOE_ACT_GEGLU, experts=(0, 64))  # plan path
+    ref = ref_plan.forward(xt, dl).clone()
+    torch.cuda.synchronize()
+    cfg = q.make_config(shape.E, shape.top_k, shape.D, shape.F, max_tokens=3,
+                        activation=q.MOE_ACT_GEGLU, expert_begin=0, expert_end=64)
+    out = torch.empty_like(ref)
+    q.moe_decode_forward_noalloc(cfg, xt, dl.router_w, dl.router_bias, dl.c_planes, 3, shape.top_k, out)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
