@@ -67,7 +67,12 @@ typedef enum {
     MOE_ERR_UNSUPPORTED = 2,  /* a shape or format this library declines */
     MOE_ERR_CUDA = 3,         /* a CUDA call or launch failed */
     MOE_ERR_OOM = 4,          /* workspace allocation failed */
-    MOE_ERR_TIMEOUT = 5       /* a device-side wait gave up (bounded spin) */
+    MOE_ERR_TIMEOUT = 5,      /* a device-side wait gave up (bounded spin) */
+    MOE_ERR_RANGE = 6         /* an intermediate of the single-launch kernel left
+                                 the range of its f16 operand (|h| > 65504): that
+                                 step's output is invalid (reported like a
+                                 timeout; MOE_FLAG_F32_DEBUG computes such
+                                 layers in f32) */
 } moe_status;
 
 /* element types of x, router weights and out */
@@ -217,7 +222,8 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan **out);
  * that gives up records MOE_ERR_TIMEOUT in the plan and the step's output is
  * garbage. Once that step has finished on the device, the next call on the
  * plan (this one, moe_decode_forward_host, or moe_plan_check) returns
- * MOE_ERR_TIMEOUT (MOE_ERR_CUDA for an internal error) and clears it; a
+ * MOE_ERR_TIMEOUT (MOE_ERR_RANGE for a saturated f16 intermediate, MOE_ERR_CUDA
+ * for an internal error) and clears it; a
  * forward call that reports it launches nothing and only enqueues two small
  * memsets that reset the plan's error state on `stream`. A step that was
  * still running at the time is reported by a later call. The steps after a

@@ -18,6 +18,7 @@ from ._abi import (  # noqa: F401
     MOE_ERR_CUDA,
     MOE_ERR_INVALID_ARG,
     MOE_ERR_OOM,
+    MOE_ERR_RANGE,
     MOE_ERR_TIMEOUT,
     MOE_ERR_UNSUPPORTED,
     MOE_FLAG_F32_DEBUG,

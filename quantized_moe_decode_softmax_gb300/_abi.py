@@ -16,7 +16,8 @@ import numpy as np
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmoe_decode.so")
 
-MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_OOM, MOE_ERR_TIMEOUT = range(6)
+(MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_OOM, MOE_ERR_TIMEOUT,
+ MOE_ERR_RANGE) = range(7)
 MOE_DTYPE_F32, MOE_DTYPE_BF16 = 0, 1
 MOE_FLAG_F32_DEBUG = 1 << 0
 MOE_FLAG_TRACE = 1 << 1

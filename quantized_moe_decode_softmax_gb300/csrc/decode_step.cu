@@ -20,7 +20,7 @@
 //      each on its own pair of input groups, running m16n8k16 MMAs on the raw
 //      4-bit codes; each warp writes its partial sums to one of two buffers and
 //      a reducer warp sums the 16 partials in warp order and writes
-//      w * silu(g) * u as bf16, one row per (token, expert) slot. -> barrier 2
+//      h = w * act(g, u) as f16, one row per (token, expert) slot. -> barrier 2
 //   B  down + combine: each CTA owns a slice of the D output rows for every
 //      selected expert. The down codes stream into the same ring (issued as soon
 //      as ring stages free up, before barrier 2); because the routing weight is
@@ -43,9 +43,12 @@
 //     high nibbles divided by 16, so per group sum((1024 + m q) x / m) =
 //     1024 sum(x / m) + sum(q x), and the row's contribution is
 //     s * (acc - 1024 sum(x / m)) + b * sum(x).
-//   down (bf16): 128 + q, row contribution s * acc + (b - 128 s) * sum(h); tile
-//     row 15 is fed zero codes, so its MMA row returns 128 * sum(h) for free.
-// x enters the MMA as f16 (|x| < 65504 is assumed) and h as bf16, so this path
+//   down (f16): every nibble shifted down and OR-ed onto 1024.0 gives 1024 + q;
+//     the row contribution is s * acc + (b - 1024 s) * sum(h); tile row 15 is
+//     fed zero codes, so its MMA row returns 1024 * sum(h) for free.
+// x and h enter the MMA as f16 (10 mantissa bits): x is scaled per token by a
+// power of two when its magnitudes leave f16's comfortable range (phase R), and
+// an |h| beyond f16's range is saturated and reported (MOE_ERR_RANGE). This path
 // is held to the bf16 tolerance; the f32 check path keeps every product in f32.
 // Every reduction has a fixed order: results are bitwise reproducible.
 //
@@ -62,6 +65,7 @@
 #include <cudaTypedefs.h>
 
 #include "activation.cuh"
+#include "device_status.cuh"
 #include "moe_internal.h"
 #include "ptx.cuh"
 #include "routing.cuh"
@@ -104,18 +108,28 @@ __device__ __forceinline__ uint16_t f2bf(float f) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
-// codes of inputs p and p+4 of a packed word, as bf16x2 values 128 + q
+// f16 bits of f (round to nearest even); a magnitude beyond the largest f16
+// saturates to +-65504 and sets *over
+__device__ __forceinline__ uint16_t f2h_sat(float f, bool &over) {
+    if (!(fabsf(f) <= 65504.0f)) {
+        over = true;
+        f = f != f ? 0.0f : copysignf(65504.0f, f);
+    }
+    return __half_as_ushort(__float2half_rn(f));
+}
+
+// codes of inputs p and p+4 of a packed word, as f16x2 values 1024 + q
 __device__ __forceinline__ uint32_t code_pair(uint32_t word, int p) {
-    return ((word >> (4 * p)) & 0x000F000Fu) | 0x43004300u;
+    return ((word >> (4 * p)) & 0x000F000Fu) | 0x64006400u;
 }
 
 // two k16 MMA steps over one packed word per MMA row (rows g and g+8) and the
 // matching activation word (4 bf16x2 pairs: (v0,v4) (v1,v5) (v2,v6) (v3,v7))
 __device__ __forceinline__ void mma_word(float (&acc)[4], uint32_t wg, uint32_t wg8, uint4 v) {
     uint32_t a0[4] = {code_pair(wg, 0), code_pair(wg8, 0), code_pair(wg, 1), code_pair(wg8, 1)};
-    ptx::mma_bf16_16816(acc, a0, v.x, v.y);
+    ptx::mma_f16_16816(acc, a0, v.x, v.y);
     uint32_t a1[4] = {code_pair(wg, 2), code_pair(wg8, 2), code_pair(wg, 3), code_pair(wg8, 3)};
-    ptx::mma_bf16_16816(acc, a1, v.z, v.w);
+    ptx::mma_f16_16816(acc, a1, v.z, v.w);
 }
 
 // f16 variant: f16 carries 10 mantissa bits, so both nibbles of a byte are
@@ -170,9 +184,12 @@ __device__ __forceinline__ int h_pos(int f) {
 struct Smem {
     uint64_t *full, *empty;  // ring slots: data landed / consumed by every consumer warp
     uint64_t *pfull, *pempty;  // gate/up partial buffers: all partials written / reduced
+    uint64_t *hbar;          // the step's h rows landed in shared memory (down phase)
     int *misc;             // [0] abort [1] barrier ok [2] U [3] tiles [4] b0 [5] b1
-                           // [6] stages issued [8..9] partials written [10..11] shares reduced
+                           // [6] stages issued [7] x needs per-token scaling
+                           // [8..9] partials written [10..11] shares reduced
                            // [16..23] stage release counts [24..39] grouping scans
+                           // [40..47] per-token scale of x as f32 (2^e, 1 unless scaled)
     unsigned long long *s_mask;
     int *s_idx, *s_st, *s_sk, *s_of, *s_counts, *s_off, *s_unique;
     float *s_w, *slot_w;
@@ -182,6 +199,8 @@ struct Smem {
     unsigned char *xs;
     float *xsum;
     float *red;            // gate/up partials [2][kCW][32][8]; router / final scratch
+    unsigned char *hs;     // h rows for the down phase: the x, xsum and red areas,
+                           // dead once gate/up is done
     unsigned char *ring;
 };
 
@@ -191,6 +210,7 @@ __device__ __forceinline__ Smem carve_smem(unsigned char *base, const DecodeLayo
     s.empty = s.full + kMaxRing;
     s.pfull = s.full + 2 * kMaxRing;
     s.pempty = s.pfull + 2;
+    s.hbar = s.pempty + 2;
     s.misc = reinterpret_cast<int *>(base + L.off_misc);
     unsigned char *r = base + L.off_route;
     s.s_mask = reinterpret_cast<unsigned long long *>(r);
@@ -209,18 +229,9 @@ __device__ __forceinline__ Smem carve_smem(unsigned char *base, const DecodeLayo
     s.xs = base + L.off_x;
     s.xsum = reinterpret_cast<float *>(base + L.off_xsum);
     s.red = reinterpret_cast<float *>(base + L.off_red);
+    s.hs = base + L.off_x;
     s.ring = base + L.off_ring;
     return s;
-}
-
-// Record a device-side error: the bit in the plan's status word, and a 1 in the
-// host-mapped words whose device address the host stored in status words 2..3
-// (word 0 for a timeout, word 1 for an internal error; address 0 when the host
-// has none), so that the next forward call can report it without synchronising.
-__device__ __forceinline__ void report_error(unsigned *status, unsigned bit) {
-    atomicOr(status, bit);
-    const unsigned long long host = *reinterpret_cast<volatile unsigned long long *>(status + 2);
-    if (host) reinterpret_cast<volatile unsigned *>(host)[bit == kDevErrTimeout ? 0 : 1] = 1u;
 }
 
 __device__ __forceinline__ void set_timeout(volatile int *abort_flag, unsigned *status) {
@@ -415,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     volatile int *bar_ok = S.misc + 1;
     const bool timing = (A.s.flags & MOE_FLAG_PHASE_TIMES) != 0;
     unsigned long long *gsync = reinterpret_cast<unsigned long long *>(W.sync);
-    uint16_t *Hg = reinterpret_cast<uint16_t *>(W.h);  // [slots][F] bf16, h_pos order
+    uint16_t *Hg = reinterpret_cast<uint16_t *>(W.h);  // [slots][F] f16, h_pos order
 
     // Prologue on shared memory and kernel parameters only: it may overlap the
     // tail of the previous kernel in the stream (programmatic dependent launch).
@@ -429,7 +440,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
             ptx::mbar_init(&S.pfull[b], kCW);
             ptx::mbar_init(&S.pempty[b], 1);
         }
+        ptx::mbar_init(S.hbar, 1);
         for (int i = 0; i < 32; ++i) S.misc[i] = 0;
+        for (int t = 0; t < kNFast; ++t) reinterpret_cast<float *>(S.misc + 40)[t] = 1.0f;
         ptx::mbar_fence_init();
     }
     if (tid == 32) {
@@ -456,12 +469,45 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     // the chunk's sums, and dots the chunk with this CTA's router rows. A warp's
     // 32 threads share the token, so the per-token sums over chunks are warp
     // sums, combined over the chunk-warps in a fixed order.
+    // f16 range: a chunk whose largest |x| is at least 2^15, or non-zero below
+    // 2^-10, marks the step; the tokens are then staged again scaled by 2^-e
+    // (e = ilogb(max |x_t|) - 14, exact), and the reducers multiply the token's
+    // gate and up sums by 2^e. Ordinary activations never take that path.
     {
         const int nE = (cta < E ? 1 : 0) + (cta + (int)G < E ? 1 : 0);
         const int chunks = D >> 3;                  // a multiple of 32, at most kThreads
         const int NW = chunks >> 5;                 // chunk-warps per token
         const int TG = min(kThreads / chunks, kNFast);
         float *rs = S.red;                          // [token][router row][chunk-warp]
+        float *xscale = reinterpret_cast<float *>(S.misc + 40);
+        // x -> f16 in B-operand order (pairs (0,4) (1,5) (2,6) (3,7)), odd inputs
+        // divided by 16 (see mma_word_f16), times `inv`; the group's sums of x
+        // and of x / m as the MMA sees them. Called by whole warps (one token).
+        auto stage_chunk = [&](int t, int ch, const float (&xv)[8], float inv) {
+            uint16_t b[8];
+            float sm = 0.f, smd = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const __half hv = __float2half_rn((j & 1) ? xv[j] * inv * 0.0625f : xv[j] * inv);
+                b[j] = __half_as_ushort(hv);
+                const float f = __half2float(hv);
+                smd += f;
+                sm += (j & 1) ? f * 16.f : f;
+            }
+            uint4 o;
+            o.x = (uint32_t)b[0] | ((uint32_t)b[4] << 16);
+            o.y = (uint32_t)b[1] | ((uint32_t)b[5] << 16);
+            o.z = (uint32_t)b[2] | ((uint32_t)b[6] << 16);
+            o.w = (uint32_t)b[3] | ((uint32_t)b[7] << 16);
+            *reinterpret_cast<uint4 *>(S.xs + (size_t)t * L.x_stride + (size_t)ch * 16) = o;
+            // group sums: the 8 chunks of a group are 8 consecutive threads
+#pragma unroll
+            for (int off = 1; off < 8; off <<= 1) {
+                sm += __shfl_xor_sync(0xffffffffu, sm, off);
+                smd += __shfl_xor_sync(0xffffffffu, smd, off);
+            }
+            if ((lane & 7) == 0) *reinterpret_cast<float2 *>(S.xsum + ((ch >> 3) * kNFast + t) * 2) = make_float2(sm, smd);
+        };
         if (tid < TG * chunks) {
             const int tg = tid / chunks, ch = tid - tg * chunks;
             float w0[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, w1[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -471,34 +517,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
             for (int t = tg; t < n; t += TG) {
                 float xv[8];
                 load8f(A.x, (size_t)t * D + (size_t)ch * 8, A.s.x_dtype, xv);
-                // x -> f16 in B-operand order (pairs (0,4) (1,5) (2,6) (3,7)), odd
-                // inputs divided by 16 (see mma_word_f16); sums of x and of x / m
-                // as the MMA sees them
-                uint16_t b[8];
-                float sm = 0.f, smd = 0.f, d0 = 0.f, d1 = 0.f;
+                float d0 = 0.f, d1 = 0.f, am = 0.f;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const __half hv = __float2half_rn((j & 1) ? xv[j] * 0.0625f : xv[j]);
-                    b[j] = __half_as_ushort(hv);
-                    const float f = __half2float(hv);
-                    smd += f;
-                    sm += (j & 1) ? f * 16.f : f;
                     d0 = fmaf(xv[j], w0[j], d0);
                     d1 = fmaf(xv[j], w1[j], d1);
+                    am = fmaxf(am, fabsf(xv[j]));
                 }
-                uint4 o;
-                o.x = (uint32_t)b[0] | ((uint32_t)b[4] << 16);
-                o.y = (uint32_t)b[1] | ((uint32_t)b[5] << 16);
-                o.z = (uint32_t)b[2] | ((uint32_t)b[6] << 16);
-                o.w = (uint32_t)b[3] | ((uint32_t)b[7] << 16);
-                *reinterpret_cast<uint4 *>(S.xs + (size_t)t * L.x_stride + (size_t)ch * 16) = o;
-                // group sums: the 8 chunks of a group are 8 consecutive threads
-#pragma unroll
-                for (int off = 1; off < 8; off <<= 1) {
-                    sm += __shfl_xor_sync(0xffffffffu, sm, off);
-                    smd += __shfl_xor_sync(0xffffffffu, smd, off);
-                }
-                if ((lane & 7) == 0) *reinterpret_cast<float2 *>(S.xsum + ((ch >> 3) * kNFast + t) * 2) = make_float2(sm, smd);
+                if (am >= 32768.0f || (am > 0.0f && am < 0.0009765625f)) S.misc[7] = 1;
+                stage_chunk(t, ch, xv, 1.0f);
                 if (nE > 0) {
                     d0 = warp_sum(d0);
                     d1 = warp_sum(d1);
@@ -517,6 +544,36 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
             if ((ch & 7) == 0) *reinterpret_cast<float2 *>(S.xsum + ((ch >> 3) * kNFast + t) * 2) = make_float2(0.f, 0.f);
         }
         __syncthreads();
+        if (S.misc[7]) {
+            // per-token scales: warp t finds max |x_t|
+            if (warp < n) {
+                float am = 0.f;
+#pragma unroll 1
+                for (int ch = lane; ch < chunks; ch += 32) {
+                    float xv[8];
+                    load8f(A.x, (size_t)warp * D + (size_t)ch * 8, A.s.x_dtype, xv);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) am = fmaxf(am, fabsf(xv[j]));
+                }
+#pragma unroll
+                for (int o = 16; o; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+                if (lane == 0) {
+                    const int e = (am > 0.0f && am <= 3.0e38f) ? min(max(ilogbf(am) - 14, -100), 100) : 0;
+                    xscale[warp] = ldexpf(1.0f, e);
+                }
+            }
+            __syncthreads();
+            if (tid < TG * chunks) {
+                const int tg = tid / chunks, ch = tid - tg * chunks;
+#pragma unroll 1
+                for (int t = tg; t < n; t += TG) {
+                    float xv[8];
+                    load8f(A.x, (size_t)t * D + (size_t)ch * 8, A.s.x_dtype, xv);
+                    stage_chunk(t, ch, xv, 1.0f / xscale[t]);
+                }
+            }
+            __syncthreads();
+        }
         if (tid < nE * n) {
             const int ei = tid / n, t = tid - ei * n;
             float l = 0.f;
@@ -756,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
             // Reducer of partial buffer b = warp - kReducer0, i.e. of tiles b, b + 2, ...
             // Lane l sums fragment lane l's four (row, token) values of the 16
             // consumer warps in warp order, frees the buffer, then writes
-            // h = w * silu(g) * u as bf16 for the valid (row, token) pairs.
+            // h = w * act(g, u) as f16 for the valid (row, token) pairs.
             const int b = warp - kReducer0;
             for (int t = b, r = 0; t < nTiles; t += 2, ++r) {
                 if (!__shfl_sync(0xffffffffu, (int)wait_phase_inl(&S.pfull[b], (uint32_t)(r & 1), abort_flag, W.status), 0))
@@ -775,16 +832,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
                 if (lane == 0) ptx::mbar_arrive(&S.pempty[b], 1);
                 const int4 tl = S.tiles[2 * t], tr = S.tiles[2 * t + 1];
                 const unsigned m = (unsigned)tr.y;
+                bool over = false;
                 const float gv[4] = {gs.x, gs.y, gs.z, gs.w}, uv[4] = {us.x, us.y, us.z, us.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int row = 2 * (lane >> 2) + (i >> 1), tok = 2 * (lane & 3) + (i & 1);
                     if (row >= tl.z && row < tl.w && ((m >> tok) & 1u)) {
                         const int pslot = tr.z + __popc(m & ((1u << tok) - 1u));
+                        const float xsc = reinterpret_cast<const float *>(S.misc + 40)[tok];
                         Hg[(size_t)pslot * F + h_pos(tl.y + row)] =
-                            f2bf(S.slot_w[pslot] * glu_act<false>(A.s.act, A.s.act_limit, gv[i], uv[i]));
+                            f2h_sat(S.slot_w[pslot] * glu_act<false>(A.s.act, A.s.act_limit, gv[i] * xsc, uv[i] * xsc), over);
                     }
                 }
+                if (over) report_error(W.status, kDevErrRange);
             }
             // every h row of this CTA written: the consumers pass grid barrier 2 after this
             ptx::named_bar(2, kConsThreads + 64);
@@ -941,6 +1001,39 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     stamp(W.phase_ns, timing, 4);
     ptx::named_bar(2, kConsThreads + 64);  // the reducers have written every h row of this CTA
     grid_barrier(gsync, epoch + 2ull * G, bar_ok, abort_flag, W.status, true);
+    // The step's h rows (every slot: this CTA's D rows need every expert) fit
+    // in the areas x, xsum and the partials held during gate/up: one round of
+    // bulk copies from L2 now, and the down loop reads h from shared memory.
+    // Otherwise each down stage loads its h fragments from L2 one stage ahead.
+    const int nslots = S.s_off[E];
+    const bool hsm = nslots * L.h_stride <= L.h_cap;
+    if (hsm && warp == 0) {
+        const bool issue = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
+        if (issue) {
+            // h was written by other CTAs' generic stores, acquired through the
+            // barrier; order those writes before this warp's async-proxy reads
+            ptx::fence_proxy_async_global();
+            if (lane == 0) ptx::mbar_arrive_expect_tx(S.hbar, (uint32_t)(nslots * F * 2));
+            __syncwarp();
+#pragma unroll 1
+            for (int p = lane; p < nslots; p += 32)
+                ptx::bulk_g2s(S.hs + (size_t)p * L.h_stride, Hg + (size_t)p * F, (uint32_t)(F * 2), S.hbar, pol);
+            // the copies must land before this CTA may exit: wait for them even
+            // after an abort (bounded)
+            if (lane == 0) {
+                const unsigned long long t0 = globaltimer();
+                while (!ptx::mbar_try_wait(S.hbar, 0)) {
+                    if (globaltimer() - t0 > kWaitNs) {
+                        set_timeout(abort_flag, W.status);
+                        break;
+                    }
+                }
+            }
+            __syncwarp();
+        }
+    } else if (hsm && !*abort_flag) {
+        __shfl_sync(0xffffffffu, (int)wait_phase(S.hbar, 0, abort_flag, W.status), 0);
+    }
     stamp(W.phase_ns, timing, 5);
 
     // ---- phase B: down, all experts summed per warp ----------------------------
@@ -966,12 +1059,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
             const unsigned m = (unsigned)ur.y;
             if ((m >> g) & 1u) {
                 const int ps = ur.z + __popc(m & ((1u << g) - 1u));
-                const unsigned char *hp = reinterpret_cast<const unsigned char *>(Hg + (size_t)ps * F) +
-                                          (size_t)itg[q] * 256 + c * 32;
-                hv[0] = ptx::ld_cg_v4(hp);
-                hv[1] = ptx::ld_cg_v4(hp + 16);
-                hv[2] = ptx::ld_cg_v4(hp + 128);
-                hv[3] = ptx::ld_cg_v4(hp + 144);
+                if (hsm) {
+                    const unsigned char *hp = S.hs + (size_t)ps * L.h_stride + (size_t)itg[q] * 256 + c * 32;
+                    hv[0] = *reinterpret_cast<const uint4 *>(hp);
+                    hv[1] = *reinterpret_cast<const uint4 *>(hp + 16);
+                    hv[2] = *reinterpret_cast<const uint4 *>(hp + 128);
+                    hv[3] = *reinterpret_cast<const uint4 *>(hp + 144);
+                } else {
+                    const unsigned char *hp = reinterpret_cast<const unsigned char *>(Hg + (size_t)ps * F) +
+                                              (size_t)itg[q] * 256 + c * 32;
+                    hv[0] = ptx::ld_cg_v4(hp);
+                    hv[1] = ptx::ld_cg_v4(hp + 16);
+                    hv[2] = ptx::ld_cg_v4(hp + 128);
+                    hv[3] = ptx::ld_cg_v4(hp + 144);
+                }
             }
         }
     };
@@ -1027,7 +1128,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
                     const uint2 wa1 = *reinterpret_cast<const uint2 *>(ubase + o[1]);
                     uint2 wb0 = *reinterpret_cast<const uint2 *>(ubase + o[2]);
                     uint2 wb1 = *reinterpret_cast<const uint2 *>(ubase + o[3]);
-                    if (g == 7) wb0 = wb1 = make_uint2(0u, 0u);  // tile row 15: zero codes -> 128 * sum(h)
+                    if (g == 7) wb0 = wb1 = make_uint2(0u, 0u);  // tile row 15: zero codes -> 1024 * sum(h)
                     float ca[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
                     mma_word(ca, wa0.x, wb0.x, hq[q][0]);
                     mma_word(cb, wa1.x, wb1.x, hq[q][2]);
@@ -1048,8 +1149,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
                         const float *cd = hh ? cb : ca;
                         const float hs0 = hh ? hb0 : ha0, hs1 = hh ? hb1 : ha1;
                         const float s0 = bf_half(s0w, hh), s1 = bf_half(s1w, hh);
-                        const float o0 = fmaf(-128.f, s0, bf_half(b0w, hh)) * 0.0078125f;
-                        const float o1 = fmaf(-128.f, s1, bf_half(b1w, hh)) * 0.0078125f;
+                        const float o0 = fmaf(-1024.f, s0, bf_half(b0w, hh)) * 0.0009765625f;
+                        const float o1 = fmaf(-1024.f, s1, bf_half(b1w, hh)) * 0.0009765625f;
                         if (hh == 0) {
                             v[0] = fmaf(s0, cd[0], o0 * hs0);
                             v[1] = fmaf(s0, cd[1], o0 * hs1);
@@ -1092,6 +1193,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     }
 
     // ---- final: fixed-order sum over warps of their partial outputs -------------
+    // (the partials go where h was staged: every consumer is done reading it)
+    if (hsm) cta_sync(true);
     {
         float *red = S.red + ((size_t)warp * 32 + lane) * 8;
         *reinterpret_cast<float4 *>(red) = make_float4(acc0[0], acc0[1], acc0[2], acc0[3]);
@@ -1199,6 +1302,7 @@ bool fused_layout(const moe_config &c, int num_sms, int max_smem, DecodeLayout *
     if (tiles > kMaxTilesF) return false;
     L.max_tiles = kMaxTilesF;
     L.x_stride = 2 * D + 16;
+    L.h_stride = 2 * F + 16;
     int off = 0;
     L.off_bar = off;
     off += 256;
@@ -1216,6 +1320,7 @@ bool fused_layout(const moe_config &c, int num_sms, int max_smem, DecodeLayout *
     off += 2 * kCW * kPartStride * 4;
     off = round_up(off, 1024);
     L.off_ring = off;
+    L.h_cap = L.off_ring - L.off_x;
     const int tail = 2048 + 1024;  // over-read pad of the last stage + base alignment slack
     const int room = max_smem - off - tail;
     int ns = room / L.stage_bytes;

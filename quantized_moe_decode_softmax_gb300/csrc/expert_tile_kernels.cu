@@ -4,7 +4,9 @@
 // Where an expert serves many tokens the step is a real (small) matrix product,
 // so these kernels dequantise each weight tile once into shared memory as f16
 // (w = s*q + b in f32, rounded once; f16 keeps three more mantissa bits than
-// bf16 and the weights and activations of this path are far inside its range)
+// bf16). A weight or activation beyond f16's range saturates at +-65504 and is
+// reported (MOE_ERR_RANGE on the plan's next call); the f32 check path
+// (MOE_FLAG_F32_DEBUG) has no such limit.
 // and multiply it on the tensor cores against all of the expert's tokens at
 // once: weights on M, tokens on N in n8 tiles (up to 64 tokens), f32
 // accumulation. The GEMV kernels of the same launch sequence
@@ -25,6 +27,7 @@
 #include <cuda_fp16.h>
 
 #include "activation.cuh"
+#include "device_status.cuh"
 #include "moe_internal.h"
 #include "ptx.cuh"
 #include "routing.cuh"
@@ -44,13 +47,21 @@ static_assert(kTR * 65 * 4 <= kSmem, "the gate/up epilogue reuses the tile's sha
 
 __device__ __forceinline__ float bf16f(uint16_t h) { return __uint_as_float(((uint32_t)h) << 16); }
 
-__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+// two values as f16x2; a magnitude beyond the largest f16 saturates to
+// +-65504 and is reported (MOE_ERR_RANGE on the plan's next call)
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi, unsigned *status) {
+    if (fabsf(lo) > 65504.0f || fabsf(hi) > 65504.0f) {
+        report_error(status, kDevErrRange);
+        lo = fminf(fmaxf(lo, -65504.0f), 65504.0f);
+        hi = fminf(fmaxf(hi, -65504.0f), 65504.0f);
+    }
     const __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
 // one group of one row (8 packed words, 64 inputs) dequantised to f16 at dst
-__device__ __forceinline__ void dequant_group(const uint32_t *q, float s, float b, unsigned char *dst) {
+__device__ __forceinline__ void dequant_group(const uint32_t *q, float s, float b, unsigned char *dst,
+                                              unsigned *status) {
     const uint4 w0 = __ldg(reinterpret_cast<const uint4 *>(q));
     const uint4 w1 = __ldg(reinterpret_cast<const uint4 *>(q) + 1);
     const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
@@ -61,7 +72,7 @@ __device__ __forceinline__ void dequant_group(const uint32_t *q, float s, float 
         for (int j = 0; j < 4; ++j) {
             const float lo = fmaf(s, (float)((w[i] >> (8 * j)) & 0xFu), b);
             const float hi = fmaf(s, (float)((w[i] >> (8 * j + 4)) & 0xFu), b);
-            o[j] = pack_f16(lo, hi);
+            o[j] = pack_f16(lo, hi, status);
         }
         *reinterpret_cast<uint4 *>(dst + i * 16) = make_uint4(o[0], o[1], o[2], o[3]);
     }
@@ -69,7 +80,8 @@ __device__ __forceinline__ void dequant_group(const uint32_t *q, float s, float 
 
 // one group of one 6-bit row (48 bytes, a little-endian bit stream of 64
 // codes) dequantised to f16 at dst
-__device__ __forceinline__ void dequant_group6(const unsigned char *q, float s, float b, unsigned char *dst) {
+__device__ __forceinline__ void dequant_group6(const unsigned char *q, float s, float b, unsigned char *dst,
+                                               unsigned *status) {
     const uint4 c0 = __ldg(reinterpret_cast<const uint4 *>(q));
     const uint4 c1 = __ldg(reinterpret_cast<const uint4 *>(q) + 1);
     const uint4 c2 = __ldg(reinterpret_cast<const uint4 *>(q) + 2);
@@ -86,14 +98,14 @@ __device__ __forceinline__ void dequant_group6(const unsigned char *q, float s, 
                 const uint32_t code = __funnelshift_r(v[wi], wi + 1 < 12 ? v[wi + 1] : 0u, sh) & 0x3Fu;
                 w2[h] = fmaf(s, (float)code, b);
             }
-            o[j] = pack_f16(w2[0], w2[1]);
+            o[j] = pack_f16(w2[0], w2[1], status);
         }
         *reinterpret_cast<uint4 *>(dst + i * 16) = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }
 
 // 8 consecutive activations as f16 (x may be f32 or bf16; h is f32)
-__device__ __forceinline__ uint4 load8_f16(const void *p, size_t i, int dtype) {
+__device__ __forceinline__ uint4 load8_f16(const void *p, size_t i, int dtype, unsigned *status) {
     float v[8];
     if (dtype == MOE_DTYPE_BF16) {
         const uint4 a = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p) + i));
@@ -109,7 +121,8 @@ __device__ __forceinline__ uint4 load8_f16(const void *p, size_t i, int dtype) {
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
         v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
     }
-    return make_uint4(pack_f16(v[0], v[1]), pack_f16(v[2], v[3]), pack_f16(v[4], v[5]), pack_f16(v[6], v[7]));
+    return make_uint4(pack_f16(v[0], v[1], status), pack_f16(v[2], v[3], status), pack_f16(v[4], v[5], status),
+                      pack_f16(v[6], v[7], status));
 }
 
 // The shared K-chunk loop of both kernels: rows [16 w, 16 w + 16) of the
@@ -169,11 +182,11 @@ __global__ void __launch_bounds__(kTT) gateup_tile_kernel(StepArgs a, Workspace 
         const size_t gi = row * (D / kGroup) + k / kGroup;
         const float s = bf16f((up ? a.planes.up_s : a.planes.gate_s)[gi]);
         const float b = bf16f((up ? a.planes.up_b : a.planes.gate_b)[gi]);
-        dequant_group(q, s, b, dst);
+        dequant_group(q, s, b, dst, ws.status);
     };
     auto load_x = [&](int j, int k) -> uint4 {
         if (j >= cnt) return make_uint4(0, 0, 0, 0);
-        return load8_f16(a.x, (size_t)ws.slot_token[off + j] * D + k, a.s.x_dtype);
+        return load8_f16(a.x, (size_t)ws.slot_token[off + j] * D + k, a.s.x_dtype, ws.status);
     };
     tile_product(As, Xs, D, NT, load_w, load_x, acc);
     // accumulators -> shared [kTR rows][65] f32, then h = silu(gate) * up per (slot, f)
@@ -216,14 +229,14 @@ __global__ void __launch_bounds__(kTT) down_tile_kernel(StepArgs a, Workspace ws
         const size_t gi = row * (F / kGroup) + k / kGroup;
         if (a.s.down_bits == 6)
             dequant_group6(reinterpret_cast<const unsigned char *>(a.planes.down_q) + row * (3 * F / 4) + k / 64 * 48,
-                           bf16f(a.planes.down_s[gi]), bf16f(a.planes.down_b[gi]), dst);
+                           bf16f(a.planes.down_s[gi]), bf16f(a.planes.down_b[gi]), dst, ws.status);
         else
             dequant_group(a.planes.down_q + row * (F / 8) + k / 8, bf16f(a.planes.down_s[gi]),
-                          bf16f(a.planes.down_b[gi]), dst);
+                          bf16f(a.planes.down_b[gi]), dst, ws.status);
     };
     auto load_x = [&](int j, int k) -> uint4 {
         if (j >= cnt) return make_uint4(0, 0, 0, 0);
-        return load8_f16(ws.h, (size_t)(off + j) * F + k, MOE_DTYPE_F32);
+        return load8_f16(ws.h, (size_t)(off + j) * F + k, MOE_DTYPE_F32, ws.status);
     };
     tile_product(As, Xs, F, NT, load_w, load_x, acc);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;

@@ -129,6 +129,7 @@ const char *moe_status_str(moe_status s) {
         case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
         case MOE_ERR_OOM: return "MOE_ERR_OOM";
         case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+        case MOE_ERR_RANGE: return "MOE_ERR_RANGE";
     }
     return "MOE_ERR_UNKNOWN";
 }
@@ -237,15 +238,16 @@ moe_status moe_decode_forward(moe_plan *plan, const void *x, const void *router_
     cudaStream_t s = (cudaStream_t)stream;
     // an error a finished earlier step recorded on the device: report it, clear
     // the plan's error state on this stream, and run nothing
-    if (plan->host_err && (plan->host_err[0] || plan->host_err[1])) {
-        const bool timeout = plan->host_err[0] != 0u;
-        plan->host_err[0] = plan->host_err[1] = 0u;
+    if (plan->host_err && (plan->host_err[0] || plan->host_err[1] || plan->host_err[2])) {
+        const moe_status err = plan->host_err[0] ? MOE_ERR_TIMEOUT
+                             : plan->host_err[2] ? MOE_ERR_RANGE : MOE_ERR_CUDA;
+        plan->host_err[0] = plan->host_err[1] = plan->host_err[2] = 0u;
         if (cudaMemsetAsync(plan->ws.status, 0, sizeof(unsigned), s) != cudaSuccess ||
             cudaMemsetAsync(plan->ws.sync, 0, 64 * sizeof(unsigned), s) != cudaSuccess) {
             cudaGetLastError();
             return MOE_ERR_CUDA;
         }
-        return timeout ? MOE_ERR_TIMEOUT : MOE_ERR_CUDA;
+        return err;
     }
     StepArgs a{};
     // the test hook stalls only the plan's first step
@@ -365,14 +367,15 @@ moe_status moe_plan_check(moe_plan *plan) {
         cudaGetLastError();
         return MOE_ERR_CUDA;
     }
-    if (plan->host_err) plan->host_err[0] = plan->host_err[1] = 0u;
+    if (plan->host_err) plan->host_err[0] = plan->host_err[1] = plan->host_err[2] = 0u;
     if (status) {
         // clear the error bits (words 2..3 keep the host word's address) and the
         // grid-barrier counters
         cudaMemset(plan->ws.status, 0, sizeof(unsigned));
         cudaMemset(plan->ws.sync, 0, 64 * sizeof(unsigned));
         cudaDeviceSynchronize();
-        return (status & kDevErrTimeout) ? MOE_ERR_TIMEOUT : MOE_ERR_CUDA;
+        return (status & kDevErrTimeout) ? MOE_ERR_TIMEOUT
+             : (status & kDevErrRange) ? MOE_ERR_RANGE : MOE_ERR_CUDA;
     }
     return MOE_OK;
 }

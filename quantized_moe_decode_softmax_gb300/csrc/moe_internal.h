@@ -25,6 +25,7 @@ constexpr int kChunkMaxTokens = 16;
 enum : unsigned {
     kDevErrTimeout = 1u << 0,   // a bounded spin-wait gave up
     kDevErrInternal = 1u << 1,  // an impossible index was seen and skipped
+    kDevErrRange = 1u << 2,     // an f16 operand saturated (|h| > 65504)
 };
 
 // Device workspace of one plan (one cudaMalloc, carved in this order).
@@ -110,6 +111,9 @@ struct DecodeLayout {
     // shared memory carve (byte offsets from the 1024-aligned base)
     int off_bar, off_misc, off_route, off_tiles, off_x, off_xsum, off_red, off_ring;
     int x_stride;     // bytes per staged token row of x
+    int h_cap;        // bytes from off_x to off_ring: after gate/up these hold the
+                      // step's h rows when they fit (h_stride per slot)
+    int h_stride;     // bytes per staged h row: 2 * Dff + 16
     int smem_bytes;   // dynamic shared memory requested (includes alignment slack)
 };
 
