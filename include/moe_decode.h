@@ -232,6 +232,31 @@ moe_status moe_decode_forward(moe_plan *plan, const void *x, const void *router_
                               const float *router_bias, const moe_expert_planes *planes,
                               int n_tokens, int top_k, void *out, void *stream);
 
+/* One layer's arguments of moe_decode_forward_layers (device pointers, as for
+ * moe_decode_forward). */
+typedef struct {
+    const void *x;              /* [n_tokens, D] of cfg.x_dtype */
+    const void *router_w;       /* [E, D] of cfg.router_dtype */
+    const float *router_bias;   /* [E] f32 or NULL */
+    moe_expert_planes planes;   /* this layer's expert planes */
+    void *out;                  /* [n_tokens, D] of cfg.out_dtype; must not alias
+                                   this layer's x (it may be the next layer's x) */
+} moe_layer_io;
+
+/* Decode steps of n_layers consecutive MoE layers of the plan's shape, in
+ * order, on one stream: layer l is exactly moe_decode_forward on layers[l].
+ * Source: #1616 Current Behavior (the routed decode block runs on all 48
+ * layers every tick). On the single-launch path the launches form a chain with
+ * programmatic dependent launch, and layer l's launch prefetches layer l+1's
+ * router rows (and bias) into L2 while it streams its own experts, so the next
+ * router GEMV reads L2 instead of HBM. A layer's x may be the previous layer's
+ * out (a residual-free stack). Every layer's arguments are checked on the host
+ * before the first launch (INVALID_ARG: nothing launched; n_layers must be at
+ * least 1). Errors and ordering as for moe_decode_forward; moe_get_routing
+ * then reports the last layer. */
+moe_status moe_decode_forward_layers(moe_plan *plan, const moe_layer_io *layers, int n_layers,
+                                     int n_tokens, int top_k, void *stream);
+
 /* The same step with x and out in HOST memory (#1616 Current Behavior: the
  * decode tick of a serving loop hands activations in and out): copies x to the plan's device
  * staging buffer, runs moe_decode_forward, copies out back and synchronises

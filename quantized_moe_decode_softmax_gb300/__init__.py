@@ -37,10 +37,12 @@ from ._abi import (  # noqa: F401
     moe_config,
     moe_decode_forward,
     moe_decode_forward_host,
+    moe_decode_forward_layers,
     moe_decode_forward_noalloc,
     moe_expert_planes,
     moe_get_phase_times,
     moe_get_routing,
+    moe_layer_io,
     moe_plan_check,
     moe_plan_create,
     moe_plan_free,

@@ -30,6 +30,7 @@ EXPORTED = (
     "moe_abi_version", "moe_status_str", "moe_plan_workspace_bytes", "moe_plan_create",
     "moe_decode_forward", "moe_decode_forward_host", "moe_plan_check", "moe_get_routing",
     "moe_get_phase_times", "moe_plan_launch_count", "moe_plan_free", "moe_decode_forward_noalloc",
+    "moe_decode_forward_layers",
 )
 
 
@@ -57,6 +58,11 @@ class moe_expert_planes(ctypes.Structure):
     _fields_ = [(f, ctypes.c_void_p) for f in PLANE_FIELDS]
 
 
+class moe_layer_io(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("router_w", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
+                ("planes", moe_expert_planes), ("out", ctypes.c_void_p)]
+
+
 _lib = None
 
 
@@ -82,9 +88,10 @@ def lib():
         L.moe_plan_launch_count.argtypes = [vp, P(ctypes.c_uint64)]
         L.moe_get_phase_times.argtypes = [vp, vp, i32, P(i32)]
         L.moe_plan_free.argtypes = [vp]
+        L.moe_decode_forward_layers.argtypes = [vp, P(moe_layer_io), i32, i32, i32, vp]
         for name in ("moe_plan_workspace_bytes", "moe_plan_create", "moe_decode_forward",
                      "moe_decode_forward_host", "moe_plan_check", "moe_get_routing", "moe_plan_launch_count",
-                     "moe_get_phase_times", "moe_plan_free"):
+                     "moe_get_phase_times", "moe_plan_free", "moe_decode_forward_layers"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -163,6 +170,16 @@ def moe_decode_forward(plan: int, x, router_w, router_bias, planes, n_tokens: in
                                   ctypes.byref(pl), int(n_tokens), int(top_k), _ptr(out),
                                   _stream(stream))
     _check(st, "moe_decode_forward")
+
+
+def moe_decode_forward_layers(plan: int, layers, n_tokens: int, top_k: int, stream=None) -> None:
+    """layers: sequence of (x, router_w, router_bias, planes, out)."""
+    arr = (moe_layer_io * len(layers))()
+    for i, (x, rw, rb, planes, out) in enumerate(layers):
+        pl = planes if isinstance(planes, moe_expert_planes) else make_planes(planes)
+        arr[i] = moe_layer_io(_ptr(x), _ptr(rw), _ptr(rb), pl, _ptr(out))
+    st = lib().moe_decode_forward_layers(plan, arr, len(layers), int(n_tokens), int(top_k), _stream(stream))
+    _check(st, "moe_decode_forward_layers")
 
 
 def moe_decode_forward_host(plan: int, x_host, router_w, router_bias, planes, n_tokens: int,

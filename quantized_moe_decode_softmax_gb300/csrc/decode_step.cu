@@ -779,6 +779,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
         // next two reduce the consumers' gate/up partials
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsProducer));
         if (warp >= kReducer0 + 2) {
+            if (warp == kReducer0 + 2 && lane == 0 && A.next_router_w) {
+                // the next layer of a chain routes right after this step: bring
+                // the router rows its CTA c will read (experts c and c + G) and
+                // the bias into L2 while this step streams its experts
+                const size_t rb = (size_t)D * (A.s.w_dtype == MOE_DTYPE_F32 ? 4 : 2);
+                const unsigned char *nr = static_cast<const unsigned char *>(A.next_router_w);
+                if (cta < E) ptx::prefetch_l2_bulk(nr + (size_t)cta * rb, (uint32_t)rb);
+                if (cta + (int)G < E) ptx::prefetch_l2_bulk(nr + (size_t)(cta + (int)G) * rb, (uint32_t)rb);
+                if (cta == 0 && A.next_router_bias && ((uintptr_t)A.next_router_bias & 15u) == 0 && (E & 3) == 0)
+                    ptx::prefetch_l2_bulk(A.next_router_bias, (uint32_t)(E * 4));
+            }
             if (warp == kReducer0 + 2 && cta == 0) {
                 // the routing tables the host may read back (CTA 0's copy)
 #pragma unroll 1

@@ -222,18 +222,28 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan **out) {
     return MOE_OK;
 }
 
-moe_status moe_decode_forward(moe_plan *plan, const void *x, const void *router_w,
-                              const float *router_bias, const moe_expert_planes *planes,
-                              int n_tokens, int top_k, void *out, void *stream) {
+}  // extern "C"
+
+namespace {
+
+moe_status check_step_args(const moe_plan *plan, const void *x, const void *router_w,
+                           const float *router_bias, const moe_expert_planes *planes, int n_tokens,
+                           int top_k, const void *out) {
     if (!plan || !x || !router_w || !out) return MOE_ERR_INVALID_ARG;
     if (n_tokens < 1 || n_tokens > plan->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
     if (top_k != plan->cfg.top_k) return MOE_ERR_INVALID_ARG;
     if (x == out) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(router_w) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
     if (router_bias && ((uintptr_t)router_bias & 3u)) return MOE_ERR_INVALID_ARG;
-    moe_status st = check_planes(planes);
-    if (st != MOE_OK) return st;
+    return check_planes(planes);
+}
 
+// one step, arguments already checked; next_router_w / next_router_bias: the
+// next layer's router for the single launch to prefetch (or null)
+moe_status forward_checked(moe_plan *plan, const void *x, const void *router_w,
+                           const float *router_bias, const moe_expert_planes *planes, int n_tokens,
+                           void *out, void *stream, const void *next_router_w,
+                           const float *next_router_bias) {
     DeviceGuard guard(plan->device);
     cudaStream_t s = (cudaStream_t)stream;
     // an error a finished earlier step recorded on the device: report it, clear
@@ -258,6 +268,8 @@ moe_status moe_decode_forward(moe_plan *plan, const void *x, const void *router_
     a.router_bias = router_bias;
     a.planes = *planes;
     a.out = out;
+    a.next_router_w = next_router_w;
+    a.next_router_bias = next_router_bias;
 
     // n <= 8: one single-launch step; 9..kChunkMaxTokens: chunks of at most 8
     // tokens through it (unless the plan asks for the grouped path); else the
@@ -327,6 +339,38 @@ moe_status moe_decode_forward(moe_plan *plan, const void *x, const void *router_
         fprintf(stderr, "[moe] forward launch failed (%s path): %s\n", path, cudaGetErrorString(err));
         cudaGetLastError();
         return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_decode_forward(moe_plan *plan, const void *x, const void *router_w,
+                              const float *router_bias, const moe_expert_planes *planes,
+                              int n_tokens, int top_k, void *out, void *stream) {
+    moe_status st = check_step_args(plan, x, router_w, router_bias, planes, n_tokens, top_k, out);
+    if (st != MOE_OK) return st;
+    return forward_checked(plan, x, router_w, router_bias, planes, n_tokens, out, stream, nullptr, nullptr);
+}
+
+moe_status moe_decode_forward_layers(moe_plan *plan, const moe_layer_io *layers, int n_layers,
+                                     int n_tokens, int top_k, void *stream) {
+    if (!plan || !layers || n_layers < 1) return MOE_ERR_INVALID_ARG;
+    for (int l = 0; l < n_layers; ++l) {
+        const moe_layer_io &io = layers[l];
+        moe_status st = check_step_args(plan, io.x, io.router_w, io.router_bias, &io.planes, n_tokens,
+                                        top_k, io.out);
+        if (st != MOE_OK) return st;
+    }
+    for (int l = 0; l < n_layers; ++l) {
+        const moe_layer_io &io = layers[l];
+        const moe_layer_io *next = l + 1 < n_layers ? &layers[l + 1] : nullptr;
+        moe_status st = forward_checked(plan, io.x, io.router_w, io.router_bias, &io.planes, n_tokens,
+                                        io.out, stream, next ? next->router_w : nullptr,
+                                        next ? next->router_bias : nullptr);
+        if (st != MOE_OK) return st;
     }
     return MOE_OK;
 }

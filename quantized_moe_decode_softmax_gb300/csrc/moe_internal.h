@@ -79,6 +79,10 @@ struct StepArgs {
     const float *router_bias;
     moe_expert_planes planes;
     void *out;
+    // the next layer's router (rows and bias) to prefetch into L2 during this
+    // step, or null (moe_decode_forward_layers)
+    const void *next_router_w;
+    const float *next_router_bias;
 };
 
 // Shared-memory and work layout of the single-launch decode step (host-computed).

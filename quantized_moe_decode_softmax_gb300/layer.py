@@ -88,6 +88,14 @@ class MoeDecodeLayer:
                                 self.cfg.top_k, out, stream)
         return out
 
+    def forward_layers(self, steps, stream=None):
+        """steps: sequence of (x, DeviceLayer, out), run in order as one chain
+        (moe_decode_forward_layers); returns the outs."""
+        _abi.moe_decode_forward_layers(
+            self.plan, [(x, w.router_w, w.router_bias, w.c_planes, out) for x, w, out in steps],
+            steps[0][0].shape[0], self.cfg.top_k, stream)
+        return [out for _, _, out in steps]
+
     def forward_host(self, x_host, w: DeviceLayer, out_host, stream=None):
         n = x_host.shape[0]
         _abi.moe_decode_forward_host(self.plan, x_host, w.router_w, w.router_bias, w.c_planes, n,

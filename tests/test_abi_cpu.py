@@ -87,6 +87,7 @@ def test_null_arguments_rejected_before_any_cuda_call(libpath):
     assert L.moe_plan_check(None) == q.MOE_ERR_INVALID_ARG
     assert L.moe_get_routing(None, *([None] * 8)) == q.MOE_ERR_INVALID_ARG
     assert L.moe_plan_free(None) == q.MOE_OK
+    assert L.moe_decode_forward_layers(None, None, 1, 1, 8, None) == q.MOE_ERR_INVALID_ARG
     cfg = q.make_config(**GOOD)
     assert L.moe_plan_workspace_bytes(ctypes.byref(cfg), None) == q.MOE_ERR_INVALID_ARG
 

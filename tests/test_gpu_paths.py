@@ -114,3 +114,51 @@ def test_phase_times_are_ordered():
     assert t.shape[0] >= 1 and t.shape[1] == 16
     assert np.all(np.diff(t[:, :8], axis=1) >= 0)
     assert np.all(t[:, 0] > 0)
+
+
+@pytest.mark.parametrize("n", [1, 4, 24])
+def test_layer_chain_matches_the_oracle_per_layer(n):
+    """moe_decode_forward_layers over three layers with their own weights and
+    cohorts: each layer's output matches the oracle (single launch for n <= 8,
+    the grouped path for 24), and the chain launches what the three separate
+    calls would."""
+    import torch
+    import moe_synth as ms
+    shape = ms.SHAPES["qwen3"]
+    steps, refs = [], []
+    for l in range(3):
+        router_w, bias = ms.draw_router(shape, 70 + l, 0)
+        x = ms.draw_tokens(shape, router_w, bias, 70 + l, 0, n)
+        lay = ms.make_layer(shape, 70 + l, 0, ms.routed_experts(x, router_w, bias, shape.top_k))
+        refs.append(run_oracle(lay, x))
+        out = torch.empty((n, shape.D), dtype=torch.bfloat16, device="cuda")
+        steps.append((x_tensor(shape, x), device_layer(lay), out))
+    plan = make_plan(shape)
+    c0 = q.moe_plan_launch_count(plan.plan)
+    plan.forward_layers(steps)
+    torch.cuda.synchronize()
+    plan.check()
+    chain_launches = q.moe_plan_launch_count(plan.plan) - c0
+    for (_, _, out), ref in zip(steps, refs):
+        assert_out_close(out.float().cpu().numpy(), ref["out"], TOL_BF16)
+    assert_routing_equal(plan.routing(n), refs[-1])
+    c1 = q.moe_plan_launch_count(plan.plan)
+    for x, dl, out in steps:
+        plan.forward(x, dl, out)
+    torch.cuda.synchronize()
+    assert q.moe_plan_launch_count(plan.plan) - c1 == chain_launches
+
+
+def test_layer_chain_checks_every_layer_before_launching():
+    import torch
+    lay, x = case("qwen3", 2, 2)
+    shape = lay.shape
+    dl = device_layer(lay)
+    plan = make_plan(shape)
+    xt = x_tensor(shape, x)
+    out = torch.empty((2, shape.D), dtype=torch.bfloat16, device="cuda")
+    c0 = q.moe_plan_launch_count(plan.plan)
+    with pytest.raises(q.MoeError) as ei:  # the third layer's out aliases its x
+        plan.forward_layers([(xt, dl, out), (xt, dl, out.clone()), (xt, dl, xt)])
+    assert ei.value.status == q.MOE_ERR_INVALID_ARG
+    assert q.moe_plan_launch_count(plan.plan) == c0
