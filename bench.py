@@ -64,6 +64,9 @@ def parse_args():
                          "per layer) and print one line per --sweep cohort size")
     ap.add_argument("--sweep", default="1,2,4,8,16,32,64",
                     help="cohort sizes of the --stack run")
+    ap.add_argument("--no-chain", action="store_true",
+                    help="--stack: one moe_decode_forward call per layer instead of one "
+                         "moe_decode_forward_layers chain per step")
     ap.add_argument("--phases", action="store_true",
                     help="also time the fused kernel's phases (router / gate-up / down)")
     ap.add_argument("--sustain-seconds", type=float, default=1.5,
@@ -576,8 +579,12 @@ def run_stack(args, world, rank, local, pg):
         K, W = max(1, min(args.steps, 20)), max(3, min(args.warmup, 5))
 
         def step(i):
-            for l in range(L):
-                layer.forward(xs[l][i % P], layers[l], outs[l % 2], stream=stream)
+            if args.no_chain:
+                for l in range(L):
+                    layer.forward(xs[l][i % P], layers[l], outs[l % 2], stream=stream)
+            else:
+                layer.forward_layers([(xs[l][i % P], layers[l], outs[l % 2]) for l in range(L)],
+                                     stream=stream)
 
         c0 = q.moe_plan_launch_count(layer.plan)
         with torch.cuda.stream(stream):
@@ -629,6 +636,8 @@ def run_stack(args, world, rank, local, pg):
                 "config": {"workload": f"{L}-layer stack of {shape.E}-expert top-{shape.top_k} "
                                        f"D={shape.D} Dff={shape.F} MoE layers, n_tokens={n}",
                            "layers": L, "n_tokens": n, "cohorts": args.kind,
+                           "calls": "one forward call per layer" if args.no_chain
+                           else "one moe_decode_forward_layers chain per step",
                            "expert_plane_bytes": L * shape.E * shape.plane_bytes,
                            "l2": "every layer's planes are read once per step (stack >> L2)",
                            "parallelism": f"replicas x{world}"},
