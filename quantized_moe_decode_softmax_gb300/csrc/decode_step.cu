@@ -184,12 +184,12 @@ __device__ __forceinline__ int h_pos(int f) {
 struct Smem {
     uint64_t *full, *empty;  // ring slots: data landed / consumed by every consumer warp
     uint64_t *pfull, *pempty;  // gate/up partial buffers: all partials written / reduced
-    uint64_t *hbar;          // the step's h rows landed in shared memory (down phase)
     int *misc;             // [0] abort [1] barrier ok [2] U [3] tiles [4] b0 [5] b1
                            // [6] stages issued [7] x needs per-token scaling
                            // [8..9] partials written [10..11] shares reduced
                            // [16..23] stage release counts [24..39] grouping scans
                            // [40..47] per-token scale of x as f32 (2^e, 1 unless scaled)
+                           // [48..55] per-token scale of h as f32 (2^2e or 1)
     unsigned long long *s_mask;
     int *s_idx, *s_st, *s_sk, *s_of, *s_counts, *s_off, *s_unique;
     float *s_w, *slot_w;
@@ -199,8 +199,6 @@ struct Smem {
     unsigned char *xs;
     float *xsum;
     float *red;            // gate/up partials [2][kCW][32][8]; router / final scratch
-    unsigned char *hs;     // h rows for the down phase: the x, xsum and red areas,
-                           // dead once gate/up is done
     unsigned char *ring;
 };
 
@@ -210,7 +208,6 @@ __device__ __forceinline__ Smem carve_smem(unsigned char *base, const DecodeLayo
     s.empty = s.full + kMaxRing;
     s.pfull = s.full + 2 * kMaxRing;
     s.pempty = s.pfull + 2;
-    s.hbar = s.pempty + 2;
     s.misc = reinterpret_cast<int *>(base + L.off_misc);
     unsigned char *r = base + L.off_route;
     s.s_mask = reinterpret_cast<unsigned long long *>(r);
@@ -229,7 +226,6 @@ __device__ __forceinline__ Smem carve_smem(unsigned char *base, const DecodeLayo
     s.xs = base + L.off_x;
     s.xsum = reinterpret_cast<float *>(base + L.off_xsum);
     s.red = reinterpret_cast<float *>(base + L.off_red);
-    s.hs = base + L.off_x;
     s.ring = base + L.off_ring;
     return s;
 }
@@ -440,9 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
             ptx::mbar_init(&S.pfull[b], kCW);
             ptx::mbar_init(&S.pempty[b], 1);
         }
-        ptx::mbar_init(S.hbar, 1);
         for (int i = 0; i < 32; ++i) S.misc[i] = 0;
-        for (int t = 0; t < kNFast; ++t) reinterpret_cast<float *>(S.misc + 40)[t] = 1.0f;
+        for (int t = 0; t < 2 * kNFast; ++t) reinterpret_cast<float *>(S.misc + 40)[t] = 1.0f;
         ptx::mbar_fence_init();
     }
     if (tid == 32) {
@@ -471,8 +466,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     // sums, combined over the chunk-warps in a fixed order.
     // f16 range: a chunk whose largest |x| is at least 2^15, or non-zero below
     // 2^-10, marks the step; the tokens are then staged again scaled by 2^-e
-    // (e = ilogb(max |x_t|) - 14, exact), and the reducers multiply the token's
-    // gate and up sums by 2^e. Ordinary activations never take that path.
+    // (e = ilogb(max |x_t|) - 2, exact: max |x_t| 2^-e in [4, 8)). The reducers
+    // multiply the token's gate and up sums by 2^e; h, which grows as x^2 for
+    // the unclamped activations, is stored times 2^-2e and the token's output
+    // multiplied by 2^2e, so h stays inside f16's range too. Ordinary
+    // activations never take that path.
     {
         const int nE = (cta < E ? 1 : 0) + (cta + (int)G < E ? 1 : 0);
         const int chunks = D >> 3;                  // a multiple of 32, at most kThreads
@@ -480,6 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
         const int TG = min(kThreads / chunks, kNFast);
         float *rs = S.red;                          // [token][router row][chunk-warp]
         float *xscale = reinterpret_cast<float *>(S.misc + 40);
+        float *hscale = reinterpret_cast<float *>(S.misc + 48);
         // x -> f16 in B-operand order (pairs (0,4) (1,5) (2,6) (3,7)), odd inputs
         // divided by 16 (see mma_word_f16), times `inv`; the group's sums of x
         // and of x / m as the MMA sees them. Called by whole warps (one token).
@@ -558,8 +557,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
 #pragma unroll
                 for (int o = 16; o; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
                 if (lane == 0) {
-                    const int e = (am > 0.0f && am <= 3.0e38f) ? min(max(ilogbf(am) - 14, -100), 100) : 0;
+                    const int e = (am > 0.0f && am <= 3.0e38f) ? min(max(ilogbf(am) - 2, -60), 60) : 0;
                     xscale[warp] = ldexpf(1.0f, e);
+                    // the clamped activation bounds h whatever x is: no h scale
+                    hscale[warp] = A.s.act == MOE_ACT_SWIGLU_CLAMPED ? 1.0f : ldexpf(1.0f, 2 * e);
                 }
             }
             __syncthreads();
@@ -851,8 +852,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
                     if (row >= tl.z && row < tl.w && ((m >> tok) & 1u)) {
                         const int pslot = tr.z + __popc(m & ((1u << tok) - 1u));
                         const float xsc = reinterpret_cast<const float *>(S.misc + 40)[tok];
+                        const float hinv = 1.0f / reinterpret_cast<const float *>(S.misc + 48)[tok];
                         Hg[(size_t)pslot * F + h_pos(tl.y + row)] =
-                            f2h_sat(S.slot_w[pslot] * glu_act<false>(A.s.act, A.s.act_limit, gv[i] * xsc, uv[i] * xsc), over);
+                            f2h_sat(S.slot_w[pslot] * glu_act<false>(A.s.act, A.s.act_limit, gv[i] * xsc, uv[i] * xsc) * hinv,
+                                    over);
                     }
                 }
                 if (over) report_error(W.status, kDevErrRange);
@@ -1012,39 +1015,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     stamp(W.phase_ns, timing, 4);
     ptx::named_bar(2, kConsThreads + 64);  // the reducers have written every h row of this CTA
     grid_barrier(gsync, epoch + 2ull * G, bar_ok, abort_flag, W.status, true);
-    // The step's h rows (every slot: this CTA's D rows need every expert) fit
-    // in the areas x, xsum and the partials held during gate/up: one round of
-    // bulk copies from L2 now, and the down loop reads h from shared memory.
-    // Otherwise each down stage loads its h fragments from L2 one stage ahead.
-    const int nslots = S.s_off[E];
-    const bool hsm = nslots * L.h_stride <= L.h_cap;
-    if (hsm && warp == 0) {
-        const bool issue = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
-        if (issue) {
-            // h was written by other CTAs' generic stores, acquired through the
-            // barrier; order those writes before this warp's async-proxy reads
-            ptx::fence_proxy_async_global();
-            if (lane == 0) ptx::mbar_arrive_expect_tx(S.hbar, (uint32_t)(nslots * F * 2));
-            __syncwarp();
-#pragma unroll 1
-            for (int p = lane; p < nslots; p += 32)
-                ptx::bulk_g2s(S.hs + (size_t)p * L.h_stride, Hg + (size_t)p * F, (uint32_t)(F * 2), S.hbar, pol);
-            // the copies must land before this CTA may exit: wait for them even
-            // after an abort (bounded)
-            if (lane == 0) {
-                const unsigned long long t0 = globaltimer();
-                while (!ptx::mbar_try_wait(S.hbar, 0)) {
-                    if (globaltimer() - t0 > kWaitNs) {
-                        set_timeout(abort_flag, W.status);
-                        break;
-                    }
-                }
-            }
-            __syncwarp();
-        }
-    } else if (hsm && !*abort_flag) {
-        __shfl_sync(0xffffffffu, (int)wait_phase(S.hbar, 0, abort_flag, W.status), 0);
-    }
     stamp(W.phase_ns, timing, 5);
 
     // ---- phase B: down, all experts summed per warp ----------------------------
@@ -1070,20 +1040,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
             const unsigned m = (unsigned)ur.y;
             if ((m >> g) & 1u) {
                 const int ps = ur.z + __popc(m & ((1u << g) - 1u));
-                if (hsm) {
-                    const unsigned char *hp = S.hs + (size_t)ps * L.h_stride + (size_t)itg[q] * 256 + c * 32;
-                    hv[0] = *reinterpret_cast<const uint4 *>(hp);
-                    hv[1] = *reinterpret_cast<const uint4 *>(hp + 16);
-                    hv[2] = *reinterpret_cast<const uint4 *>(hp + 128);
-                    hv[3] = *reinterpret_cast<const uint4 *>(hp + 144);
-                } else {
-                    const unsigned char *hp = reinterpret_cast<const unsigned char *>(Hg + (size_t)ps * F) +
-                                              (size_t)itg[q] * 256 + c * 32;
-                    hv[0] = ptx::ld_cg_v4(hp);
-                    hv[1] = ptx::ld_cg_v4(hp + 16);
-                    hv[2] = ptx::ld_cg_v4(hp + 128);
-                    hv[3] = ptx::ld_cg_v4(hp + 144);
-                }
+                const unsigned char *hp = reinterpret_cast<const unsigned char *>(Hg + (size_t)ps * F) +
+                                          (size_t)itg[q] * 256 + c * 32;
+                hv[0] = ptx::ld_cg_v4(hp);
+                hv[1] = ptx::ld_cg_v4(hp + 16);
+                hv[2] = ptx::ld_cg_v4(hp + 128);
+                hv[3] = ptx::ld_cg_v4(hp + 144);
             }
         }
     };
@@ -1204,8 +1166,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     }
 
     // ---- final: fixed-order sum over warps of their partial outputs -------------
-    // (the partials go where h was staged: every consumer is done reading it)
-    if (hsm) cta_sync(true);
     {
         float *red = S.red + ((size_t)warp * 32 + lane) * 8;
         *reinterpret_cast<float4 *>(red) = make_float4(acc0[0], acc0[1], acc0[2], acc0[3]);
@@ -1221,6 +1181,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
         const int ln = (rt >> 1) * 4 + (t >> 1), idx = dt * 4 + (rt & 1) * 2 + (t & 1);
         float v = 0.f;
         for (int w = 0; w < kCW; ++w) v += S.red[((size_t)w * 32 + ln) * 8 + idx];
+        v *= reinterpret_cast<const float *>(S.misc + 48)[t];  // 1 unless token t was scaled
         const size_t at = (size_t)t * D + b0 + r;
         if (A.s.out_dtype == MOE_DTYPE_F32)
             static_cast<float *>(A.out)[at] = v;
@@ -1313,7 +1274,6 @@ bool fused_layout(const moe_config &c, int num_sms, int max_smem, DecodeLayout *
     if (tiles > kMaxTilesF) return false;
     L.max_tiles = kMaxTilesF;
     L.x_stride = 2 * D + 16;
-    L.h_stride = 2 * F + 16;
     int off = 0;
     L.off_bar = off;
     off += 256;
@@ -1331,7 +1291,6 @@ bool fused_layout(const moe_config &c, int num_sms, int max_smem, DecodeLayout *
     off += 2 * kCW * kPartStride * 4;
     off = round_up(off, 1024);
     L.off_ring = off;
-    L.h_cap = L.off_ring - L.off_x;
     const int tail = 2048 + 1024;  // over-read pad of the last stage + base alignment slack
     const int room = max_smem - off - tail;
     int ns = room / L.stage_bytes;

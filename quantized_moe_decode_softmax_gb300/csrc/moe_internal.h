@@ -115,9 +115,6 @@ struct DecodeLayout {
     // shared memory carve (byte offsets from the 1024-aligned base)
     int off_bar, off_misc, off_route, off_tiles, off_x, off_xsum, off_red, off_ring;
     int x_stride;     // bytes per staged token row of x
-    int h_cap;        // bytes from off_x to off_ring: after gate/up these hold the
-                      // step's h rows when they fit (h_stride per slot)
-    int h_stride;     // bytes per staged h row: 2 * Dff + 16
     int smem_bytes;   // dynamic shared memory requested (includes alignment slack)
 };
 
