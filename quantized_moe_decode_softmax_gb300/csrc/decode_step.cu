@@ -5,10 +5,11 @@
 //
 // Phases inside one launch:
 //   R  router GEMV: logits[t, e] = x[t] . Wr[e] (+ bias). Each CTA owns at most
-//      two experts (e = cta, cta + G). Every CTA also stages x in shared memory
-//      as f16 in the B-operand order of the tensor-core MMA, with per-group
-//      sums of x.                                            -> grid barrier 1
-//   T  every CTA reads the logits and computes softmax, top-k, renormalised
+//      two experts (e = cta, cta + G) and publishes their logits as 64-bit words
+//      (launch tag << 32 | value). Every CTA also stages x in shared memory as
+//      f16 in the B-operand order of the tensor-core MMA, with per-group sums.
+//   T  every CTA polls the tagged logits until all carry this launch's tag (the
+//      exchange needs no grid barrier), then computes top-k, renormalised
 //      weights and the grouping by expert itself (the same deterministic result
 //      in every CTA, so there is no second exchange); one warp builds the
 //      grouping, the slot table and the CTA's gate/up tile list.
@@ -344,23 +345,48 @@ __device__ __forceinline__ float key2f(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// Top-k of one token's logits (warp-wide; lane l holds experts l + 32 i, i < 8):
-// the k largest in descending order, ties to the lower expert id, and their
-// renormalised softmax weights. The softmax denominator over all experts cancels
-// in the renormalisation, so only the k selected logits are exponentiated.
-// Each lane first sorts its eight (key, i) pairs (descending key, ascending i);
-// every round then takes the warp maximum of the lanes' heads, the lowest
-// expert id among the lanes holding it, and the winning lane drops its head.
-__device__ __forceinline__ void warp_topk8(const float *lt, int E, int k, int lane, int *idx_out,
-                                           float *w_out) {
-    uint32_t key[8], ix[8];
+// Top-k of one token's logits (warp-wide; lane l holds experts l + 32 i, i < NPL,
+// E <= 32 NPL): the k largest in descending order, ties to the lower expert id,
+// and their renormalised softmax weights. The softmax denominator over all
+// experts cancels in the renormalisation, so only the k selected logits are
+// exponentiated.
+// The logits come from the CTAs that own each expert, as 64-bit words (launch
+// tag << 32 | f32 bits): the warp polls each word until it carries this
+// launch's tag, so the exchange needs no grid barrier (bounded wait; on a
+// timeout the flag is set and the result is garbage).
+// Each lane then sorts its NPL (key, i) pairs (descending key, ascending i);
+// every round takes the warp maximum of the lanes' heads, the lowest expert id
+// among the lanes holding it, and the winning lane drops its head.
+template <int NPL>
+__device__ __forceinline__ void warp_topk_tagged(const unsigned long long *lt, uint32_t tag, int E, int k,
+                                                 int lane, int *idx_out, float *w_out,
+                                                 volatile int *abort_flag, unsigned *status) {
+    uint32_t key[NPL], ix[NPL];
+    unsigned need = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int e = lane + 32 * i;
-        key[i] = e < E ? f2key(__ldcg(lt + e)) : 0u;
+    for (int i = 0; i < NPL; ++i) {
+        key[i] = 0u;
         ix[i] = (uint32_t)i;
+        if (lane + 32 * i < E) need |= 1u << i;
     }
-    // Batcher's odd-even merge sort of 8 elements (19 compare-exchanges)
+    const unsigned long long t0 = globaltimer();
+    for (;;) {
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) {
+            if ((need >> i) & 1u) {
+                const unsigned long long v = ptx::ld_relaxed_gpu_u64(lt + lane + 32 * i);
+                if ((uint32_t)(v >> 32) == tag) {
+                    key[i] = f2key(__uint_as_float((uint32_t)v));
+                    need &= ~(1u << i);
+                }
+            }
+        }
+        if (__all_sync(0xffffffffu, need == 0u)) break;
+        if (*abort_flag || globaltimer() - t0 > kWaitNs) {
+            if (lane == 0) set_timeout(abort_flag, status);
+            break;
+        }
+    }
     auto cx = [&](int a, int b) {
         const bool sw = key[b] > key[a] || (key[b] == key[a] && ix[b] < ix[a]);
         const uint32_t ka = key[a], ia = ix[a];
@@ -369,27 +395,35 @@ __device__ __forceinline__ void warp_topk8(const float *lt, int E, int k, int la
         key[b] = sw ? ka : key[b];
         ix[b] = sw ? ia : ix[b];
     };
-    cx(0, 1); cx(2, 3); cx(4, 5); cx(6, 7);
-    cx(0, 2); cx(1, 3); cx(4, 6); cx(5, 7);
-    cx(1, 2); cx(5, 6);
-    cx(0, 4); cx(1, 5); cx(2, 6); cx(3, 7);
-    cx(2, 4); cx(3, 5);
-    cx(1, 2); cx(3, 4); cx(5, 6);
+    if (NPL == 8) {
+        // Batcher's odd-even merge sort of 8 elements (19 compare-exchanges)
+        cx(0, 1); cx(2, 3); cx(4, 5); cx(6, 7);
+        cx(0, 2); cx(1, 3); cx(4, 6); cx(5, 7);
+        cx(1, 2); cx(5, 6);
+        cx(0, 4); cx(1, 5); cx(2, 6); cx(3, 7);
+        cx(2, 4); cx(3, 5);
+        cx(1, 2); cx(3, 4); cx(5, 6);
+    } else {
+        // 4 elements (5 compare-exchanges)
+        cx(0, 1); cx(2, 3);
+        cx(0, 2); cx(1, 3);
+        cx(1, 2);
+    }
     float lsel = 0.f, lmax = 0.f;
 #pragma unroll 1
     for (int j = 0; j < k; ++j) {
         const uint32_t wk = __reduce_max_sync(0xffffffffu, key[0]);
-        // a popped-out slot has i = 8: its id lane + 256 loses every tie
+        // a popped-out slot has i = NPL: its id lane + 32 NPL loses every tie
         const uint32_t ce = key[0] == wk ? (uint32_t)lane + 32u * ix[0] : 0xFFFFFFFFu;
         const uint32_t e = __reduce_min_sync(0xffffffffu, ce);
         if ((int)(e & 31u) == lane) {
 #pragma unroll
-            for (int i = 0; i < 7; ++i) {
+            for (int i = 0; i < NPL - 1; ++i) {
                 key[i] = key[i + 1];
                 ix[i] = ix[i + 1];
             }
-            key[7] = 0u;
-            ix[7] = 8u;
+            key[NPL - 1] = 0u;
+            ix[NPL - 1] = (uint32_t)NPL;
         }
         const float l = key2f(wk);
         if (j == 0) lmax = l;
@@ -453,10 +487,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
     stamp(W.phase_ns, timing, 0);
-    // barrier epoch (thread 0 only): the counter grows by 2G per launch and no
-    // CTA of this launch can pass barrier 1 before this CTA arrives there
-    if (tid == 0) epoch = ptx::ld_acquire_gpu_u64(gsync);
+    // barrier epoch (thread 0 only): the counter grows by G per launch and no
+    // CTA of this launch can pass barrier 2 before this CTA arrives there. The
+    // launch tag of the logit exchange is the previous launch's plus one; CTA 0
+    // stores it back only once every CTA has arrived at barrier 2, after all
+    // of them have read it here.
+    if (tid == 0) {
+        epoch = ptx::ld_acquire_gpu_u64(gsync);
+        S.misc[56] = (int)(W.sync[32] + 1u);
+    }
     __syncthreads();
+    const uint32_t tag = (uint32_t)S.misc[56];
 
     // ---- phase R: router logits of this CTA's experts, x staging ----------------
     // Thread (token group tg, chunk ch) handles the 8-input chunk ch of tokens
@@ -465,12 +506,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     // 32 threads share the token, so the per-token sums over chunks are warp
     // sums, combined over the chunk-warps in a fixed order.
     // f16 range: a chunk whose largest |x| is at least 2^15, or non-zero below
-    // 2^-10, marks the step; the tokens are then staged again scaled by 2^-e
+    // 2^-4, marks the step; the tokens are then staged again scaled by 2^-e
     // (e = ilogb(max |x_t|) - 2, exact: max |x_t| 2^-e in [4, 8)). The reducers
-    // multiply the token's gate and up sums by 2^e; h, which grows as x^2 for
-    // the unclamped activations, is stored times 2^-2e and the token's output
-    // multiplied by 2^2e, so h stays inside f16's range too. Ordinary
-    // activations never take that path.
+    // multiply the token's gate and up sums by 2^e. A token scaled up (e < 0)
+    // has h shrinking as x^2 for the unclamped activations: its h is stored
+    // times 2^-2e and its output multiplied by 2^2e, so h keeps f16's
+    // precision. An h beyond f16's range saturates and is reported. N(0,1)-like
+    // activations never take that path (a chunk of 8 all below 2^-4 has
+    // probability below 1e-10).
     {
         const int nE = (cta < E ? 1 : 0) + (cta + (int)G < E ? 1 : 0);
         const int chunks = D >> 3;                  // a multiple of 32, at most kThreads
@@ -523,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
                     d1 = fmaf(xv[j], w1[j], d1);
                     am = fmaxf(am, fabsf(xv[j]));
                 }
-                if (am >= 32768.0f || (am > 0.0f && am < 0.0009765625f)) S.misc[7] = 1;
+                if (am >= 32768.0f || (am > 0.0f && am < 0.0625f)) S.misc[7] = 1;
                 stage_chunk(t, ch, xv, 1.0f);
                 if (nE > 0) {
                     d0 = warp_sum(d0);
@@ -559,8 +602,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
                 if (lane == 0) {
                     const int e = (am > 0.0f && am <= 3.0e38f) ? min(max(ilogbf(am) - 2, -60), 60) : 0;
                     xscale[warp] = ldexpf(1.0f, e);
-                    // the clamped activation bounds h whatever x is: no h scale
-                    hscale[warp] = A.s.act == MOE_ACT_SWIGLU_CLAMPED ? 1.0f : ldexpf(1.0f, 2 * e);
+                    // h of a token scaled up shrinks as x^2 (the clamp bounds h
+                    // from above only, which a small token never reaches)
+                    hscale[warp] = e < 0 ? ldexpf(1.0f, 2 * e) : 1.0f;
                 }
             }
             __syncthreads();
@@ -575,6 +619,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
             }
             __syncthreads();
         }
+        if ((A.s.flags & MOE_FLAG_TEST_STALL) && cta == 0) {
+            // test hook: CTA 0 publishes its logits late, only once another CTA's
+            // bounded wait for them has given up (or after 2 s), so the others
+            // time out while every CTA still arrives at barrier 2
+            if (tid == 0) {
+                const unsigned long long t0 = globaltimer();
+                while (!(*reinterpret_cast<volatile unsigned *>(W.status) & kDevErrTimeout) &&
+                       globaltimer() - t0 < 2 * kWaitNs) {
+                }
+            }
+            __syncthreads();
+        }
         if (tid < nE * n) {
             const int ei = tid / n, t = tid - ei * n;
             float l = 0.f;
@@ -582,34 +638,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
             for (int w = 0; w < NW; ++w) l += rs[(t * 2 + ei) * NW + w];
             const int e = cta + ei * (int)G;
             if (A.router_bias) l += A.router_bias[e];
-            W.logits[(size_t)t * E + e] = l;
+            W.logits[(size_t)t * E + e] = l;  // for the grouping kernel of chunked cohorts
+            ptx::st_relaxed_gpu_u64(W.tlog + (size_t)t * kTagSlots + e,
+                                    ((unsigned long long)tag << 32) | __float_as_uint(l));
         }
     }
 
-    // ---- grid barrier 1: all logits written -------------------------------------
-    // Every CTA arrives at both grid barriers exactly once on every path (after
-    // a timeout too), so the counter is base + 2G when a launch ends and the
-    // next launch starts from a multiple of 2G; the rounding below only guards
-    // against a counter corrupted from outside.
+    // ---- no grid barrier: phase T polls the tagged logits ------------------------
     stamp(W.phase_ns, timing, 1);
-    if (tid == 0) epoch = epoch / (2ull * G) * (2ull * G);
-    if ((A.s.flags & MOE_FLAG_TEST_STALL) && cta == 0) {
-        // test hook: CTA 0 arrives late, only once another CTA's bounded wait has
-        // given up (or after 2 s), so the others time out while the counter still
-        // ends the launch consistent
-        if (tid == 0) {
-            const unsigned long long t0 = globaltimer();
-            while (!(*reinterpret_cast<volatile unsigned *>(W.status) & kDevErrTimeout) &&
-                   globaltimer() - t0 < 2 * kWaitNs) {
-            }
-        }
-        __syncthreads();
-    }
-    grid_barrier(gsync, epoch + G, bar_ok, abort_flag, W.status);
+    if (tid == 0) epoch = epoch / G * G;
     stamp(W.phase_ns, timing, 2);
 
     // ---- phase T: routing and grouping, redundantly in every CTA ---------------
-    if (warp < n) warp_topk8(W.logits + (size_t)warp * E, E, K, lane, S.s_idx + warp * K, S.s_w + warp * K);
+    if (warp < n) {
+        const unsigned long long *lt = W.tlog + (size_t)warp * kTagSlots;
+        if (E <= 128)
+            warp_topk_tagged<4>(lt, tag, E, K, lane, S.s_idx + warp * K, S.s_w + warp * K, abort_flag, W.status);
+        else
+            warp_topk_tagged<8>(lt, tag, E, K, lane, S.s_idx + warp * K, S.s_w + warp * K, abort_flag, W.status);
+    }
     __syncthreads();
     const int Sl = n * K;
     // Grouping, slot table and tile list by warp 0 alone (no CTA barrier in
@@ -1014,7 +1061,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     // ---- grid barrier 2: every h row written ----------------------------------
     stamp(W.phase_ns, timing, 4);
     ptx::named_bar(2, kConsThreads + 64);  // the reducers have written every h row of this CTA
-    grid_barrier(gsync, epoch + 2ull * G, bar_ok, abort_flag, W.status, true);
+    grid_barrier(gsync, epoch + G, bar_ok, abort_flag, W.status, true);
+    // every CTA has read the launch tag (it arrived here): publish it for the
+    // next launch (also after a timeout, so a later launch never reuses it)
+    if (cta == 0 && tid == 0) W.sync[32] = tag;
     stamp(W.phase_ns, timing, 5);
 
     // ---- phase B: down, all experts summed per warp ----------------------------

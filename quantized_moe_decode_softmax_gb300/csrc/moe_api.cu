@@ -79,6 +79,7 @@ size_t carve(const moe_config &c, char *base, Workspace *ws) {
     w.y = (float *)take(S * D * 4);
     w.status = (unsigned *)take(4 * 4);
     w.sync = (unsigned *)take(64 * 4);
+    w.tlog = (unsigned long long *)take(n * kTagSlots * 8);
     w.phase_ns = (unsigned long long *)take(16 * 1024 * 8);
     w.x_stage = take(n * D * elem_size(c.x_dtype));
     w.out_stage = take(n * D * elem_size(c.out_dtype));
@@ -252,8 +253,11 @@ moe_status forward_checked(moe_plan *plan, const void *x, const void *router_w,
         const moe_status err = plan->host_err[0] ? MOE_ERR_TIMEOUT
                              : plan->host_err[2] ? MOE_ERR_RANGE : MOE_ERR_CUDA;
         plan->host_err[0] = plan->host_err[1] = plan->host_err[2] = 0u;
+        // reset the error bits, the barrier counter, the launch tag and the
+        // tagged logits (a restarted tag must not meet an old logit)
         if (cudaMemsetAsync(plan->ws.status, 0, sizeof(unsigned), s) != cudaSuccess ||
-            cudaMemsetAsync(plan->ws.sync, 0, 64 * sizeof(unsigned), s) != cudaSuccess) {
+            cudaMemsetAsync(plan->ws.sync, 0, 64 * sizeof(unsigned), s) != cudaSuccess ||
+            cudaMemsetAsync(plan->ws.tlog, 0, (size_t)plan->cfg.max_tokens * kTagSlots * 8, s) != cudaSuccess) {
             cudaGetLastError();
             return MOE_ERR_CUDA;
         }
@@ -417,6 +421,7 @@ moe_status moe_plan_check(moe_plan *plan) {
         // grid-barrier counters
         cudaMemset(plan->ws.status, 0, sizeof(unsigned));
         cudaMemset(plan->ws.sync, 0, 64 * sizeof(unsigned));
+        cudaMemset(plan->ws.tlog, 0, (size_t)plan->cfg.max_tokens * kTagSlots * 8);
         cudaDeviceSynchronize();
         return (status & kDevErrTimeout) ? MOE_ERR_TIMEOUT
              : (status & kDevErrRange) ? MOE_ERR_RANGE : MOE_ERR_CUDA;

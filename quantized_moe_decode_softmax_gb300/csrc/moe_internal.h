@@ -17,6 +17,7 @@ constexpr int kMaxTopK = 16;
 constexpr int kMaxDff = 8192;
 constexpr int kMaxD = 16384;
 constexpr int kMaxSlots = kMaxTokens * kMaxTopK;
+constexpr int kTagSlots = 256;  // tagged logits per token (the single launch: E <= 256)
 // largest cohort that runs as chunks of the single-launch kernel by default
 // (larger ones take the grouped multi-kernel path)
 constexpr int kChunkMaxTokens = 16;
@@ -44,7 +45,10 @@ struct Workspace {
     float *y;           // [max_n * k, D]    grouped position major
     unsigned *status;   // [4]   [0] device error bits; [2..3] device address of the
                         //       plan's host-mapped error word (0: none)
-    unsigned *sync;     // [64]  barrier counters (zeroed at plan creation)
+    unsigned *sync;     // [64]  [0..1] grid-barrier counter; [32] the single launch's
+                        //       last launch tag (zeroed at plan creation)
+    unsigned long long *tlog;  // [max_n, kTagSlots] logits of the single launch,
+                               // each (launch tag << 32 | f32 bits)
     unsigned long long *phase_ns;  // [256] optional phase timestamps
     void *x_stage;      // [max_n, D] host-call staging for x
     void *out_stage;    // [max_n, D] host-call staging for out

@@ -52,6 +52,7 @@ size_t carve_noalloc(const moe_config &c, int n, unsigned char *base, Workspace 
     Workspace w{};
     w.status = (unsigned *)take(4 * 4);
     w.sync = (unsigned *)take(64 * 4);
+    w.tlog = (unsigned long long *)take((size_t)n * kTagSlots * 8);
     w.logits = (float *)take((size_t)n * E * 4);
     w.topk_idx = (int *)take(S * 4);
     w.topk_w = (float *)take(S * 4);
@@ -149,8 +150,9 @@ extern "C" moe_status moe_decode_forward_noalloc(const moe_config *cfg, const vo
     Workspace ws{};
     carve_noalloc(c, n_tokens, scratch, &ws);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // the status word and the grid-barrier counter start at zero on every call
-    // (the array keeps the previous call's contents)
+    // the status word, the grid-barrier counter, the launch tag and the tagged
+    // logits start at zero on every call (the array keeps the previous call's
+    // contents)
     if (cudaMemsetAsync(ws.status, 0, (unsigned char *)ws.logits - (unsigned char *)ws.status, st) !=
         cudaSuccess) {
         cudaGetLastError();
