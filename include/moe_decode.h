@@ -1,7 +1,8 @@
 /*
  * moe_decode.h -- C ABI of the quantized MoE decode library (GB300, sm_103a).
  *
- * One call runs one MoE layer's decode step for a cohort of 1..64 tokens:
+ * One call runs one MoE layer's decode step for a cohort of 1..64 tokens
+ * (and, on the prefill path, for cohorts of up to 8192 tokens):
  *   1. router GEMV, softmax over all experts, top-k, renormalise the k weights
  *   2. group the n*k (token, rank) slots by expert, de-duplicated, so every
  *      selected expert's planes are streamed from HBM once per step (once
@@ -120,7 +121,9 @@ typedef struct {
     int Dff;            /* expert intermediate size; multiple of 64, <= 8192 */
     int bits;           /* must be 4 */
     int group_size;     /* must be 64 */
-    int max_tokens;     /* largest cohort a forward call may pass, 1..64 */
+    int max_tokens;     /* largest cohort a forward call may pass, 1..8192;
+                           above 64 the plan also holds the prefill path's
+                           workspace (h and y for max_tokens * top_k slots) */
     int x_dtype;        /* MOE_DTYPE_* of x */
     int router_dtype;   /* MOE_DTYPE_* of the router weights */
     int out_dtype;      /* MOE_DTYPE_* of out */
@@ -175,7 +178,7 @@ moe_status moe_plan_workspace_bytes(const moe_config *cfg, size_t *bytes);
  * group_size != 64, D or Dff not a multiple of 64, D > 16384, Dff > 8192,
  * E > 1024, top_k > 16, activation not a MOE_ACT_*, down_bits not 0, 4 or 6.
  * INVALID_ARG: null pointers, non-positive sizes, top_k > E, max_tokens
- * outside 1..64, unknown dtypes, negative mma_min_tokens, unknown flags, a
+ * outside 1..8192, unknown dtypes, negative mma_min_tokens, unknown flags, a
  * clamp bound that is not finite and positive (MOE_ACT_SWIGLU_CLAMPED), an
  * expert range other than 0 <= expert_begin < expert_end <= E (or 0, 0).
  * A plan with 6-bit down planes runs every cohort on the grouped path.
@@ -209,7 +212,14 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan **out);
  *                    the grouped multi-kernel path (router, top-k and
  *                    grouping, per-expert tile or GEMV kernels, combine);
  *   MOE_FLAG_F32_DEBUG, or a shape the single-launch kernel declines:
- *                    the grouped multi-kernel path with f32 GEMV kernels.
+ *                    the grouped multi-kernel path with f32 GEMV kernels;
+ *   n_tokens 65..max_tokens: the prefill path (#1616 Current Behavior and #1859
+ *                    Problem / Background: the sorted matrix path, qmm, of
+ *                    prompt processing): routing per token, grouping through
+ *                    per-expert token bitmaps, then per expert a grouped GEMM
+ *                    (the tile kernels over its tokens in blocks of 64, each
+ *                    weight tile read once per block) or the f32 GEMV for
+ *                    experts under mma_min_tokens, and the combine.
  * Expert range. A plan that owns the experts [expert_begin, expert_end)
  * writes out[t] = sum over the ranks j whose expert it owns of w[t,j] *
  * y[t,j] (0 where it owns none): the plans of a partition of the experts

@@ -386,6 +386,9 @@ __device__ __forceinline__ void warp_topk_tagged(const unsigned long long *lt, u
             if (lane == 0) set_timeout(abort_flag, status);
             break;
         }
+        // back off: every CTA's token warps poll at once, and a tight loop of
+        // L2 loads slows the CTAs still writing their logits
+        __nanosleep(200);
     }
     auto cx = [&](int a, int b) {
         const bool sw = key[b] > key[a] || (key[b] == key[a] && ix[b] < ix[a]);
@@ -492,12 +495,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     // launch tag of the logit exchange is the previous launch's plus one; CTA 0
     // stores it back only once every CTA has arrived at barrier 2, after all
     // of them have read it here.
+    // Both loads are issued here and consumed later (the tag just before phase
+    // R's CTA barrier, the epoch at barrier 2), so their latency overlaps the
+    // router loads; the previous launch's writes are visible after
+    // griddepcontrol.wait.
+    unsigned prev_tag = 0;
     if (tid == 0) {
-        epoch = ptx::ld_acquire_gpu_u64(gsync);
-        S.misc[56] = (int)(W.sync[32] + 1u);
+        epoch = *reinterpret_cast<volatile unsigned long long *>(gsync);
+        prev_tag = *reinterpret_cast<volatile unsigned *>(W.sync + 32);
     }
     __syncthreads();
-    const uint32_t tag = (uint32_t)S.misc[56];
 
     // ---- phase R: router logits of this CTA's experts, x staging ----------------
     // Thread (token group tg, chunk ch) handles the 8-input chunk ch of tokens
@@ -585,6 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
             *reinterpret_cast<uint4 *>(S.xs + (size_t)t * L.x_stride + (size_t)ch * 16) = make_uint4(0, 0, 0, 0);
             if ((ch & 7) == 0) *reinterpret_cast<float2 *>(S.xsum + ((ch >> 3) * kNFast + t) * 2) = make_float2(0.f, 0.f);
         }
+        if (tid == 0) S.misc[56] = (int)(prev_tag + 1u);  // this launch's tag
         __syncthreads();
         if (S.misc[7]) {
             // per-token scales: warp t finds max |x_t|
@@ -631,6 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
             }
             __syncthreads();
         }
+        const uint32_t tag = (uint32_t)S.misc[56];
         if (tid < nE * n) {
             const int ei = tid / n, t = tid - ei * n;
             float l = 0.f;
@@ -644,6 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
         }
     }
 
+    const uint32_t tag = (uint32_t)S.misc[56];
     // ---- no grid barrier: phase T polls the tagged logits ------------------------
     stamp(W.phase_ns, timing, 1);
     if (tid == 0) epoch = epoch / G * G;

@@ -39,9 +39,10 @@ constexpr int kTR = 64;                // weight-tile rows per block (one MMA ro
 constexpr int kTT = 2 * kTR;           // threads per block: two per tile row (4 warps)
 constexpr int kKC = 128;               // inputs per K chunk (two groups)
 constexpr int kRowB = kKC * 2 + 16;    // shared row stride in bytes (ldmatrix without bank conflicts)
-constexpr int kMaxNT = kMaxTokens / 8; // token tiles
+constexpr int kTokB = 64;              // tokens of one block pass (an expert's tokens in blocks of 64)
+constexpr int kMaxNT = kTokB / 8;      // token tiles
 constexpr int kSmemA = kTR * kRowB;    // weights: kTR rows x kKC f16
-constexpr int kSmemX = kMaxTokens * kRowB;
+constexpr int kSmemX = kTokB * kRowB;
 constexpr int kSmem = kSmemA + kSmemX;
 static_assert(kTR * 65 * 4 <= kSmem, "the gate/up epilogue reuses the tile's shared memory");
 
@@ -161,14 +162,18 @@ __device__ __forceinline__ void tile_product(unsigned char *As, unsigned char *X
 }
 
 // block (kTR / 2 rows f of expert unique[blockIdx.y]): tile rows [0, kTR / 2) gate,
-// [kTR / 2, kTR) up
+// [kTR / 2, kTR) up; the expert's tokens in blocks of 64 (blocks z, z + gridDim.z,
+// ... for z = blockIdx.z), so a prefill expert with hundreds of tokens reuses
+// each weight tile across them
 __global__ void __launch_bounds__(kTT) gateup_tile_kernel(StepArgs a, Workspace ws, int thr) {
     extern __shared__ __align__(16) unsigned char sm[];
     const int u = blockIdx.y;
     if (u >= *ws.U) return;
     const int e = ws.unique[u];
-    const int off = ws.offsets[e], cnt = ws.offsets[e + 1] - off;
-    if (cnt < thr) return;
+    const int off_e = ws.offsets[e], cnt_e = ws.offsets[e + 1] - off_e;
+    if (cnt_e < thr) return;
+    for (int tb = blockIdx.z; tb * kTokB < cnt_e; tb += gridDim.z) {
+    const int off = off_e + tb * kTokB, cnt = min(kTokB, cnt_e - tb * kTokB);
     const int D = a.s.D, F = a.s.F, f0 = blockIdx.x * (kTR / 2);
     const int NT = (cnt + 7) / 8;
     unsigned char *As = sm, *Xs = sm + kSmemA;
@@ -208,16 +213,20 @@ __global__ void __launch_bounds__(kTT) gateup_tile_kernel(StepArgs a, Workspace 
         const float gv = E[fr * 65 + j], uv = E[(kTR / 2 + fr) * 65 + j];
         ws.h[(size_t)(off + j) * F + f0 + fr] = glu_act<true>(a.s.act, a.s.act_limit, gv, uv);
     }
+    __syncthreads();  // the next block's tiles overwrite the epilogue's shared memory
+    }
 }
 
-// block (kTR rows d of expert unique[blockIdx.y])
+// block (kTR rows d of expert unique[blockIdx.y]); token blocks as above
 __global__ void __launch_bounds__(kTT) down_tile_kernel(StepArgs a, Workspace ws, int thr) {
     extern __shared__ __align__(16) unsigned char sm[];
     const int u = blockIdx.y;
     if (u >= *ws.U) return;
     const int e = ws.unique[u];
-    const int off = ws.offsets[e], cnt = ws.offsets[e + 1] - off;
-    if (cnt < thr) return;
+    const int off_e = ws.offsets[e], cnt_e = ws.offsets[e + 1] - off_e;
+    if (cnt_e < thr) return;
+    for (int tb = blockIdx.z; tb * kTokB < cnt_e; tb += gridDim.z) {
+    const int off = off_e + tb * kTokB, cnt = min(kTokB, cnt_e - tb * kTokB);
     const int D = a.s.D, F = a.s.F, d0 = blockIdx.x * kTR;
     const int NT = (cnt + 7) / 8;
     unsigned char *As = sm, *Xs = sm + kSmemA;
@@ -254,6 +263,7 @@ __global__ void __launch_bounds__(kTT) down_tile_kernel(StepArgs a, Workspace ws
             }
         }
     }
+    }
 }
 
 }  // namespace
@@ -266,10 +276,13 @@ cudaError_t launch_expert_tiles(const StepArgs &a, const Workspace &ws, int thr,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (err != cudaSuccess) return err;
     const int maxU = min(a.s.E, a.s.n * a.s.k);
+    // token blocks per expert in the grid (each block loops over the rest): an
+    // expert holds at most n tokens
+    const int zb = min((a.s.n + kTokB - 1) / kTokB, 8);
     if (!down) {
-        gateup_tile_kernel<<<dim3(a.s.F / (kTR / 2), maxU), kTT, kSmem, st>>>(a, ws, thr);
+        gateup_tile_kernel<<<dim3(a.s.F / (kTR / 2), maxU, zb), kTT, kSmem, st>>>(a, ws, thr);
     } else {
-        down_tile_kernel<<<dim3(a.s.D / kTR, maxU), kTT, kSmem, st>>>(a, ws, thr);
+        down_tile_kernel<<<dim3(a.s.D / kTR, maxU, zb), kTT, kSmem, st>>>(a, ws, thr);
     }
     launched += 1;
     return cudaGetLastError();

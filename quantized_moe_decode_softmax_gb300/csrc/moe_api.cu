@@ -8,6 +8,8 @@
 // runtime extent and never a specialisation key.
 #include <cuda_runtime.h>
 #include <stdio.h>
+
+#include <algorithm>
 #include <stdlib.h>
 #include <string.h>
 
@@ -29,7 +31,7 @@ moe_status validate_config(const moe_config *c) {
     if (c->E < 1 || c->top_k < 1 || c->D < 1 || c->Dff < 1 || c->max_tokens < 1)
         return MOE_ERR_INVALID_ARG;
     if (c->top_k > c->E) return MOE_ERR_INVALID_ARG;
-    if (c->max_tokens > kMaxTokens) return MOE_ERR_INVALID_ARG;
+    if (c->max_tokens > kMaxPrefillTokens) return MOE_ERR_INVALID_ARG;
     for (int dt : {c->x_dtype, c->router_dtype, c->out_dtype})
         if (dt != MOE_DTYPE_F32 && dt != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
     if (c->mma_min_tokens < 0) return MOE_ERR_INVALID_ARG;
@@ -79,8 +81,11 @@ size_t carve(const moe_config &c, char *base, Workspace *ws) {
     w.y = (float *)take(S * D * 4);
     w.status = (unsigned *)take(4 * 4);
     w.sync = (unsigned *)take(64 * 4);
-    w.tlog = (unsigned long long *)take(n * kTagSlots * 8);
+    w.tlog = (unsigned long long *)take((n < 8 ? n : 8) * kTagSlots * 8);  // single launch: <= 8 tokens
     w.phase_ns = (unsigned long long *)take(16 * 1024 * 8);
+    const size_t words = n > (size_t)kMaxTokens ? (n + 31) / 32 : 0;  // prefill cohorts only
+    w.tbits = (unsigned *)take(E * words * 4);
+    w.wbase = (int *)take(E * words * 4);
     w.x_stage = take(n * D * elem_size(c.x_dtype));
     w.out_stage = take(n * D * elem_size(c.out_dtype));
     if (ws) *ws = w;
@@ -257,7 +262,7 @@ moe_status forward_checked(moe_plan *plan, const void *x, const void *router_w,
         // tagged logits (a restarted tag must not meet an old logit)
         if (cudaMemsetAsync(plan->ws.status, 0, sizeof(unsigned), s) != cudaSuccess ||
             cudaMemsetAsync(plan->ws.sync, 0, 64 * sizeof(unsigned), s) != cudaSuccess ||
-            cudaMemsetAsync(plan->ws.tlog, 0, (size_t)plan->cfg.max_tokens * kTagSlots * 8, s) != cudaSuccess) {
+            cudaMemsetAsync(plan->ws.tlog, 0, (size_t)std::min(plan->cfg.max_tokens, 8) * kTagSlots * 8, s) != cudaSuccess) {
             cudaGetLastError();
             return MOE_ERR_CUDA;
         }
@@ -300,7 +305,8 @@ moe_status forward_checked(moe_plan *plan, const void *x, const void *router_w,
         }
         fused = tm != nullptr;
     }
-    const char *path = !fused ? "grouped" : n_tokens <= fmax ? "fused" : "fused-chunks";
+    const bool prefill = n_tokens > kMaxTokens;
+    const char *path = prefill ? "prefill" : !fused ? "grouped" : n_tokens <= fmax ? "fused" : "fused-chunks";
     if (trace_enabled(plan))
         fprintf(stderr, "[moe] forward n=%d E=%d k=%d D=%d Dff=%d path=%s\n", n_tokens,
                 a.s.E, a.s.k, a.s.D, a.s.F, path);
@@ -328,6 +334,13 @@ moe_status forward_checked(moe_plan *plan, const void *x, const void *router_w,
             t0 += nc;
         }
         if (err == cudaSuccess) err = launch_topk_group(a, plan->ws, s, launched);
+    } else if (prefill) {
+        // more tokens than a decode cohort: token bitmaps for the grouping, and
+        // the tile kernels loop over each expert's tokens (a grouped GEMM)
+        err = launch_router_logits(a, plan->ws, s, launched);
+        if (err == cudaSuccess) err = launch_prefill_route(a, plan->ws, plan->cfg.max_tokens, s, launched);
+        const int thr = (plan->cfg.flags & MOE_FLAG_F32_DEBUG) ? 0 : plan->mma_min_tokens;
+        if (err == cudaSuccess) err = launch_experts_f32(a, plan->ws, thr, s, launched);
     } else {
         err = launch_router_logits(a, plan->ws, s, launched);
         if (err == cudaSuccess) err = launch_topk_group(a, plan->ws, s, launched);
@@ -421,7 +434,7 @@ moe_status moe_plan_check(moe_plan *plan) {
         // grid-barrier counters
         cudaMemset(plan->ws.status, 0, sizeof(unsigned));
         cudaMemset(plan->ws.sync, 0, 64 * sizeof(unsigned));
-        cudaMemset(plan->ws.tlog, 0, (size_t)plan->cfg.max_tokens * kTagSlots * 8);
+        cudaMemset(plan->ws.tlog, 0, (size_t)std::min(plan->cfg.max_tokens, 8) * kTagSlots * 8);
         cudaDeviceSynchronize();
         return (status & kDevErrTimeout) ? MOE_ERR_TIMEOUT
              : (status & kDevErrRange) ? MOE_ERR_RANGE : MOE_ERR_CUDA;

@@ -11,7 +11,8 @@
 namespace moe {
 
 constexpr int kGroup = 64;
-constexpr int kMaxTokens = 64;
+constexpr int kMaxTokens = 64;         // decode cohorts (single launch, chunks, grouped path)
+constexpr int kMaxPrefillTokens = 8192; // larger cohorts: the prefill path (grouped GEMM)
 constexpr int kMaxE = 1024;
 constexpr int kMaxTopK = 16;
 constexpr int kMaxDff = 8192;
@@ -50,6 +51,8 @@ struct Workspace {
     unsigned long long *tlog;  // [max_n, kTagSlots] logits of the single launch,
                                // each (launch tag << 32 | f32 bits)
     unsigned long long *phase_ns;  // [256] optional phase timestamps
+    unsigned *tbits;    // prefill grouping: [E][W] token bitmaps, W = ceil(max_n / 32)
+    int *wbase;         // prefill grouping: [E][W] exclusive scan of the words' popcounts
     void *x_stage;      // [max_n, D] host-call staging for x
     void *out_stage;    // [max_n, D] host-call staging for out
 };
@@ -169,6 +172,10 @@ cudaError_t launch_router_logits(const StepArgs &a, const Workspace &ws, cudaStr
                                  int &launched);
 cudaError_t launch_topk_group(const StepArgs &a, const Workspace &ws, cudaStream_t st,
                               int &launched);
+// routing and grouping of a prefill cohort (more than kMaxTokens tokens) from
+// the logits: top-k per token, per-expert token bitmaps, counts, offsets, slots
+cudaError_t launch_prefill_route(const StepArgs &a, const Workspace &ws, int max_n, cudaStream_t st,
+                                 int &launched);
 
 // exact f32 expert path (expert_f32_kernels.cu)
 // expert MLP and combine: experts with at least tile_thr tokens take the tile

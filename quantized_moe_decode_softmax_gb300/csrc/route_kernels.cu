@@ -91,7 +91,136 @@ __global__ void __launch_bounds__(1024) topk_group_kernel(Workspace ws, int n, i
     }
 }
 
+// ---- prefill cohorts (more than 64 tokens) ------------------------------------
+// The decode kernel above keeps one 64-bit token mask per expert; a prefill
+// cohort keeps a bitmap of W = ceil(n / 32) words per expert in global memory.
+// The grouped order is the same (experts ascending, tokens ascending within an
+// expert), built in four data-parallel steps with no order-dependent atomics.
+
+// one warp per token: top-k and renormalised weights
+__global__ void topk_tokens_kernel(Workspace ws, int n, int E, int k) {
+    const int t = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+    if (t >= n) return;
+    const float *lt = ws.logits + (size_t)t * E;
+    int *io = ws.topk_idx + (size_t)t * k;
+    float *wo = ws.topk_w + (size_t)t * k;
+    if (E <= 32) warp_topk_token<1>(lt, E, k, lane, io, wo);
+    else if (E <= 64) warp_topk_token<2>(lt, E, k, lane, io, wo);
+    else if (E <= 128) warp_topk_token<4>(lt, E, k, lane, io, wo);
+    else if (E <= 256) warp_topk_token<8>(lt, E, k, lane, io, wo);
+    else if (E <= 512) warp_topk_token<16>(lt, E, k, lane, io, wo);
+    else warp_topk_token<32>(lt, E, k, lane, io, wo);
+}
+
+// slot s = (t, j) sets bit t of its expert's bitmap (owned experts only)
+__global__ void group_mark_kernel(Workspace ws, int n, int k, int e_lo, int e_hi, int W) {
+    const int s = blockIdx.x * blockDim.x + threadIdx.x;
+    if (s >= n * k) return;
+    const int e = ws.topk_idx[s], t = s / k;
+    if (e < e_lo || e >= e_hi) {
+        ws.slot_of[s] = -1;  // an expert this plan does not own
+        return;
+    }
+    atomicOr(&ws.tbits[(size_t)e * W + (t >> 5)], 1u << (t & 31));
+}
+
+// block per expert: popcount of every bitmap word, exclusive scan over words
+__global__ void __launch_bounds__(256) group_count_kernel(Workspace ws, int W) {
+    __shared__ int warp_tot[8];
+    const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int running = 0;
+    for (int w0 = 0; w0 < W; w0 += 256) {
+        const int w = w0 + tid;
+        const int c = w < W ? __popc(ws.tbits[(size_t)e * W + w]) : 0;
+        int inc = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += v;
+        }
+        if (lane == 31) warp_tot[warp] = inc;
+        __syncthreads();
+        int before = 0, total = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            before += i < warp ? warp_tot[i] : 0;
+            total += warp_tot[i];
+        }
+        if (w < W) ws.wbase[(size_t)e * W + w] = running + before + inc - c;
+        running += total;
+        __syncthreads();
+    }
+    if (tid == 0) ws.counts[e] = running;
+}
+
+// one block: offsets = exclusive scan of counts, the ascending unique list, U
+__global__ void __launch_bounds__(32) group_offsets_kernel(Workspace ws, int E) {
+    const int lane = threadIdx.x;
+    int base = 0, ubase = 0;
+    for (int c0 = 0; c0 < E; c0 += 32) {
+        const int e = c0 + lane;
+        const int c = e < E ? ws.counts[e] : 0, u = c > 0 ? 1 : 0;
+        int ic = c, iu = u;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int a = __shfl_up_sync(0xffffffffu, ic, o);
+            const int b = __shfl_up_sync(0xffffffffu, iu, o);
+            if (lane >= o) {
+                ic += a;
+                iu += b;
+            }
+        }
+        if (e < E) {
+            ws.offsets[e] = base + ic - c;
+            ws.unique[e] = -1;
+        }
+        __syncwarp();
+        if (e < E && u) ws.unique[ubase + iu - 1] = e;
+        base += __shfl_sync(0xffffffffu, ic, 31);
+        ubase += __shfl_sync(0xffffffffu, iu, 31);
+    }
+    if (lane == 0) {
+        ws.offsets[E] = base;
+        *ws.U = ubase;
+    }
+}
+
+// thread per (expert, bitmap word): the grouped positions of its tokens
+__global__ void group_fill_kernel(Workspace ws, int k, int W) {
+    const int e = blockIdx.y, w = blockIdx.x * blockDim.x + threadIdx.x;
+    if (w >= W) return;
+    uint32_t bits = ws.tbits[(size_t)e * W + w];
+    int pos = ws.offsets[e] + ws.wbase[(size_t)e * W + w];
+    while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1u;
+        const int t = 32 * w + b;
+        int j = 0;
+        while (j < k && ws.topk_idx[(size_t)t * k + j] != e) ++j;
+        ws.slot_token[pos] = t;
+        ws.slot_k[pos] = j;
+        ws.slot_of[(size_t)t * k + j] = pos;
+        ++pos;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_prefill_route(const StepArgs &a, const Workspace &ws, int max_n, cudaStream_t st,
+                                 int &launched) {
+    const int n = a.s.n, E = a.s.E, k = a.s.k;
+    const int W = (n + 31) / 32, Wcap = (max_n + 31) / 32;
+    (void)Wcap;
+    cudaError_t err = cudaMemsetAsync(ws.tbits, 0, (size_t)E * W * 4, st);
+    if (err != cudaSuccess) return err;
+    topk_tokens_kernel<<<(n + 7) / 8, 256, 0, st>>>(ws, n, E, k);
+    group_mark_kernel<<<(n * k + 255) / 256, 256, 0, st>>>(ws, n, k, a.s.e_lo, a.s.e_hi, W);
+    group_count_kernel<<<E, 256, 0, st>>>(ws, W);
+    group_offsets_kernel<<<1, 32, 0, st>>>(ws, E);
+    group_fill_kernel<<<dim3((W + 127) / 128, E), 128, 0, st>>>(ws, k, W);
+    launched += 5;
+    return cudaGetLastError();
+}
 
 cudaError_t launch_router_logits(const StepArgs &a, const Workspace &ws, cudaStream_t st,
                                  int &launched) {

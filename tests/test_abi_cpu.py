@@ -57,7 +57,7 @@ GOOD = dict(E=128, top_k=8, D=2048, Dff=768, max_tokens=64)
     (dict(top_k=0), q.MOE_ERR_INVALID_ARG),
     (dict(E=4, top_k=5), q.MOE_ERR_INVALID_ARG),
     (dict(max_tokens=0), q.MOE_ERR_INVALID_ARG),
-    (dict(max_tokens=65), q.MOE_ERR_INVALID_ARG),
+    (dict(max_tokens=8193), q.MOE_ERR_INVALID_ARG),
     (dict(x_dtype=7), q.MOE_ERR_INVALID_ARG),
     (dict(mma_min_tokens=-1), q.MOE_ERR_INVALID_ARG),
 ])
@@ -125,7 +125,7 @@ _SINGLE_VIOLATIONS = [
     ("E", 1025, q.MOE_ERR_UNSUPPORTED), ("top_k", 17, q.MOE_ERR_UNSUPPORTED),
     ("E", 0, q.MOE_ERR_INVALID_ARG), ("top_k", 0, q.MOE_ERR_INVALID_ARG),
     ("D", 0, q.MOE_ERR_INVALID_ARG), ("Dff", -64, q.MOE_ERR_INVALID_ARG),
-    ("max_tokens", 0, q.MOE_ERR_INVALID_ARG), ("max_tokens", 65, q.MOE_ERR_INVALID_ARG),
+    ("max_tokens", 0, q.MOE_ERR_INVALID_ARG), ("max_tokens", 8193, q.MOE_ERR_INVALID_ARG),
     ("x_dtype", 2, q.MOE_ERR_INVALID_ARG), ("router_dtype", -1, q.MOE_ERR_INVALID_ARG),
     ("out_dtype", 9, q.MOE_ERR_INVALID_ARG), ("mma_min_tokens", -3, q.MOE_ERR_INVALID_ARG),
     ("flags", 1 << 5, q.MOE_ERR_INVALID_ARG),
