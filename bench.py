@@ -116,6 +116,25 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
+def load_tensor_peak():
+    """bf16 dense TFLOP/s: the sustained figure (a kernel timed inside a long
+    step), else the burst one, else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        if "bf16_tflops_sustained" in p:
+            return float(p["bf16_tflops_sustained"]), "measured sustained"
+        return float(p["bf16_tflops"]), "measured burst"
+    return 1700.0, "fallback sustained"
+
+
+def step_flops(shape, n):
+    """Algorithmic flops of one step: the router GEMV and, per (token, slot),
+    the gate, up and down products (6 D Dff multiply-adds counted as 2 flops)."""
+    return 2.0 * n * shape.E * shape.D + n * shape.top_k * 6.0 * shape.D * shape.F
+
+
 # ----------------------------------------------------------------------------
 # clocks sampler
 # ----------------------------------------------------------------------------
@@ -453,6 +472,28 @@ def run_ours(args, world, rank, local, pg):
     if args.phases:
         phases = phase_split(q, shape, args, xs, reps, dev, n)
 
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak,
+                "traffic": None if launches_per_step != 1.0
+                else traffic_per_launch(args.shape, n, avg_U),
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback",
+                "kernel_us": t_kernel * 1e6,
+                "timing": "CUDA events around the K-step graph replay on the "
+                          "launching stream / launches",
+                "kernel_us_event_bracketed": None if kernel_ms is None
+                else kernel_ms * 1000.0}
+    if n > 64:
+        # prefill cohorts: a grouped GEMM per expert, bound by the tensor cores
+        tpeak, tkind = load_tensor_peak()
+        tflops = step_flops(shape, n) / (ms_per_step / 1000.0) / 1e12
+        roofline = {"bound": "tensor", "achieved": tflops, "peak": tpeak, "unit": "TFLOP/s",
+                    "frac": tflops / tpeak, "traffic": None,
+                    "peak_source": f"{tkind} (MEASURED_PEAKS.json bf16 dense)",
+                    "flops_per_step": step_flops(shape, n),
+                    "timing": "whole step (router, routing, grouped GEMMs, combine) over the "
+                              "K-step graph replay; f16 mma.sync tiles",
+                    "hbm_frac_unique_expert_bytes": achieved * launches_per_step / peak}
     if rank == 0:
         cb = None if args.no_cpu_baseline else cpu_baseline(args)
         tok = sorted(world * n * K / (m / 1000.0) for m in run_ms)
@@ -470,17 +511,7 @@ def run_ours(args, world, rank, local, pg):
             "unique_experts_per_step": avg_U,
             "bytes_per_step": bytes_per_step,
             "router_bytes_per_step": router_bytes,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak,
-                         "traffic": None if launches_per_step != 1.0
-                         else traffic_per_launch(args.shape, n, avg_U),
-                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
-                         if peak_kind == "measured" else "fallback",
-                         "kernel_us": t_kernel * 1e6,
-                         "timing": "CUDA events around the K-step graph replay on the "
-                                   "launching stream / launches",
-                         "kernel_us_event_bracketed": None if kernel_ms is None
-                         else kernel_ms * 1000.0},
+            "roofline": roofline,
             "e2e": {"value": world * n * E2E / e2e_s, "unit": "tokens/s",
                     "h2d_bytes_per_step": n * shape.D * esize,
                     "d2h_bytes_per_step": n * shape.D * esize, "steps": E2E},
