@@ -660,6 +660,28 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     stamp(W.phase_ns, timing, 2);
 
     // ---- phase T: routing and grouping, redundantly in every CTA ---------------
+    // Warp 0 first waits for token 0's row: one polling warp per CTA keeps the
+    // L2 traffic on these few lines low while the slowest CTAs still write. The
+    // rows of the other tokens come from the same CTAs at the same time, so
+    // their warps then usually read them once (and poll only on a mismatch).
+    if (n > 1) {
+        if (warp == 0) {
+            const unsigned long long *lt = W.tlog;
+            const unsigned long long t0 = globaltimer();
+            unsigned need = 0;
+#pragma unroll 1
+            for (int e = lane; e < E; e += 32) need |= 1u << (e >> 5);
+            while (!__all_sync(0xffffffffu, need == 0u)) {
+#pragma unroll 1
+                for (int i = 0; i < 8; ++i)
+                    if (((need >> i) & 1u) && (uint32_t)(ptx::ld_relaxed_gpu_u64(lt + lane + 32 * i) >> 32) == tag)
+                        need &= ~(1u << i);
+                if (__all_sync(0xffffffffu, need == 0u) || *abort_flag || globaltimer() - t0 > kWaitNs) break;
+                __nanosleep(200);
+            }
+        }
+        __syncthreads();
+    }
     if (warp < n) {
         const unsigned long long *lt = W.tlog + (size_t)warp * kTagSlots;
         if (E <= 128)
