@@ -19,6 +19,7 @@
 
 #include "activation.cuh"
 #include "moe_internal.h"
+#include "prefill_tc.h"
 #include "routing.cuh"
 
 namespace moe {
@@ -330,13 +331,19 @@ __global__ void combine_kernel(StepArgs a, Workspace ws) {
 
 }  // namespace
 
-cudaError_t launch_experts_f32(const StepArgs &a, const Workspace &ws, int tile_thr, cudaStream_t st,
-                               int &launched) {
+static cudaError_t launch_experts(const StepArgs &a, const Workspace &ws, int tile_thr, cudaStream_t st,
+                           int &launched, bool tc) {
     const int maxU = min(a.s.E, a.s.n * a.s.k);
-    const int thr = tile_thr > 0 && tile_variant_supported(a.s) ? tile_thr : 0;
+    // experts from tile_thr tokens: the tcgen05 GEMMs (prefill) or the mma.sync tiles
+    tc = tc && tc_variant_supported(a.s);
+    const int thr = tile_thr > 0 && (tc || tile_variant_supported(a.s)) ? tile_thr : 0;
+    auto tiles = [&](bool down) {
+        return tc ? launch_expert_tc(a, ws, thr, down, st, launched)
+                  : launch_expert_tiles(a, ws, thr, down, st, launched);
+    };
     dim3 block(256);
     cudaError_t err;
-    if (thr > 0 && (err = launch_expert_tiles(a, ws, thr, false, st, launched)) != cudaSuccess) return err;
+    if (thr > 0 && (err = tiles(false)) != cudaSuccess) return err;
     const int T1 = pass_tokens(a.s.D), T2 = pass_tokens(a.s.F);
     const int sm1 = T1 * a.s.D * 4, sm2 = T2 * a.s.F * 4;
     dim3 g1((a.s.F + kRowThreads - 1) / kRowThreads, maxU);
@@ -354,7 +361,7 @@ cudaError_t launch_experts_f32(const StepArgs &a, const Workspace &ws, int tile_
     launched += 1;
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    if (thr > 0 && (err = launch_expert_tiles(a, ws, thr, true, st, launched)) != cudaSuccess) return err;
+    if (thr > 0 && (err = tiles(true)) != cudaSuccess) return err;
     if ((err = cudaFuncSetAttribute(down_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sm2)) !=
         cudaSuccess)
         return err;
@@ -371,6 +378,16 @@ cudaError_t launch_experts_f32(const StepArgs &a, const Workspace &ws, int tile_
         combine_kernel<MOE_DTYPE_BF16><<<g3, block, 0, st>>>(a, ws);
     launched += 1;
     return cudaGetLastError();
+}
+
+cudaError_t launch_experts_f32(const StepArgs &a, const Workspace &ws, int tile_thr, cudaStream_t st,
+                               int &launched) {
+    return launch_experts(a, ws, tile_thr, st, launched, false);
+}
+
+cudaError_t launch_experts_prefill(const StepArgs &a, const Workspace &ws, int tile_thr, cudaStream_t st,
+                                   int &launched) {
+    return launch_experts(a, ws, tile_thr, st, launched, true);
 }
 
 }  // namespace moe

@@ -14,6 +14,7 @@
 #include <string.h>
 
 #include "moe_internal.h"
+#include "prefill_tc.h"
 
 using namespace moe;
 
@@ -340,7 +341,7 @@ moe_status forward_checked(moe_plan *plan, const void *x, const void *router_w,
         err = launch_router_logits(a, plan->ws, s, launched);
         if (err == cudaSuccess) err = launch_prefill_route(a, plan->ws, plan->cfg.max_tokens, s, launched);
         const int thr = (plan->cfg.flags & MOE_FLAG_F32_DEBUG) ? 0 : plan->mma_min_tokens;
-        if (err == cudaSuccess) err = launch_experts_f32(a, plan->ws, thr, s, launched);
+        if (err == cudaSuccess) err = launch_experts_prefill(a, plan->ws, thr, s, launched);
     } else {
         err = launch_router_logits(a, plan->ws, s, launched);
         if (err == cudaSuccess) err = launch_topk_group(a, plan->ws, s, launched);
