@@ -49,7 +49,6 @@ constexpr int kM = 128;          // weight rows per A tile
 constexpr int kN = 64;           // tokens per block
 constexpr int kK = 64;           // inputs per chunk
 constexpr int kSbo = 1024;       // bytes between 8-row swizzle atoms (8 rows x 128 B)
-constexpr int kTileA = kM * kK * 2;   // 16 KB: one f16 weight tile
 constexpr int kTileB = kN * kK * 2;   // 8 KB: one f16 activation tile
 constexpr unsigned long long kWaitNs = 1000000000ull;
 
@@ -214,8 +213,7 @@ __global__ void __launch_bounds__(GATEUP ? 512 : 256, 1) expert_tc_kernel(StepAr
     const int off_codes = kTileB, off_sc = kTileB + MATS * kM * cb;
 
     unsigned char *ring = base;
-    unsigned char *Abuf = base + S * stage_stride;              // [2][MATS][kTileA]
-    uint64_t *bar = reinterpret_cast<uint64_t *>(Abuf + 2 * MATS * kTileA);  // [2]
+    uint64_t *bar = reinterpret_cast<uint64_t *>(base + S * stage_stride);  // [2]
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
 
@@ -225,7 +223,11 @@ __global__ void __launch_bounds__(GATEUP ? 512 : 256, 1) expert_tc_kernel(StepAr
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc::smem_u32(&bar[1])) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if ((tid >> 5) == 0) tc::tmem_alloc(tslot, GATEUP ? 128 : 64);
+    // tensor memory: accumulators (gate, up or y: 64 columns each), then the
+    // two A buffers (MATS tiles of 32 columns each)
+    constexpr uint32_t kCols = GATEUP ? 256 : 128;
+    constexpr uint32_t kAcol = MATS * kN;
+    if ((tid >> 5) == 0) tc::tmem_alloc(tslot, kCols);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -285,23 +287,24 @@ __global__ void __launch_bounds__(GATEUP ? 512 : 256, 1) expert_tc_kernel(StepAr
     for (int i = 0; i < S - 1; ++i) issue(i);
 
     const uint32_t idesc = tc::idesc_f16_f32(kM, kN);
-    // matrix descriptors of the two A tile sets and of the first ring stage
-    // (a K step of 16 inputs adds 32 bytes, 2 in the start field)
-    const uint64_t descA0 = tc::smem_desc_sw128(tc::smem_u32(Abuf), kSbo);
+    // matrix descriptor of the first ring stage's B tile (a K step of 16 inputs
+    // adds 32 bytes, 2 in the start field)
     const uint64_t descB0 = tc::smem_desc_sw128(tc::smem_u32(ring), kSbo);
+    // dequantisation: warp -> (lane quadrant q, matrix m, half of the row's 8
+    // pieces); lane -> row 32 q + lane, the tensor-memory lane of that row
+    const int warp = tid >> 5, lane = tid & 31;
+    const int dq_m = (warp >> 2) % MATS, dq_half = warp / (4 * MATS);
+    const int dq_rr = 32 * (warp & 3) + lane;
+    const uint32_t dq_lane = (uint32_t)(32 * (warp & 3)) << 16;
     int issued = -1;  // the last chunk whose MMAs were committed
     for (int idx = 0; idx < total; ++idx) {
         const int bsel = idx & 1, c = idx % nchunks, blk = (int)blockIdx.z + (idx / nchunks) * (int)gridDim.z;
         const unsigned char *st = ring + (idx % S) * stage_stride;
         tc::cp_async_wait<S - 2>();
         __syncthreads();
-        // dequantisation: thread -> (matrix, row, half of the 8 pieces); 8
-        // consecutive threads take 8 consecutive rows of one half
-        unsigned char *A = Abuf + bsel * MATS * kTileA;
+        // dequantise this thread's 32 inputs into its lane of A buffer bsel
         {
-            const int p = tid;
-            const int m = p / (kM * 2), w = p % (kM * 2);
-            const int rr = (w & 7) | ((w >> 4) << 3), half = (w >> 3) & 1;
+            const int m = dq_m, rr = dq_rr, half = dq_half;
             const uint32_t *scw = reinterpret_cast<const uint32_t *>(st + off_sc) + (m * kM + rr) * 2;
             const int sh = (c & 1) * 16;
             float s = bf16f((uint16_t)(scw[0] >> sh)), b = bf16f((uint16_t)(scw[1] >> sh));
@@ -312,7 +315,7 @@ __global__ void __launch_bounds__(GATEUP ? 512 : 256, 1) expert_tc_kernel(StepAr
             }
             const __half2 s2 = __floats2half2_rn(s, s), b2 = __floats2half2_rn(b, b);
             const unsigned char *cr = st + off_codes + (m * kM + rr) * cb;
-            unsigned char *At = A + m * kTileA;
+            uint32_t o[16];
             if (six) {
                 uint32_t v[12];
 #pragma unroll
@@ -321,37 +324,37 @@ __global__ void __launch_bounds__(GATEUP ? 512 : 256, 1) expert_tc_kernel(StepAr
                     v[4 * i] = t4.x; v[4 * i + 1] = t4.y; v[4 * i + 2] = t4.z; v[4 * i + 3] = t4.w;
                 }
                 // compile-time core indices keep v[] in registers
-                if (half) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        *reinterpret_cast<uint4 *>(At + core_off(rr, 4 + j)) = deq_6bit(v, 4 + j, s2, b2);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        *reinterpret_cast<uint4 *>(At + core_off(rr, j)) = deq_6bit(v, j, s2, b2);
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 r4 = half ? deq_6bit(v, 4 + j, s2, b2) : deq_6bit(v, j, s2, b2);
+                    o[4 * j] = r4.x; o[4 * j + 1] = r4.y; o[4 * j + 2] = r4.z; o[4 * j + 3] = r4.w;
                 }
             } else {
                 const uint4 w4 = *reinterpret_cast<const uint4 *>(cr + 16 * (half ^ code_swz(rr)));
                 const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<uint4 *>(At + core_off(rr, 4 * half + j)) = deq_word(wv[j], s2, b2);
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 r4 = deq_word(wv[j], s2, b2);
+                    o[4 * j] = r4.x; o[4 * j + 1] = r4.y; o[4 * j + 2] = r4.z; o[4 * j + 3] = r4.w;
+                }
             }
+            // two f16 per 32-bit column in the stored input order
+            tc::st_32x32b_x16(tmem + dq_lane + kAcol + (uint32_t)((bsel * MATS + m) * 32 + half * 16), o);
         }
-        tc::fence_async_shared();
+        tc::fence_before_sync();
         __syncthreads();
         if ((tid >> 5) == 0) {
             // warp 0 forms the descriptors (warp-uniform), one elected lane issues
             const uint64_t bd0 = descB0 + (uint64_t)(((idx % S) * stage_stride) >> 4);
-            const uint64_t ad0 = descA0 + (uint64_t)((bsel * MATS * kTileA) >> 4);
+            const uint32_t a0 = tmem + kAcol + (uint32_t)(bsel * MATS * 32);
             if (tc::elect_one()) {
                 tc::fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < kK / 16; ++ks) {
 #pragma unroll
                     for (int m = 0; m < MATS; ++m)
-                        tc::mma_f16(tmem + m * kN, ad0 + (uint64_t)((m * kTileA + ks * 32) >> 4), bd0 + 2 * ks,
-                                    idesc, (c > 0 || ks > 0) ? 1u : 0u);
+                        tc::mma_f16_ts(tmem + m * kN, a0 + (uint32_t)(m * 32 + ks * 8), bd0 + 2 * ks, idesc,
+                                       (c > 0 || ks > 0) ? 1u : 0u);
                 }
                 tc::commit(&bar[bsel]);
             }
@@ -367,7 +370,6 @@ __global__ void __launch_bounds__(GATEUP ? 512 : 256, 1) expert_tc_kernel(StepAr
             // epilogue of this token block, once its last MMAs have completed
             if (!wait_bar(&bar[bsel], (uint32_t)((idx >> 1) & 1), ws.status)) *abort_flag = 1;
             tc::fence_after_sync();
-            const int warp = tid >> 5, lane = tid & 31;
             const int rr = 32 * (warp & 3) + lane;          // this thread's TMEM lane = weight row
             constexpr int kTokW = kN / (kThr / 128);         // tokens per warp (32 or 16)
             const int t0 = kTokW * (warp >> 2);              // tokens [t0, t0 + kTokW) of the block
@@ -410,17 +412,17 @@ __global__ void __launch_bounds__(GATEUP ? 512 : 256, 1) expert_tc_kernel(StepAr
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    if ((tid >> 5) == 0) tc::tmem_dealloc(tmem, GATEUP ? 128 : 64);
+    if ((tid >> 5) == 0) tc::tmem_dealloc(tmem, kCols);
 }
 
-// ring stages per variant (shared memory: S stages + two A tiles)
-constexpr int kStagesGateUp = 6;   // 6 x 18 KB + 64 KB
-constexpr int kStagesDown = 6;     // 6 x 13-15 KB + 32 KB
+// ring stages per variant (the ring is all of the shared memory)
+constexpr int kStagesGateUp = 8;   // 8 x 18 KB
+constexpr int kStagesDown = 8;     // 8 x 13 KB (two CTAs per SM) or 15 KB (6-bit)
 
 size_t tc_smem_bytes(bool gateup, int cb) {
     const int mats = gateup ? 2 : 1;
     const int S = gateup ? kStagesGateUp : kStagesDown;
-    return 1024 + (size_t)S * stage_bytes_of(mats, cb) + 2 * mats * kTileA + 64;
+    return 1024 + (size_t)S * stage_bytes_of(mats, cb) + 64;
 }
 
 }  // namespace
