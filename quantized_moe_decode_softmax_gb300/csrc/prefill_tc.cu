@@ -170,24 +170,50 @@ __global__ void x_to_f16_kernel(StepArgs a, Workspace ws) {
 }
 
 // ---- the GEMMs -------------------------------------------------------------------
-// Ring stage layout (bytes): [B tile 8 KB][codes: MATS x 128 rows x cb][scale
-// and bias words: MATS x 128 rows x 2 x 4 B]. Codes of 4-bit rows are two
-// 16-byte halves, swapped on rows 4..7 of every 8 (no shared-memory bank
-// conflicts when 8 consecutive rows read the same half).
-__host__ __device__ constexpr int stage_bytes_of(int mats, int cb) {
-    return (kTileB + mats * kM * cb + mats * kM * 8 + 1023) & ~1023;
+// Warp roles (MATS = 2 for gate/up, 1 for down):
+//   - MATS x 8 dequantisation warps: thread (lane quadrant q, matrix m, half of
+//     the 8 pieces) owns weight row 32 q + lane of matrix m -- the tensor-memory
+//     lane of that row. It copies its own codes and scale/bias words S - 1
+//     chunks ahead (cp.async, its own wait groups: nobody else reads them),
+//     dequantises into A buffer (chunk % 3) once the MMAs of chunk - 3 are done,
+//     and arrives on a_full. After the last chunk of a token block the same
+//     warps run the epilogue.
+//   - four producer warps, one per SM sub-partition (a single one held up the
+//     dequantisation warps of its sub-partition behind its copies), copy the B
+//     tiles (64 tokens x 64 inputs, f16) into the ring, each lane arriving on
+//     b_full when its copies have landed.
+//   - one MMA warp waits for a_full and b_full, and one elected lane issues the
+//     chunk's MMAs and commits them to mma_done (A buffer free), b_empty (ring
+//     stage free) and, after a block's last chunk, acc_full.
+// Every wait gives up after 1 s: it reports a timeout and sets the CTA's abort
+// flag, which every role checks once per chunk.
+//
+// Ring stage layout (bytes): [B tile 8 KB][codes: one slot of cb bytes per
+// dequantisation thread][scale and bias words: 8 bytes per thread].
+__host__ __device__ constexpr int stage_bytes_of(int dq_threads, int cb) {
+    return (kTileB + dq_threads * cb + dq_threads * 8 + 1023) & ~1023;
 }
 
-__host__ __device__ constexpr int code_swz(int rr) { return (rr >> 2) & 1; }
+__device__ __forceinline__ void bar_init(uint64_t *bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(tc::smem_u32(bar)), "r"(count) : "memory");
+}
 
-// GATEUP: gate and up rows (two A tiles, two accumulators), x as B, epilogue
-// h = act(g, u) written as f16; else the down projection: Wd rows, h as B,
-// epilogue y (f32). S: ring stages. One dequantisation item (matrix, row, half
-// of the row's 8 pieces) per thread: 512 threads for gate/up, 256 for down.
+__device__ __forceinline__ void bar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
+}
+
+// arrive on the mbarrier once every earlier cp.async of this thread has landed
+// (the barrier's count includes this arrival)
+__device__ __forceinline__ void bar_arrive_cp_async(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
+}
+
 template <bool GATEUP, int S>
-__global__ void __launch_bounds__(GATEUP ? 512 : 256, 1) expert_tc_kernel(StepArgs a, Workspace ws, int thr) {
+__global__ void __launch_bounds__(GATEUP ? 672 : 416, 1) expert_tc_kernel(StepArgs a, Workspace ws, int thr) {
     constexpr int MATS = GATEUP ? 2 : 1;
-    constexpr int kThr = MATS * 256;
+    constexpr int kDq = MATS * 256;            // dequantisation threads
+    constexpr int kProdW = kDq / 32;           // first of the four producer warps
+    constexpr int kMmaW = kProdW + 4;          // MMA warp
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                             ~static_cast<uintptr_t>(1023));
@@ -205,148 +231,96 @@ __global__ void __launch_bounds__(GATEUP ? 512 : 256, 1) expert_tc_kernel(StepAr
     const int D = a.s.D, F = a.s.F;
     const int K = GATEUP ? D : F;            // reduction length
     const int nchunks = K / kK;
+    const int total = my_blocks * nchunks;
     const int r0 = blockIdx.x * kM;          // first weight row (gate/up: f; down: d)
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool six = !GATEUP && a.s.down_bits == 6;
-    const int cb = six ? 48 : 32;            // code bytes per row and chunk
-    const int stage_stride = stage_bytes_of(MATS, cb);
-    const int off_codes = kTileB, off_sc = kTileB + MATS * kM * cb;
+    const int cb = six ? 48 : 16;            // code bytes per dequantisation thread and chunk
+    const int stage_stride = stage_bytes_of(kDq, cb);
+    const int off_codes = kTileB, off_sc = kTileB + kDq * cb;
 
     unsigned char *ring = base;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(base + S * stage_stride);  // [2]
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 2);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(base + S * stage_stride);
+    constexpr int NA = 3;                      // A buffers in tensor memory
+    uint64_t *a_full = bars, *mma_done = bars + NA, *b_full = bars + 2 * NA, *b_empty = b_full + S;
+    uint64_t *acc_full = b_empty + S, *acc_empty = acc_full + 1;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(acc_empty + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
 
+    // tensor memory: accumulators (gate, up or y: 64 columns each), then the
+    // NA A buffers (MATS tiles of 32 columns each)
+    constexpr uint32_t kCols = GATEUP ? 512 : 256;
+    constexpr uint32_t kAcol = MATS * kN;
     if (tid == 0) {
         *abort_flag = 0;
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc::smem_u32(&bar[0])) : "memory");
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc::smem_u32(&bar[1])) : "memory");
+        for (int i = 0; i < NA; ++i) {
+            bar_init(&a_full[i], kDq);
+            bar_init(&mma_done[i], 1);
+        }
+        for (int i = 0; i < S; ++i) {
+            bar_init(&b_full[i], 128);
+            bar_init(&b_empty[i], 1);
+        }
+        bar_init(acc_full, 1);
+        bar_init(acc_empty, kDq);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    // tensor memory: accumulators (gate, up or y: 64 columns each), then the
-    // two A buffers (MATS tiles of 32 columns each)
-    constexpr uint32_t kCols = GATEUP ? 256 : 128;
-    constexpr uint32_t kAcol = MATS * kN;
-    if ((tid >> 5) == 0) tc::tmem_alloc(tslot, kCols);
+    if (warp == 0) tc::tmem_alloc(tslot, kCols);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tslot;
 
-    const uint32_t *q0 = GATEUP ? a.planes.gate_q : a.planes.down_q;
-    const uint16_t *s0 = GATEUP ? a.planes.gate_s : a.planes.down_s;
-    const uint16_t *b0 = GATEUP ? a.planes.gate_b : a.planes.down_b;
-    const size_t rows_per_e = GATEUP ? (size_t)F : (size_t)D;
-    const size_t groups = (size_t)K / 64;    // scale/bias entries per row (even: K % 128 == 0)
-    // B rows: x in f16 (y area, n x D) or h in f16 (first half of each h row)
-    const uint16_t *xb = reinterpret_cast<const uint16_t *>(ws.y);
-    const uint16_t *hb = reinterpret_cast<const uint16_t *>(ws.h);
-
-    const int total = my_blocks * nchunks;
-    // fill ring stage idx % S with chunk idx (token block, chunk) -- or, past
-    // the end, commit an empty group so the wait counts stay uniform
-    auto issue = [&](int idx) {
-        if (idx < total) {
-            const int blk = (int)blockIdx.z + (idx / nchunks) * (int)gridDim.z, c = idx % nchunks;
-            unsigned char *st = ring + (idx % S) * stage_stride;
-            // B: 64 tokens x 8 cores of 16 bytes (tokens past the expert's count
-            // are not copied: their accumulator columns are never read)
-            for (int p = tid; p < kN * 8; p += kThr) {
-                const int t = p >> 3, j = p & 7, jj = blk * kN + t;
-                if (jj >= cnt_e) continue;
-                const uint16_t *src = GATEUP ? xb + (size_t)ws.slot_token[off_e + jj] * D
-                                             : hb + (size_t)(off_e + jj) * F * 2;
-                tc::cp_async16(st + core_off(t, j), src + (size_t)c * kK + 8 * j);
-            }
-            // codes: MATS x 128 rows x cb bytes
-            const int pr = cb / 16;
-            for (int p = tid; p < MATS * kM * pr; p += kThr) {
-                const int m = p / (kM * pr), rr = (p / pr) % kM, h = p % pr;
-                const size_t row = (size_t)e * rows_per_e + r0 + rr;
-                const unsigned char *src;
-                if (six) {
-                    src = reinterpret_cast<const unsigned char *>(a.planes.down_q) + row * ((size_t)K * 3 / 4) +
-                          (size_t)c * 48 + h * 16;
-                } else {
-                    const uint32_t *qq = (GATEUP && m) ? a.planes.up_q : q0;
-                    src = reinterpret_cast<const unsigned char *>(qq + row * ((size_t)K / 8) + (size_t)c * 8) + h * 16;
+    if (warp >= kProdW && warp < kMmaW) {
+        // ---- producers: B tiles -----------------------------------------------
+        // B rows: x in f16 (y area, n x D) or h in f16 (first half of each h row)
+        // producer warp pw, lane -> 16-byte piece j of tokens 16 pw + tq + 4 i;
+        // the tokens' row offsets (f16 elements, below 2^31 for every allowed
+        // shape: n D <= 8192 x 16384, n k x 2 Dff <= 131072 x 16384) are looked
+        // up once per block
+        const uint16_t *bsrc = reinterpret_cast<const uint16_t *>(GATEUP ? (const void *)ws.y : (const void *)ws.h);
+        const int j = lane & 7, tq = 16 * (warp - kProdW) + (lane >> 3);
+        uint32_t roff[kN / 16];
+        for (int idx = 0; idx < total; ++idx) {
+            const int sidx = idx % S, blk = (int)blockIdx.z + (idx / nchunks) * (int)gridDim.z, c = idx % nchunks;
+            if (c == 0) {
+#pragma unroll
+                for (int i = 0; i < kN / 16; ++i) {
+                    const int jj = blk * kN + tq + 4 * i;
+                    // tokens past the expert's count are not copied: their
+                    // accumulator columns are never read
+                    roff[i] = jj >= cnt_e ? 0xFFFFFFFFu
+                              : GATEUP    ? (uint32_t)ws.slot_token[off_e + jj] * (uint32_t)D
+                                          : (uint32_t)(off_e + jj) * (uint32_t)(2 * F);
                 }
-                const int hd = six ? h : (h ^ code_swz(rr));
-                tc::cp_async16(st + off_codes + (m * kM + rr) * cb + hd * 16, src);
             }
-            // scale and bias: the 4-byte word holding entry (row, c) of each
-            for (int p = tid; p < MATS * kM * 2; p += kThr) {
-                const int m = p / (kM * 2), rr = (p >> 1) % kM, arr = p & 1;
-                const size_t gi = ((size_t)e * rows_per_e + r0 + rr) * groups + c;
-                const uint16_t *sp = (GATEUP && m) ? (arr ? a.planes.up_b : a.planes.up_s) : (arr ? b0 : s0);
-                tc::cp_async4(st + off_sc + ((m * kM + rr) * 2 + arr) * 4, sp + (gi & ~(size_t)1));
-            }
+            if (idx >= S && !wait_bar(&b_empty[sidx], (uint32_t)((idx / S - 1) & 1), ws.status)) *abort_flag = 1;
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;  // warp-uniform
+            unsigned char *st = ring + sidx * stage_stride;
+            const uint16_t *src = bsrc + (size_t)c * kK + 8 * j;
+#pragma unroll
+            for (int i = 0; i < kN / 16; ++i)
+                if (roff[i] != 0xFFFFFFFFu) tc::cp_async16(st + core_off(tq + 4 * i, j), src + roff[i]);
+            bar_arrive_cp_async(&b_full[sidx]);
         }
-        tc::cp_async_commit();
-    };
-    for (int i = 0; i < S - 1; ++i) issue(i);
-
-    const uint32_t idesc = tc::idesc_f16_f32(kM, kN);
-    // matrix descriptor of the first ring stage's B tile (a K step of 16 inputs
-    // adds 32 bytes, 2 in the start field)
-    const uint64_t descB0 = tc::smem_desc_sw128(tc::smem_u32(ring), kSbo);
-    // dequantisation: warp -> (lane quadrant q, matrix m, half of the row's 8
-    // pieces); lane -> row 32 q + lane, the tensor-memory lane of that row
-    const int warp = tid >> 5, lane = tid & 31;
-    const int dq_m = (warp >> 2) % MATS, dq_half = warp / (4 * MATS);
-    const int dq_rr = 32 * (warp & 3) + lane;
-    const uint32_t dq_lane = (uint32_t)(32 * (warp & 3)) << 16;
-    int issued = -1;  // the last chunk whose MMAs were committed
-    for (int idx = 0; idx < total; ++idx) {
-        const int bsel = idx & 1, c = idx % nchunks, blk = (int)blockIdx.z + (idx / nchunks) * (int)gridDim.z;
-        const unsigned char *st = ring + (idx % S) * stage_stride;
-        tc::cp_async_wait<S - 2>();
-        __syncthreads();
-        // dequantise this thread's 32 inputs into its lane of A buffer bsel
-        {
-            const int m = dq_m, rr = dq_rr, half = dq_half;
-            const uint32_t *scw = reinterpret_cast<const uint32_t *>(st + off_sc) + (m * kM + rr) * 2;
-            const int sh = (c & 1) * 16;
-            float s = bf16f((uint16_t)(scw[0] >> sh)), b = bf16f((uint16_t)(scw[1] >> sh));
-            if (fabsf(s) > 65504.0f || fabsf(b) > 65504.0f) {  // beyond f16: saturate, report
-                report_error(ws.status, kDevErrRange);
-                s = fminf(fmaxf(s, -65504.0f), 65504.0f);
-                b = fminf(fmaxf(b, -65504.0f), 65504.0f);
-            }
-            const __half2 s2 = __floats2half2_rn(s, s), b2 = __floats2half2_rn(b, b);
-            const unsigned char *cr = st + off_codes + (m * kM + rr) * cb;
-            uint32_t o[16];
-            if (six) {
-                uint32_t v[12];
-#pragma unroll
-                for (int i = 0; i < 3; ++i) {
-                    const uint4 t4 = *reinterpret_cast<const uint4 *>(cr + 16 * i);
-                    v[4 * i] = t4.x; v[4 * i + 1] = t4.y; v[4 * i + 2] = t4.z; v[4 * i + 3] = t4.w;
-                }
-                // compile-time core indices keep v[] in registers
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint4 r4 = half ? deq_6bit(v, 4 + j, s2, b2) : deq_6bit(v, j, s2, b2);
-                    o[4 * j] = r4.x; o[4 * j + 1] = r4.y; o[4 * j + 2] = r4.z; o[4 * j + 3] = r4.w;
-                }
-            } else {
-                const uint4 w4 = *reinterpret_cast<const uint4 *>(cr + 16 * (half ^ code_swz(rr)));
-                const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint4 r4 = deq_word(wv[j], s2, b2);
-                    o[4 * j] = r4.x; o[4 * j + 1] = r4.y; o[4 * j + 2] = r4.z; o[4 * j + 3] = r4.w;
-                }
-            }
-            // two f16 per 32-bit column in the stored input order
-            tc::st_32x32b_x16(tmem + dq_lane + kAcol + (uint32_t)((bsel * MATS + m) * 32 + half * 16), o);
-        }
-        tc::fence_before_sync();
-        __syncthreads();
-        if ((tid >> 5) == 0) {
-            // warp 0 forms the descriptors (warp-uniform), one elected lane issues
-            const uint64_t bd0 = descB0 + (uint64_t)(((idx % S) * stage_stride) >> 4);
+    } else if (warp == kMmaW) {
+        // ---- MMA issue --------------------------------------------------------
+        const uint32_t idesc = tc::idesc_f16_f32(kM, kN);
+        // matrix descriptor of the first ring stage's B tile (a K step of 16
+        // inputs adds 32 bytes, 2 in the start field)
+        const uint64_t descB0 = tc::smem_desc_sw128(tc::smem_u32(ring), kSbo);
+        int issued = -1;
+        for (int idx = 0; idx < total; ++idx) {
+            const int bsel = idx % NA, sidx = idx % S, c = idx % nchunks, bi = idx / nchunks;
+            bool ok = wait_bar(&a_full[bsel], (uint32_t)((idx / NA) & 1), ws.status);
+            ok = ok && wait_bar(&b_full[sidx], (uint32_t)((idx / S) & 1), ws.status);
+            // a block's first MMAs overwrite the accumulators of the one before
+            if (ok && c == 0 && bi > 0) ok = wait_bar(acc_empty, (uint32_t)((bi - 1) & 1), ws.status);
+            if (!ok) *abort_flag = 1;
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;  // warp-uniform
+            const uint64_t bd0 = descB0 + (uint64_t)((sidx * stage_stride) >> 4);
             const uint32_t a0 = tmem + kAcol + (uint32_t)(bsel * MATS * 32);
+            __syncwarp();
             if (tc::elect_one()) {
                 tc::fence_after_sync();
 #pragma unroll
@@ -356,73 +330,163 @@ __global__ void __launch_bounds__(GATEUP ? 512 : 256, 1) expert_tc_kernel(StepAr
                         tc::mma_f16_ts(tmem + m * kN, a0 + (uint32_t)(m * 32 + ks * 8), bd0 + 2 * ks, idesc,
                                        (c > 0 || ks > 0) ? 1u : 0u);
                 }
-                tc::commit(&bar[bsel]);
+                tc::commit(&mma_done[bsel]);
+                tc::commit(&b_empty[sidx]);
+                if (c == nchunks - 1) tc::commit(acc_full);
             }
             __syncwarp();
+            issued = idx;
         }
-        issued = idx;
-        // the MMAs of chunk idx - 1 have read their A tile and ring stage: the
-        // stage takes chunk idx + S - 1, the A tile chunk idx + 1
-        if (idx >= 1 && !wait_bar(&bar[(idx - 1) & 1], (uint32_t)(((idx - 1) >> 1) & 1), ws.status))
-            *abort_flag = 1;
-        issue(idx + S - 1);
-        if (c == nchunks - 1) {
-            // epilogue of this token block, once its last MMAs have completed
-            if (!wait_bar(&bar[bsel], (uint32_t)((idx >> 1) & 1), ws.status)) *abort_flag = 1;
-            tc::fence_after_sync();
-            const int rr = 32 * (warp & 3) + lane;          // this thread's TMEM lane = weight row
-            constexpr int kTokW = kN / (kThr / 128);         // tokens per warp (32 or 16)
-            const int t0 = kTokW * (warp >> 2);              // tokens [t0, t0 + kTokW) of the block
-            const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-            const int r = r0 + rr;
+        // after an abort: wait (bounded) for the MMAs still in flight before
+        // the tensor memory is freed
+        if (*abort_flag && issued >= 0)
+            wait_bar(&mma_done[issued % NA], (uint32_t)((issued / NA) & 1), ws.status);
+    } else {
+        // ---- dequantisation and epilogue ------------------------------------
+        const int m = (warp >> 2) % MATS, half = warp / (4 * MATS);
+        const int rr = 32 * (warp & 3) + lane;
+        const uint32_t tlane = (uint32_t)(32 * (warp & 3)) << 16;
+        const size_t row = (size_t)e * (GATEUP ? F : D) + r0 + rr;
+        const size_t groups = (size_t)K / 64;   // scale/bias entries per row (even: K % 128 == 0)
+        const uint16_t *srow = (GATEUP ? (m ? a.planes.up_s : a.planes.gate_s) : a.planes.down_s) + row * groups;
+        const uint16_t *brow = (GATEUP ? (m ? a.planes.up_b : a.planes.gate_b) : a.planes.down_b) + row * groups;
+        const unsigned char *qrow;
+        if (six)
+            qrow = reinterpret_cast<const unsigned char *>(a.planes.down_q) + row * ((size_t)K * 3 / 4);
+        else
+            qrow = reinterpret_cast<const unsigned char *>((GATEUP ? (m ? a.planes.up_q : a.planes.gate_q)
+                                                                   : a.planes.down_q) +
+                                                           row * ((size_t)K / 8)) + half * 16;
+        // this thread's codes (16 bytes: its half of the 4-bit row chunk; 6-bit:
+        // the whole 48-byte chunk) and, on even chunks, the 4-byte words holding
+        // the scale and bias of this chunk and the next
+        auto issue_own = [&](int idx) {
+            if (idx < total) {
+                const int c = idx % nchunks;
+                unsigned char *st = ring + (idx % S) * stage_stride;
+                if (six) {
 #pragma unroll
-            for (int half = 0; half < kTokW / 16; ++half) {
-                const int tc0 = t0 + 16 * half;
-                float g[16];
-                tc::ld_32x32b_x16(ta + tc0, g);
-                if (GATEUP) {
-                    float uu[16];
-                    tc::ld_32x32b_x16(ta + kN + tc0, uu);
-                    // h row of the slot, f16 in the core order, in the first half of the f32 row
-                    const int pos = (r & ~7) | core_pos(r & 7);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int j = blk * kN + tc0 + i;
-                        if (j < cnt_e)
-                            reinterpret_cast<__half *>(ws.h + (size_t)(off_e + j) * F)[pos] =
-                                sat_h(glu_act<true>(a.s.act, a.s.act_limit, g[i], uu[i]), ws.status);
-                    }
+                    for (int i = 0; i < 3; ++i)
+                        tc::cp_async16(st + off_codes + tid * 48 + 16 * i, qrow + (size_t)c * 48 + 16 * i);
                 } else {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int j = blk * kN + tc0 + i;
-                        if (j < cnt_e) ws.y[(size_t)(off_e + j) * D + r] = g[i];
-                    }
+                    tc::cp_async16(st + off_codes + tid * 16, qrow + (size_t)c * 32);
+                }
+                if ((c & 1) == 0) {
+                    tc::cp_async4(st + off_sc + tid * 8, srow + c);
+                    tc::cp_async4(st + off_sc + tid * 8 + 4, brow + c);
                 }
             }
+            tc::cp_async_commit();
+        };
+        for (int i = 0; i < S - 1; ++i) issue_own(i);
+        for (int idx = 0; idx < total; ++idx) {
+            const int bsel = idx % NA, c = idx % nchunks, bi = idx / nchunks;
+            const int blk = (int)blockIdx.z + bi * (int)gridDim.z;
+            const unsigned char *st = ring + (idx % S) * stage_stride;
+            tc::cp_async_wait<S - 2>();
+            // A buffer bsel is free once the MMAs of chunk idx - NA are done
+            if (idx >= NA && !wait_bar(&mma_done[bsel], (uint32_t)((idx / NA - 1) & 1), ws.status))
+                *abort_flag = 1;
+            // warp-uniform: tcgen05.st and tcgen05.ld below are warp-collective
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+            {
+                // scale/bias words: in the stage of the even chunk of the pair
+                // (read before that stage is refilled below)
+                const uint32_t *scw = reinterpret_cast<const uint32_t *>(
+                    ring + ((idx & ~1) % S) * stage_stride + off_sc + tid * 8);
+                const int sh = (c & 1) * 16;
+                float s = bf16f((uint16_t)(scw[0] >> sh)), b = bf16f((uint16_t)(scw[1] >> sh));
+                if (fabsf(s) > 65504.0f || fabsf(b) > 65504.0f) {  // beyond f16: saturate, report
+                    report_error(ws.status, kDevErrRange);
+                    s = fminf(fmaxf(s, -65504.0f), 65504.0f);
+                    b = fminf(fmaxf(b, -65504.0f), 65504.0f);
+                }
+                const __half2 s2 = __floats2half2_rn(s, s), b2 = __floats2half2_rn(b, b);
+                uint32_t o[16];
+                if (six) {
+                    const unsigned char *cr = st + off_codes + tid * 48;
+                    uint32_t v[12];
+#pragma unroll
+                    for (int i = 0; i < 3; ++i) {
+                        const uint4 t4 = *reinterpret_cast<const uint4 *>(cr + 16 * i);
+                        v[4 * i] = t4.x; v[4 * i + 1] = t4.y; v[4 * i + 2] = t4.z; v[4 * i + 3] = t4.w;
+                    }
+                    // compile-time piece indices keep v[] in registers
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint4 r4 = half ? deq_6bit(v, 4 + j, s2, b2) : deq_6bit(v, j, s2, b2);
+                        o[4 * j] = r4.x; o[4 * j + 1] = r4.y; o[4 * j + 2] = r4.z; o[4 * j + 3] = r4.w;
+                    }
+                } else {
+                    const uint4 w4 = *reinterpret_cast<const uint4 *>(st + off_codes + tid * 16);
+                    const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint4 r4 = deq_word(wv[j], s2, b2);
+                        o[4 * j] = r4.x; o[4 * j + 1] = r4.y; o[4 * j + 2] = r4.z; o[4 * j + 3] = r4.w;
+                    }
+                }
+                // two f16 per 32-bit column in the stored input order
+                tc::st_32x32b_x16_async(tmem + tlane + kAcol + (uint32_t)((bsel * MATS + m) * 32 + half * 16), o);
+            }
+            // this thread read its slot of chunk idx - 1 last iteration: refill it
+            // (while the tensor-memory stores complete)
+            issue_own(idx + S - 1);
+            tc::wait_st();
             tc::fence_before_sync();
+            bar_arrive(&a_full[bsel]);
+            if (c == nchunks - 1) {
+                // epilogue of this token block, once its last MMAs have completed
+                if (!wait_bar(acc_full, (uint32_t)(bi & 1), ws.status)) *abort_flag = 1;
+                tc::fence_after_sync();
+                constexpr int kTokW = kN / (kDq / 128);          // tokens per warp (16 or 32)
+                const int t0 = kTokW * (warp >> 2);               // tokens [t0, t0 + kTokW) of the block
+                const int r = r0 + rr;
+#pragma unroll
+                for (int hh = 0; hh < kTokW / 16; ++hh) {
+                    const int tc0 = t0 + 16 * hh;
+                    float g[16];
+                    tc::ld_32x32b_x16(tmem + tlane + tc0, g);
+                    if (GATEUP) {
+                        float uu[16];
+                        tc::ld_32x32b_x16(tmem + tlane + kN + tc0, uu);
+                        // h row of the slot, f16 in the core order, in the first half of the f32 row
+                        const int pos = (r & ~7) | core_pos(r & 7);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int j = blk * kN + tc0 + i;
+                            if (j < cnt_e)
+                                reinterpret_cast<__half *>(ws.h + (size_t)(off_e + j) * F)[pos] =
+                                    sat_h(glu_act<true>(a.s.act, a.s.act_limit, g[i], uu[i]), ws.status);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int j = blk * kN + tc0 + i;
+                            if (j < cnt_e) ws.y[(size_t)(off_e + j) * D + r] = g[i];
+                        }
+                    }
+                }
+                tc::fence_before_sync();
+                bar_arrive(acc_empty);
+            }
         }
-        __syncthreads();  // abort flag; the next block's MMAs overwrite the accumulators
-        if (*abort_flag) break;
     }
-    // after a timeout: wait (bounded) for the MMAs still in flight before the
-    // tensor memory is freed
-    if (*abort_flag && issued >= 0) wait_bar(&bar[issued & 1], (uint32_t)((issued >> 1) & 1), ws.status);
     tc::cp_async_wait<0>();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    if ((tid >> 5) == 0) tc::tmem_dealloc(tmem, kCols);
+    if (warp == 0) tc::tmem_dealloc(tmem, kCols);
 }
 
 // ring stages per variant (the ring is all of the shared memory)
-constexpr int kStagesGateUp = 8;   // 8 x 18 KB
-constexpr int kStagesDown = 8;     // 8 x 13 KB (two CTAs per SM) or 15 KB (6-bit)
+constexpr int kStagesGateUp = 8;   // 8 x 20 KB
+constexpr int kStagesDown = 7;     // 7 x 14 KB (two CTAs per SM) or 7 x 22 KB (6-bit)
 
-size_t tc_smem_bytes(bool gateup, int cb) {
-    const int mats = gateup ? 2 : 1;
+size_t tc_smem_bytes(bool gateup, int six) {
+    const int dq = gateup ? 512 : 256;
     const int S = gateup ? kStagesGateUp : kStagesDown;
-    return 1024 + (size_t)S * stage_bytes_of(mats, cb) + 64;
+    return 1024 + (size_t)S * stage_bytes_of(dq, six ? 48 : 16) + (6 + 2 * S + 2) * 8 + 16;
 }
 
 }  // namespace
@@ -443,8 +507,7 @@ cudaError_t launch_expert_tc(const StepArgs &a, const Workspace &ws, int thr, bo
         launched += 1;
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
-    const int cb = (down && a.s.down_bits == 6) ? 48 : 32;
-    const size_t smem = tc_smem_bytes(!down, cb);
+    const size_t smem = tc_smem_bytes(!down, down && a.s.down_bits == 6);
     const void *k = down ? (const void *)expert_tc_kernel<false, kStagesDown>
                          : (const void *)expert_tc_kernel<true, kStagesGateUp>;
     if ((err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
@@ -455,9 +518,9 @@ cudaError_t launch_expert_tc(const StepArgs &a, const Workspace &ws, int thr, bo
     const long mean = ((long)a.s.n * a.s.k + maxU - 1) / maxU;
     const int zb = (int)max(1L, min(8L, (3 * mean / 2 + kN - 1) / kN));
     if (!down)
-        expert_tc_kernel<true, kStagesGateUp><<<dim3(a.s.F / kM, maxU, zb), 512, smem, st>>>(a, ws, thr);
+        expert_tc_kernel<true, kStagesGateUp><<<dim3(a.s.F / kM, maxU, zb), 672, smem, st>>>(a, ws, thr);
     else
-        expert_tc_kernel<false, kStagesDown><<<dim3(a.s.D / kM, maxU, zb), 256, smem, st>>>(a, ws, thr);
+        expert_tc_kernel<false, kStagesDown><<<dim3(a.s.D / kM, maxU, zb), 416, smem, st>>>(a, ws, thr);
     launched += 1;
     return cudaGetLastError();
 }
