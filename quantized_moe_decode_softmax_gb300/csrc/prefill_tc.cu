@@ -35,6 +35,7 @@
 // An operand beyond f16's range saturates and is reported (MOE_ERR_RANGE);
 // every mbarrier wait gives up after 1 s and reports a timeout.
 #include <cuda_fp16.h>
+#include <cudaTypedefs.h>
 
 #include "activation.cuh"
 #include "device_status.cuh"
@@ -173,26 +174,36 @@ __global__ void x_to_f16_kernel(StepArgs a, Workspace ws) {
 // Warp roles (MATS = 2 for gate/up, 1 for down):
 //   - MATS x 8 dequantisation warps: thread (lane quadrant q, matrix m, half of
 //     the 8 pieces) owns weight row 32 q + lane of matrix m -- the tensor-memory
-//     lane of that row. It copies its own codes and scale/bias words S - 1
-//     chunks ahead (cp.async, its own wait groups: nobody else reads them),
-//     dequantises into A buffer (chunk % 3) once the MMAs of chunk - 3 are done,
-//     and arrives on a_full. After the last chunk of a token block the same
-//     warps run the epilogue.
+//     lane of that row. It copies its own row's scales and biases, V groups at
+//     a time (V = 8, 4 or 2: the widest that divides the groups of a row), into
+//     a double-buffered slot of its own (cp.async, its own wait groups), reads
+//     its codes from the ring once c_full says the chunk's TMA box landed,
+//     arrives on c_empty, dequantises into A buffer (chunk % 3) once the MMAs of
+//     chunk - 3 are done, and arrives on a_full. After the last chunk of a
+//     token block the same warps run the epilogue.
 //   - four producer warps, one per SM sub-partition (a single one held up the
 //     dequantisation warps of its sub-partition behind its copies), copy the B
 //     tiles (64 tokens x 64 inputs, f16) into the ring, each lane arriving on
-//     b_full when its copies have landed.
+//     b_full when its copies have landed; lane 0 of the first also loads the
+//     chunk's codes (one TMA box of 128 rows per matrix, completing on c_full).
+//     A stage is refilled once its MMAs (b_empty) and its dequantisation
+//     (c_empty) are done.
 //   - one MMA warp waits for a_full and b_full, and one elected lane issues the
 //     chunk's MMAs and commits them to mma_done (A buffer free), b_empty (ring
 //     stage free) and, after a block's last chunk, acc_full.
 // Every wait gives up after 1 s: it reports a timeout and sets the CTA's abort
 // flag, which every role checks once per chunk.
 //
-// Ring stage layout (bytes): [B tile 8 KB][codes: one slot of cb bytes per
-// dequantisation thread][scale and bias words: 8 bytes per thread].
-__host__ __device__ constexpr int stage_bytes_of(int dq_threads, int cb) {
-    return (kTileB + dq_threads * cb + dq_threads * 8 + 1023) & ~1023;
+// Ring stage layout (bytes): [B tile 8 KB][codes: MATS x 128 rows x cbr bytes,
+// cbr = 32 (4-bit, 32-byte TMA swizzle: the 16-byte halves of rows 4..7 of
+// every 8 swap places, which spreads 8 consecutive rows reading the same half
+// over all banks) or 48 (6-bit, no swizzle)]. After the ring: the per-thread
+// scale slots, [2][dequantisation threads][16 bytes scales, 16 bytes biases].
+__host__ __device__ constexpr int stage_bytes_of(int mats, int cbr) {
+    return (kTileB + mats * kM * cbr + 1023) & ~1023;
 }
+
+__host__ __device__ constexpr int code_swz(int rr) { return (rr >> 2) & 1; }
 
 __device__ __forceinline__ void bar_init(uint64_t *bar, unsigned count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(tc::smem_u32(bar)), "r"(count) : "memory");
@@ -208,8 +219,12 @@ __device__ __forceinline__ void bar_arrive_cp_async(uint64_t *bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
 }
 
+// tm0, tm1: tensor maps of the code planes (gate and up, or down and unused),
+// 2-D {row bytes, rows} with boxes of {cbr, 128}
 template <bool GATEUP, int S>
-__global__ void __launch_bounds__(GATEUP ? 672 : 416, 1) expert_tc_kernel(StepArgs a, Workspace ws, int thr) {
+__global__ void __launch_bounds__(GATEUP ? 672 : 416, 1)
+    expert_tc_kernel(StepArgs a, Workspace ws, int thr, const __grid_constant__ CUtensorMap tm0,
+                     const __grid_constant__ CUtensorMap tm1) {
     constexpr int MATS = GATEUP ? 2 : 1;
     constexpr int kDq = MATS * 256;            // dequantisation threads
     constexpr int kProdW = kDq / 32;           // first of the four producer warps
@@ -235,15 +250,19 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, 1) expert_tc_kernel(StepAr
     const int r0 = blockIdx.x * kM;          // first weight row (gate/up: f; down: d)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool six = !GATEUP && a.s.down_bits == 6;
-    const int cb = six ? 48 : 16;            // code bytes per dequantisation thread and chunk
-    const int stage_stride = stage_bytes_of(kDq, cb);
-    const int off_codes = kTileB, off_sc = kTileB + kDq * cb;
+    const int cbr = six ? 48 : 32;           // code bytes per row and chunk
+    const int stage_stride = stage_bytes_of(MATS, cbr);
+    const int off_codes = kTileB;
+    const int groups = K / 64;               // scale/bias entries per row (even)
+    const int V = groups % 8 == 0 ? 8 : groups % 4 == 0 ? 4 : 2;  // groups per scale copy
 
     unsigned char *ring = base;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(base + S * stage_stride);
+    unsigned char *sc_area = base + S * stage_stride;              // [2][kDq][32]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sc_area + 2 * kDq * 32);
     constexpr int NA = 3;                      // A buffers in tensor memory
     uint64_t *a_full = bars, *mma_done = bars + NA, *b_full = bars + 2 * NA, *b_empty = b_full + S;
-    uint64_t *acc_full = b_empty + S, *acc_empty = acc_full + 1;
+    uint64_t *c_full = b_empty + S, *c_empty = c_full + S;
+    uint64_t *acc_full = c_empty + S, *acc_empty = acc_full + 1;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(acc_empty + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
 
@@ -260,6 +279,8 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, 1) expert_tc_kernel(StepAr
         for (int i = 0; i < S; ++i) {
             bar_init(&b_full[i], 128);
             bar_init(&b_empty[i], 1);
+            bar_init(&c_full[i], 1);
+            bar_init(&c_empty[i], kDq);
         }
         bar_init(acc_full, 1);
         bar_init(acc_empty, kDq);
@@ -294,9 +315,20 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, 1) expert_tc_kernel(StepAr
                                           : (uint32_t)(off_e + jj) * (uint32_t)(2 * F);
                 }
             }
-            if (idx >= S && !wait_bar(&b_empty[sidx], (uint32_t)((idx / S - 1) & 1), ws.status)) *abort_flag = 1;
+            if (idx >= S) {
+                const uint32_t par = (uint32_t)((idx / S - 1) & 1);
+                if (!wait_bar(&b_empty[sidx], par, ws.status) || !wait_bar(&c_empty[sidx], par, ws.status))
+                    *abort_flag = 1;
+            }
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;  // warp-uniform
             unsigned char *st = ring + sidx * stage_stride;
+            if (warp == kProdW && lane == 0) {
+                // the chunk's codes: one box of 128 rows x cbr bytes per matrix
+                tc::arrive_expect_tx(&c_full[sidx], (uint32_t)(MATS * kM * cbr));
+                const int y = e * (GATEUP ? F : D) + r0;
+                tc::tma_load_2d(st + off_codes, &tm0, c * cbr, y, &c_full[sidx]);
+                if (GATEUP) tc::tma_load_2d(st + off_codes + kM * cbr, &tm1, c * cbr, y, &c_full[sidx]);
+            }
             const uint16_t *src = bsrc + (size_t)c * kK + 8 * j;
 #pragma unroll
             for (int i = 0; i < kN / 16; ++i)
@@ -347,55 +379,47 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, 1) expert_tc_kernel(StepAr
         const int rr = 32 * (warp & 3) + lane;
         const uint32_t tlane = (uint32_t)(32 * (warp & 3)) << 16;
         const size_t row = (size_t)e * (GATEUP ? F : D) + r0 + rr;
-        const size_t groups = (size_t)K / 64;   // scale/bias entries per row (even: K % 128 == 0)
         const uint16_t *srow = (GATEUP ? (m ? a.planes.up_s : a.planes.gate_s) : a.planes.down_s) + row * groups;
         const uint16_t *brow = (GATEUP ? (m ? a.planes.up_b : a.planes.gate_b) : a.planes.down_b) + row * groups;
-        const unsigned char *qrow;
-        if (six)
-            qrow = reinterpret_cast<const unsigned char *>(a.planes.down_q) + row * ((size_t)K * 3 / 4);
-        else
-            qrow = reinterpret_cast<const unsigned char *>((GATEUP ? (m ? a.planes.up_q : a.planes.gate_q)
-                                                                   : a.planes.down_q) +
-                                                           row * ((size_t)K / 8)) + half * 16;
-        // this thread's codes (16 bytes: its half of the 4-bit row chunk; 6-bit:
-        // the whole 48-byte chunk) and, on even chunks, the 4-byte words holding
-        // the scale and bias of this chunk and the next
-        auto issue_own = [&](int idx) {
-            if (idx < total) {
-                const int c = idx % nchunks;
-                unsigned char *st = ring + (idx % S) * stage_stride;
-                if (six) {
-#pragma unroll
-                    for (int i = 0; i < 3; ++i)
-                        tc::cp_async16(st + off_codes + tid * 48 + 16 * i, qrow + (size_t)c * 48 + 16 * i);
+        // scale block sb: groups V sb .. V sb + V - 1 of the row (modulo the
+        // groups: the chunk sequence restarts with every token block) into slot
+        // sb % 2 of this thread
+        auto issue_sc = [&](int sb) {
+            if (sb * V < total) {
+                const int g0 = (sb * V) % groups;
+                unsigned char *dst = sc_area + ((sb & 1) * kDq + tid) * 32;
+                if (V == 8) {
+                    tc::cp_async16(dst, srow + g0);
+                    tc::cp_async16(dst + 16, brow + g0);
+                } else if (V == 4) {
+                    tc::cp_async8(dst, srow + g0);
+                    tc::cp_async8(dst + 16, brow + g0);
                 } else {
-                    tc::cp_async16(st + off_codes + tid * 16, qrow + (size_t)c * 32);
-                }
-                if ((c & 1) == 0) {
-                    tc::cp_async4(st + off_sc + tid * 8, srow + c);
-                    tc::cp_async4(st + off_sc + tid * 8 + 4, brow + c);
+                    tc::cp_async4(dst, srow + g0);
+                    tc::cp_async4(dst + 16, brow + g0);
                 }
             }
             tc::cp_async_commit();
         };
-        for (int i = 0; i < S - 1; ++i) issue_own(i);
+        issue_sc(0);
         for (int idx = 0; idx < total; ++idx) {
-            const int bsel = idx % NA, c = idx % nchunks, bi = idx / nchunks;
+            const int bsel = idx % NA, sidx = idx % S, c = idx % nchunks, bi = idx / nchunks;
             const int blk = (int)blockIdx.z + bi * (int)gridDim.z;
-            const unsigned char *st = ring + (idx % S) * stage_stride;
-            tc::cp_async_wait<S - 2>();
+            const unsigned char *st = ring + sidx * stage_stride;
+            if (idx % V == 0) {
+                // start the next scale block, wait for this one
+                issue_sc(idx / V + 1);
+                tc::cp_async_wait<1>();
+            }
+            bool ok = wait_bar(&c_full[sidx], (uint32_t)((idx / S) & 1), ws.status);
             // A buffer bsel is free once the MMAs of chunk idx - NA are done
-            if (idx >= NA && !wait_bar(&mma_done[bsel], (uint32_t)((idx / NA - 1) & 1), ws.status))
-                *abort_flag = 1;
+            if (ok && idx >= NA) ok = wait_bar(&mma_done[bsel], (uint32_t)((idx / NA - 1) & 1), ws.status);
+            if (!ok) *abort_flag = 1;
             // warp-uniform: tcgen05.st and tcgen05.ld below are warp-collective
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
             {
-                // scale/bias words: in the stage of the even chunk of the pair
-                // (read before that stage is refilled below)
-                const uint32_t *scw = reinterpret_cast<const uint32_t *>(
-                    ring + ((idx & ~1) % S) * stage_stride + off_sc + tid * 8);
-                const int sh = (c & 1) * 16;
-                float s = bf16f((uint16_t)(scw[0] >> sh)), b = bf16f((uint16_t)(scw[1] >> sh));
+                const uint16_t *scs = reinterpret_cast<const uint16_t *>(sc_area + (((idx / V) & 1) * kDq + tid) * 32);
+                float s = bf16f(scs[idx % V]), b = bf16f(scs[8 + idx % V]);
                 if (fabsf(s) > 65504.0f || fabsf(b) > 65504.0f) {  // beyond f16: saturate, report
                     report_error(ws.status, kDevErrRange);
                     s = fminf(fmaxf(s, -65504.0f), 65504.0f);
@@ -404,7 +428,7 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, 1) expert_tc_kernel(StepAr
                 const __half2 s2 = __floats2half2_rn(s, s), b2 = __floats2half2_rn(b, b);
                 uint32_t o[16];
                 if (six) {
-                    const unsigned char *cr = st + off_codes + tid * 48;
+                    const unsigned char *cr = st + off_codes + (m * kM + rr) * 48;
                     uint32_t v[12];
 #pragma unroll
                     for (int i = 0; i < 3; ++i) {
@@ -418,7 +442,8 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, 1) expert_tc_kernel(StepAr
                         o[4 * j] = r4.x; o[4 * j + 1] = r4.y; o[4 * j + 2] = r4.z; o[4 * j + 3] = r4.w;
                     }
                 } else {
-                    const uint4 w4 = *reinterpret_cast<const uint4 *>(st + off_codes + tid * 16);
+                    const uint4 w4 = *reinterpret_cast<const uint4 *>(st + off_codes + (m * kM + rr) * 32 +
+                                                                      16 * (half ^ code_swz(rr)));
                     const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -429,9 +454,8 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, 1) expert_tc_kernel(StepAr
                 // two f16 per 32-bit column in the stored input order
                 tc::st_32x32b_x16_async(tmem + tlane + kAcol + (uint32_t)((bsel * MATS + m) * 32 + half * 16), o);
             }
-            // this thread read its slot of chunk idx - 1 last iteration: refill it
-            // (while the tensor-memory stores complete)
-            issue_own(idx + S - 1);
+            // the codes of this stage have been read
+            bar_arrive(&c_empty[sidx]);
             tc::wait_st();
             tc::fence_before_sync();
             bar_arrive(&a_full[bsel]);
@@ -479,14 +503,43 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, 1) expert_tc_kernel(StepAr
     if (warp == 0) tc::tmem_dealloc(tmem, kCols);
 }
 
-// ring stages per variant (the ring is all of the shared memory)
-constexpr int kStagesGateUp = 8;   // 8 x 20 KB
-constexpr int kStagesDown = 7;     // 7 x 14 KB (two CTAs per SM) or 7 x 22 KB (6-bit)
+// ring stages per variant
+constexpr int kStagesGateUp = 8;   // 8 x 16 KB + 32 KB scale slots
+constexpr int kStagesDown = 7;     // 7 x 12 KB + 16 KB (two CTAs per SM), 6-bit 7 x 14 KB + 16 KB
 
-size_t tc_smem_bytes(bool gateup, int six) {
-    const int dq = gateup ? 512 : 256;
+size_t tc_smem_bytes(bool gateup, bool six) {
+    const int mats = gateup ? 2 : 1, dq = mats * 256;
     const int S = gateup ? kStagesGateUp : kStagesDown;
-    return 1024 + (size_t)S * stage_bytes_of(dq, six ? 48 : 16) + (6 + 2 * S + 2) * 8 + 16;
+    return 1024 + (size_t)S * stage_bytes_of(mats, six ? 48 : 32) + 2 * dq * 32 + (6 + 4 * S + 2) * 8 + 16;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        cudaGetLastError();
+    }
+    return fn;
+}
+
+// a code plane [rows][row_bytes] as 2-D bytes with boxes of {cbr, 128 rows}
+bool encode_code_plane(CUtensorMap *m, const void *base, long long row_bytes, long long rows, int cbr) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)cbr, (cuuint32_t)kM};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, cbr == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -507,7 +560,19 @@ cudaError_t launch_expert_tc(const StepArgs &a, const Workspace &ws, int thr, bo
         launched += 1;
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
-    const size_t smem = tc_smem_bytes(!down, down && a.s.down_bits == 6);
+    const bool six = down && a.s.down_bits == 6;
+    const size_t smem = tc_smem_bytes(!down, six);
+    // tensor maps of the code planes (rows of D or Dff inputs)
+    alignas(64) CUtensorMap tm0, tm1;
+    const int K = down ? a.s.F : a.s.D;
+    const long long rows = (long long)a.s.E * (down ? a.s.D : a.s.F);
+    const int cbr = six ? 48 : 32;
+    const long long row_bytes = six ? (long long)K * 3 / 4 : (long long)K / 2;
+    if (!encode_code_plane(&tm0, down ? (const void *)a.planes.down_q : (const void *)a.planes.gate_q, row_bytes,
+                           rows, cbr) ||
+        !encode_code_plane(&tm1, down ? (const void *)a.planes.down_q : (const void *)a.planes.up_q, row_bytes,
+                           rows, cbr))
+        return cudaErrorInvalidValue;
     const void *k = down ? (const void *)expert_tc_kernel<false, kStagesDown>
                          : (const void *)expert_tc_kernel<true, kStagesGateUp>;
     if ((err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
@@ -518,9 +583,9 @@ cudaError_t launch_expert_tc(const StepArgs &a, const Workspace &ws, int thr, bo
     const long mean = ((long)a.s.n * a.s.k + maxU - 1) / maxU;
     const int zb = (int)max(1L, min(8L, (3 * mean / 2 + kN - 1) / kN));
     if (!down)
-        expert_tc_kernel<true, kStagesGateUp><<<dim3(a.s.F / kM, maxU, zb), 672, smem, st>>>(a, ws, thr);
+        expert_tc_kernel<true, kStagesGateUp><<<dim3(a.s.F / kM, maxU, zb), 672, smem, st>>>(a, ws, thr, tm0, tm1);
     else
-        expert_tc_kernel<false, kStagesDown><<<dim3(a.s.D / kM, maxU, zb), 416, smem, st>>>(a, ws, thr);
+        expert_tc_kernel<false, kStagesDown><<<dim3(a.s.D / kM, maxU, zb), 416, smem, st>>>(a, ws, thr, tm0, tm1);
     launched += 1;
     return cudaGetLastError();
 }

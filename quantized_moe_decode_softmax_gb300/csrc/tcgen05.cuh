@@ -165,9 +165,32 @@ __device__ __forceinline__ void st_32x32b_x16(uint32_t taddr, const uint32_t (&r
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ---- TMA ---------------------------------------------------------------------------
+// 2-D tiled load of one box of `tmap` (a __grid_constant__ kernel parameter) at
+// element coordinates (x, y), completing `bytes` of transaction on the mbarrier
+__device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(smem_u32(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// arrive on the mbarrier, announcing `bytes` of transaction still to complete
+__device__ __forceinline__ void arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
 // ---- Ampere-style asynchronous copies ------------------------------------------
 __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+// 8 bytes (both addresses 8-byte aligned), through L1
+__device__ __forceinline__ void cp_async8(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 
 // 4 bytes (both addresses 4-byte aligned), through L1
