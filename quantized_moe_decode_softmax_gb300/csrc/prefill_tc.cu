@@ -23,7 +23,7 @@
 //     rounding, as the grouped path's tile variant.
 //
 // Per CTA: one expert, 128 weight rows, 64 of the expert's tokens at a time,
-// K (the reduction) in chunks of 64 inputs = one quantisation group:
+// K (the reduction) in chunks of 128 inputs = two quantisation groups:
 //   - a ring of S stages holds, per chunk, the B tile, the raw codes and the
 //     scale/bias words of the CTA's rows, filled S - 1 chunks ahead;
 //   - the CUDA cores dequantise chunk i into one of two A tiles while the
@@ -48,9 +48,10 @@ namespace {
 
 constexpr int kM = 128;          // weight rows per A tile
 constexpr int kN = 64;           // tokens per block
-constexpr int kK = 64;           // inputs per chunk
+constexpr int kK = 128;          // inputs per chunk: two quantisation groups
 constexpr int kSbo = 1024;       // bytes between 8-row swizzle atoms (8 rows x 128 B)
-constexpr int kTileB = kN * kK * 2;   // 8 KB: one f16 activation tile
+constexpr int kSubB = kN * 64 * 2;    // 8 KB: 64 tokens x 64 inputs, one 128-byte swizzled sub-tile
+constexpr int kTileB = 2 * kSubB;     // 16 KB: the chunk's activation tile
 constexpr unsigned long long kWaitNs = 1000000000ull;
 
 __device__ __forceinline__ unsigned long long globaltimer() {
@@ -172,18 +173,19 @@ __global__ void x_to_f16_kernel(StepArgs a, Workspace ws) {
 
 // ---- the GEMMs -------------------------------------------------------------------
 // Warp roles (MATS = 2 for gate/up, 1 for down):
-//   - MATS x 8 dequantisation warps: thread (lane quadrant q, matrix m, half of
-//     the 8 pieces) owns weight row 32 q + lane of matrix m -- the tensor-memory
-//     lane of that row. It copies its own row's scales and biases, V groups at
-//     a time (V = 8, 4 or 2: the widest that divides the groups of a row), into
-//     a double-buffered slot of its own (cp.async, its own wait groups), reads
-//     its codes from the ring once c_full says the chunk's TMA box landed,
-//     arrives on c_empty, dequantises into A buffer (chunk % 3) once the MMAs of
-//     chunk - 3 are done, and arrives on a_full. After the last chunk of a
-//     token block the same warps run the epilogue.
+//   - MATS x 8 dequantisation warps: thread (lane quadrant q, matrix m, group
+//     g of the chunk) owns weight row 32 q + lane of matrix m -- the
+//     tensor-memory lane of that row -- and dequantises that row's 64 weights
+//     of group g of every chunk. It copies its own row's scales and biases, V
+//     groups at a time (V = 8, 4 or 2: the widest that divides the groups of a
+//     row), into a double-buffered slot of its own (cp.async, its own wait
+//     groups), reads its codes from the ring once c_full says the chunk's TMA
+//     box landed, arrives on c_empty, dequantises into A buffer (chunk % 3)
+//     once the MMAs of chunk - 3 are done, and arrives on a_full. After the last
+//     chunk of a token block the same warps run the epilogue.
 //   - four producer warps, one per SM sub-partition (a single one held up the
 //     dequantisation warps of its sub-partition behind its copies), copy the B
-//     tiles (64 tokens x 64 inputs, f16) into the ring, each lane arriving on
+//     tiles (64 tokens x 128 inputs, f16) into the ring, each lane arriving on
 //     b_full when its copies have landed; lane 0 of the first also loads the
 //     chunk's codes (one TMA box of 128 rows per matrix, completing on c_full).
 //     A stage is refilled once its MMAs (b_empty) and its dequantisation
@@ -194,16 +196,17 @@ __global__ void x_to_f16_kernel(StepArgs a, Workspace ws) {
 // Every wait gives up after 1 s: it reports a timeout and sets the CTA's abort
 // flag, which every role checks once per chunk.
 //
-// Ring stage layout (bytes): [B tile 8 KB][codes: MATS x 128 rows x cbr bytes,
-// cbr = 32 (4-bit, 32-byte TMA swizzle: the 16-byte halves of rows 4..7 of
-// every 8 swap places, which spreads 8 consecutive rows reading the same half
-// over all banks) or 48 (6-bit, no swizzle)]. After the ring: the per-thread
-// scale slots, [2][dequantisation threads][16 bytes scales, 16 bytes biases].
+// Ring stage layout (bytes): [B tile: two 8 KB sub-tiles, inputs 0..63 and
+// 64..127 of the chunk][codes: MATS x 128 rows x cbr bytes, cbr = 64 (4-bit,
+// 64-byte TMA swizzle: 16-byte piece p of row r stored at p ^ ((r / 2) % 4),
+// which spreads 8 consecutive rows reading the same piece over all banks) or
+// 96 (6-bit, no swizzle)]. After the ring: the per-thread scale slots,
+// [2][dequantisation threads][16 bytes scales, 16 bytes biases].
 __host__ __device__ constexpr int stage_bytes_of(int mats, int cbr) {
     return (kTileB + mats * kM * cbr + 1023) & ~1023;
 }
 
-__host__ __device__ constexpr int code_swz(int rr) { return (rr >> 2) & 1; }
+__host__ __device__ constexpr int code_swz(int rr) { return (rr >> 1) & 3; }
 
 __device__ __forceinline__ void bar_init(uint64_t *bar, unsigned count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(tc::smem_u32(bar)), "r"(count) : "memory");
@@ -222,7 +225,7 @@ __device__ __forceinline__ void bar_arrive_cp_async(uint64_t *bar) {
 // tm0, tm1: tensor maps of the code planes (gate and up, or down and unused),
 // 2-D {row bytes, rows} with boxes of {cbr, 128}
 template <bool GATEUP, int S>
-__global__ void __launch_bounds__(GATEUP ? 672 : 416, 1)
+__global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
     expert_tc_kernel(StepArgs a, Workspace ws, int thr, const __grid_constant__ CUtensorMap tm0,
                      const __grid_constant__ CUtensorMap tm1) {
     constexpr int MATS = GATEUP ? 2 : 1;
@@ -250,11 +253,12 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, 1)
     const int r0 = blockIdx.x * kM;          // first weight row (gate/up: f; down: d)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool six = !GATEUP && a.s.down_bits == 6;
-    const int cbr = six ? 48 : 32;           // code bytes per row and chunk
+    const int cbr = six ? 96 : 64;           // code bytes per row and chunk
     const int stage_stride = stage_bytes_of(MATS, cbr);
     const int off_codes = kTileB;
     const int groups = K / 64;               // scale/bias entries per row (even)
     const int V = groups % 8 == 0 ? 8 : groups % 4 == 0 ? 4 : 2;  // groups per scale copy
+    const int cpb = V / 2;                   // chunks per scale copy
 
     unsigned char *ring = base;
     unsigned char *sc_area = base + S * stage_stride;              // [2][kDq][32]
@@ -267,7 +271,7 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
 
     // tensor memory: accumulators (gate, up or y: 64 columns each), then the
-    // NA A buffers (MATS tiles of 32 columns each)
+    // NA A buffers (MATS tiles of 64 columns: 128 inputs, two f16 per column)
     constexpr uint32_t kCols = GATEUP ? 512 : 256;
     constexpr uint32_t kAcol = MATS * kN;
     if (tid == 0) {
@@ -295,19 +299,19 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, 1)
     if (warp >= kProdW && warp < kMmaW) {
         // ---- producers: B tiles -----------------------------------------------
         // B rows: x in f16 (y area, n x D) or h in f16 (first half of each h row)
-        // producer warp pw, lane -> 16-byte piece j of tokens 16 pw + tq + 4 i;
+        // producer warp pw, lane -> 16-byte piece j (of 16) of tokens 16 pw + tq + 2 i;
         // the tokens' row offsets (f16 elements, below 2^31 for every allowed
         // shape: n D <= 8192 x 16384, n k x 2 Dff <= 131072 x 16384) are looked
         // up once per block
         const uint16_t *bsrc = reinterpret_cast<const uint16_t *>(GATEUP ? (const void *)ws.y : (const void *)ws.h);
-        const int j = lane & 7, tq = 16 * (warp - kProdW) + (lane >> 3);
-        uint32_t roff[kN / 16];
+        const int j = lane & 15, tq = 16 * (warp - kProdW) + (lane >> 4);
+        uint32_t roff[kN / 8];
         for (int idx = 0; idx < total; ++idx) {
             const int sidx = idx % S, blk = (int)blockIdx.z + (idx / nchunks) * (int)gridDim.z, c = idx % nchunks;
             if (c == 0) {
 #pragma unroll
-                for (int i = 0; i < kN / 16; ++i) {
-                    const int jj = blk * kN + tq + 4 * i;
+                for (int i = 0; i < kN / 8; ++i) {
+                    const int jj = blk * kN + tq + 2 * i;
                     // tokens past the expert's count are not copied: their
                     // accumulator columns are never read
                     roff[i] = jj >= cnt_e ? 0xFFFFFFFFu
@@ -330,9 +334,10 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, 1)
                 if (GATEUP) tc::tma_load_2d(st + off_codes + kM * cbr, &tm1, c * cbr, y, &c_full[sidx]);
             }
             const uint16_t *src = bsrc + (size_t)c * kK + 8 * j;
+            unsigned char *sub = st + (j >> 3) * kSubB;
 #pragma unroll
-            for (int i = 0; i < kN / 16; ++i)
-                if (roff[i] != 0xFFFFFFFFu) tc::cp_async16(st + core_off(tq + 4 * i, j), src + roff[i]);
+            for (int i = 0; i < kN / 8; ++i)
+                if (roff[i] != 0xFFFFFFFFu) tc::cp_async16(sub + core_off(tq + 2 * i, j & 7), src + roff[i]);
             bar_arrive_cp_async(&b_full[sidx]);
         }
     } else if (warp == kMmaW) {
@@ -351,15 +356,17 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, 1)
             if (!ok) *abort_flag = 1;
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;  // warp-uniform
             const uint64_t bd0 = descB0 + (uint64_t)((sidx * stage_stride) >> 4);
-            const uint32_t a0 = tmem + kAcol + (uint32_t)(bsel * MATS * 32);
+            const uint32_t a0 = tmem + kAcol + (uint32_t)(bsel * MATS * 64);
             __syncwarp();
             if (tc::elect_one()) {
                 tc::fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < kK / 16; ++ks) {
+                    // K step ks: sub-tile ks / 4 of B, 32 bytes per step inside it
+                    const uint64_t bd = bd0 + (uint64_t)(((ks >> 2) * kSubB) >> 4) + 2 * (ks & 3);
 #pragma unroll
                     for (int m = 0; m < MATS; ++m)
-                        tc::mma_f16_ts(tmem + m * kN, a0 + (uint32_t)(m * 32 + ks * 8), bd0 + 2 * ks, idesc,
+                        tc::mma_f16_ts(tmem + m * kN, a0 + (uint32_t)(m * 64 + ks * 8), bd, idesc,
                                        (c > 0 || ks > 0) ? 1u : 0u);
                 }
                 tc::commit(&mma_done[bsel]);
@@ -375,17 +382,17 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, 1)
             wait_bar(&mma_done[issued % NA], (uint32_t)((issued / NA) & 1), ws.status);
     } else {
         // ---- dequantisation and epilogue ------------------------------------
-        const int m = (warp >> 2) % MATS, half = warp / (4 * MATS);
+        const int m = (warp >> 2) % MATS, gsel = warp / (4 * MATS);
         const int rr = 32 * (warp & 3) + lane;
         const uint32_t tlane = (uint32_t)(32 * (warp & 3)) << 16;
         const size_t row = (size_t)e * (GATEUP ? F : D) + r0 + rr;
         const uint16_t *srow = (GATEUP ? (m ? a.planes.up_s : a.planes.gate_s) : a.planes.down_s) + row * groups;
         const uint16_t *brow = (GATEUP ? (m ? a.planes.up_b : a.planes.gate_b) : a.planes.down_b) + row * groups;
-        // scale block sb: groups V sb .. V sb + V - 1 of the row (modulo the
-        // groups: the chunk sequence restarts with every token block) into slot
-        // sb % 2 of this thread
+        // scale block sb: groups V sb .. V sb + V - 1 of the row = chunks
+        // cpb sb .. cpb sb + cpb - 1 (modulo the groups: the chunk sequence
+        // restarts with every token block) into slot sb % 2 of this thread
         auto issue_sc = [&](int sb) {
-            if (sb * V < total) {
+            if (sb * cpb < total) {
                 const int g0 = (sb * V) % groups;
                 unsigned char *dst = sc_area + ((sb & 1) * kDq + tid) * 32;
                 if (V == 8) {
@@ -406,9 +413,9 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, 1)
             const int bsel = idx % NA, sidx = idx % S, c = idx % nchunks, bi = idx / nchunks;
             const int blk = (int)blockIdx.z + bi * (int)gridDim.z;
             const unsigned char *st = ring + sidx * stage_stride;
-            if (idx % V == 0) {
+            if (idx % cpb == 0) {
                 // start the next scale block, wait for this one
-                issue_sc(idx / V + 1);
+                issue_sc(idx / cpb + 1);
                 tc::cp_async_wait<1>();
             }
             bool ok = wait_bar(&c_full[sidx], (uint32_t)((idx / S) & 1), ws.status);
@@ -418,41 +425,46 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, 1)
             // warp-uniform: tcgen05.st and tcgen05.ld below are warp-collective
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
             {
-                const uint16_t *scs = reinterpret_cast<const uint16_t *>(sc_area + (((idx / V) & 1) * kDq + tid) * 32);
-                float s = bf16f(scs[idx % V]), b = bf16f(scs[8 + idx % V]);
+                const uint16_t *scs = reinterpret_cast<const uint16_t *>(sc_area + (((idx / cpb) & 1) * kDq + tid) * 32);
+                const int gi = 2 * (idx % cpb) + gsel;   // this thread's group inside the block
+                float s = bf16f(scs[gi]), b = bf16f(scs[8 + gi]);
                 if (fabsf(s) > 65504.0f || fabsf(b) > 65504.0f) {  // beyond f16: saturate, report
                     report_error(ws.status, kDevErrRange);
                     s = fminf(fmaxf(s, -65504.0f), 65504.0f);
                     b = fminf(fmaxf(b, -65504.0f), 65504.0f);
                 }
                 const __half2 s2 = __floats2half2_rn(s, s), b2 = __floats2half2_rn(b, b);
-                uint32_t o[16];
+                uint32_t o[32];
                 if (six) {
-                    const unsigned char *cr = st + off_codes + (m * kM + rr) * 48;
+                    const unsigned char *cr = st + off_codes + (m * kM + rr) * 96 + 48 * gsel;
                     uint32_t v[12];
 #pragma unroll
                     for (int i = 0; i < 3; ++i) {
                         const uint4 t4 = *reinterpret_cast<const uint4 *>(cr + 16 * i);
                         v[4 * i] = t4.x; v[4 * i + 1] = t4.y; v[4 * i + 2] = t4.z; v[4 * i + 3] = t4.w;
                     }
-                    // compile-time piece indices keep v[] in registers
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint4 r4 = half ? deq_6bit(v, 4 + j, s2, b2) : deq_6bit(v, j, s2, b2);
+                    for (int j = 0; j < 8; ++j) {
+                        const uint4 r4 = deq_6bit(v, j, s2, b2);
                         o[4 * j] = r4.x; o[4 * j + 1] = r4.y; o[4 * j + 2] = r4.z; o[4 * j + 3] = r4.w;
                     }
                 } else {
-                    const uint4 w4 = *reinterpret_cast<const uint4 *>(st + off_codes + (m * kM + rr) * 32 +
-                                                                      16 * (half ^ code_swz(rr)));
-                    const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+                    // 16-byte pieces 2 gsel and 2 gsel + 1 of the row's 64 bytes
+                    const unsigned char *cr = st + off_codes + (m * kM + rr) * 64;
+                    const uint4 w0 = *reinterpret_cast<const uint4 *>(cr + 16 * ((2 * gsel) ^ code_swz(rr)));
+                    const uint4 w1 = *reinterpret_cast<const uint4 *>(cr + 16 * ((2 * gsel + 1) ^ code_swz(rr)));
+                    const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
+                    for (int j = 0; j < 8; ++j) {
                         const uint4 r4 = deq_word(wv[j], s2, b2);
                         o[4 * j] = r4.x; o[4 * j + 1] = r4.y; o[4 * j + 2] = r4.z; o[4 * j + 3] = r4.w;
                     }
                 }
-                // two f16 per 32-bit column in the stored input order
-                tc::st_32x32b_x16_async(tmem + tlane + kAcol + (uint32_t)((bsel * MATS + m) * 32 + half * 16), o);
+                // two f16 per 32-bit column in the stored input order: columns
+                // 32 gsel .. 32 gsel + 31 of this matrix's A tile
+                const uint32_t ta = tmem + tlane + kAcol + (uint32_t)((bsel * MATS + m) * 64 + gsel * 32);
+                tc::st_32x32b_x16_async(ta, *reinterpret_cast<const uint32_t(*)[16]>(o));
+                tc::st_32x32b_x16_async(ta + 16, *reinterpret_cast<const uint32_t(*)[16]>(o + 16));
             }
             // the codes of this stage have been read
             bar_arrive(&c_empty[sidx]);
@@ -504,13 +516,13 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, 1)
 }
 
 // ring stages per variant
-constexpr int kStagesGateUp = 8;   // 8 x 16 KB + 32 KB scale slots
-constexpr int kStagesDown = 7;     // 7 x 12 KB + 16 KB (two CTAs per SM), 6-bit 7 x 14 KB + 16 KB
+constexpr int kStagesGateUp = 4;   // 4 x 32 KB + 32 KB scale slots
+constexpr int kStagesDown = 3;     // 3 x 24 KB (6-bit 28 KB) + 16 KB: two CTAs per SM
 
 size_t tc_smem_bytes(bool gateup, bool six) {
     const int mats = gateup ? 2 : 1, dq = mats * 256;
     const int S = gateup ? kStagesGateUp : kStagesDown;
-    return 1024 + (size_t)S * stage_bytes_of(mats, six ? 48 : 32) + 2 * dq * 32 + (6 + 4 * S + 2) * 8 + 16;
+    return 1024 + (size_t)S * stage_bytes_of(mats, six ? 96 : 64) + 2 * dq * 32 + (6 + 4 * S + 2) * 8 + 16;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -538,7 +550,7 @@ bool encode_code_plane(CUtensorMap *m, const void *base, long long row_bytes, lo
     cuuint32_t box[2] = {(cuuint32_t)cbr, (cuuint32_t)kM};
     cuuint32_t es[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, cbr == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, cbr == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -566,7 +578,7 @@ cudaError_t launch_expert_tc(const StepArgs &a, const Workspace &ws, int thr, bo
     alignas(64) CUtensorMap tm0, tm1;
     const int K = down ? a.s.F : a.s.D;
     const long long rows = (long long)a.s.E * (down ? a.s.D : a.s.F);
-    const int cbr = six ? 48 : 32;
+    const int cbr = six ? 96 : 64;
     const long long row_bytes = six ? (long long)K * 3 / 4 : (long long)K / 2;
     if (!encode_code_plane(&tm0, down ? (const void *)a.planes.down_q : (const void *)a.planes.gate_q, row_bytes,
                            rows, cbr) ||
