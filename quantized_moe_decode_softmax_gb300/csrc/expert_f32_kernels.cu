@@ -310,23 +310,36 @@ __global__ void __launch_bounds__(kRowThreads) down_f32_kernel(StepArgs a, Works
     }
 }
 
-// thread per output element; rank-ordered weighted sum, one final rounding
+// thread per 4 consecutive output elements (D % 4 == 0); for each, the
+// rank-ordered weighted sum and one final rounding
 template <int OT>
 __global__ void combine_kernel(StepArgs a, Workspace ws) {
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    const int i4 = blockIdx.x * blockDim.x + threadIdx.x;
     const int D = a.s.D, k = a.s.k;
-    if (i >= a.s.n * D) return;
-    const int t = i / D, d = i - t * D;
-    float acc = 0.f;
+    if (i4 >= a.s.n * (D / 4)) return;
+    const int t = i4 / (D / 4), d = 4 * (i4 - t * (D / 4));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < k; ++j) {
         const int p = ws.slot_of[t * k + j];
         if (p < 0) continue;  // an expert this plan does not own
-        acc = fmaf(ws.topk_w[t * k + j], ws.y[(size_t)p * D + d], acc);
+        const float wj = ws.topk_w[t * k + j];
+        const float4 yv = *reinterpret_cast<const float4 *>(ws.y + (size_t)p * D + d);
+        acc.x = fmaf(wj, yv.x, acc.x);
+        acc.y = fmaf(wj, yv.y, acc.y);
+        acc.z = fmaf(wj, yv.z, acc.z);
+        acc.w = fmaf(wj, yv.w, acc.w);
     }
-    if (OT == MOE_DTYPE_F32)
-        static_cast<float *>(a.out)[i] = acc;
-    else
-        static_cast<__nv_bfloat16 *>(a.out)[i] = __float2bfloat16_rn(acc);
+    const size_t i = (size_t)t * D + d;
+    if (OT == MOE_DTYPE_F32) {
+        *reinterpret_cast<float4 *>(static_cast<float *>(a.out) + i) = acc;
+    } else {
+        __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) + i;
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 pk;
+        pk.x = *reinterpret_cast<const uint32_t *>(&lo);
+        pk.y = *reinterpret_cast<const uint32_t *>(&hi);
+        *reinterpret_cast<uint2 *>(o) = pk;
+    }
 }
 
 }  // namespace
@@ -370,7 +383,7 @@ static cudaError_t launch_experts(const StepArgs &a, const Workspace &ws, int ti
     launched += 1;
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    const int total = a.s.n * a.s.D;
+    const int total = a.s.n * (a.s.D / 4);
     dim3 g3((total + 255) / 256);
     if (a.s.out_dtype == MOE_DTYPE_F32)
         combine_kernel<MOE_DTYPE_F32><<<g3, block, 0, st>>>(a, ws);

@@ -37,25 +37,46 @@ __device__ __forceinline__ void load8<MOE_DTYPE_BF16>(const void *p, size_t i, f
     }
 }
 
-// one warp per (expert, token); grid (ceil(E / warps), n)
+// one warp per expert and kRouterTokens tokens, computed side by side (one
+// accumulator per token); grid (ceil(E / warps), ceil(n / kRouterTokens)).
+// Each logit is the same sum in the same order for any grouping (lane l
+// accumulates inputs 8 l .. 8 l + 7 of every 256 in turn, then the warp's
+// butterfly sum); the expert's router row is read once for the warp's tokens.
+constexpr int kRouterTokens = 4;
+
 template <int XT, int WT>
 __global__ void router_logits_kernel(const void *__restrict__ x, const void *__restrict__ w,
                                      const float *__restrict__ bias, float *__restrict__ logits,
-                                     int E, int D) {
+                                     int E, int D, int n) {
     const int lane = threadIdx.x & 31;
     const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int t = blockIdx.y;
     if (e >= E) return;
-    float acc = 0.f;
+    const int t0 = blockIdx.y * kRouterTokens;
+    const int nt = min(kRouterTokens, n - t0);
+    float acc[kRouterTokens];
+#pragma unroll
+    for (int q = 0; q < kRouterTokens; ++q) acc[q] = 0.f;
     for (int i = lane * 8; i < D; i += 256) {
-        float xv[8], wv[8];
-        load8<XT>(x, (size_t)t * D + i, xv);
+        float wv[8];
         load8<WT>(w, (size_t)e * D + i, wv);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc = fmaf(xv[j], wv[j], acc);
+        for (int q = 0; q < kRouterTokens; ++q) {
+            if (q < nt) {
+                float xv[8];
+                load8<XT>(x, (size_t)(t0 + q) * D + i, xv);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[q] = fmaf(xv[j], wv[j], acc[q]);
+            }
+        }
     }
-    acc = warp_sum(acc);
-    if (lane == 0) logits[(size_t)t * E + e] = acc + (bias ? bias[e] : 0.f);
+    const float be = bias ? bias[e] : 0.f;
+#pragma unroll
+    for (int q = 0; q < kRouterTokens; ++q) {
+        if (q < nt) {
+            const float v = warp_sum(acc[q]);
+            if (lane == 0) logits[(size_t)(t0 + q) * E + e] = v + be;
+        }
+    }
 }
 
 // one CTA: softmax, top-k, renormalise, then group; writes the workspace
@@ -225,21 +246,21 @@ cudaError_t launch_prefill_route(const StepArgs &a, const Workspace &ws, int max
 cudaError_t launch_router_logits(const StepArgs &a, const Workspace &ws, cudaStream_t st,
                                  int &launched) {
     const int warps = 8;
-    dim3 grid((a.s.E + warps - 1) / warps, a.s.n);
+    dim3 grid((a.s.E + warps - 1) / warps, (a.s.n + kRouterTokens - 1) / kRouterTokens);
     dim3 block(32 * warps);
     const bool xf = a.s.x_dtype == MOE_DTYPE_F32, wf = a.s.w_dtype == MOE_DTYPE_F32;
     if (xf && wf)
         router_logits_kernel<MOE_DTYPE_F32, MOE_DTYPE_F32><<<grid, block, 0, st>>>(
-            a.x, a.router_w, a.router_bias, ws.logits, a.s.E, a.s.D);
+            a.x, a.router_w, a.router_bias, ws.logits, a.s.E, a.s.D, a.s.n);
     else if (xf)
         router_logits_kernel<MOE_DTYPE_F32, MOE_DTYPE_BF16><<<grid, block, 0, st>>>(
-            a.x, a.router_w, a.router_bias, ws.logits, a.s.E, a.s.D);
+            a.x, a.router_w, a.router_bias, ws.logits, a.s.E, a.s.D, a.s.n);
     else if (wf)
         router_logits_kernel<MOE_DTYPE_BF16, MOE_DTYPE_F32><<<grid, block, 0, st>>>(
-            a.x, a.router_w, a.router_bias, ws.logits, a.s.E, a.s.D);
+            a.x, a.router_w, a.router_bias, ws.logits, a.s.E, a.s.D, a.s.n);
     else
         router_logits_kernel<MOE_DTYPE_BF16, MOE_DTYPE_BF16><<<grid, block, 0, st>>>(
-            a.x, a.router_w, a.router_bias, ws.logits, a.s.E, a.s.D);
+            a.x, a.router_w, a.router_bias, ws.logits, a.s.E, a.s.D, a.s.n);
     launched += 1;
     return cudaGetLastError();
 }
