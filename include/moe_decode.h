@@ -90,9 +90,9 @@ enum {
      * moe_get_phase_times); costs a few global stores per CTA */
     MOE_FLAG_PHASE_TIMES = 1u << 2,
     /* cohorts of 9..16 tokens take the grouped multi-kernel path (every
-     * selected expert streamed once per step, tile kernels for experts with
-     * at least mma_min_tokens tokens) instead of chunks of the single-launch
-     * kernel; see moe_decode_forward */
+     * selected expert streamed once per step, tensor-core GEMMs for experts
+     * with at least mma_min_tokens tokens) instead of chunks of the
+     * single-launch kernel; see moe_decode_forward */
     MOE_FLAG_GROUPED_COHORTS = 1u << 3,
     /* TEST ONLY: in the plan's first forward call on the fused path, CTA 0
      * reaches the first grid barrier only after another CTA's bounded wait has
@@ -128,8 +128,11 @@ typedef struct {
     int router_dtype;   /* MOE_DTYPE_* of the router weights */
     int out_dtype;      /* MOE_DTYPE_* of out */
     unsigned flags;     /* MOE_FLAG_* */
-    int mma_min_tokens; /* per-expert token count from which an expert takes
-                           the tensor-core tile path; 0 = library default */
+    int mma_min_tokens; /* per-expert token count from which an expert of the
+                           grouped and prefill paths takes the tensor-core GEMM
+                           (the rest take the f32 GEMV); 0 = library default:
+                           1 where the tcgen05 GEMMs apply (D and Dff multiples
+                           of 128), else 16 (the mma.sync tile kernels) */
     /* ABI version 2 */
     int activation;     /* MOE_ACT_* */
     float act_limit;    /* the clamp bound L of MOE_ACT_SWIGLU_CLAMPED (finite,
@@ -210,16 +213,19 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan **out);
  *                    kernel that writes the whole cohort's routing tables;
  *   n_tokens 17..64, or any n_tokens > 8 with MOE_FLAG_GROUPED_COHORTS:
  *                    the grouped multi-kernel path (router, top-k and
- *                    grouping, per-expert tile or GEMV kernels, combine);
+ *                    grouping, per-expert tensor-core GEMMs -- tcgen05 where
+ *                    D and Dff are multiples of 128, else mma.sync tiles --
+ *                    or GEMV kernels, combine);
  *   MOE_FLAG_F32_DEBUG, or a shape the single-launch kernel declines:
  *                    the grouped multi-kernel path with f32 GEMV kernels;
  *   n_tokens 65..max_tokens: the prefill path (#1616 Current Behavior and #1859
  *                    Problem / Background: the sorted matrix path, qmm, of
  *                    prompt processing): routing per token, grouping through
  *                    per-expert token bitmaps, then per expert a grouped GEMM
- *                    (the tile kernels over its tokens in blocks of 64, each
- *                    weight tile read once per block) or the f32 GEMV for
- *                    experts under mma_min_tokens, and the combine.
+ *                    (tcgen05, or the mma.sync tiles, over its tokens in
+ *                    blocks of 64, each weight tile read once per block) or
+ *                    the f32 GEMV for experts under mma_min_tokens, and the
+ *                    combine.
  * Expert range. A plan that owns the experts [expert_begin, expert_end)
  * writes out[t] = sum over the ranks j whose expert it owns of w[t,j] *
  * y[t,j] (0 where it owns none): the plans of a partition of the experts

@@ -679,6 +679,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
                 if (__all_sync(0xffffffffu, need == 0u) || *abort_flag || globaltimer() - t0 > kWaitNs) break;
                 __nanosleep(200);
             }
+            // gave up: report it now, so the token warps below stop at once
+            // instead of spending a second bound of their own
+            if (!__all_sync(0xffffffffu, need == 0u) && lane == 0 && !*abort_flag) set_timeout(abort_flag, W.status);
         }
         __syncthreads();
     }
