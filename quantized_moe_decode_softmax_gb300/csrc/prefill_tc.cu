@@ -222,11 +222,52 @@ __device__ __forceinline__ void bar_arrive_cp_async(uint64_t *bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
 }
 
+// A work item: one expert, one block of 128 weight rows, token blocks z, z + ZB,
+// ... of the expert's tokens. Only items with work are numbered: unique
+// expert u (with at least thr tokens) owns items pref[u] .. pref[u + 1] - 1,
+// RB x min(ZB, its token blocks) of them, row block fastest. CTA c of G takes
+// items c, c + G, c + 2 G, ... (item costs differ by at most one token block).
+struct TcItem {
+    int e, off_e, cnt_e, r0, z, total;  // total: chunks (token blocks x chunks per row)
+};
+
+struct TcGrid {
+    int RB, ZB, U, nchunks, G, NI;
+    const int *pref;  // [U + 1] in shared memory
+};
+
+__device__ __forceinline__ int tc_item(const Workspace &ws, const TcGrid &g, int k, TcItem &it) {
+    if (k >= g.NI) return -1;
+    int lo = 0, hi = g.U;                 // last u with pref[u] <= k
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (g.pref[mid] <= k) lo = mid;
+        else hi = mid;
+    }
+    const int local = k - g.pref[lo];
+    const int e = ws.unique[lo];
+    it.e = e;
+    it.off_e = ws.offsets[e];
+    it.cnt_e = ws.offsets[e + 1] - it.off_e;
+    it.r0 = (local % g.RB) * kM;
+    it.z = local / g.RB;
+    const int nblk = (it.cnt_e + kN - 1) / kN;
+    it.total = ((nblk - it.z + g.ZB - 1) / g.ZB) * g.nchunks;
+    return k;
+}
+
+// the item after k in this CTA's list, or -1
+__device__ __forceinline__ int tc_seek(const Workspace &ws, const TcGrid &g, int k, TcItem &it) {
+    return tc_item(ws, g, k, it);
+}
+
 // tm0, tm1: tensor maps of the code planes (gate and up, or down and unused),
-// 2-D {row bytes, rows} with boxes of {cbr, 128}
+// 2-D {row bytes, rows} with boxes of {cbr, 128}. The kernel is persistent: the
+// ring, the A buffers, the scale stream and the accumulator hand-off run on
+// across item boundaries, so the next item's loads overlap this one's tail.
 template <bool GATEUP, int S>
 __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
-    expert_tc_kernel(StepArgs a, Workspace ws, int thr, const __grid_constant__ CUtensorMap tm0,
+    expert_tc_kernel(StepArgs a, Workspace ws, int thr, int ZB, const __grid_constant__ CUtensorMap tm0,
                      const __grid_constant__ CUtensorMap tm1) {
     constexpr int MATS = GATEUP ? 2 : 1;
     constexpr int kDq = MATS * 256;            // dequantisation threads
@@ -235,23 +276,49 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                             ~static_cast<uintptr_t>(1023));
-    const int u = blockIdx.y;
-    if (u >= *ws.U) return;
-    // after a timeout anywhere in the launch, later blocks do no work
+    // after a timeout anywhere in the launch, later CTAs do no work
     if (*reinterpret_cast<volatile unsigned *>(ws.status) & kDevErrTimeout) return;
-    const int e = ws.unique[u];
-    const int off_e = ws.offsets[e], cnt_e = ws.offsets[e + 1] - off_e;
-    if (cnt_e < thr) return;
-    const int nblk = (cnt_e + kN - 1) / kN;
-    if ((int)blockIdx.z >= nblk) return;
-    const int my_blocks = (nblk - (int)blockIdx.z + (int)gridDim.z - 1) / (int)gridDim.z;
-
     const int D = a.s.D, F = a.s.F;
     const int K = GATEUP ? D : F;            // reduction length
-    const int nchunks = K / kK;
-    const int total = my_blocks * nchunks;
-    const int r0 = blockIdx.x * kM;          // first weight row (gate/up: f; down: d)
+    const int rows_pe = GATEUP ? F : D;      // weight rows per expert
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // the item numbering: prefix over the unique experts of their items
+    __shared__ int s_pref[kMaxE + 1];
+    TcGrid g;
+    g.RB = rows_pe / kM;
+    g.ZB = ZB;
+    g.U = *ws.U;
+    g.nchunks = K / kK;
+    g.G = (int)gridDim.x;
+    g.pref = s_pref;
+    if (warp == 0) {
+        int run = 0;
+        for (int u0 = 0; u0 < g.U; u0 += 32) {
+            const int u = u0 + lane;
+            int v = 0;
+            if (u < g.U) {
+                const int e = ws.unique[u];
+                const int cnt = ws.offsets[e + 1] - ws.offsets[e];
+                v = cnt >= thr ? g.RB * min(ZB, (cnt + kN - 1) / kN) : 0;
+            }
+            int inc = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += t;
+            }
+            if (u < g.U) s_pref[u] = run + inc - v;
+            run += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        if (lane == 0) s_pref[g.U] = run;
+    }
+    __syncthreads();
+    g.NI = s_pref[g.U];
+    TcItem first;
+    const int i0 = tc_seek(ws, g, (int)blockIdx.x, first);
+    if (i0 < 0) return;                      // no work for this CTA
+    const int nchunks = g.nchunks;
+
     const bool six = !GATEUP && a.s.down_bits == 6;
     const int cbr = six ? 96 : 64;           // code bytes per row and chunk
     const int stage_stride = stage_bytes_of(MATS, cbr);
@@ -297,48 +364,56 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
     const uint32_t tmem = *tslot;
 
     if (warp >= kProdW && warp < kMmaW) {
-        // ---- producers: B tiles -----------------------------------------------
+        // ---- producers: codes (TMA) and B tiles ----------------------------------
         // B rows: x in f16 (y area, n x D) or h in f16 (first half of each h row)
         // producer warp pw, lane -> 16-byte piece j (of 16) of tokens 16 pw + tq + 2 i;
         // the tokens' row offsets (f16 elements, below 2^31 for every allowed
         // shape: n D <= 8192 x 16384, n k x 2 Dff <= 131072 x 16384) are looked
-        // up once per block
+        // up once per token block
         const uint16_t *bsrc = reinterpret_cast<const uint16_t *>(GATEUP ? (const void *)ws.y : (const void *)ws.h);
         const int j = lane & 15, tq = 16 * (warp - kProdW) + (lane >> 4);
         uint32_t roff[kN / 8];
-        for (int idx = 0; idx < total; ++idx) {
-            const int sidx = idx % S, blk = (int)blockIdx.z + (idx / nchunks) * (int)gridDim.z, c = idx % nchunks;
-            if (c == 0) {
+        int gidx = 0;
+        bool stop = false;
+        TcItem it = first;
+        for (int i = i0; i >= 0 && !stop; i = tc_seek(ws, g, i + g.G, it)) {
+            for (int li = 0; li < it.total; ++li, ++gidx) {
+                const int sidx = gidx % S, blk = it.z + (li / nchunks) * ZB, c = li % nchunks;
+                if (c == 0) {
 #pragma unroll
-                for (int i = 0; i < kN / 8; ++i) {
-                    const int jj = blk * kN + tq + 2 * i;
-                    // tokens past the expert's count are not copied: their
-                    // accumulator columns are never read
-                    roff[i] = jj >= cnt_e ? 0xFFFFFFFFu
-                              : GATEUP    ? (uint32_t)ws.slot_token[off_e + jj] * (uint32_t)D
-                                          : (uint32_t)(off_e + jj) * (uint32_t)(2 * F);
+                    for (int q = 0; q < kN / 8; ++q) {
+                        const int jj = blk * kN + tq + 2 * q;
+                        // tokens past the expert's count are not copied: their
+                        // accumulator columns are never read
+                        roff[q] = jj >= it.cnt_e ? 0xFFFFFFFFu
+                                  : GATEUP       ? (uint32_t)ws.slot_token[it.off_e + jj] * (uint32_t)D
+                                                 : (uint32_t)(it.off_e + jj) * (uint32_t)(2 * F);
+                    }
                 }
-            }
-            if (idx >= S) {
-                const uint32_t par = (uint32_t)((idx / S - 1) & 1);
-                if (!wait_bar(&b_empty[sidx], par, ws.status) || !wait_bar(&c_empty[sidx], par, ws.status))
-                    *abort_flag = 1;
-            }
-            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;  // warp-uniform
-            unsigned char *st = ring + sidx * stage_stride;
-            if (warp == kProdW && lane == 0) {
-                // the chunk's codes: one box of 128 rows x cbr bytes per matrix
-                tc::arrive_expect_tx(&c_full[sidx], (uint32_t)(MATS * kM * cbr));
-                const int y = e * (GATEUP ? F : D) + r0;
-                tc::tma_load_2d(st + off_codes, &tm0, c * cbr, y, &c_full[sidx]);
-                if (GATEUP) tc::tma_load_2d(st + off_codes + kM * cbr, &tm1, c * cbr, y, &c_full[sidx]);
-            }
-            const uint16_t *src = bsrc + (size_t)c * kK + 8 * j;
-            unsigned char *sub = st + (j >> 3) * kSubB;
+                if (gidx >= S) {
+                    const uint32_t par = (uint32_t)((gidx / S - 1) & 1);
+                    if (!wait_bar(&b_empty[sidx], par, ws.status) || !wait_bar(&c_empty[sidx], par, ws.status))
+                        *abort_flag = 1;
+                }
+                if (__any_sync(0xffffffffu, *abort_flag != 0)) {  // warp-uniform
+                    stop = true;
+                    break;
+                }
+                unsigned char *st = ring + sidx * stage_stride;
+                if (warp == kProdW && lane == 0) {
+                    // the chunk's codes: one box of 128 rows x cbr bytes per matrix
+                    tc::arrive_expect_tx(&c_full[sidx], (uint32_t)(MATS * kM * cbr));
+                    const int y = it.e * rows_pe + it.r0;
+                    tc::tma_load_2d(st + off_codes, &tm0, c * cbr, y, &c_full[sidx]);
+                    if (GATEUP) tc::tma_load_2d(st + off_codes + kM * cbr, &tm1, c * cbr, y, &c_full[sidx]);
+                }
+                const uint16_t *src = bsrc + (size_t)c * kK + 8 * j;
+                unsigned char *sub = st + (j >> 3) * kSubB;
 #pragma unroll
-            for (int i = 0; i < kN / 8; ++i)
-                if (roff[i] != 0xFFFFFFFFu) tc::cp_async16(sub + core_off(tq + 2 * i, j & 7), src + roff[i]);
-            bar_arrive_cp_async(&b_full[sidx]);
+                for (int q = 0; q < kN / 8; ++q)
+                    if (roff[q] != 0xFFFFFFFFu) tc::cp_async16(sub + core_off(tq + 2 * q, j & 7), src + roff[q]);
+                bar_arrive_cp_async(&b_full[sidx]);
+            }
         }
     } else if (warp == kMmaW) {
         // ---- MMA issue --------------------------------------------------------
@@ -346,35 +421,43 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
         // matrix descriptor of the first ring stage's B tile (a K step of 16
         // inputs adds 32 bytes, 2 in the start field)
         const uint64_t descB0 = tc::smem_desc_sw128(tc::smem_u32(ring), kSbo);
-        int issued = -1;
-        for (int idx = 0; idx < total; ++idx) {
-            const int bsel = idx % NA, sidx = idx % S, c = idx % nchunks, bi = idx / nchunks;
-            bool ok = wait_bar(&a_full[bsel], (uint32_t)((idx / NA) & 1), ws.status);
-            ok = ok && wait_bar(&b_full[sidx], (uint32_t)((idx / S) & 1), ws.status);
-            // a block's first MMAs overwrite the accumulators of the one before
-            if (ok && c == 0 && bi > 0) ok = wait_bar(acc_empty, (uint32_t)((bi - 1) & 1), ws.status);
-            if (!ok) *abort_flag = 1;
-            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;  // warp-uniform
-            const uint64_t bd0 = descB0 + (uint64_t)((sidx * stage_stride) >> 4);
-            const uint32_t a0 = tmem + kAcol + (uint32_t)(bsel * MATS * 64);
-            __syncwarp();
-            if (tc::elect_one()) {
-                tc::fence_after_sync();
-#pragma unroll
-                for (int ks = 0; ks < kK / 16; ++ks) {
-                    // K step ks: sub-tile ks / 4 of B, 32 bytes per step inside it
-                    const uint64_t bd = bd0 + (uint64_t)(((ks >> 2) * kSubB) >> 4) + 2 * (ks & 3);
-#pragma unroll
-                    for (int m = 0; m < MATS; ++m)
-                        tc::mma_f16_ts(tmem + m * kN, a0 + (uint32_t)(m * 64 + ks * 8), bd, idesc,
-                                       (c > 0 || ks > 0) ? 1u : 0u);
+        int issued = -1, gidx = 0, gblk = 0;
+        bool stop = false;
+        TcItem it = first;
+        for (int i = i0; i >= 0 && !stop; i = tc_seek(ws, g, i + g.G, it)) {
+            for (int li = 0; li < it.total; ++li, ++gidx) {
+                const int bsel = gidx % NA, sidx = gidx % S, c = li % nchunks;
+                bool ok = wait_bar(&a_full[bsel], (uint32_t)((gidx / NA) & 1), ws.status);
+                ok = ok && wait_bar(&b_full[sidx], (uint32_t)((gidx / S) & 1), ws.status);
+                // a block's first MMAs overwrite the accumulators of the one before
+                if (ok && c == 0 && gblk > 0) ok = wait_bar(acc_empty, (uint32_t)((gblk - 1) & 1), ws.status);
+                if (!ok) *abort_flag = 1;
+                if (__any_sync(0xffffffffu, *abort_flag != 0)) {  // warp-uniform
+                    stop = true;
+                    break;
                 }
-                tc::commit(&mma_done[bsel]);
-                tc::commit(&b_empty[sidx]);
-                if (c == nchunks - 1) tc::commit(acc_full);
+                const uint64_t bd0 = descB0 + (uint64_t)((sidx * stage_stride) >> 4);
+                const uint32_t a0 = tmem + kAcol + (uint32_t)(bsel * MATS * 64);
+                __syncwarp();
+                if (tc::elect_one()) {
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int ks = 0; ks < kK / 16; ++ks) {
+                        // K step ks: sub-tile ks / 4 of B, 32 bytes per step inside it
+                        const uint64_t bd = bd0 + (uint64_t)(((ks >> 2) * kSubB) >> 4) + 2 * (ks & 3);
+#pragma unroll
+                        for (int m = 0; m < MATS; ++m)
+                            tc::mma_f16_ts(tmem + m * kN, a0 + (uint32_t)(m * 64 + ks * 8), bd, idesc,
+                                           (c > 0 || ks > 0) ? 1u : 0u);
+                    }
+                    tc::commit(&mma_done[bsel]);
+                    tc::commit(&b_empty[sidx]);
+                    if (c == nchunks - 1) tc::commit(acc_full);
+                }
+                __syncwarp();
+                issued = gidx;
+                if (c == nchunks - 1) ++gblk;
             }
-            __syncwarp();
-            issued = idx;
         }
         // after an abort: wait (bounded) for the MMAs still in flight before
         // the tensor memory is freed
@@ -385,126 +468,147 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
         const int m = (warp >> 2) % MATS, gsel = warp / (4 * MATS);
         const int rr = 32 * (warp & 3) + lane;
         const uint32_t tlane = (uint32_t)(32 * (warp & 3)) << 16;
-        const size_t row = (size_t)e * (GATEUP ? F : D) + r0 + rr;
-        const uint16_t *srow = (GATEUP ? (m ? a.planes.up_s : a.planes.gate_s) : a.planes.down_s) + row * groups;
-        const uint16_t *brow = (GATEUP ? (m ? a.planes.up_b : a.planes.gate_b) : a.planes.down_b) + row * groups;
-        // scale block sb: groups V sb .. V sb + V - 1 of the row = chunks
-        // cpb sb .. cpb sb + cpb - 1 (modulo the groups: the chunk sequence
-        // restarts with every token block) into slot sb % 2 of this thread
-        auto issue_sc = [&](int sb) {
-            if (sb * cpb < total) {
-                const int g0 = (sb * V) % groups;
-                unsigned char *dst = sc_area + ((sb & 1) * kDq + tid) * 32;
+        const uint16_t *s_pl = GATEUP ? (m ? a.planes.up_s : a.planes.gate_s) : a.planes.down_s;
+        const uint16_t *b_pl = GATEUP ? (m ? a.planes.up_b : a.planes.gate_b) : a.planes.down_b;
+        // the scale stream: blocks of V groups (cpb chunks) of this thread's row,
+        // item after item, each into slot (block number) % 2 of this thread; the
+        // cursor (sc_i, sc_it, sc_sb) is the next block to copy
+        int sc_i = i0, sc_sb = 0;
+        TcItem sc_it = first;
+        auto issue_sc = [&](int nb) {
+            if (sc_i >= 0) {
+                const size_t row = (size_t)sc_it.e * rows_pe + sc_it.r0 + rr;
+                const int g0 = (sc_sb * V) % groups;
+                const uint16_t *sr = s_pl + row * groups + g0, *br = b_pl + row * groups + g0;
+                unsigned char *dst = sc_area + ((nb & 1) * kDq + tid) * 32;
                 if (V == 8) {
-                    tc::cp_async16(dst, srow + g0);
-                    tc::cp_async16(dst + 16, brow + g0);
+                    tc::cp_async16(dst, sr);
+                    tc::cp_async16(dst + 16, br);
                 } else if (V == 4) {
-                    tc::cp_async8(dst, srow + g0);
-                    tc::cp_async8(dst + 16, brow + g0);
+                    tc::cp_async8(dst, sr);
+                    tc::cp_async8(dst + 16, br);
                 } else {
-                    tc::cp_async4(dst, srow + g0);
-                    tc::cp_async4(dst + 16, brow + g0);
+                    tc::cp_async4(dst, sr);
+                    tc::cp_async4(dst + 16, br);
+                }
+                if ((sc_sb + 1) * cpb < sc_it.total) {
+                    ++sc_sb;
+                } else {
+                    sc_i = tc_seek(ws, g, sc_i + g.G, sc_it);
+                    sc_sb = 0;
                 }
             }
             tc::cp_async_commit();
         };
+        int nb = 0;       // scale blocks reached so far
         issue_sc(0);
-        for (int idx = 0; idx < total; ++idx) {
-            const int bsel = idx % NA, sidx = idx % S, c = idx % nchunks, bi = idx / nchunks;
-            const int blk = (int)blockIdx.z + bi * (int)gridDim.z;
-            const unsigned char *st = ring + sidx * stage_stride;
-            if (idx % cpb == 0) {
-                // start the next scale block, wait for this one
-                issue_sc(idx / cpb + 1);
-                tc::cp_async_wait<1>();
-            }
-            bool ok = wait_bar(&c_full[sidx], (uint32_t)((idx / S) & 1), ws.status);
-            // A buffer bsel is free once the MMAs of chunk idx - NA are done
-            if (ok && idx >= NA) ok = wait_bar(&mma_done[bsel], (uint32_t)((idx / NA - 1) & 1), ws.status);
-            if (!ok) *abort_flag = 1;
-            // warp-uniform: tcgen05.st and tcgen05.ld below are warp-collective
-            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-            {
-                const uint16_t *scs = reinterpret_cast<const uint16_t *>(sc_area + (((idx / cpb) & 1) * kDq + tid) * 32);
-                const int gi = 2 * (idx % cpb) + gsel;   // this thread's group inside the block
-                float s = bf16f(scs[gi]), b = bf16f(scs[8 + gi]);
-                if (fabsf(s) > 65504.0f || fabsf(b) > 65504.0f) {  // beyond f16: saturate, report
-                    report_error(ws.status, kDevErrRange);
-                    s = fminf(fmaxf(s, -65504.0f), 65504.0f);
-                    b = fminf(fmaxf(b, -65504.0f), 65504.0f);
+        int gidx = 0, gblk = 0;
+        bool stop = false;
+        TcItem it = first;
+        for (int i = i0; i >= 0 && !stop; i = tc_seek(ws, g, i + g.G, it)) {
+            for (int li = 0; li < it.total; ++li, ++gidx) {
+                const int bsel = gidx % NA, sidx = gidx % S, c = li % nchunks;
+                const int blk = it.z + (li / nchunks) * ZB;
+                const unsigned char *st = ring + sidx * stage_stride;
+                if (li % cpb == 0) {
+                    // start the next scale block, wait for this one
+                    issue_sc(nb + 1);
+                    tc::cp_async_wait<1>();
+                    ++nb;
                 }
-                const __half2 s2 = __floats2half2_rn(s, s), b2 = __floats2half2_rn(b, b);
-                uint32_t o[32];
-                if (six) {
-                    const unsigned char *cr = st + off_codes + (m * kM + rr) * 96 + 48 * gsel;
-                    uint32_t v[12];
-#pragma unroll
-                    for (int i = 0; i < 3; ++i) {
-                        const uint4 t4 = *reinterpret_cast<const uint4 *>(cr + 16 * i);
-                        v[4 * i] = t4.x; v[4 * i + 1] = t4.y; v[4 * i + 2] = t4.z; v[4 * i + 3] = t4.w;
-                    }
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint4 r4 = deq_6bit(v, j, s2, b2);
-                        o[4 * j] = r4.x; o[4 * j + 1] = r4.y; o[4 * j + 2] = r4.z; o[4 * j + 3] = r4.w;
-                    }
-                } else {
-                    // 16-byte pieces 2 gsel and 2 gsel + 1 of the row's 64 bytes
-                    const unsigned char *cr = st + off_codes + (m * kM + rr) * 64;
-                    const uint4 w0 = *reinterpret_cast<const uint4 *>(cr + 16 * ((2 * gsel) ^ code_swz(rr)));
-                    const uint4 w1 = *reinterpret_cast<const uint4 *>(cr + 16 * ((2 * gsel + 1) ^ code_swz(rr)));
-                    const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint4 r4 = deq_word(wv[j], s2, b2);
-                        o[4 * j] = r4.x; o[4 * j + 1] = r4.y; o[4 * j + 2] = r4.z; o[4 * j + 3] = r4.w;
-                    }
+                bool ok = wait_bar(&c_full[sidx], (uint32_t)((gidx / S) & 1), ws.status);
+                // A buffer bsel is free once the MMAs of chunk gidx - NA are done
+                if (ok && gidx >= NA) ok = wait_bar(&mma_done[bsel], (uint32_t)((gidx / NA - 1) & 1), ws.status);
+                if (!ok) *abort_flag = 1;
+                // warp-uniform: tcgen05.st and tcgen05.ld below are warp-collective
+                if (__any_sync(0xffffffffu, *abort_flag != 0)) {
+                    stop = true;
+                    break;
                 }
-                // two f16 per 32-bit column in the stored input order: columns
-                // 32 gsel .. 32 gsel + 31 of this matrix's A tile
-                const uint32_t ta = tmem + tlane + kAcol + (uint32_t)((bsel * MATS + m) * 64 + gsel * 32);
-                tc::st_32x32b_x16_async(ta, *reinterpret_cast<const uint32_t(*)[16]>(o));
-                tc::st_32x32b_x16_async(ta + 16, *reinterpret_cast<const uint32_t(*)[16]>(o + 16));
-            }
-            // the codes of this stage have been read
-            bar_arrive(&c_empty[sidx]);
-            tc::wait_st();
-            tc::fence_before_sync();
-            bar_arrive(&a_full[bsel]);
-            if (c == nchunks - 1) {
-                // epilogue of this token block, once its last MMAs have completed
-                if (!wait_bar(acc_full, (uint32_t)(bi & 1), ws.status)) *abort_flag = 1;
-                tc::fence_after_sync();
-                constexpr int kTokW = kN / (kDq / 128);          // tokens per warp (16 or 32)
-                const int t0 = kTokW * (warp >> 2);               // tokens [t0, t0 + kTokW) of the block
-                const int r = r0 + rr;
+                {
+                    const uint16_t *scs =
+                        reinterpret_cast<const uint16_t *>(sc_area + ((((nb - 1) & 1) * kDq) + tid) * 32);
+                    const int gi = 2 * (li % cpb) + gsel;   // this thread's group inside the block
+                    float s = bf16f(scs[gi]), b = bf16f(scs[8 + gi]);
+                    if (fabsf(s) > 65504.0f || fabsf(b) > 65504.0f) {  // beyond f16: saturate, report
+                        report_error(ws.status, kDevErrRange);
+                        s = fminf(fmaxf(s, -65504.0f), 65504.0f);
+                        b = fminf(fmaxf(b, -65504.0f), 65504.0f);
+                    }
+                    const __half2 s2 = __floats2half2_rn(s, s), b2 = __floats2half2_rn(b, b);
+                    uint32_t o[32];
+                    if (six) {
+                        const unsigned char *cr = st + off_codes + (m * kM + rr) * 96 + 48 * gsel;
+                        uint32_t v[12];
 #pragma unroll
-                for (int hh = 0; hh < kTokW / 16; ++hh) {
-                    const int tc0 = t0 + 16 * hh;
-                    float g[16];
-                    tc::ld_32x32b_x16(tmem + tlane + tc0, g);
-                    if (GATEUP) {
-                        float uu[16];
-                        tc::ld_32x32b_x16(tmem + tlane + kN + tc0, uu);
-                        // h row of the slot, f16 in the core order, in the first half of the f32 row
-                        const int pos = (r & ~7) | core_pos(r & 7);
+                        for (int q = 0; q < 3; ++q) {
+                            const uint4 t4 = *reinterpret_cast<const uint4 *>(cr + 16 * q);
+                            v[4 * q] = t4.x; v[4 * q + 1] = t4.y; v[4 * q + 2] = t4.z; v[4 * q + 3] = t4.w;
+                        }
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int j = blk * kN + tc0 + i;
-                            if (j < cnt_e)
-                                reinterpret_cast<__half *>(ws.h + (size_t)(off_e + j) * F)[pos] =
-                                    sat_h(glu_act<true>(a.s.act, a.s.act_limit, g[i], uu[i]), ws.status);
+                        for (int q = 0; q < 8; ++q) {
+                            const uint4 r4 = deq_6bit(v, q, s2, b2);
+                            o[4 * q] = r4.x; o[4 * q + 1] = r4.y; o[4 * q + 2] = r4.z; o[4 * q + 3] = r4.w;
                         }
                     } else {
+                        // 16-byte pieces 2 gsel and 2 gsel + 1 of the row's 64 bytes
+                        const unsigned char *cr = st + off_codes + (m * kM + rr) * 64;
+                        const uint4 w0 = *reinterpret_cast<const uint4 *>(cr + 16 * ((2 * gsel) ^ code_swz(rr)));
+                        const uint4 w1 = *reinterpret_cast<const uint4 *>(cr + 16 * ((2 * gsel + 1) ^ code_swz(rr)));
+                        const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int j = blk * kN + tc0 + i;
-                            if (j < cnt_e) ws.y[(size_t)(off_e + j) * D + r] = g[i];
+                        for (int q = 0; q < 8; ++q) {
+                            const uint4 r4 = deq_word(wv[q], s2, b2);
+                            o[4 * q] = r4.x; o[4 * q + 1] = r4.y; o[4 * q + 2] = r4.z; o[4 * q + 3] = r4.w;
                         }
                     }
+                    // two f16 per 32-bit column in the stored input order: columns
+                    // 32 gsel .. 32 gsel + 31 of this matrix's A tile
+                    const uint32_t ta = tmem + tlane + kAcol + (uint32_t)((bsel * MATS + m) * 64 + gsel * 32);
+                    tc::st_32x32b_x16_async(ta, *reinterpret_cast<const uint32_t(*)[16]>(o));
+                    tc::st_32x32b_x16_async(ta + 16, *reinterpret_cast<const uint32_t(*)[16]>(o + 16));
                 }
+                // the codes of this stage have been read
+                bar_arrive(&c_empty[sidx]);
+                tc::wait_st();
                 tc::fence_before_sync();
-                bar_arrive(acc_empty);
+                bar_arrive(&a_full[bsel]);
+                if (c == nchunks - 1) {
+                    // epilogue of this token block, once its last MMAs have completed
+                    if (!wait_bar(acc_full, (uint32_t)(gblk & 1), ws.status)) *abort_flag = 1;
+                    tc::fence_after_sync();
+                    constexpr int kTokW = kN / (kDq / 128);          // tokens per warp (16 or 32)
+                    const int t0 = kTokW * (warp >> 2);               // tokens [t0, t0 + kTokW) of the block
+                    const int r = it.r0 + rr;
+#pragma unroll
+                    for (int hh = 0; hh < kTokW / 16; ++hh) {
+                        const int tc0 = t0 + 16 * hh;
+                        float gv[16];
+                        tc::ld_32x32b_x16(tmem + tlane + tc0, gv);
+                        if (GATEUP) {
+                            float uu[16];
+                            tc::ld_32x32b_x16(tmem + tlane + kN + tc0, uu);
+                            // h row of the slot, f16 in the core order, in the first half of the f32 row
+                            const int pos = (r & ~7) | core_pos(r & 7);
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) {
+                                const int jj = blk * kN + tc0 + q;
+                                if (jj < it.cnt_e)
+                                    reinterpret_cast<__half *>(ws.h + (size_t)(it.off_e + jj) * F)[pos] =
+                                        sat_h(glu_act<true>(a.s.act, a.s.act_limit, gv[q], uu[q]), ws.status);
+                            }
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) {
+                                const int jj = blk * kN + tc0 + q;
+                                if (jj < it.cnt_e) ws.y[(size_t)(it.off_e + jj) * D + r] = gv[q];
+                            }
+                        }
+                    }
+                    tc::fence_before_sync();
+                    bar_arrive(acc_empty);
+                    ++gblk;
+                }
             }
         }
     }
@@ -591,13 +695,24 @@ cudaError_t launch_expert_tc(const StepArgs &a, const Workspace &ws, int thr, bo
         return err;
     const int maxU = min(a.s.E, a.s.n * a.s.k);
     // token-block slices: about 1.5x the mean tokens per selected expert, in
-    // blocks of 64 (a CTA loops over its slice's blocks; empty CTAs exit)
+    // blocks of 64 (an item loops over its slice's blocks)
     const long mean = ((long)a.s.n * a.s.k + maxU - 1) / maxU;
     const int zb = (int)max(1L, min(8L, (3 * mean / 2 + kN - 1) / kN));
+    // persistent: as many CTAs as fit at once (gate/up one per SM, down two),
+    // at most one per item
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        if ((err = cudaGetDevice(&dev)) != cudaSuccess ||
+            (err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return err;
+    }
+    const long items = (long)((down ? a.s.D : a.s.F) / kM) * maxU * zb;
+    const int grid = (int)min(items, (long)sms * (down ? 2 : 1));
     if (!down)
-        expert_tc_kernel<true, kStagesGateUp><<<dim3(a.s.F / kM, maxU, zb), 672, smem, st>>>(a, ws, thr, tm0, tm1);
+        expert_tc_kernel<true, kStagesGateUp><<<grid, 672, smem, st>>>(a, ws, thr, zb, tm0, tm1);
     else
-        expert_tc_kernel<false, kStagesDown><<<dim3(a.s.D / kM, maxU, zb), 416, smem, st>>>(a, ws, thr, tm0, tm1);
+        expert_tc_kernel<false, kStagesDown><<<grid, 416, smem, st>>>(a, ws, thr, zb, tm0, tm1);
     launched += 1;
     return cudaGetLastError();
 }
