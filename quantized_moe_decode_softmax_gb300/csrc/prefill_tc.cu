@@ -99,14 +99,22 @@ __device__ __forceinline__ uint32_t h2u(__half lo, __half hi) {
 __host__ __device__ __forceinline__ int core_pos(int p) { return p < 4 ? 2 * p : 2 * (p - 4) + 1; }
 
 // one 8-input core of f16 weights from a packed 4-bit word (inputs 8i..8i+7,
-// code j at bits 4j): the pairs (0,4) (1,5) (2,6) (3,7), each w = s q + b
+// code j at bits 4j): the pairs (0,4) (1,5) (2,6) (3,7), each w = s q + b with
+// one rounding. Codes 0 and 4 (2 and 6 after one shift) masked into an f16's
+// mantissa give 1024 + q; codes 1 and 5 (3 and 7) masked in place give
+// 1024 + 16 q, and (1024 + 16 q) / 16 - 64 = q exactly: five integer ops per
+// eight codes
 __device__ __forceinline__ uint4 deq_word(uint32_t w, __half2 s2, __half2 b2) {
     const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
+    const __half2 k16th = __floats2half2_rn(0.0625f, 0.0625f), km64 = __floats2half2_rn(-64.f, -64.f);
+    const uint32_t w8 = w >> 8;
+    const uint32_t v[4] = {(w & 0x000F000Fu) | 0x64006400u, (w & 0x00F000F0u) | 0x64006400u,
+                           (w8 & 0x000F000Fu) | 0x64006400u, (w8 & 0x00F000F0u) | 0x64006400u};
     uint32_t o[4];
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
-        const uint32_t v = ((w >> (4 * p)) & 0x000F000Fu) | 0x64006400u;  // 1024 + q, exact
-        const __half2 q = __hsub2(*reinterpret_cast<const __half2 *>(&v), k1024);
+        const __half2 h = *reinterpret_cast<const __half2 *>(&v[p]);
+        const __half2 q = (p & 1) ? __hfma2(h, k16th, km64) : __hsub2(h, k1024);  // q, exact
         const __half2 r = __hfma2(q, s2, b2);
         o[p] = *reinterpret_cast<const uint32_t *>(&r);
     }
@@ -595,7 +603,7 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
                                 const int jj = blk * kN + tc0 + q;
                                 if (jj < it.cnt_e)
                                     reinterpret_cast<__half *>(ws.h + (size_t)(it.off_e + jj) * F)[pos] =
-                                        sat_h(glu_act<true>(a.s.act, a.s.act_limit, gv[q], uu[q]), ws.status);
+                                        sat_h(glu_act<false>(a.s.act, a.s.act_limit, gv[q], uu[q]), ws.status);
                             }
                         } else {
 #pragma unroll
