@@ -354,13 +354,17 @@ static cudaError_t launch_experts(const StepArgs &a, const Workspace &ws, int ti
         return tc ? launch_expert_tc(a, ws, thr, down, st, launched)
                   : launch_expert_tiles(a, ws, thr, down, st, launched);
     };
+    // with a threshold of one token every selected expert takes the
+    // tensor-core kernels: the GEMV kernels would have nothing to do
+    const bool gemv = thr != 1;
     dim3 block(256);
     cudaError_t err;
     if (thr > 0 && (err = tiles(false)) != cudaSuccess) return err;
     const int T1 = pass_tokens(a.s.D), T2 = pass_tokens(a.s.F);
     const int sm1 = T1 * a.s.D * 4, sm2 = T2 * a.s.F * 4;
     dim3 g1((a.s.F + kRowThreads - 1) / kRowThreads, maxU);
-    if (a.s.x_dtype == MOE_DTYPE_F32) {
+    if (!gemv) {
+    } else if (a.s.x_dtype == MOE_DTYPE_F32) {
         if ((err = cudaFuncSetAttribute(gateup_f32_kernel<MOE_DTYPE_F32>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, sm1)) != cudaSuccess)
             return err;
@@ -371,18 +375,22 @@ static cudaError_t launch_experts(const StepArgs &a, const Workspace &ws, int ti
             return err;
         gateup_f32_kernel<MOE_DTYPE_BF16><<<g1, kRowThreads, sm1, st>>>(a, ws, thr, T1);
     }
-    launched += 1;
-    err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
+    if (gemv) {
+        launched += 1;
+        err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+    }
     if (thr > 0 && (err = tiles(true)) != cudaSuccess) return err;
-    if ((err = cudaFuncSetAttribute(down_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sm2)) !=
-        cudaSuccess)
-        return err;
-    dim3 g2((a.s.D + kRowThreads - 1) / kRowThreads, maxU);
-    down_f32_kernel<<<g2, kRowThreads, sm2, st>>>(a, ws, thr, T2);
-    launched += 1;
-    err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
+    if (gemv) {
+        if ((err = cudaFuncSetAttribute(down_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sm2)) !=
+            cudaSuccess)
+            return err;
+        dim3 g2((a.s.D + kRowThreads - 1) / kRowThreads, maxU);
+        down_f32_kernel<<<g2, kRowThreads, sm2, st>>>(a, ws, thr, T2);
+        launched += 1;
+        err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+    }
     const int total = a.s.n * (a.s.D / 4);
     dim3 g3((total + 255) / 256);
     if (a.s.out_dtype == MOE_DTYPE_F32)
