@@ -492,7 +492,7 @@ def run_ours(args, world, rank, local, pg):
                     "peak_source": f"{tkind} (MEASURED_PEAKS.json bf16 dense)",
                     "flops_per_step": step_flops(shape, n),
                     "timing": "whole step (router, routing, grouped GEMMs, combine) over the "
-                              "K-step graph replay; f16 mma.sync tiles",
+                              "K-step graph replay; tcgen05 grouped GEMMs",
                     "hbm_frac_unique_expert_bytes": achieved * launches_per_step / peak}
     if rank == 0:
         cb = None if args.no_cpu_baseline else cpu_baseline(args)

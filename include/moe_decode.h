@@ -129,10 +129,10 @@ typedef struct {
     int out_dtype;      /* MOE_DTYPE_* of out */
     unsigned flags;     /* MOE_FLAG_* */
     int mma_min_tokens; /* per-expert token count from which an expert of the
-                           grouped and prefill paths takes the tensor-core GEMM
-                           (the rest take the f32 GEMV); 0 = library default:
-                           1 where the tcgen05 GEMMs apply (D and Dff multiples
-                           of 128), else 16 (the mma.sync tile kernels) */
+                           grouped and prefill paths takes the tcgen05 GEMMs
+                           (the rest take the f32 GEMV; shapes whose D or Dff is
+                           not a multiple of 128 keep every expert on the GEMV);
+                           0 = library default, 1 */
     /* ABI version 2 */
     int activation;     /* MOE_ACT_* */
     float act_limit;    /* the clamp bound L of MOE_ACT_SWIGLU_CLAMPED (finite,
@@ -213,17 +213,16 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan **out);
  *                    kernel that writes the whole cohort's routing tables;
  *   n_tokens 17..64, or any n_tokens > 8 with MOE_FLAG_GROUPED_COHORTS:
  *                    the grouped multi-kernel path (router, top-k and
- *                    grouping, per-expert tensor-core GEMMs -- tcgen05 where
- *                    D and Dff are multiples of 128, else mma.sync tiles --
- *                    or GEMV kernels, combine);
+ *                    grouping, per-expert tcgen05 GEMMs (D and Dff multiples
+ *                    of 128) or f32 GEMV kernels, combine);
  *   MOE_FLAG_F32_DEBUG, or a shape the single-launch kernel declines:
  *                    the grouped multi-kernel path with f32 GEMV kernels;
  *   n_tokens 65..max_tokens: the prefill path (#1616 Current Behavior and #1859
  *                    Problem / Background: the sorted matrix path, qmm, of
  *                    prompt processing): routing per token, grouping through
  *                    per-expert token bitmaps, then per expert a grouped GEMM
- *                    (tcgen05, or the mma.sync tiles, over its tokens in
- *                    blocks of 64, each weight tile read once per block) or
+ *                    (tcgen05 over its tokens in blocks of 64, each weight
+ *                    tile read once per block) or
  *                    the f32 GEMV for experts under mma_min_tokens, and the
  *                    combine.
  * Expert range. A plan that owns the experts [expert_begin, expert_end)

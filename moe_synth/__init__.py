@@ -98,10 +98,13 @@ K1 = LayerShape(E=16, top_k=1, D=512, F=256, act_dtype="f32", router_std=1.0 / 5
 DOTS = LayerShape(E=16, top_k=4, D=512, F=256, act_dtype="bf16", router_std=1.0 / 512 ** 0.5,
                   down_bits=6)
 QWEN3_D6 = LayerShape(E=128, top_k=8, D=2048, F=768, act_dtype="bf16", router_std=0.02, down_bits=6)
+# Dff a multiple of 64 but not of 128: outside the single launch's and the
+# tensor-core GEMMs' shape rules (every expert on the f32 GEMV)
+F192 = LayerShape(E=16, top_k=4, D=512, F=192, act_dtype="bf16", router_std=1.0 / 512 ** 0.5)
 
 SHAPES: Dict[str, LayerShape] = {"tiny": TINY, "qwen3": QWEN3, "e256": E256, "k16": K16,
                                  "e1024": E1024, "kall": KALL, "k1": K1, "dots": DOTS,
-                                 "qwen3_d6": QWEN3_D6}
+                                 "qwen3_d6": QWEN3_D6, "f192": F192}
 
 # named workloads: shape, seed, cohort sizes and cohort kinds
 WORKLOADS = {

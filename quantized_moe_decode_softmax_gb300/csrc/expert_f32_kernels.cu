@@ -1,8 +1,11 @@
 // expert_f32_kernels.cu -- the GEMV variant of the grouped path's expert half.
 // Every weight is dequantised exactly to f32 (w = s*q + b) and every product
 // is accumulated in f32 on the CUDA cores. It serves the experts below the
-// tile threshold on the grouped path, and every expert under MOE_FLAG_F32_DEBUG,
-// where it is held to 1e-4 of RMS(out) against the oracle.
+// tensor-core threshold (mma_min_tokens) of the grouped and prefill paths, every
+// expert of a shape the tcgen05 GEMMs decline, and every expert under
+// MOE_FLAG_F32_DEBUG, where it is held to 1e-4 of RMS(out) against the oracle.
+// launch_experts (end of this file) runs the tcgen05 GEMMs, these kernels and
+// the combine for a step.
 //
 // Stages (one launch each), over the de-duplicated expert list:
 //   gate/up : h[p, f] = act(sum_d Wg[e,f,d] x[t,d], sum_d Wu[e,f,d] x[t,d])
@@ -121,7 +124,7 @@ __device__ __forceinline__ void gateup_row(const uint4 *gq, const uint4 *uq, con
 }
 
 // Thread per gate/up row f of expert unique[blockIdx.y] (experts with at
-// least `thr` tokens are left to the tile kernels when thr > 0). Per pass of up
+// least `thr` tokens are left to the tcgen05 GEMMs when thr > 0). Per pass of up
 // to T of the expert's slots, the block stages their activations as f32 in
 // shared memory; every thread then walks its two rows (gate and up) in 16-byte
 // code loads, dequantises each weight exactly and accumulates its products
@@ -344,22 +347,18 @@ __global__ void combine_kernel(StepArgs a, Workspace ws) {
 
 }  // namespace
 
-static cudaError_t launch_experts(const StepArgs &a, const Workspace &ws, int tile_thr, cudaStream_t st,
-                           int &launched, bool tc) {
+cudaError_t launch_experts(const StepArgs &a, const Workspace &ws, int mma_thr, cudaStream_t st,
+                           int &launched) {
     const int maxU = min(a.s.E, a.s.n * a.s.k);
-    // experts from tile_thr tokens: the tcgen05 GEMMs (prefill) or the mma.sync tiles
-    tc = tc && tc_variant_supported(a.s);
-    const int thr = tile_thr > 0 && (tc || tile_variant_supported(a.s)) ? tile_thr : 0;
-    auto tiles = [&](bool down) {
-        return tc ? launch_expert_tc(a, ws, thr, down, st, launched)
-                  : launch_expert_tiles(a, ws, thr, down, st, launched);
-    };
+    // experts from mma_thr tokens on the tcgen05 GEMMs, where the shape allows
+    const int thr = mma_thr > 0 && tc_variant_supported(a.s) ? mma_thr : 0;
+    auto gemms = [&](bool down) { return launch_expert_tc(a, ws, thr, down, st, launched); };
     // with a threshold of one token every selected expert takes the
     // tensor-core kernels: the GEMV kernels would have nothing to do
     const bool gemv = thr != 1;
     dim3 block(256);
     cudaError_t err;
-    if (thr > 0 && (err = tiles(false)) != cudaSuccess) return err;
+    if (thr > 0 && (err = gemms(false)) != cudaSuccess) return err;
     const int T1 = pass_tokens(a.s.D), T2 = pass_tokens(a.s.F);
     const int sm1 = T1 * a.s.D * 4, sm2 = T2 * a.s.F * 4;
     dim3 g1((a.s.F + kRowThreads - 1) / kRowThreads, maxU);
@@ -380,7 +379,7 @@ static cudaError_t launch_experts(const StepArgs &a, const Workspace &ws, int ti
         err = cudaGetLastError();
         if (err != cudaSuccess) return err;
     }
-    if (thr > 0 && (err = tiles(true)) != cudaSuccess) return err;
+    if (thr > 0 && (err = gemms(true)) != cudaSuccess) return err;
     if (gemv) {
         if ((err = cudaFuncSetAttribute(down_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sm2)) !=
             cudaSuccess)
@@ -399,16 +398,6 @@ static cudaError_t launch_experts(const StepArgs &a, const Workspace &ws, int ti
         combine_kernel<MOE_DTYPE_BF16><<<g3, block, 0, st>>>(a, ws);
     launched += 1;
     return cudaGetLastError();
-}
-
-cudaError_t launch_experts_f32(const StepArgs &a, const Workspace &ws, int tile_thr, cudaStream_t st,
-                               int &launched) {
-    return launch_experts(a, ws, tile_thr, st, launched, false);
-}
-
-cudaError_t launch_experts_prefill(const StepArgs &a, const Workspace &ws, int tile_thr, cudaStream_t st,
-                                   int &launched) {
-    return launch_experts(a, ws, tile_thr, st, launched, true);
 }
 
 }  // namespace moe

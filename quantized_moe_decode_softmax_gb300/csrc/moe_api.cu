@@ -161,11 +161,8 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan **out) {
     memset((void *)p, 0, plan_bytes);
     p->cfg = *cfg;
     // default: every selected expert on the tcgen05 GEMMs where they apply (a
-    // 128-row weight tile is dequantised once per 64 tokens, whatever the
-    // count); the mma.sync tiles only pay from about 16 tokens
-    p->mma_min_tokens = cfg->mma_min_tokens > 0 ? cfg->mma_min_tokens
-                        : tc_variant_supported(shape_of(*cfg, 1, cfg->flags)) ? 1
-                                                                               : 16;
+    // 128-row weight tile is dequantised once per 64 tokens, whatever the count)
+    p->mma_min_tokens = cfg->mma_min_tokens > 0 ? cfg->mma_min_tokens : 1;
     if (const char *env = getenv("MOE_MMA_MIN_TOKENS")) {
         int v = atoi(env);
         if (v > 0) p->mma_min_tokens = v;
@@ -342,19 +339,19 @@ moe_status forward_checked(moe_plan *plan, const void *x, const void *router_w,
         if (err == cudaSuccess) err = launch_topk_group(a, plan->ws, s, launched);
     } else if (prefill) {
         // more tokens than a decode cohort: token bitmaps for the grouping, and
-        // the tile kernels loop over each expert's tokens (a grouped GEMM)
+        // the tcgen05 GEMMs loop over each expert's tokens (a grouped GEMM)
         err = launch_router_logits(a, plan->ws, s, launched);
         if (err == cudaSuccess) err = launch_prefill_route(a, plan->ws, plan->cfg.max_tokens, s, launched);
         const int thr = (plan->cfg.flags & MOE_FLAG_F32_DEBUG) ? 0 : plan->mma_min_tokens;
-        if (err == cudaSuccess) err = launch_experts_prefill(a, plan->ws, thr, s, launched);
+        if (err == cudaSuccess) err = launch_experts(a, plan->ws, thr, s, launched);
     } else {
         err = launch_router_logits(a, plan->ws, s, launched);
         if (err == cudaSuccess) err = launch_topk_group(a, plan->ws, s, launched);
         // the f32 check path keeps every expert on the exact f32 kernels; the
         // others with at least mma_min_tokens tokens take the tcgen05 GEMMs
-        // (the mma.sync tiles where the shape does not allow them)
+        // where the shape allows them
         const int thr = (plan->cfg.flags & MOE_FLAG_F32_DEBUG) ? 0 : plan->mma_min_tokens;
-        if (err == cudaSuccess) err = launch_experts_prefill(a, plan->ws, thr, s, launched);
+        if (err == cudaSuccess) err = launch_experts(a, plan->ws, thr, s, launched);
     }
     plan->launches += launched;
     plan->forwards += 1;

@@ -178,13 +178,6 @@ cudaError_t launch_prefill_route(const StepArgs &a, const Workspace &ws, int max
                                  int &launched);
 
 // exact f32 expert path (expert_f32_kernels.cu)
-// expert MLP and combine: experts with at least tile_thr tokens take the tile
-// kernels (tile_thr > 0 and the shape supports them), the rest the f32 GEMV
-cudaError_t launch_experts_f32(const StepArgs &a, const Workspace &ws, int tile_thr, cudaStream_t st,
-                               int &launched);
-bool tile_variant_supported(const Shape &s);
-cudaError_t launch_expert_tiles(const StepArgs &a, const Workspace &ws, int thr, bool down,
-                                cudaStream_t st, int &launched);
 
 // single-launch path (decode_step.cu)
 bool fused_layout(const moe_config &c, int num_sms, int max_smem, DecodeLayout *out);

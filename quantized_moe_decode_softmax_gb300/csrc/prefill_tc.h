@@ -1,5 +1,5 @@
-// prefill_tc.h -- entry points of the prefill path's tcgen05 expert GEMMs
-// (prefill_tc.cu) and of the expert launcher that uses them.
+// prefill_tc.h -- entry points of the tcgen05 expert GEMMs (prefill_tc.cu) and
+// of the expert launcher of the grouped and prefill paths.
 #pragma once
 
 #include "moe_internal.h"
@@ -12,9 +12,10 @@ bool tc_variant_supported(const Shape &s);
 // least `thr` tokens: per block one expert, 128 weight rows, 64 tokens at a time
 cudaError_t launch_expert_tc(const StepArgs &a, const Workspace &ws, int thr, bool down, cudaStream_t st,
                              int &launched);
-// launch_experts_f32 with the tcgen05 GEMMs in place of the mma.sync tiles for
-// the experts with at least tile_thr tokens (the prefill path)
-cudaError_t launch_experts_prefill(const StepArgs &a, const Workspace &ws, int tile_thr, cudaStream_t st,
-                                   int &launched);
+// the per-expert MLPs and the combine of the grouped and prefill paths: experts
+// with at least mma_thr tokens (mma_thr > 0, shape supported) on the tcgen05
+// GEMMs, the others on the f32 GEMV kernels (expert_f32_kernels.cu)
+cudaError_t launch_experts(const StepArgs &a, const Workspace &ws, int mma_thr, cudaStream_t st,
+                           int &launched);
 
 }  // namespace moe

@@ -1,7 +1,7 @@
 """Numerics of the tensor-core paths beyond the bf16 tolerance (GPU).
 
 1. Cohort order. A row permutation of x permutes the output rows bit for bit,
-   on the single launch and the grouped path (tile and GEMV variants): every
+   on the single launch and the grouped path (tcgen05 and GEMV variants): every
    token's result is computed independently of its position. On the chunks of
    the single launch (9..16 tokens) this holds for permutations inside each
    chunk; across chunks the rows agree within the bf16 tolerance.
@@ -30,7 +30,7 @@
 3. f16 range. Activations far below or beyond f16's range take a per-token
    power-of-two scale on the single launch and still match the oracle; an
    intermediate h beyond f16's range is reported as MOE_ERR_RANGE (single
-   launch and tile variant), and the f32 check path computes the same layer.
+   launch and the tcgen05 GEMMs), and the f32 check path computes the same layer.
 """
 import numpy as np
 import pytest
@@ -176,7 +176,7 @@ def test_single_launch_scales_tokens_outside_f16_range(scale_exp):
 def test_h_beyond_f16_range_is_reported():
     """Activations of order 2^12 on the 128-expert layer make h of order 10^6:
     the single launch reports MOE_ERR_RANGE (on moe_plan_check and on the next
-    forward call), the tile variant too, and the f32 check path computes the
+    forward call), the tcgen05 GEMMs too, and the f32 check path computes the
     step."""
     import torch
     import quantized_moe_decode_softmax_gb300 as q
@@ -198,7 +198,7 @@ def test_h_beyond_f16_range_is_reported():
     ref = run_oracle(lay, x)
     out, _ = run_gpu(plan, dl, shape, x)
     assert_out_close(out, ref["out"], TOL_BF16)
-    # tile variant (every expert on the tile kernels)
+    # grouped path (every expert on the tcgen05 GEMMs)
     tplan = make_plan(shape, flags=q.MOE_FLAG_GROUPED_COHORTS, mma_min_tokens=1)
     lay16, x16 = case("qwen3", 2, 16)
     dl16 = device_layer(lay16)

@@ -19,12 +19,13 @@ GROUPED = 1 << 3  # MOE_FLAG_GROUPED_COHORTS
 
 
 def _check(shape_name, seed, n, kind="independent", full=False, flags=0, out_dtype=None,
-           tol=None, mma_min_tokens=0):
+           tol=None, mma_min_tokens=0, max_tokens=64):
     import os
     lay, x = case(shape_name, seed, n, kind, full=full)
     shape = lay.shape
     ref = run_oracle(lay, x)
-    plan = make_plan(shape, flags=flags, out_dtype=out_dtype, mma_min_tokens=mma_min_tokens)
+    plan = make_plan(shape, flags=flags, out_dtype=out_dtype, mma_min_tokens=mma_min_tokens,
+                     max_tokens=max_tokens)
     launches = []
     out, routing = run_gpu(plan, device_layer(lay), shape, x, launches)
     assert_routing_equal(routing, ref)
@@ -34,7 +35,7 @@ def _check(shape_name, seed, n, kind="independent", full=False, flags=0, out_dty
     err_rel = err / max(float(np.sqrt(np.mean(np.square(ref["out"].astype(np.float64))))), 1e-30)
     path = path_name(n, launches[0], flags)
     if mma_min_tokens:
-        path += f", tile threshold {mma_min_tokens}"
+        path += f", tensor-core threshold {mma_min_tokens}"
     record_margin(os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0], shape_name, n, kind,
                   path, out_dtype, tol, err_rel)
     return assert_out_close(out, ref["out"], tol)
@@ -85,17 +86,26 @@ def test_qwen3_shared_64_tokens_single_expert_set():
 
 @pytest.mark.parametrize("shape_name,seed,n,full", [("qwen3", 2, 16, False), ("e256", 3, 16, False),
                                                    ("tiny", 0, 12, True)])
-def test_tile_variant_for_every_expert(shape_name, seed, n, full):
+def test_tensor_core_gemms_for_every_expert(shape_name, seed, n, full):
     # mma_min_tokens = 1 on the grouped path: every selected expert takes the
-    # tile kernels (weights dequantised in shared memory, tensor-core tiles over
-    # its tokens)
+    # tcgen05 GEMMs (weights dequantised into tensor memory, its tokens in
+    # blocks of 64)
     _check(shape_name, seed, n, full=full, flags=GROUPED, mma_min_tokens=1)
 
 
-def test_tile_variant_with_mixed_counts():
+def test_tensor_core_gemms_with_mixed_counts():
     # threshold 3 on a 64-token cohort: experts with at least 3 tokens take the
-    # tile kernels, the others the GEMV kernels, in the same step
+    # tcgen05 GEMMs, the others the GEMV kernels, in the same step
     _check("qwen3", 2, 64, mma_min_tokens=3)
+
+
+@pytest.mark.parametrize("n,kind", [(3, "independent"), (24, "independent"), (64, "shared"),
+                                    (200, "independent")])
+def test_shape_outside_the_tcgen05_rule_runs_on_the_gemv(n, kind):
+    # Dff = 192 (a multiple of 64, not of 128): the single launch and the
+    # tcgen05 GEMMs decline the shape, so every cohort takes the grouped (or
+    # prefill) path with every expert on the f32 GEMV kernels
+    _check("f192", 7, n, kind, full=True, tol=TOL_BF16, max_tokens=max(n, 64))
 
 
 # ---- 256-expert top-6 layer (D=4096, Dff=2048, Zipf router bias) ------------------

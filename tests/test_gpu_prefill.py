@@ -2,7 +2,7 @@
 
 Routing is bit-exact against the oracle, grouping too (token bitmaps per
 expert give the oracle's order: experts ascending, tokens ascending), and the
-outputs are within the bf16 tolerance (the tile variant for experts with at
+outputs are within the bf16 tolerance (the tcgen05 GEMMs for experts with at
 least mma_min_tokens tokens, looping over each expert's tokens in blocks of
 64) or the f32 tolerance (the f32 check path). Sizes span several token
 blocks per expert and ragged tails.

@@ -1,9 +1,9 @@
 """Layer variants and the expert-parallel split on the GPU, against the oracle.
 
 - Activations (GeGLU, GeGLU in its tanh form, clamped SwiGLU) on the single
-  launch, its chunks, the grouped path's GEMV and tile variants and the f32
-  check path.
-- 6-bit down planes (4-bit gate/up) on the grouped path, GEMV and tile
+  launch, its chunks, the grouped path's GEMV and tcgen05 variants and the
+  f32 check path.
+- 6-bit down planes (4-bit gate/up) on the grouped path, GEMV and tcgen05
   variants and the f32 check path (the single launch declines them).
 - Expert-parallel shards: G plans over a partition of the experts, each
   writing an f32 partial; each partial matches the oracle on planes whose
@@ -45,7 +45,7 @@ def _check(shape_name, seed, n, kind="independent", full=False, flags=0, out_dty
     assert_routing_equal(routing, ref)
     tol = tol or (TOL_F32 if flags & F32_DEBUG else TOL_BF16)
     err_rel = float(np.abs(out.astype(np.float64) - ref["out"]).max()) / max(rms(ref["out"]), 1e-30)
-    path = path_name(n, launches[0], flags) + (f", tile threshold {mma_min_tokens}" if mma_min_tokens else "")
+    path = path_name(n, launches[0], flags) + (f", tensor-core threshold {mma_min_tokens}" if mma_min_tokens else "")
     record_margin(os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0], shape_name, n, kind,
                   path + f", {act}", out_dtype, tol, err_rel)
     assert_out_close(out, ref["out"], tol)
@@ -57,7 +57,7 @@ def _check(shape_name, seed, n, kind="independent", full=False, flags=0, out_dty
     (8, "shared", 0, 0),               # single launch, 8 tokens on 8 experts
     (12, "independent", 0, 0),         # chunks of the single launch
     (24, "independent", 0, 0),         # grouped, GEMV variant
-    (24, "shared", GROUPED, 0),        # grouped, tile variant (24 tokens per expert)
+    (24, "shared", GROUPED, 0),        # grouped, tcgen05 GEMMs (24 tokens per expert)
     (4, "independent", F32_DEBUG, 0),  # f32 check path
 ])
 def test_activation_variants_qwen3(act, n, kind, flags, mma):
@@ -68,14 +68,14 @@ def test_activation_variants_qwen3(act, n, kind, flags, mma):
 @pytest.mark.parametrize("act", sorted(ACTS))
 def test_activation_variants_other_shapes(act):
     _check("tiny", 0, 3, full=True, act=act)                            # grouped, f32 x
-    _check("tiny", 0, 12, full=True, act=act, flags=GROUPED, mma_min_tokens=1)  # tile variant
+    _check("tiny", 0, 12, full=True, act=act, flags=GROUPED, mma_min_tokens=1)  # tcgen05 GEMMs
     _check("e256", 3, 4, act=act)                                       # single launch, D = 4096
 
 
 @pytest.mark.parametrize("n,flags,mma,out_dtype", [
     (1, 0, 0, None),             # grouped (the single launch declines 6-bit down)
     (3, 0, 0, None),
-    (12, GROUPED, 1, None),      # tile variant for every expert
+    (12, GROUPED, 1, None),      # tcgen05 GEMMs for every expert
     (5, F32_DEBUG, 0, "f32"),    # f32 check path
 ])
 def test_six_bit_down_planes(n, flags, mma, out_dtype):
@@ -114,7 +114,7 @@ def _expected_shard_grouping(ref, lo, hi, E):
     ("qwen3", 4, "independent", 0, 0),        # single launch
     ("qwen3", 12, "independent", 0, 0),       # chunks of the single launch
     ("qwen3", 24, "independent", 0, 0),       # grouped, GEMV variant
-    ("qwen3", 24, "shared", GROUPED, 0),      # grouped, tile variant
+    ("qwen3", 24, "shared", GROUPED, 0),      # grouped, tcgen05 GEMMs
     ("qwen3", 4, "independent", F32_DEBUG, 0),  # f32 check path
     ("dots", 6, "independent", 0, 0),         # 6-bit down planes
 ])
