@@ -339,9 +339,11 @@ moe_status forward_checked(moe_plan *plan, const void *x, const void *router_w,
         if (err == cudaSuccess) err = launch_topk_group(a, plan->ws, s, launched);
     } else if (prefill) {
         // more tokens than a decode cohort: token bitmaps for the grouping, and
-        // the tcgen05 GEMMs loop over each expert's tokens (a grouped GEMM)
-        err = launch_router_logits(a, plan->ws, s, launched);
-        if (err == cudaSuccess) err = launch_prefill_route(a, plan->ws, plan->cfg.max_tokens, s, launched);
+        // the tcgen05 GEMMs loop over each expert's tokens (a grouped GEMM); the
+        // router on the tensor cores too, except on the f32 check path
+        const bool rtc = !(plan->cfg.flags & MOE_FLAG_F32_DEBUG) && router_tc_supported(a.s);
+        err = rtc ? launch_router_tc(a, plan->ws, s, launched) : launch_router_logits(a, plan->ws, s, launched);
+        if (err == cudaSuccess) err = launch_prefill_route(a, plan->ws, plan->cfg.max_tokens, s, launched, rtc);
         const int thr = (plan->cfg.flags & MOE_FLAG_F32_DEBUG) ? 0 : plan->mma_min_tokens;
         if (err == cudaSuccess) err = launch_experts(a, plan->ws, thr, s, launched);
     } else {

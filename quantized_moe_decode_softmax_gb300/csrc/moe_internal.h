@@ -170,12 +170,14 @@ namespace moe {
 // Each launcher adds the number of kernels it enqueued to `launched`.
 cudaError_t launch_router_logits(const StepArgs &a, const Workspace &ws, cudaStream_t st,
                                  int &launched);
+// refine: the logits came from the tensor-core router; the weights are taken
+// from the k selected logits recomputed with the CUDA-core router's sum
 cudaError_t launch_topk_group(const StepArgs &a, const Workspace &ws, cudaStream_t st,
-                              int &launched);
+                              int &launched, bool refine = false);
 // routing and grouping of a prefill cohort (more than kMaxTokens tokens) from
 // the logits: top-k per token, per-expert token bitmaps, counts, offsets, slots
 cudaError_t launch_prefill_route(const StepArgs &a, const Workspace &ws, int max_n, cudaStream_t st,
-                                 int &launched);
+                                 int &launched, bool refine = false);
 
 // exact f32 expert path (expert_f32_kernels.cu)
 

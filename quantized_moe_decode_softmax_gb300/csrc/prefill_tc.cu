@@ -627,6 +627,103 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
     if (warp == 0) tc::tmem_dealloc(tmem, kCols);
 }
 
+// ---- router logits -----------------------------------------------------------------
+// logits[t, e] = x[t] . Wr[e] (+ bias[e]) as a bf16 x bf16 -> f32 GEMM: per CTA
+// 128 tokens (M) x 32 experts (N: more CTAs share the router matrix's read),
+// K in chunks of 64 inputs (one 128-byte
+// swizzled row per token or expert), both operands by TMA into a 4-stage ring,
+// the accumulator in tensor memory. One thread issues the loads and the MMAs;
+// the CTA's four warps read the accumulator back (lane = token) and add the
+// bias. Products of bf16 are exact in f32; only the order of the f32 sum
+// differs from the CUDA-core router, far inside the top-k margins.
+constexpr int kRM = 128, kRN = 32, kRK = 64, kRS = 4;
+constexpr int kRTileA = kRM * kRK * 2;    // 16 KB of x per stage
+constexpr int kRTileB = kRN * kRK * 2;    // 4 KB of router rows per stage
+constexpr int kRStage = kRTileA + kRTileB;
+
+__global__ void __launch_bounds__(128, 1)
+    router_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
+                     const float *bias, float *logits, int n, int E, int D, unsigned *status) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *base = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                            ~static_cast<uintptr_t>(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + kRS * kRStage);
+    uint64_t *empty = full + kRS, *acc = empty + kRS;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(acc + 1);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int t0 = blockIdx.x * kRM, e0 = blockIdx.y * kRN, nk = D / kRK;
+    if (tid == 0) {
+        for (int i = 0; i < kRS; ++i) {
+            bar_init(&full[i], 1);
+            bar_init(&empty[i], 1);
+        }
+        bar_init(acc, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) tc::tmem_alloc(tslot, kRN);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    if (warp == 0) {
+        if (tc::elect_one()) {
+            const uint32_t idesc = tc::idesc_bf16_f32(kRM, kRN);
+            auto load = [&](int kc) {
+                unsigned char *st = base + (kc % kRS) * kRStage;
+                tc::arrive_expect_tx(&full[kc % kRS], (uint32_t)kRStage);
+                tc::tma_load_2d(st, &tmx, kc * kRK, t0, &full[kc % kRS]);
+                tc::tma_load_2d(st + kRTileA, &tmw, kc * kRK, e0, &full[kc % kRS]);
+            };
+            int issued = 0, used = 0;
+            bool ok = true;
+            for (; issued < min(kRS - 1, nk); ++issued) load(issued);
+            for (int kc = 0; kc < nk && ok; ++kc) {
+                if (issued < nk) {
+                    // the slot of chunk issued - kRS = kc - 1 is free once its MMAs are done
+                    if (issued >= kRS)
+                        ok = wait_bar(&empty[issued % kRS], (uint32_t)((issued / kRS - 1) & 1), status);
+                    if (!ok) break;
+                    load(issued++);
+                }
+                ok = wait_bar(&full[kc % kRS], (uint32_t)((kc / kRS) & 1), status);
+                if (!ok) break;
+                tc::fence_after_sync();
+                const unsigned char *st = base + (kc % kRS) * kRStage;
+                const uint64_t ad = tc::smem_desc_sw128(tc::smem_u32(st), kSbo);
+                const uint64_t bd = tc::smem_desc_sw128(tc::smem_u32(st + kRTileA), kSbo);
+#pragma unroll
+                for (int ks = 0; ks < kRK / 16; ++ks)
+                    tc::mma_f16(tmem, ad + 2 * ks, bd + 2 * ks, idesc, (kc > 0 || ks > 0) ? 1u : 0u);
+                tc::commit(&empty[kc % kRS]);
+                used = kc + 1;
+            }
+            tc::commit(acc);  // arrives once every MMA issued above has completed
+            // after a timeout: let the loads still in flight land before the CTA exits
+            for (int i = used; i < issued; ++i) wait_bar(&full[i % kRS], (uint32_t)((i / kRS) & 1), status);
+        }
+        __syncwarp();
+    }
+    const bool done = wait_bar(acc, 0u, status);
+    tc::fence_after_sync();
+    const int t = t0 + 32 * warp + lane;   // this thread's TMEM lane = token
+#pragma unroll 1
+    for (int c = 0; c < kRN; c += 16) {
+        float v[16];
+        tc::ld_32x32b_x16(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)c, v);
+        if (done && t < n) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int e = e0 + c + i;
+                if (e < E) logits[(size_t)t * E + e] = v[i] + (bias ? bias[e] : 0.f);
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 0) tc::tmem_dealloc(tmem, kRN);
+}
+
 // ring stages per variant
 constexpr int kStagesGateUp = 4;   // 4 x 32 KB + 32 KB scale slots
 constexpr int kStagesDown = 3;     // 3 x 24 KB (6-bit 28 KB) + 16 KB: two CTAs per SM
@@ -721,6 +818,38 @@ cudaError_t launch_expert_tc(const StepArgs &a, const Workspace &ws, int thr, bo
         expert_tc_kernel<true, kStagesGateUp><<<grid, 672, smem, st>>>(a, ws, thr, zb, tm0, tm1);
     else
         expert_tc_kernel<false, kStagesDown><<<grid, 416, smem, st>>>(a, ws, thr, zb, tm0, tm1);
+    launched += 1;
+    return cudaGetLastError();
+}
+
+
+bool router_tc_supported(const Shape &s) {
+    return s.x_dtype == MOE_DTYPE_BF16 && s.w_dtype == MOE_DTYPE_BF16 && s.D % kRK == 0;
+}
+
+cudaError_t launch_router_tc(const StepArgs &a, const Workspace &ws, cudaStream_t st, int &launched) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return cudaErrorInvalidValue;
+    alignas(64) CUtensorMap tmx, tmw;
+    // 2-D bf16 views {D, rows}, boxes of {64 inputs, 128 tokens or 32 experts},
+    // 128-byte swizzle; rows past the end (tokens or experts) read as zeros
+    auto enc = [&](CUtensorMap *m, const void *p, int rows, int box_rows) {
+        cuuint64_t dims[2] = {(cuuint64_t)a.s.D, (cuuint64_t)rows};
+        cuuint64_t strides[1] = {(cuuint64_t)a.s.D * 2u};
+        cuuint32_t box[2] = {(cuuint32_t)kRK, (cuuint32_t)box_rows};
+        cuuint32_t es[2] = {1, 1};
+        return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(p), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    // a map the driver declines: the CUDA-core router computes the same logits
+    if (!enc(&tmx, a.x, a.s.n, kRM) || !enc(&tmw, a.router_w, a.s.E, kRN))
+        return launch_router_logits(a, ws, st, launched);
+    const int smem = 1024 + kRS * kRStage + 64;
+    cudaError_t err = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    dim3 grid((a.s.n + kRM - 1) / kRM, (a.s.E + kRN - 1) / kRN);
+    router_tc_kernel<<<grid, 128, smem, st>>>(tmx, tmw, a.router_bias, ws.logits, a.s.n, a.s.E, a.s.D, ws.status);
     launched += 1;
     return cudaGetLastError();
 }

@@ -12,6 +12,11 @@ bool tc_variant_supported(const Shape &s);
 // least `thr` tokens: per block one expert, 128 weight rows, 64 tokens at a time
 cudaError_t launch_expert_tc(const StepArgs &a, const Workspace &ws, int thr, bool down, cudaStream_t st,
                              int &launched);
+// router logits on the tensor cores (bf16 x and router rows, f32 accumulation):
+// logits[t, e] = x[t] . Wr[e] (+ bias[e]) for the grouped and prefill paths
+bool router_tc_supported(const Shape &s);
+cudaError_t launch_router_tc(const StepArgs &a, const Workspace &ws, cudaStream_t st, int &launched);
+
 // the per-expert MLPs and the combine of the grouped and prefill paths: experts
 // with at least mma_thr tokens (mma_thr > 0, shape supported) on the tcgen05
 // GEMMs, the others on the f32 GEMV kernels (expert_f32_kernels.cu)

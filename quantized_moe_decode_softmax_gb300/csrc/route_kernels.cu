@@ -79,9 +79,49 @@ __global__ void router_logits_kernel(const void *__restrict__ x, const void *__r
     }
 }
 
+// When the logits came from the tensor-core router (bf16 x and router rows,
+// a different f32 summation order), the top-k selection uses them (the
+// top-k margins make it order-independent), and the k selected logits are
+// recomputed with router_logits_kernel's sum -- lane l takes inputs 8 l ..
+// 8 l + 7 of every 256 in turn, then the butterfly -- and renormalised over
+// the k (the full softmax's maximum and denominator cancel), so the weights
+// keep the CUDA-core router's rounding. x == nullptr: no recomputation.
+struct RefineArgs {
+    const void *x, *w;
+    const float *bias;
+    int D;
+};
+
+__device__ __forceinline__ void warp_refine_weights(const RefineArgs &rf, int t, int k, int lane,
+                                                    const int *idx, float *w_out) {
+    float lk[kMaxTopK];
+    float mx = -INFINITY;
+    for (int j = 0; j < k; ++j) {
+        const int e = idx[j];
+        float acc = 0.f;
+        for (int i = lane * 8; i < rf.D; i += 256) {
+            float xv[8], wv[8];
+            load8<MOE_DTYPE_BF16>(rf.x, (size_t)t * rf.D + i, xv);
+            load8<MOE_DTYPE_BF16>(rf.w, (size_t)e * rf.D + i, wv);
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) acc = fmaf(xv[jj], wv[jj], acc);
+        }
+        lk[j] = warp_sum(acc) + (rf.bias ? rf.bias[e] : 0.f);
+        mx = fmaxf(mx, lk[j]);
+    }
+    if (lane == 0) {
+        float ex[kMaxTopK], s = 0.f;
+        for (int j = 0; j < k; ++j) {
+            ex[j] = expf(lk[j] - mx);
+            s += ex[j];
+        }
+        for (int j = 0; j < k; ++j) w_out[j] = ex[j] / s;
+    }
+}
+
 // one CTA: softmax, top-k, renormalise, then group; writes the workspace
 __global__ void __launch_bounds__(1024) topk_group_kernel(Workspace ws, int n, int E, int k, int e_lo,
-                                                          int e_hi) {
+                                                          int e_hi, RefineArgs rf) {
     __shared__ int s_idx[kMaxSlots];
     __shared__ float s_w[kMaxSlots];
     __shared__ unsigned long long s_mask[kMaxE];
@@ -92,6 +132,11 @@ __global__ void __launch_bounds__(1024) topk_group_kernel(Workspace ws, int n, i
     __shared__ int s_U;
     block_topk(ws.logits, n, E, k, s_idx, s_w);
     __syncthreads();
+    if (rf.x) {
+        const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+        for (int t = threadIdx.x >> 5; t < n; t += nw) warp_refine_weights(rf, t, k, lane, s_idx + t * k, s_w + t * k);
+        __syncthreads();
+    }
     block_group(s_idx, n, E, k, e_lo, e_hi, s_mask, s_counts, s_off, s_st, s_sk, s_of, s_unique, &s_U);
     const int S = n * k;
     for (int s = threadIdx.x; s < S; s += blockDim.x) {
@@ -119,7 +164,7 @@ __global__ void __launch_bounds__(1024) topk_group_kernel(Workspace ws, int n, i
 // expert), built in four data-parallel steps with no order-dependent atomics.
 
 // one warp per token: top-k and renormalised weights
-__global__ void topk_tokens_kernel(Workspace ws, int n, int E, int k) {
+__global__ void topk_tokens_kernel(Workspace ws, int n, int E, int k, RefineArgs rf) {
     const int t = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
     if (t >= n) return;
     const float *lt = ws.logits + (size_t)t * E;
@@ -131,6 +176,10 @@ __global__ void topk_tokens_kernel(Workspace ws, int n, int E, int k) {
     else if (E <= 256) warp_topk_token<8>(lt, E, k, lane, io, wo);
     else if (E <= 512) warp_topk_token<16>(lt, E, k, lane, io, wo);
     else warp_topk_token<32>(lt, E, k, lane, io, wo);
+    if (rf.x) {
+        __syncwarp();  // lane 0 wrote the indices
+        warp_refine_weights(rf, t, k, lane, io, wo);
+    }
 }
 
 // slot s = (t, j) sets bit t of its expert's bitmap (owned experts only)
@@ -228,13 +277,14 @@ __global__ void group_fill_kernel(Workspace ws, int k, int W) {
 }  // namespace
 
 cudaError_t launch_prefill_route(const StepArgs &a, const Workspace &ws, int max_n, cudaStream_t st,
-                                 int &launched) {
+                                 int &launched, bool refine) {
+    const RefineArgs rf{refine ? a.x : nullptr, a.router_w, a.router_bias, a.s.D};
     const int n = a.s.n, E = a.s.E, k = a.s.k;
     const int W = (n + 31) / 32, Wcap = (max_n + 31) / 32;
     (void)Wcap;
     cudaError_t err = cudaMemsetAsync(ws.tbits, 0, (size_t)E * W * 4, st);
     if (err != cudaSuccess) return err;
-    topk_tokens_kernel<<<(n + 7) / 8, 256, 0, st>>>(ws, n, E, k);
+    topk_tokens_kernel<<<(n + 7) / 8, 256, 0, st>>>(ws, n, E, k, rf);
     group_mark_kernel<<<(n * k + 255) / 256, 256, 0, st>>>(ws, n, k, a.s.e_lo, a.s.e_hi, W);
     group_count_kernel<<<E, 256, 0, st>>>(ws, W);
     group_offsets_kernel<<<1, 32, 0, st>>>(ws, E);
@@ -266,8 +316,9 @@ cudaError_t launch_router_logits(const StepArgs &a, const Workspace &ws, cudaStr
 }
 
 cudaError_t launch_topk_group(const StepArgs &a, const Workspace &ws, cudaStream_t st,
-                              int &launched) {
-    topk_group_kernel<<<1, 1024, 0, st>>>(ws, a.s.n, a.s.E, a.s.k, a.s.e_lo, a.s.e_hi);
+                              int &launched, bool refine) {
+    const RefineArgs rf{refine ? a.x : nullptr, a.router_w, a.router_bias, a.s.D};
+    topk_group_kernel<<<1, 1024, 0, st>>>(ws, a.s.n, a.s.E, a.s.k, a.s.e_lo, a.s.e_hi, rf);
     launched += 1;
     return cudaGetLastError();
 }

@@ -93,6 +93,14 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
            | ((uint32_t)(M >> 4) << 24);      // M / 16
 }
 
+// the same with bf16 A and B
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return (1u << 4)                          // D format: f32
+           | (1u << 7) | (1u << 10)           // A, B format: bf16
+           | ((uint32_t)(N >> 3) << 17)       // N / 8
+           | ((uint32_t)(M >> 4) << 24);      // M / 16
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                         uint32_t accumulate) {
