@@ -92,31 +92,37 @@ struct RefineArgs {
     int D;
 };
 
+// logit of expert e for token t with router_logits_kernel's sum (a whole warp)
+__device__ __forceinline__ float warp_router_logit(const RefineArgs &rf, int t, int e, int lane) {
+    float acc = 0.f;
+    for (int i = lane * 8; i < rf.D; i += 256) {
+        float xv[8], wv[8];
+        load8<MOE_DTYPE_BF16>(rf.x, (size_t)t * rf.D + i, xv);
+        load8<MOE_DTYPE_BF16>(rf.w, (size_t)e * rf.D + i, wv);
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) acc = fmaf(xv[jj], wv[jj], acc);
+    }
+    return warp_sum(acc) + (rf.bias ? rf.bias[e] : 0.f);
+}
+
+// weights renormalised over the k logits lk (one thread)
+__device__ __forceinline__ void renorm_selected(const float *lk, int k, float *w_out) {
+    float mx = -INFINITY, s = 0.f;
+    for (int j = 0; j < k; ++j) mx = fmaxf(mx, lk[j]);
+    float ex[kMaxTopK];
+    for (int j = 0; j < k; ++j) {
+        ex[j] = expf(lk[j] - mx);
+        s += ex[j];
+    }
+    for (int j = 0; j < k; ++j) w_out[j] = ex[j] / s;
+}
+
+// one warp: the k selected logits in turn, then the weights
 __device__ __forceinline__ void warp_refine_weights(const RefineArgs &rf, int t, int k, int lane,
                                                     const int *idx, float *w_out) {
     float lk[kMaxTopK];
-    float mx = -INFINITY;
-    for (int j = 0; j < k; ++j) {
-        const int e = idx[j];
-        float acc = 0.f;
-        for (int i = lane * 8; i < rf.D; i += 256) {
-            float xv[8], wv[8];
-            load8<MOE_DTYPE_BF16>(rf.x, (size_t)t * rf.D + i, xv);
-            load8<MOE_DTYPE_BF16>(rf.w, (size_t)e * rf.D + i, wv);
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) acc = fmaf(xv[jj], wv[jj], acc);
-        }
-        lk[j] = warp_sum(acc) + (rf.bias ? rf.bias[e] : 0.f);
-        mx = fmaxf(mx, lk[j]);
-    }
-    if (lane == 0) {
-        float ex[kMaxTopK], s = 0.f;
-        for (int j = 0; j < k; ++j) {
-            ex[j] = expf(lk[j] - mx);
-            s += ex[j];
-        }
-        for (int j = 0; j < k; ++j) w_out[j] = ex[j] / s;
-    }
+    for (int j = 0; j < k; ++j) lk[j] = warp_router_logit(rf, t, idx[j], lane);
+    if (lane == 0) renorm_selected(lk, k, w_out);
 }
 
 // one CTA: softmax, top-k, renormalise, then group; writes the workspace
@@ -163,22 +169,35 @@ __global__ void __launch_bounds__(1024) topk_group_kernel(Workspace ws, int n, i
 // The grouped order is the same (experts ascending, tokens ascending within an
 // expert), built in four data-parallel steps with no order-dependent atomics.
 
-// one warp per token: top-k and renormalised weights
-__global__ void topk_tokens_kernel(Workspace ws, int n, int E, int k, RefineArgs rf) {
-    const int t = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+// one CTA of 8 warps per token: warp 0 takes the top-k and renormalised
+// weights; with rf.x, the 8 warps then recompute the k selected logits side by
+// side and thread 0 renormalises over them
+__global__ void __launch_bounds__(256) topk_tokens_kernel(Workspace ws, int n, int E, int k, RefineArgs rf) {
+    __shared__ int s_i[kMaxTopK];
+    __shared__ float s_wt[kMaxTopK], s_l[kMaxTopK];
+    const int t = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (t >= n) return;
-    const float *lt = ws.logits + (size_t)t * E;
-    int *io = ws.topk_idx + (size_t)t * k;
-    float *wo = ws.topk_w + (size_t)t * k;
-    if (E <= 32) warp_topk_token<1>(lt, E, k, lane, io, wo);
-    else if (E <= 64) warp_topk_token<2>(lt, E, k, lane, io, wo);
-    else if (E <= 128) warp_topk_token<4>(lt, E, k, lane, io, wo);
-    else if (E <= 256) warp_topk_token<8>(lt, E, k, lane, io, wo);
-    else if (E <= 512) warp_topk_token<16>(lt, E, k, lane, io, wo);
-    else warp_topk_token<32>(lt, E, k, lane, io, wo);
-    if (rf.x) {
-        __syncwarp();  // lane 0 wrote the indices
-        warp_refine_weights(rf, t, k, lane, io, wo);
+    if (warp == 0) {
+        const float *lt = ws.logits + (size_t)t * E;
+        int *io = rf.x ? s_i : ws.topk_idx + (size_t)t * k;
+        float *wo = rf.x ? s_wt : ws.topk_w + (size_t)t * k;
+        if (E <= 32) warp_topk_token<1>(lt, E, k, lane, io, wo);
+        else if (E <= 64) warp_topk_token<2>(lt, E, k, lane, io, wo);
+        else if (E <= 128) warp_topk_token<4>(lt, E, k, lane, io, wo);
+        else if (E <= 256) warp_topk_token<8>(lt, E, k, lane, io, wo);
+        else if (E <= 512) warp_topk_token<16>(lt, E, k, lane, io, wo);
+        else warp_topk_token<32>(lt, E, k, lane, io, wo);
+    }
+    if (!rf.x) return;
+    __syncthreads();
+    for (int j = warp; j < k; j += (int)(blockDim.x >> 5)) {
+        const float l = warp_router_logit(rf, t, s_i[j], lane);
+        if (lane == 0) s_l[j] = l;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        renorm_selected(s_l, k, ws.topk_w + (size_t)t * k);
+        for (int j = 0; j < k; ++j) ws.topk_idx[(size_t)t * k + j] = s_i[j];
     }
 }
 
@@ -284,7 +303,7 @@ cudaError_t launch_prefill_route(const StepArgs &a, const Workspace &ws, int max
     (void)Wcap;
     cudaError_t err = cudaMemsetAsync(ws.tbits, 0, (size_t)E * W * 4, st);
     if (err != cudaSuccess) return err;
-    topk_tokens_kernel<<<(n + 7) / 8, 256, 0, st>>>(ws, n, E, k, rf);
+    topk_tokens_kernel<<<n, 256, 0, st>>>(ws, n, E, k, rf);
     group_mark_kernel<<<(n * k + 255) / 256, 256, 0, st>>>(ws, n, k, a.s.e_lo, a.s.e_hi, W);
     group_count_kernel<<<E, 256, 0, st>>>(ws, W);
     group_offsets_kernel<<<1, 32, 0, st>>>(ws, E);
