@@ -1,5 +1,7 @@
-// prefill_tc.cu -- the prefill path's expert GEMMs on the 5th-generation tensor
-// cores (tcgen05.mma, accumulators in tensor memory).
+// prefill_tc.cu -- the grouped (17..64 tokens) and prefill paths' tensor-core
+// kernels on the 5th-generation tensor cores (tcgen05.mma, accumulators in
+// tensor memory): the expert GEMMs (expert_tc_kernel, with x_to_f16_kernel for
+// their B operand) and the prefill router (router_tc_kernel, near the end).
 //
 // A prefill cohort gives each selected expert tens to hundreds of tokens, so
 // its MLP is a real matrix product (the sorted qmm path of prompt processing in

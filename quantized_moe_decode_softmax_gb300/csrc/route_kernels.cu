@@ -1,5 +1,7 @@
-// route_kernels.cu -- stand-alone routing kernels (used by the f32 check path):
-// the router GEMV, and a single-CTA kernel for softmax / top-k / grouping.
+// route_kernels.cu -- the routing kernels of the multi-kernel paths: the
+// CUDA-core router GEMV (grouped path, f32 check path, f32 activations), a
+// single-CTA kernel for softmax / top-k / grouping of up to 64 tokens, and the
+// prefill cohort's per-token top-k and bitmap grouping.
 //
 // Router: logits[t, e] = sum_d x[t, d] * Wr[e, d] (+ bias[e]), f32 accumulate.
 // Source: mlxcel issue #1616 "perf(moe): batched decode scales 1.55x against
