@@ -806,13 +806,15 @@ cudaError_t launch_expert_tc(const StepArgs &a, const Workspace &ws, int thr, bo
     const long mean = ((long)a.s.n * a.s.k + maxU - 1) / maxU;
     const int zb = (int)max(1L, min(8L, (3 * mean / 2 + kN - 1) / kN));
     // persistent: as many CTAs as fit at once (gate/up one per SM, down two),
-    // at most one per item
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        if ((err = cudaGetDevice(&dev)) != cudaSuccess ||
-            (err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-            return err;
+    // at most one per item; SM counts cached per device
+    static int sm_count[64] = {0};
+    int dev = 0, sms = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    if (dev < 64 && sm_count[dev] > 0) {
+        sms = sm_count[dev];
+    } else {
+        if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+        if (dev < 64) sm_count[dev] = sms;
     }
     const long items = (long)((down ? a.s.D : a.s.F) / kM) * maxU * zb;
     const int grid = (int)min(items, (long)sms * (down ? 2 : 1));
