@@ -444,8 +444,8 @@ __device__ __forceinline__ void warp_topk_tagged(const unsigned long long *lt, u
 template <int NKC>
 __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_constant__ DecodeArgs P) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char *sbase = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // 1024-byte aligned start, as an offset into smem_raw (accesses stay shared-memory accesses)
+    unsigned char *sbase = smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u);
     const DecodeLayout &L = P.L;
     const StepArgs &A = P.a;
     const Workspace &W = P.ws;

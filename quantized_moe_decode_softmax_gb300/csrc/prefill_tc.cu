@@ -241,34 +241,32 @@ struct TcItem {
     int e, off_e, cnt_e, r0, z, total;  // total: chunks (token blocks x chunks per row)
 };
 
+// the CTA's table of the unique experts, in shared memory: per unique expert u,
+// {first item number pref[u], expert id, first slot, slot count}
 struct TcGrid {
     int RB, ZB, U, nchunks, G, NI;
-    const int *pref;  // [U + 1] in shared memory
+    const int4 *tab;  // [U]
 };
 
-__device__ __forceinline__ int tc_item(const Workspace &ws, const TcGrid &g, int k, TcItem &it) {
+// item k (or -1 past the last): a binary search over the table, shared memory only
+__device__ __forceinline__ int tc_seek(const TcGrid &g, int k, TcItem &it) {
     if (k >= g.NI) return -1;
     int lo = 0, hi = g.U;                 // last u with pref[u] <= k
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (g.pref[mid] <= k) lo = mid;
+        if (g.tab[mid].x <= k) lo = mid;
         else hi = mid;
     }
-    const int local = k - g.pref[lo];
-    const int e = ws.unique[lo];
-    it.e = e;
-    it.off_e = ws.offsets[e];
-    it.cnt_e = ws.offsets[e + 1] - it.off_e;
+    const int4 t = g.tab[lo];
+    const int local = k - t.x;
+    it.e = t.y;
+    it.off_e = t.z;
+    it.cnt_e = t.w;
     it.r0 = (local % g.RB) * kM;
     it.z = local / g.RB;
     const int nblk = (it.cnt_e + kN - 1) / kN;
     it.total = ((nblk - it.z + g.ZB - 1) / g.ZB) * g.nchunks;
     return k;
-}
-
-// the item after k in this CTA's list, or -1
-__device__ __forceinline__ int tc_seek(const Workspace &ws, const TcGrid &g, int k, TcItem &it) {
-    return tc_item(ws, g, k, it);
 }
 
 // tm0, tm1: tensor maps of the code planes (gate and up, or down and unused),
@@ -277,57 +275,22 @@ __device__ __forceinline__ int tc_seek(const Workspace &ws, const TcGrid &g, int
 // across item boundaries, so the next item's loads overlap this one's tail.
 template <bool GATEUP, int S>
 __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
-    expert_tc_kernel(StepArgs a, Workspace ws, int thr, int ZB, const __grid_constant__ CUtensorMap tm0,
+    expert_tc_kernel(StepArgs a, Workspace ws, int thr, int ZB, int ucap, const __grid_constant__ CUtensorMap tm0,
                      const __grid_constant__ CUtensorMap tm1) {
     constexpr int MATS = GATEUP ? 2 : 1;
     constexpr int kDq = MATS * 256;            // dequantisation threads
     constexpr int kProdW = kDq / 32;           // first of the four producer warps
     constexpr int kMmaW = kProdW + 4;          // MMA warp
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char *base = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                            ~static_cast<uintptr_t>(1023));
+    // 1024-byte aligned start of the dynamic area, as an offset into smem_raw
+    // (so every access below stays a shared-memory access)
+    unsigned char *base = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
     // after a timeout anywhere in the launch, later CTAs do no work
     if (*reinterpret_cast<volatile unsigned *>(ws.status) & kDevErrTimeout) return;
     const int D = a.s.D, F = a.s.F;
     const int K = GATEUP ? D : F;            // reduction length
     const int rows_pe = GATEUP ? F : D;      // weight rows per expert
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // the item numbering: prefix over the unique experts of their items
-    __shared__ int s_pref[kMaxE + 1];
-    TcGrid g;
-    g.RB = rows_pe / kM;
-    g.ZB = ZB;
-    g.U = *ws.U;
-    g.nchunks = K / kK;
-    g.G = (int)gridDim.x;
-    g.pref = s_pref;
-    if (warp == 0) {
-        int run = 0;
-        for (int u0 = 0; u0 < g.U; u0 += 32) {
-            const int u = u0 + lane;
-            int v = 0;
-            if (u < g.U) {
-                const int e = ws.unique[u];
-                const int cnt = ws.offsets[e + 1] - ws.offsets[e];
-                v = cnt >= thr ? g.RB * min(ZB, (cnt + kN - 1) / kN) : 0;
-            }
-            int inc = v;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int t = __shfl_up_sync(0xffffffffu, inc, o);
-                if (lane >= o) inc += t;
-            }
-            if (u < g.U) s_pref[u] = run + inc - v;
-            run += __shfl_sync(0xffffffffu, inc, 31);
-        }
-        if (lane == 0) s_pref[g.U] = run;
-    }
-    __syncthreads();
-    g.NI = s_pref[g.U];
-    TcItem first;
-    const int i0 = tc_seek(ws, g, (int)blockIdx.x, first);
-    if (i0 < 0) return;                      // no work for this CTA
-    const int nchunks = g.nchunks;
 
     const bool six = !GATEUP && a.s.down_bits == 6;
     const int cbr = six ? 96 : 64;           // code bytes per row and chunk
@@ -346,6 +309,50 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
     uint64_t *acc_full = c_empty + S, *acc_empty = acc_full + 1;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(acc_empty + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
+    int4 *tab = reinterpret_cast<int4 *>(tslot + 4);   // [ucap], 16-byte aligned
+
+    // the item numbering: prefix over the unique experts of their items, with
+    // each expert's id and slot range, into the table
+    TcGrid g;
+    g.RB = rows_pe / kM;
+    g.ZB = ZB;
+    g.U = *ws.U;
+    g.nchunks = K / kK;
+    g.G = (int)gridDim.x;
+    g.tab = tab;
+    if (g.U > ucap) {                        // more unique experts than selected slots: impossible
+        if (tid == 0) report_error(ws.status, kDevErrInternal);
+        return;
+    }
+    __shared__ int s_ni;
+    if (warp == 0) {
+        int run = 0;
+        for (int u0 = 0; u0 < g.U; u0 += 32) {
+            const int u = u0 + lane;
+            int v = 0, e = 0, off = 0, cnt = 0;
+            if (u < g.U) {
+                e = ws.unique[u];
+                off = ws.offsets[e];
+                cnt = ws.offsets[e + 1] - off;
+                v = cnt >= thr ? g.RB * min(ZB, (cnt + kN - 1) / kN) : 0;
+            }
+            int inc = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += t;
+            }
+            if (u < g.U) tab[u] = make_int4(run + inc - v, e, off, cnt);
+            run += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        if (lane == 0) s_ni = run;
+    }
+    __syncthreads();
+    g.NI = s_ni;
+    TcItem first;
+    const int i0 = tc_seek(g, (int)blockIdx.x, first);
+    if (i0 < 0) return;                      // no work for this CTA
+    const int nchunks = g.nchunks;
 
     // tensor memory: accumulators (gate, up or y: 64 columns each), then the
     // NA A buffers (MATS tiles of 64 columns: 128 inputs, two f16 per column)
@@ -383,12 +390,14 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
         const uint16_t *bsrc = reinterpret_cast<const uint16_t *>(GATEUP ? (const void *)ws.y : (const void *)ws.h);
         const int j = lane & 15, tq = 16 * (warp - kProdW) + (lane >> 4);
         uint32_t roff[kN / 8];
-        int gidx = 0;
+        // chunk gidx of the CTA goes to ring stage sidx = gidx % S, in that
+        // stage's use number gidx / S (parity sph)
+        int gidx = 0, sidx = 0;
+        uint32_t sph = 0;
         bool stop = false;
         TcItem it = first;
-        for (int i = i0; i >= 0 && !stop; i = tc_seek(ws, g, i + g.G, it)) {
-            for (int li = 0; li < it.total; ++li, ++gidx) {
-                const int sidx = gidx % S, blk = it.z + (li / nchunks) * ZB, c = li % nchunks;
+        for (int i = i0; i >= 0 && !stop; i = tc_seek(g, i + g.G, it)) {
+            for (int li = 0, c = 0, blk = it.z; li < it.total; ++li) {
                 if (c == 0) {
 #pragma unroll
                     for (int q = 0; q < kN / 8; ++q) {
@@ -401,8 +410,8 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
                     }
                 }
                 if (gidx >= S) {
-                    const uint32_t par = (uint32_t)((gidx / S - 1) & 1);
-                    if (!wait_bar(&b_empty[sidx], par, ws.status) || !wait_bar(&c_empty[sidx], par, ws.status))
+                    // the stage's previous use (parity sph ^ 1) has been consumed
+                    if (!wait_bar(&b_empty[sidx], sph ^ 1u, ws.status) || !wait_bar(&c_empty[sidx], sph ^ 1u, ws.status))
                         *abort_flag = 1;
                 }
                 if (__any_sync(0xffffffffu, *abort_flag != 0)) {  // warp-uniform
@@ -423,6 +432,15 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
                 for (int q = 0; q < kN / 8; ++q)
                     if (roff[q] != 0xFFFFFFFFu) tc::cp_async16(sub + core_off(tq + 2 * q, j & 7), src + roff[q]);
                 bar_arrive_cp_async(&b_full[sidx]);
+                ++gidx;
+                if (++sidx == S) {
+                    sidx = 0;
+                    sph ^= 1u;
+                }
+                if (++c == nchunks) {
+                    c = 0;
+                    blk += ZB;
+                }
             }
         }
     } else if (warp == kMmaW) {
@@ -431,14 +449,16 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
         // matrix descriptor of the first ring stage's B tile (a K step of 16
         // inputs adds 32 bytes, 2 in the start field)
         const uint64_t descB0 = tc::smem_desc_sw128(tc::smem_u32(ring), kSbo);
-        int issued = -1, gidx = 0, gblk = 0;
+        // chunk gidx: ring stage sidx = gidx % S (use parity sph), A buffer
+        // bsel = gidx % NA (use parity aph)
+        int issued = -1, gidx = 0, gblk = 0, sidx = 0, bsel = 0;
+        uint32_t sph = 0, aph = 0;
         bool stop = false;
         TcItem it = first;
-        for (int i = i0; i >= 0 && !stop; i = tc_seek(ws, g, i + g.G, it)) {
-            for (int li = 0; li < it.total; ++li, ++gidx) {
-                const int bsel = gidx % NA, sidx = gidx % S, c = li % nchunks;
-                bool ok = wait_bar(&a_full[bsel], (uint32_t)((gidx / NA) & 1), ws.status);
-                ok = ok && wait_bar(&b_full[sidx], (uint32_t)((gidx / S) & 1), ws.status);
+        for (int i = i0; i >= 0 && !stop; i = tc_seek(g, i + g.G, it)) {
+            for (int li = 0, c = 0; li < it.total; ++li) {
+                bool ok = wait_bar(&a_full[bsel], aph, ws.status);
+                ok = ok && wait_bar(&b_full[sidx], sph, ws.status);
                 // a block's first MMAs overwrite the accumulators of the one before
                 if (ok && c == 0 && gblk > 0) ok = wait_bar(acc_empty, (uint32_t)((gblk - 1) & 1), ws.status);
                 if (!ok) *abort_flag = 1;
@@ -466,7 +486,19 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
                 }
                 __syncwarp();
                 issued = gidx;
-                if (c == nchunks - 1) ++gblk;
+                ++gidx;
+                if (++sidx == S) {
+                    sidx = 0;
+                    sph ^= 1u;
+                }
+                if (++bsel == NA) {
+                    bsel = 0;
+                    aph ^= 1u;
+                }
+                if (++c == nchunks) {
+                    c = 0;
+                    ++gblk;
+                }
             }
         }
         // after an abort: wait (bounded) for the MMAs still in flight before
@@ -482,14 +514,14 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
         const uint16_t *b_pl = GATEUP ? (m ? a.planes.up_b : a.planes.gate_b) : a.planes.down_b;
         // the scale stream: blocks of V groups (cpb chunks) of this thread's row,
         // item after item, each into slot (block number) % 2 of this thread; the
-        // cursor (sc_i, sc_it, sc_sb) is the next block to copy
-        int sc_i = i0, sc_sb = 0;
+        // cursor (sc_i, sc_it; chunk sc_ch of the item, first group sc_g0) is
+        // the next block to copy
+        int sc_i = i0, sc_ch = 0, sc_g0 = 0;
         TcItem sc_it = first;
         auto issue_sc = [&](int nb) {
             if (sc_i >= 0) {
                 const size_t row = (size_t)sc_it.e * rows_pe + sc_it.r0 + rr;
-                const int g0 = (sc_sb * V) % groups;
-                const uint16_t *sr = s_pl + row * groups + g0, *br = b_pl + row * groups + g0;
+                const uint16_t *sr = s_pl + row * groups + sc_g0, *br = b_pl + row * groups + sc_g0;
                 unsigned char *dst = sc_area + ((nb & 1) * kDq + tid) * 32;
                 if (V == 8) {
                     tc::cp_async16(dst, sr);
@@ -501,34 +533,36 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
                     tc::cp_async4(dst, sr);
                     tc::cp_async4(dst + 16, br);
                 }
-                if ((sc_sb + 1) * cpb < sc_it.total) {
-                    ++sc_sb;
-                } else {
-                    sc_i = tc_seek(ws, g, sc_i + g.G, sc_it);
-                    sc_sb = 0;
+                if ((sc_g0 += V) == groups) sc_g0 = 0;
+                if ((sc_ch += cpb) >= sc_it.total) {
+                    sc_i = tc_seek(g, sc_i + g.G, sc_it);
+                    sc_ch = 0;
+                    sc_g0 = 0;
                 }
             }
             tc::cp_async_commit();
         };
         int nb = 0;       // scale blocks reached so far
         issue_sc(0);
-        int gidx = 0, gblk = 0;
+        // chunk gidx: ring stage sidx (use parity sph), A buffer bsel (use
+        // parity aph), chunk c of the row pass over token block blk, chunk sbp of
+        // the scale block
+        int gidx = 0, gblk = 0, sidx = 0, bsel = 0;
+        uint32_t sph = 0, aph = 0;
         bool stop = false;
         TcItem it = first;
-        for (int i = i0; i >= 0 && !stop; i = tc_seek(ws, g, i + g.G, it)) {
-            for (int li = 0; li < it.total; ++li, ++gidx) {
-                const int bsel = gidx % NA, sidx = gidx % S, c = li % nchunks;
-                const int blk = it.z + (li / nchunks) * ZB;
+        for (int i = i0; i >= 0 && !stop; i = tc_seek(g, i + g.G, it)) {
+            for (int li = 0, c = 0, blk = it.z, sbp = 0; li < it.total; ++li) {
                 const unsigned char *st = ring + sidx * stage_stride;
-                if (li % cpb == 0) {
+                if (sbp == 0) {
                     // start the next scale block, wait for this one
                     issue_sc(nb + 1);
                     tc::cp_async_wait<1>();
                     ++nb;
                 }
-                bool ok = wait_bar(&c_full[sidx], (uint32_t)((gidx / S) & 1), ws.status);
+                bool ok = wait_bar(&c_full[sidx], sph, ws.status);
                 // A buffer bsel is free once the MMAs of chunk gidx - NA are done
-                if (ok && gidx >= NA) ok = wait_bar(&mma_done[bsel], (uint32_t)((gidx / NA - 1) & 1), ws.status);
+                if (ok && gidx >= NA) ok = wait_bar(&mma_done[bsel], aph ^ 1u, ws.status);
                 if (!ok) *abort_flag = 1;
                 // warp-uniform: tcgen05.st and tcgen05.ld below are warp-collective
                 if (__any_sync(0xffffffffu, *abort_flag != 0)) {
@@ -538,7 +572,7 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
                 {
                     const uint16_t *scs =
                         reinterpret_cast<const uint16_t *>(sc_area + ((((nb - 1) & 1) * kDq) + tid) * 32);
-                    const int gi = 2 * (li % cpb) + gsel;   // this thread's group inside the block
+                    const int gi = 2 * sbp + gsel;          // this thread's group inside the block
                     float s = bf16f(scs[gi]), b = bf16f(scs[8 + gi]);
                     if (fabsf(s) > 65504.0f || fabsf(b) > 65504.0f) {  // beyond f16: saturate, report
                         report_error(ws.status, kDevErrRange);
@@ -585,7 +619,7 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
                 bar_arrive(&a_full[bsel]);
                 if (c == nchunks - 1) {
                     // epilogue of this token block, once its last MMAs have completed
-                    if (!wait_bar(acc_full, (uint32_t)(gblk & 1), ws.status)) *abort_flag = 1;
+                    if (!wait_bar(acc_full, (uint32_t)gblk & 1u, ws.status)) *abort_flag = 1;
                     tc::fence_after_sync();
                     constexpr int kTokW = kN / (kDq / 128);          // tokens per warp (16 or 32)
                     const int t0 = kTokW * (warp >> 2);               // tokens [t0, t0 + kTokW) of the block
@@ -619,6 +653,20 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
                     bar_arrive(acc_empty);
                     ++gblk;
                 }
+                ++gidx;
+                if (++sidx == S) {
+                    sidx = 0;
+                    sph ^= 1u;
+                }
+                if (++bsel == NA) {
+                    bsel = 0;
+                    aph ^= 1u;
+                }
+                if (++c == nchunks) {
+                    c = 0;
+                    blk += ZB;
+                }
+                if (++sbp == cpb) sbp = 0;
             }
         }
     }
@@ -647,8 +695,7 @@ __global__ void __launch_bounds__(128, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
                      const float *bias, float *logits, int n, int E, int D, unsigned *status) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char *base = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                            ~static_cast<uintptr_t>(1023));
+    unsigned char *base = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *full = reinterpret_cast<uint64_t *>(base + kRS * kRStage);
     uint64_t *empty = full + kRS, *acc = empty + kRS;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(acc + 1);
@@ -730,10 +777,13 @@ __global__ void __launch_bounds__(128, 1)
 constexpr int kStagesGateUp = 4;   // 4 x 32 KB + 32 KB scale slots
 constexpr int kStagesDown = 3;     // 3 x 24 KB (6-bit 28 KB) + 16 KB: two CTAs per SM
 
-size_t tc_smem_bytes(bool gateup, bool six) {
+// alignment slack, ring, scale slots, mbarriers, tensor-memory slot and abort
+// flag, then the table of at most ucap unique experts (16 bytes each)
+size_t tc_smem_bytes(bool gateup, bool six, int ucap) {
     const int mats = gateup ? 2 : 1, dq = mats * 256;
     const int S = gateup ? kStagesGateUp : kStagesDown;
-    return 1024 + (size_t)S * stage_bytes_of(mats, six ? 96 : 64) + 2 * dq * 32 + (6 + 4 * S + 2) * 8 + 16;
+    return 1024 + (size_t)S * stage_bytes_of(mats, six ? 96 : 64) + 2 * dq * 32 + (6 + 4 * S + 2) * 8 + 16 +
+           (size_t)ucap * 16;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -784,7 +834,9 @@ cudaError_t launch_expert_tc(const StepArgs &a, const Workspace &ws, int thr, bo
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     const bool six = down && a.s.down_bits == 6;
-    const size_t smem = tc_smem_bytes(!down, six);
+    // unique experts: at most one per selected slot
+    const int maxU = min(a.s.E, a.s.n * a.s.k);
+    const size_t smem = tc_smem_bytes(!down, six, maxU);
     // tensor maps of the code planes (rows of D or Dff inputs)
     alignas(64) CUtensorMap tm0, tm1;
     const int K = down ? a.s.F : a.s.D;
@@ -800,7 +852,6 @@ cudaError_t launch_expert_tc(const StepArgs &a, const Workspace &ws, int thr, bo
                          : (const void *)expert_tc_kernel<true, kStagesGateUp>;
     if ((err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
         return err;
-    const int maxU = min(a.s.E, a.s.n * a.s.k);
     // token-block slices: about 1.5x the mean tokens per selected expert, in
     // blocks of 64 (an item loops over its slice's blocks)
     const long mean = ((long)a.s.n * a.s.k + maxU - 1) / maxU;
@@ -819,9 +870,9 @@ cudaError_t launch_expert_tc(const StepArgs &a, const Workspace &ws, int thr, bo
     const long items = (long)((down ? a.s.D : a.s.F) / kM) * maxU * zb;
     const int grid = (int)min(items, (long)sms * (down ? 2 : 1));
     if (!down)
-        expert_tc_kernel<true, kStagesGateUp><<<grid, 672, smem, st>>>(a, ws, thr, zb, tm0, tm1);
+        expert_tc_kernel<true, kStagesGateUp><<<grid, 672, smem, st>>>(a, ws, thr, zb, maxU, tm0, tm1);
     else
-        expert_tc_kernel<false, kStagesDown><<<grid, 416, smem, st>>>(a, ws, thr, zb, tm0, tm1);
+        expert_tc_kernel<false, kStagesDown><<<grid, 416, smem, st>>>(a, ws, thr, zb, maxU, tm0, tm1);
     launched += 1;
     return cudaGetLastError();
 }
