@@ -86,8 +86,8 @@ SEEDS = {"qwen3": 1, "e256": 3, "tiny": 0}
 # timed steps' mean unique-expert count (traffic grows with it).
 KERNEL_SOURCES = ("decode_step.cu", "ptx.cuh", "routing.cuh", "moe_internal.h")
 TRAFFIC = {
-    ("qwen3", 1): {"bytes": 22277888 + 0, "unique": 8, "src": "c07cf40b9300d1e9"},
-    ("qwen3", 8): {"bytes": 139145984 + 4037888, "unique": 52, "src": "c07cf40b9300d1e9"},
+    ("qwen3", 1): {"bytes": 21859328 + 0, "unique": 8, "src": "941f32f5a6607795"},
+    ("qwen3", 8): {"bytes": 138673920 + 2810624, "unique": 52, "src": "941f32f5a6607795"},
 }
 
 

@@ -186,23 +186,23 @@ __global__ void x_to_f16_kernel(StepArgs a, Workspace ws) {
 //   - MATS x 8 dequantisation warps: thread (lane quadrant q, matrix m, group
 //     g of the chunk) owns weight row 32 q + lane of matrix m -- the
 //     tensor-memory lane of that row -- and dequantises that row's 64 weights
-//     of group g of every chunk. It copies its own row's scales and biases, V
-//     groups at a time (V = 8, 4 or 2: the widest that divides the groups of a
-//     row), into a double-buffered slot of its own (cp.async, its own wait
-//     groups), reads its codes from the ring once c_full says the chunk's TMA
-//     box landed, arrives on c_empty, dequantises into A buffer (chunk % 3)
-//     once the MMAs of chunk - 3 are done, and arrives on a_full. After the last
-//     chunk of a token block the same warps run the epilogue.
+//     of group g of every chunk. Once the chunk's codes (c_full) and scale words
+//     (b_full) are in the ring and the MMAs of chunk - 2 are done (mma_done),
+//     it dequantises into A buffer (chunk % 2), arrives on c_empty and a_full.
+//     The same warps run a token block's epilogue, one chunk after the block's
+//     last one.
 //   - four producer warps, one per SM sub-partition (a single one held up the
 //     dequantisation warps of its sub-partition behind its copies), copy the B
-//     tiles (64 tokens x 128 inputs, f16) into the ring, each lane arriving on
-//     b_full when its copies have landed; lane 0 of the first also loads the
-//     chunk's codes (one TMA box of 128 rows per matrix, completing on c_full).
-//     A stage is refilled once its MMAs (b_empty) and its dequantisation
-//     (c_empty) are done.
-//   - one MMA warp waits for a_full and b_full, and one elected lane issues the
-//     chunk's MMAs and commits them to mma_done (A buffer free), b_empty (ring
-//     stage free) and, after a block's last chunk, acc_full.
+//     tiles (64 tokens x 128 inputs, f16) and the chunk's scale and bias words
+//     into the ring, each lane arriving on b_full when its copies have landed;
+//     lane 0 of the first also loads the chunk's codes (one TMA box of 128 rows
+//     per matrix, completing on c_full). A stage is refilled once its MMAs
+//     (b_empty) and its dequantisation (c_empty) are done.
+//   - one MMA warp waits for a_full and b_full (and, at a block's first chunk,
+//     for the epilogue of block - 2 to have read the accumulator, acc_empty),
+//     and one elected lane issues the chunk's MMAs and commits them to mma_done
+//     (A buffer free), b_empty (ring stage free) and, after a block's last
+//     chunk, acc_full.
 // Every wait gives up after 1 s: it reports a timeout and sets the CTA's abort
 // flag, which every role checks once per chunk.
 //
@@ -210,10 +210,10 @@ __global__ void x_to_f16_kernel(StepArgs a, Workspace ws) {
 // 64..127 of the chunk][codes: MATS x 128 rows x cbr bytes, cbr = 64 (4-bit,
 // 64-byte TMA swizzle: 16-byte piece p of row r stored at p ^ ((r / 2) % 4),
 // which spreads 8 consecutive rows reading the same piece over all banks) or
-// 96 (6-bit, no swizzle)]. After the ring: the per-thread scale slots,
-// [2][dequantisation threads][16 bytes scales, 16 bytes biases].
+// 96 (6-bit, no swizzle)][scale words: MATS x 128 rows x 8 bytes, the bf16
+// scales of the chunk's two groups, then their two biases].
 __host__ __device__ constexpr int stage_bytes_of(int mats, int cbr) {
-    return (kTileB + mats * kM * cbr + 1023) & ~1023;
+    return (kTileB + mats * kM * cbr + mats * kM * 8 + 1023) & ~1023;
 }
 
 __host__ __device__ constexpr int code_swz(int rr) { return (rr >> 1) & 3; }
@@ -271,8 +271,8 @@ __device__ __forceinline__ int tc_seek(const TcGrid &g, int k, TcItem &it) {
 
 // tm0, tm1: tensor maps of the code planes (gate and up, or down and unused),
 // 2-D {row bytes, rows} with boxes of {cbr, 128}. The kernel is persistent: the
-// ring, the A buffers, the scale stream and the accumulator hand-off run on
-// across item boundaries, so the next item's loads overlap this one's tail.
+// ring, the A buffers and the two accumulators run on across item boundaries,
+// so the next item's loads overlap this one's tail.
 template <bool GATEUP, int S>
 __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
     expert_tc_kernel(StepArgs a, Workspace ws, int thr, int ZB, int ucap, const __grid_constant__ CUtensorMap tm0,
@@ -296,18 +296,16 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
     const int cbr = six ? 96 : 64;           // code bytes per row and chunk
     const int stage_stride = stage_bytes_of(MATS, cbr);
     const int off_codes = kTileB;
+    const int off_sc = kTileB + MATS * kM * cbr;
     const int groups = K / 64;               // scale/bias entries per row (even)
-    const int V = groups % 8 == 0 ? 8 : groups % 4 == 0 ? 4 : 2;  // groups per scale copy
-    const int cpb = V / 2;                   // chunks per scale copy
 
     unsigned char *ring = base;
-    unsigned char *sc_area = base + S * stage_stride;              // [2][kDq][32]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sc_area + 2 * kDq * 32);
-    constexpr int NA = 3;                      // A buffers in tensor memory
+    uint64_t *bars = reinterpret_cast<uint64_t *>(base + S * stage_stride);
+    constexpr int NA = 2;                      // A buffers in tensor memory
     uint64_t *a_full = bars, *mma_done = bars + NA, *b_full = bars + 2 * NA, *b_empty = b_full + S;
     uint64_t *c_full = b_empty + S, *c_empty = c_full + S;
-    uint64_t *acc_full = c_empty + S, *acc_empty = acc_full + 1;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(acc_empty + 1);
+    uint64_t *acc_full = c_empty + S, *acc_empty = acc_full + 2;   // per accumulator
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(acc_empty + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
     int4 *tab = reinterpret_cast<int4 *>(tslot + 4);   // [ucap], 16-byte aligned
 
@@ -354,10 +352,12 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
     if (i0 < 0) return;                      // no work for this CTA
     const int nchunks = g.nchunks;
 
-    // tensor memory: accumulators (gate, up or y: 64 columns each), then the
-    // NA A buffers (MATS tiles of 64 columns: 128 inputs, two f16 per column)
+    // tensor memory: two accumulators (gate and up, or y: 64 columns each per
+    // matrix), token block b in accumulator b % 2, then the NA A buffers (MATS
+    // tiles of 64 columns: 128 inputs, two f16 per column)
     constexpr uint32_t kCols = GATEUP ? 512 : 256;
-    constexpr uint32_t kAcol = MATS * kN;
+    constexpr uint32_t kAccCols = MATS * kN;
+    constexpr uint32_t kAcol = 2 * kAccCols;
     if (tid == 0) {
         *abort_flag = 0;
         for (int i = 0; i < NA; ++i) {
@@ -370,8 +370,10 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
             bar_init(&c_full[i], 1);
             bar_init(&c_empty[i], kDq);
         }
-        bar_init(acc_full, 1);
-        bar_init(acc_empty, kDq);
+        for (int i = 0; i < 2; ++i) {
+            bar_init(&acc_full[i], 1);
+            bar_init(&acc_empty[i], kDq);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) tc::tmem_alloc(tslot, kCols);
@@ -381,7 +383,7 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
     const uint32_t tmem = *tslot;
 
     if (warp >= kProdW && warp < kMmaW) {
-        // ---- producers: codes (TMA) and B tiles ----------------------------------
+        // ---- producers: codes (TMA), scales and B tiles -------------------------
         // B rows: x in f16 (y area, n x D) or h in f16 (first half of each h row)
         // producer warp pw, lane -> 16-byte piece j (of 16) of tokens 16 pw + tq + 2 i;
         // the tokens' row offsets (f16 elements, below 2^31 for every allowed
@@ -389,7 +391,14 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
         // up once per token block
         const uint16_t *bsrc = reinterpret_cast<const uint16_t *>(GATEUP ? (const void *)ws.y : (const void *)ws.h);
         const int j = lane & 15, tq = 16 * (warp - kProdW) + (lane >> 4);
+        // producer thread pt copies the scale and bias words of weight row pt of
+        // each matrix: groups 2c and 2c + 1, 4 bytes each (through L1: the next
+        // chunks read the same 32-byte sectors)
+        const int pt = tid - kProdW * 32;
+        const uint16_t *s_pl0 = GATEUP ? a.planes.gate_s : a.planes.down_s;
+        const uint16_t *b_pl0 = GATEUP ? a.planes.gate_b : a.planes.down_b;
         uint32_t roff[kN / 8];
+        size_t srow = 0;
         // chunk gidx of the CTA goes to ring stage sidx = gidx % S, in that
         // stage's use number gidx / S (parity sph)
         int gidx = 0, sidx = 0;
@@ -408,6 +417,7 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
                                   : GATEUP       ? (uint32_t)ws.slot_token[it.off_e + jj] * (uint32_t)D
                                                  : (uint32_t)(it.off_e + jj) * (uint32_t)(2 * F);
                     }
+                    srow = ((size_t)it.e * rows_pe + it.r0 + pt) * groups;
                 }
                 if (gidx >= S) {
                     // the stage's previous use (parity sph ^ 1) has been consumed
@@ -425,6 +435,15 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
                     const int y = it.e * rows_pe + it.r0;
                     tc::tma_load_2d(st + off_codes, &tm0, c * cbr, y, &c_full[sidx]);
                     if (GATEUP) tc::tma_load_2d(st + off_codes + kM * cbr, &tm1, c * cbr, y, &c_full[sidx]);
+                }
+                {
+                    unsigned char *sd = st + off_sc + pt * 8;
+                    tc::cp_async4(sd, s_pl0 + srow + 2 * c);
+                    tc::cp_async4(sd + 4, b_pl0 + srow + 2 * c);
+                    if (GATEUP) {
+                        tc::cp_async4(sd + kM * 8, a.planes.up_s + srow + 2 * c);
+                        tc::cp_async4(sd + kM * 8 + 4, a.planes.up_b + srow + 2 * c);
+                    }
                 }
                 const uint16_t *src = bsrc + (size_t)c * kK + 8 * j;
                 unsigned char *sub = st + (j >> 3) * kSubB;
@@ -450,7 +469,8 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
         // inputs adds 32 bytes, 2 in the start field)
         const uint64_t descB0 = tc::smem_desc_sw128(tc::smem_u32(ring), kSbo);
         // chunk gidx: ring stage sidx = gidx % S (use parity sph), A buffer
-        // bsel = gidx % NA (use parity aph)
+        // bsel = gidx % NA (use parity aph); token block gblk in accumulator
+        // gblk % 2
         int issued = -1, gidx = 0, gblk = 0, sidx = 0, bsel = 0;
         uint32_t sph = 0, aph = 0;
         bool stop = false;
@@ -459,8 +479,10 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
             for (int li = 0, c = 0; li < it.total; ++li) {
                 bool ok = wait_bar(&a_full[bsel], aph, ws.status);
                 ok = ok && wait_bar(&b_full[sidx], sph, ws.status);
-                // a block's first MMAs overwrite the accumulators of the one before
-                if (ok && c == 0 && gblk > 0) ok = wait_bar(acc_empty, (uint32_t)((gblk - 1) & 1), ws.status);
+                // a block's first MMAs overwrite the accumulator of block gblk - 2,
+                // whose epilogue (use (gblk / 2) - 1) must have read it
+                if (ok && c == 0 && gblk >= 2)
+                    ok = wait_bar(&acc_empty[gblk & 1], (((uint32_t)gblk >> 1) & 1u) ^ 1u, ws.status);
                 if (!ok) *abort_flag = 1;
                 if (__any_sync(0xffffffffu, *abort_flag != 0)) {  // warp-uniform
                     stop = true;
@@ -468,6 +490,7 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
                 }
                 const uint64_t bd0 = descB0 + (uint64_t)((sidx * stage_stride) >> 4);
                 const uint32_t a0 = tmem + kAcol + (uint32_t)(bsel * MATS * 64);
+                const uint32_t d0 = tmem + (uint32_t)(gblk & 1) * kAccCols;
                 __syncwarp();
                 if (tc::elect_one()) {
                     tc::fence_after_sync();
@@ -477,12 +500,12 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
                         const uint64_t bd = bd0 + (uint64_t)(((ks >> 2) * kSubB) >> 4) + 2 * (ks & 3);
 #pragma unroll
                         for (int m = 0; m < MATS; ++m)
-                            tc::mma_f16_ts(tmem + m * kN, a0 + (uint32_t)(m * 64 + ks * 8), bd, idesc,
+                            tc::mma_f16_ts(d0 + m * kN, a0 + (uint32_t)(m * 64 + ks * 8), bd, idesc,
                                            (c > 0 || ks > 0) ? 1u : 0u);
                     }
                     tc::commit(&mma_done[bsel]);
                     tc::commit(&b_empty[sidx]);
-                    if (c == nchunks - 1) tc::commit(acc_full);
+                    if (c == nchunks - 1) tc::commit(&acc_full[gblk & 1]);
                 }
                 __syncwarp();
                 issued = gidx;
@@ -510,57 +533,60 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
         const int m = (warp >> 2) % MATS, gsel = warp / (4 * MATS);
         const int rr = 32 * (warp & 3) + lane;
         const uint32_t tlane = (uint32_t)(32 * (warp & 3)) << 16;
-        const uint16_t *s_pl = GATEUP ? (m ? a.planes.up_s : a.planes.gate_s) : a.planes.down_s;
-        const uint16_t *b_pl = GATEUP ? (m ? a.planes.up_b : a.planes.gate_b) : a.planes.down_b;
-        // the scale stream: blocks of V groups (cpb chunks) of this thread's row,
-        // item after item, each into slot (block number) % 2 of this thread; the
-        // cursor (sc_i, sc_it; chunk sc_ch of the item, first group sc_g0) is
-        // the next block to copy
-        int sc_i = i0, sc_ch = 0, sc_g0 = 0;
-        TcItem sc_it = first;
-        auto issue_sc = [&](int nb) {
-            if (sc_i >= 0) {
-                const size_t row = (size_t)sc_it.e * rows_pe + sc_it.r0 + rr;
-                const uint16_t *sr = s_pl + row * groups + sc_g0, *br = b_pl + row * groups + sc_g0;
-                unsigned char *dst = sc_area + ((nb & 1) * kDq + tid) * 32;
-                if (V == 8) {
-                    tc::cp_async16(dst, sr);
-                    tc::cp_async16(dst + 16, br);
-                } else if (V == 4) {
-                    tc::cp_async8(dst, sr);
-                    tc::cp_async8(dst + 16, br);
+        // The epilogue of token block pb runs one chunk late, after the next
+        // chunk's dequantisation, so the block's last MMAs complete meanwhile
+        // (the next block accumulates into the other accumulator). Its item
+        // fields are kept: the next chunk may belong to the next item.
+        bool pend = false;
+        int p_b = 0, p_blk = 0, p_off = 0, p_cnt = 0, p_r0 = 0;
+        auto epilogue = [&]() {
+            if (!wait_bar(&acc_full[p_b & 1], ((uint32_t)p_b >> 1) & 1u, ws.status)) *abort_flag = 1;
+            __syncwarp();
+            tc::fence_after_sync();
+            const uint32_t acc = tmem + tlane + (uint32_t)(p_b & 1) * kAccCols;
+            constexpr int kTokW = kN / (kDq / 128);          // tokens per warp (16 or 32)
+            const int t0 = kTokW * (warp >> 2);               // tokens [t0, t0 + kTokW) of the block
+            const int r = p_r0 + rr;
+#pragma unroll
+            for (int hh = 0; hh < kTokW / 16; ++hh) {
+                const int tc0 = t0 + 16 * hh;
+                float gv[16];
+                tc::ld_32x32b_x16(acc + tc0, gv);
+                if (GATEUP) {
+                    float uu[16];
+                    tc::ld_32x32b_x16(acc + kN + tc0, uu);
+                    // h row of the slot, f16 in the core order, in the first half of the f32 row
+                    const int pos = (r & ~7) | core_pos(r & 7);
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const int jj = p_blk * kN + tc0 + q;
+                        if (jj < p_cnt)
+                            reinterpret_cast<__half *>(ws.h + (size_t)(p_off + jj) * F)[pos] =
+                                sat_h(glu_act<false>(a.s.act, a.s.act_limit, gv[q], uu[q]), ws.status);
+                    }
                 } else {
-                    tc::cp_async4(dst, sr);
-                    tc::cp_async4(dst + 16, br);
-                }
-                if ((sc_g0 += V) == groups) sc_g0 = 0;
-                if ((sc_ch += cpb) >= sc_it.total) {
-                    sc_i = tc_seek(g, sc_i + g.G, sc_it);
-                    sc_ch = 0;
-                    sc_g0 = 0;
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const int jj = p_blk * kN + tc0 + q;
+                        if (jj < p_cnt) ws.y[(size_t)(p_off + jj) * D + r] = gv[q];
+                    }
                 }
             }
-            tc::cp_async_commit();
+            tc::fence_before_sync();
+            bar_arrive(&acc_empty[p_b & 1]);
         };
-        int nb = 0;       // scale blocks reached so far
-        issue_sc(0);
         // chunk gidx: ring stage sidx (use parity sph), A buffer bsel (use
-        // parity aph), chunk c of the row pass over token block blk, chunk sbp of
-        // the scale block
+        // parity aph), chunk c of the row pass over token block blk
         int gidx = 0, gblk = 0, sidx = 0, bsel = 0;
         uint32_t sph = 0, aph = 0;
         bool stop = false;
         TcItem it = first;
         for (int i = i0; i >= 0 && !stop; i = tc_seek(g, i + g.G, it)) {
-            for (int li = 0, c = 0, blk = it.z, sbp = 0; li < it.total; ++li) {
+            for (int li = 0, c = 0, blk = it.z; li < it.total; ++li) {
                 const unsigned char *st = ring + sidx * stage_stride;
-                if (sbp == 0) {
-                    // start the next scale block, wait for this one
-                    issue_sc(nb + 1);
-                    tc::cp_async_wait<1>();
-                    ++nb;
-                }
-                bool ok = wait_bar(&c_full[sidx], sph, ws.status);
+                // the chunk's codes (c_full) and its scale words (b_full: the
+                // producers' copies of the stage)
+                bool ok = wait_bar(&c_full[sidx], sph, ws.status) && wait_bar(&b_full[sidx], sph, ws.status);
                 // A buffer bsel is free once the MMAs of chunk gidx - NA are done
                 if (ok && gidx >= NA) ok = wait_bar(&mma_done[bsel], aph ^ 1u, ws.status);
                 if (!ok) *abort_flag = 1;
@@ -570,10 +596,10 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
                     break;
                 }
                 {
-                    const uint16_t *scs =
-                        reinterpret_cast<const uint16_t *>(sc_area + ((((nb - 1) & 1) * kDq) + tid) * 32);
-                    const int gi = 2 * sbp + gsel;          // this thread's group inside the block
-                    float s = bf16f(scs[gi]), b = bf16f(scs[8 + gi]);
+                    // this row's scale and bias words of the chunk's two groups
+                    const uint2 sbw = *reinterpret_cast<const uint2 *>(st + off_sc + (m * kM + rr) * 8);
+                    float s = bf16f((uint16_t)(gsel ? sbw.x >> 16 : sbw.x & 0xFFFFu));
+                    float b = bf16f((uint16_t)(gsel ? sbw.y >> 16 : sbw.y & 0xFFFFu));
                     if (fabsf(s) > 65504.0f || fabsf(b) > 65504.0f) {  // beyond f16: saturate, report
                         report_error(ws.status, kDevErrRange);
                         s = fminf(fmaxf(s, -65504.0f), 65504.0f);
@@ -612,46 +638,22 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
                     tc::st_32x32b_x16_async(ta, *reinterpret_cast<const uint32_t(*)[16]>(o));
                     tc::st_32x32b_x16_async(ta + 16, *reinterpret_cast<const uint32_t(*)[16]>(o + 16));
                 }
-                // the codes of this stage have been read
+                // the codes and scale words of this stage have been read
                 bar_arrive(&c_empty[sidx]);
                 tc::wait_st();
                 tc::fence_before_sync();
                 bar_arrive(&a_full[bsel]);
+                if (pend) {
+                    epilogue();
+                    pend = false;
+                }
                 if (c == nchunks - 1) {
-                    // epilogue of this token block, once its last MMAs have completed
-                    if (!wait_bar(acc_full, (uint32_t)gblk & 1u, ws.status)) *abort_flag = 1;
-                    tc::fence_after_sync();
-                    constexpr int kTokW = kN / (kDq / 128);          // tokens per warp (16 or 32)
-                    const int t0 = kTokW * (warp >> 2);               // tokens [t0, t0 + kTokW) of the block
-                    const int r = it.r0 + rr;
-#pragma unroll
-                    for (int hh = 0; hh < kTokW / 16; ++hh) {
-                        const int tc0 = t0 + 16 * hh;
-                        float gv[16];
-                        tc::ld_32x32b_x16(tmem + tlane + tc0, gv);
-                        if (GATEUP) {
-                            float uu[16];
-                            tc::ld_32x32b_x16(tmem + tlane + kN + tc0, uu);
-                            // h row of the slot, f16 in the core order, in the first half of the f32 row
-                            const int pos = (r & ~7) | core_pos(r & 7);
-#pragma unroll
-                            for (int q = 0; q < 16; ++q) {
-                                const int jj = blk * kN + tc0 + q;
-                                if (jj < it.cnt_e)
-                                    reinterpret_cast<__half *>(ws.h + (size_t)(it.off_e + jj) * F)[pos] =
-                                        sat_h(glu_act<false>(a.s.act, a.s.act_limit, gv[q], uu[q]), ws.status);
-                            }
-                        } else {
-#pragma unroll
-                            for (int q = 0; q < 16; ++q) {
-                                const int jj = blk * kN + tc0 + q;
-                                if (jj < it.cnt_e) ws.y[(size_t)(it.off_e + jj) * D + r] = gv[q];
-                            }
-                        }
-                    }
-                    tc::fence_before_sync();
-                    bar_arrive(acc_empty);
-                    ++gblk;
+                    pend = true;
+                    p_b = gblk++;
+                    p_blk = blk;
+                    p_off = it.off_e;
+                    p_cnt = it.cnt_e;
+                    p_r0 = it.r0;
                 }
                 ++gidx;
                 if (++sidx == S) {
@@ -666,9 +668,10 @@ __global__ void __launch_bounds__(GATEUP ? 672 : 416, GATEUP ? 1 : 2)
                     c = 0;
                     blk += ZB;
                 }
-                if (++sbp == cpb) sbp = 0;
             }
         }
+        // the last token block's epilogue (warp-uniform: it holds warp-collective loads)
+        if (pend && !stop && !__any_sync(0xffffffffu, *abort_flag != 0)) epilogue();
     }
     tc::cp_async_wait<0>();
     tc::fence_before_sync();
@@ -774,16 +777,16 @@ __global__ void __launch_bounds__(128, 1)
 }
 
 // ring stages per variant
-constexpr int kStagesGateUp = 4;   // 4 x 32 KB + 32 KB scale slots
-constexpr int kStagesDown = 3;     // 3 x 24 KB (6-bit 28 KB) + 16 KB: two CTAs per SM
+constexpr int kStagesGateUp = 4;   // 4 x 35 KB
+constexpr int kStagesDown = 3;     // 3 x 26 KB (6-bit 30 KB): two CTAs per SM
 
-// alignment slack, ring, scale slots, mbarriers, tensor-memory slot and abort
-// flag, then the table of at most ucap unique experts (16 bytes each)
+// alignment slack, ring, mbarriers (2 x 2 A-buffer, 4 x S ring, 2 x 2
+// accumulator), tensor-memory slot and abort flag, then the table of at most
+// ucap unique experts (16 bytes each)
 size_t tc_smem_bytes(bool gateup, bool six, int ucap) {
-    const int mats = gateup ? 2 : 1, dq = mats * 256;
+    const int mats = gateup ? 2 : 1;
     const int S = gateup ? kStagesGateUp : kStagesDown;
-    return 1024 + (size_t)S * stage_bytes_of(mats, six ? 96 : 64) + 2 * dq * 32 + (6 + 4 * S + 2) * 8 + 16 +
-           (size_t)ucap * 16;
+    return 1024 + (size_t)S * stage_bytes_of(mats, six ? 96 : 64) + (4 + 4 * S + 4) * 8 + 16 + (size_t)ucap * 16;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
