@@ -24,16 +24,17 @@
 //   - A (weights) is dequantised by the CUDA cores: w = s q + b, one f16
 //     rounding, as the grouped path's tile variant.
 //
-// Per CTA: one expert, 128 weight rows, 64 of the expert's tokens at a time,
+// Per work item: one expert, 128 weight rows, 64 of the expert's tokens at a time,
 // K (the reduction) in chunks of 128 inputs = two quantisation groups:
 //   - a ring of S stages holds, per chunk, the B tile, the raw codes and the
 //     scale/bias words of the CTA's rows, filled S - 1 chunks ahead;
 //   - the CUDA cores dequantise chunk i into one of two A tiles while the
 //     tensor core runs chunk i - 1 (one thread issues M = 128, N = 64, K = 16
 //     MMAs and commits them to an mbarrier);
-//   - after the last chunk of a token block, tcgen05.ld brings the f32
-//     accumulators to registers: h = act(gate, up) (gate row r and up row r
-//     are both tensor-memory lane r) or y for the down projection.
+//   - token blocks alternate between two accumulators; one chunk after a
+//     block's last one, tcgen05.ld brings its f32 accumulators to registers:
+//     h = act(gate, up) (gate row r and up row r are both tensor-memory lane
+//     r) or y for the down projection.
 // An operand beyond f16's range saturates and is reported (MOE_ERR_RANGE);
 // every mbarrier wait gives up after 1 s and reports a timeout.
 #include <cuda_fp16.h>
