@@ -778,8 +778,8 @@ __global__ void __launch_bounds__(128, 1)
 }
 
 // ring stages per variant
-constexpr int kStagesGateUp = 4;   // 4 x 35 KB
-constexpr int kStagesDown = 3;     // 3 x 26 KB (6-bit 30 KB): two CTAs per SM
+constexpr int kStagesGateUp = 4;   // 4 x 34 KB (a fifth stage measured slower)
+constexpr int kStagesDown = 3;     // 3 x 25 KB (6-bit 29 KB): two CTAs per SM
 
 // alignment slack, ring, mbarriers (2 x 2 A-buffer, 4 x S ring, 2 x 2
 // accumulator), tensor-memory slot and abort flag, then the table of at most
