@@ -40,6 +40,8 @@
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
+
 #include "activation.cuh"
 #include "device_status.cuh"
 #include "moe_internal.h"
@@ -790,19 +792,21 @@ size_t tc_smem_bytes(bool gateup, bool six, int ucap) {
     return 1024 + (size_t)S * stage_bytes_of(mats, six ? 96 : 64) + (4 + 4 * S + 4) * 8 + 16 + (size_t)ucap * 16;
 }
 
+// the driver's tensor-map encoder, resolved once (a function-local static is
+// initialised once even when several host threads launch at the same time);
+// null if the driver does not provide it
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         void *p = nullptr;
         cudaDriverEntryPointQueryResult q;
+        PFN_cuTensorMapEncodeTiled_v12000 r = nullptr;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+            r = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
         cudaGetLastError();
-    }
+        return r;
+    }();
     return fn;
 }
 
@@ -861,15 +865,15 @@ cudaError_t launch_expert_tc(const StepArgs &a, const Workspace &ws, int thr, bo
     const long mean = ((long)a.s.n * a.s.k + maxU - 1) / maxU;
     const int zb = (int)max(1L, min(8L, (3 * mean / 2 + kN - 1) / kN));
     // persistent: as many CTAs as fit at once (gate/up one per SM, down two),
-    // at most one per item; SM counts cached per device
-    static int sm_count[64] = {0};
+    // at most one per item; SM counts cached per device (atomics: launches may
+    // come from several host threads)
+    static std::atomic<int> sm_count[64];
     int dev = 0, sms = 0;
     if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
-    if (dev < 64 && sm_count[dev] > 0) {
-        sms = sm_count[dev];
-    } else {
+    if (dev >= 0 && dev < 64) sms = sm_count[dev].load(std::memory_order_relaxed);
+    if (sms <= 0) {
         if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
-        if (dev < 64) sm_count[dev] = sms;
+        if (dev >= 0 && dev < 64) sm_count[dev].store(sms, std::memory_order_relaxed);
     }
     const long items = (long)((down ? a.s.D : a.s.F) / kM) * maxU * zb;
     const int grid = (int)min(items, (long)sms * (down ? 2 : 1));
